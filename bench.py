@@ -1,0 +1,340 @@
+"""Benchmark of the fused attention forward + JVP (jvp_attn_fwd_dual).
+
+One step = one fwd_dual call (the whole hot path) over the bf16 workload
+B=4, H=16, N=2048, D=128 with no mask, inputs resident in HBM.  Timed with
+CUDA events on the launching stream around each call; a 256 MiB buffer is
+written between timed calls so every step starts with a cold L2.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs the same
+workload on its own GPU (replicas, weak scaling, no collective on the data
+path); `value` is all ranks' FLOPs over the slowest rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle, timed on host cores
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+JVP attention TFLOP/s & % of GB300 tensor peak (bf16, N=2048)"
+DEFAULT_WORKLOAD = "bf16_b4h16n2048d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+TC_SOURCES = ["forward_mode_flash_gb300/csrc/fwd_dual_tc.cuh",
+              "forward_mode_flash_gb300/csrc/sm103_ptx.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target length of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in TC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the source."""
+    path = os.path.join(ROOT, "profiles", f"fwd_dual_tc_{workload}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("source_hash") != source_hash():
+        return None  # the kernel changed since the counters were taken
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v and
+                          "Not" not in v})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_baseline(workload, target_s: float):
+    """The float64 oracle on a bounded sample of rows of the same workload."""
+    import numpy as np
+
+    import oracle
+    from forward_mode_flash_gb300 import metrics, synth
+
+    w = synth.WORKLOADS[workload]
+    inp = synth.make_inputs(w)
+    f64 = [x.double().numpy() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    kind = w.mask
+    m = None
+    if w.mask == "bool":
+        m = inp.mask.numpy()
+    elif w.mask == "additive":
+        m = inp.mask.double().numpy()
+    total = w.B * w.H * w.N
+    rng = np.random.default_rng(0)
+    cores = oracle.default_threads()
+    n = max(cores, 16)
+    t0 = time.perf_counter()
+    oracle.fwd_dual_rows(*f64, rng.integers(0, total, n), kind, m)
+    dt = time.perf_counter() - t0
+    n = int(min(total, max(n, n * target_s / max(dt, 1e-3))))
+    rows = rng.integers(0, total, n)
+    t0 = time.perf_counter()
+    oracle.fwd_dual_rows(*f64, rows, kind, m)
+    dt = time.perf_counter() - t0
+    causal = w.mask == "causal"
+    if causal:
+        keys = float(np.sum(np.minimum(rows % w.N + 1, w.N)))
+        flops = 12.0 * keys * w.D
+    else:
+        flops = metrics.flops_fwd_dual(1, 1, n, w.N, w.D)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} random query rows of {workload} (every key of each row), float64 "
+                      f"dual-number oracle, {dt:.1f} s wall"}, dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from forward_mode_flash_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    vals, times = [], []
+    per_step = max(1.0, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for s in range(args.warmup + args.steps):
+        cb, dt = cpu_baseline(args.workload, per_step)
+        if s >= args.warmup:
+            vals.append(cb["value"])
+            times.append(dt)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                       "mask": w.mask, "input_dtype": w.dtype},
+            "cpu_baseline": dict(cb, value=v),
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    from forward_mode_flash_gb300 import attention, build, metrics, synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+
+    w = synth.WORKLOADS[args.workload]
+    causal = w.mask == "causal"
+    inp = synth.make_inputs(w, device=str(dev))
+    g = [inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv]
+    mask = inp.mask
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flops = metrics.flops_fwd_dual(w.B, w.H, w.N, w.N, w.D, causal)
+    elem = g[0].element_size()
+    out = (torch.empty_like(g[0]), torch.empty_like(g[0]))
+
+    def step():
+        return attention.fwd_dual(*g, attn_mask=mask, is_causal=causal, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if attention.last_path() != 1:
+        raise SystemExit("the tensor-core path did not run for the benchmark workload")
+    if world > 1:
+        dist.barrier()
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for s in range(args.steps):
+            flush.fill_(float(s))  # evict L2 between timed steps (outside the events)
+            starts[s].record(stream)
+            step()
+            ends[s].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(per_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    launches = args.steps  # one fwd_dual kernel per step
+
+    # End to end through the public API: pinned host inputs -> device -> kernel -> host.
+    e2e = None
+    if not args.no_e2e:
+        host_in = [x.cpu().pin_memory() for x in g]
+        host_mask = mask.cpu().pin_memory() if mask is not None else None
+        dev_in = [torch.empty_like(x) for x in g]
+        dev_mask = torch.empty_like(mask) if mask is not None else None
+        host_out = [torch.empty(out[0].shape, dtype=out[0].dtype).pin_memory() for _ in range(2)]
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        if host_mask is not None:
+            h2d += host_mask.numel() * host_mask.element_size()
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+        def e2e_step():
+            for d, hsrc in zip(dev_in, host_in):
+                d.copy_(hsrc, non_blocking=True)
+            if dev_mask is not None:
+                dev_mask.copy_(host_mask, non_blocking=True)
+            o, t_o = attention.fwd_dual(*dev_in, attn_mask=dev_mask, is_causal=causal, out=out)
+            host_out[0].copy_(o, non_blocking=True)
+            host_out[1].copy_(t_o, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        k_e2e = max(3, min(args.steps, 10))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / k_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": k_e2e}
+
+    pk, pk_src = peaks()
+    peak = float(pk["bf16_tflops"])
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    traffic = recorded_traffic(args.workload)
+    alg_bytes = metrics.bytes_fwd_dual(w.B, w.H, w.N, w.N, w.D, elem, w.mask, w.B)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "mask": w.mask, "flops_per_step": flops, "algorithmic_bytes_per_step": alg_bytes,
+                   "l2": "flushed: 256 MiB written between timed steps (outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{pk_src} bf16_tflops (burst; kernel timed alone)",
+                     "kernel": "fwd_dual_tc_kernel"},
+        "clocks": clocks.summary(),
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "per_step_ms": {"min": min(per_ms), "median": statistics.median(per_ms),
+                        "max": max(per_ms)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"], _ = cpu_baseline(args.workload, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,155 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+allocates the output tensors with PyTorch, reads pointers, strides and the
+current stream, and calls the entry points declared in ``include/jvp_attn.h``.
+
+API shaped after the "JVP Flash Attention" project page (Usage section):
+``attention(q, k, v, attn_mask=...)`` is the forward, and ``fwd_dual`` returns
+the output together with its tangent for tangents (dq, dk, dv), as
+``JVPAttn.fwd_dual`` does under ``torch.func.jvp``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _abi
+
+_DT = {torch.float32: _abi.JVP_F32, torch.float16: _abi.JVP_F16, torch.bfloat16: _abi.JVP_BF16}
+
+
+def _strides(t: torch.Tensor) -> _abi.Strides:
+    sb, sh, sn, sd = t.stride()
+    return _abi.Strides(sb, sh, sn, sd)
+
+
+def _check_inputs(tensors, names):
+    ref = tensors[0]
+    if ref.dim() != 4:
+        raise ValueError(f"{names[0]} must be [B, H, N, D], got {tuple(ref.shape)}")
+    if ref.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {ref.dtype}")
+    if ref.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for t, n in zip(tensors, names):
+        if t.dtype != ref.dtype or t.device != ref.device or t.dim() != 4:
+            raise ValueError(f"{n} must be a 4-D {ref.dtype} tensor on {ref.device}")
+        if t.shape[-1] != ref.shape[-1] or t.shape[0] != ref.shape[0] or t.shape[1] != ref.shape[1]:
+            raise ValueError(f"{n} has shape {tuple(t.shape)}, inconsistent with {tuple(ref.shape)}")
+        if t.stride(-1) != 1 and t.numel() > 0:
+            raise ValueError(f"{n} must have a unit innermost stride")
+
+
+def _mask_desc(attn_mask: Optional[torch.Tensor], is_causal: bool, B, H, Nq, Nk, device):
+    """Mask description (and the tensor it points into, kept alive by the caller)."""
+    if is_causal:
+        if attn_mask is not None:
+            raise ValueError("is_causal cannot be combined with attn_mask")
+        return _abi.Mask(_abi.JVP_MASK_CAUSAL, None, 0, 0, 0, 0), None
+    if attn_mask is None:
+        return _abi.Mask(_abi.JVP_MASK_NONE, None, 0, 0, 0, 0), None
+    if attn_mask.device != device:
+        raise ValueError("attn_mask must be on the same device as q")
+    if attn_mask.dtype == torch.bool:
+        kind, m = _abi.JVP_MASK_BOOL, attn_mask.view(torch.uint8)
+    elif attn_mask.dtype == torch.float32:
+        kind, m = _abi.JVP_MASK_ADDITIVE, attn_mask
+    else:
+        raise TypeError("attn_mask must be torch.bool (keep-mask) or torch.float32 (additive)")
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    m = m.expand(B, H, Nq, Nk)  # broadcast dimensions get stride 0
+    sb, sh, sq, sk = m.stride()
+    return _abi.Mask(kind, m.data_ptr(), sb, sh, sq, sk), m
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor,
+             dk: torch.Tensor, dv: torch.Tensor, attn_mask: Optional[torch.Tensor] = None,
+             is_causal: bool = False, scale: Optional[float] = None, return_stats: bool = False,
+             out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """Attention forward and its JVP in one fused pass.
+
+    Returns (o, t_o), or (o, t_o, lse, mu) with ``return_stats``: lse is the
+    natural-log log-sum-exp per row and mu its tangent, both float32 [B,H,Nq].
+    """
+    lib = _abi.load()
+    _check_inputs([q, k, v, dq, dk, dv], ["q", "k", "v", "dq", "dk", "dv"])
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    for t, n in ((v, "v"), (dk, "dk"), (dv, "dv")):
+        if t.shape[2] != Nk:
+            raise ValueError(f"{n} must have {Nk} rows")
+    if dq.shape[2] != Nq:
+        raise ValueError("dq must match q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        o = torch.empty((B, H, Nq, D), dtype=q.dtype, device=q.device)
+        t_o = torch.empty_like(o)
+    else:
+        o, t_o = out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if return_stats else None
+    mu = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if return_stats else None
+    mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
+    ins = (_abi.Strides * 6)(*[_strides(t) for t in (q, k, v, dq, dk, dv)])
+    outs = (_abi.Strides * 2)(_strides(o), _strides(t_o))
+    shape = _abi.Shape(B, H, Nq, Nk, D)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = lib.jvp_attn_fwd_dual(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), ins, ctypes.byref(mask),
+                                   float(scale), _ptr(o), _ptr(t_o), outs, _ptr(lse), _ptr(mu),
+                                   ctypes.c_void_p(stream))
+    _abi.check(st)
+    if return_stats:
+        return o, t_o, lse, mu
+    return o, t_o
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+              attn_mask: Optional[torch.Tensor] = None, is_causal: bool = False,
+              scale: Optional[float] = None, return_lse: bool = False,
+              out: Optional[torch.Tensor] = None):
+    """Attention forward only (no tangents): o, or (o, lse) with ``return_lse``."""
+    lib = _abi.load()
+    _check_inputs([q, k, v], ["q", "k", "v"])
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if v.shape[2] != Nk:
+        raise ValueError("v must match k")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty((B, H, Nq, D), dtype=q.dtype, device=q.device) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if return_lse else None
+    mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
+    ins = (_abi.Strides * 3)(*[_strides(t) for t in (q, k, v)])
+    outs = (_abi.Strides * 1)(_strides(o))
+    shape = _abi.Shape(B, H, Nq, Nk, D)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = lib.jvp_attn_fwd(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), ins,
+                              ctypes.byref(mask), float(scale), _ptr(o), outs, _ptr(lse),
+                              ctypes.c_void_p(stream))
+    _abi.check(st)
+    return (o, lse) if return_lse else o
+
+
+def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise the stream and return (and clear) the library's device status."""
+    lib = _abi.load()
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    return int(lib.jvp_attn_get_device_status(ctypes.c_void_p(s)))
+
+
+def last_path() -> int:
+    """1 if the last forward call on this thread took the tensor-core path, 2 if CUDA-core."""
+    return int(_abi.load().jvp_attn_debug_last_path())

@@ -1,0 +1,621 @@
+// fwd_dual_tc.cuh -- tensor-core (tcgen05 + TMEM + TMA) kernel for attention
+// forward + JVP on sm_103a, fp16/bf16 inputs, fp32 accumulation.
+//
+// What it computes is the dual forward of softmax attention ("JVP Flash
+// Attention" project page, Description and Usage sections):
+//   S = s Q K^T + M,  P = softmax(S),  O = P V,
+//   dS = s (dQ K^T + Q dK^T),  mu = rowsum(P * dS),
+//   tO = (P * dS) V - mu O + P dV,  lse = log rowsum(exp S).
+// It never materialises P or dS in global memory: one pass over key tiles
+// keeps, per query row, a running maximum m, the row sum l = sum p~, the
+// running sum mu~ = sum p~ * dS, and two TMEM accumulators
+//   A = sum p~ V          T = sum p~ (dS V + dV)
+// (p~ = exp(S - m)), then O = A / l, mu = mu~ / l, tO = T / l - mu O.
+//
+// Work decomposition: one CTA per (128-row query tile, batch*head), six warps.
+//   warp 0      TMA producer: Q, dQ once; then per 64-key tile the [K;dK]
+//               block and the [V|dV] block, through an NS-deep ring.
+//   warp 1      TMEM allocator and single-thread MMA issuer.
+//   warps 2..5  softmax: one query row per thread (TMEM lane = row); the
+//               epilogue writes O, tO, lse and mu.
+// Per key tile t (buffer b = t % 2 of the double-buffered score region):
+//   M1  [S | Q dK^T] = Q [K ; dK]^T          (N = 128, SMEM x SMEM)
+//   M2  Q dK^T      += dQ K^T                 (N = 64)
+//   softmax: p~ and p~ * s * dS_raw, written back to TMEM as 16-bit values
+//            over the S / dS columns they came from
+//   M3  [A | T]     += P~ [V | dV]            (N = 2D, A operand from TMEM)
+//   M4  T           += (P~ * dS) V            (N = D)
+// The MMA warp issues M1/M2 of tile t+1 before M3/M4 of tile t, so the
+// tensor core computes the next scores while the softmax warps work.
+//
+// Rescaling is conditional: the row maximum used in the exponent is only
+// moved when a tile's maximum exceeds it by more than 2^8, so A, T, l and mu~
+// are rarely touched; the final ratios are exact for any stale maximum.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "jvp_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace jvp {
+
+template <typename T>
+struct ElemTraits;
+template <>
+struct ElemTraits<__half> {
+  static constexpr bool kBF16 = false;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+template <>
+struct ElemTraits<__nv_bfloat16> {
+  static constexpr bool kBF16 = true;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+
+template <int D, bool TANGENT>
+struct TcLayout {
+  static constexpr int BM = kTcBlockM;              // query rows per CTA
+  static constexpr int BN = kTcBlockN;              // keys per tile
+  static constexpr int KCH = D / 64;                // 128-byte chunks along D
+  static constexpr int NS = (D == 128) ? 2 : 4;     // pipeline depth
+  static constexpr int Q_BYTES = KCH * BM * 128;
+  static constexpr int KROWS = TANGENT ? 2 * BN : BN;  // rows of the [K;dK] block
+  static constexpr int KCHUNK_BYTES = KROWS * 128;     // one 64-column chunk of it
+  static constexpr int KDK_BYTES = KCH * KCHUNK_BYTES;
+  static constexpr int VCHUNK_BYTES = BN * 128;        // one 64-column chunk of V
+  static constexpr int VDV_BYTES = (TANGENT ? 2 : 1) * KCH * VCHUNK_BYTES;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DQ = OFF_Q + Q_BYTES;
+  static constexpr int OFF_KDK = OFF_DQ + (TANGENT ? Q_BYTES : 0);
+  static constexpr int OFF_VDV = OFF_KDK + NS * KDK_BYTES;
+  static constexpr int OFF_CTRL = OFF_VDV + NS * VDV_BYTES;
+  static constexpr int CTRL_BYTES = 512;
+  static constexpr int USED = OFF_CTRL + CTRL_BYTES;
+  // Padded so that only one CTA fits per SM (each CTA owns all 512 TMEM columns).
+  static constexpr int SMEM_BYTES = (USED + 1024 < 120 * 1024 ? 120 * 1024 : USED + 1024);
+  // TMEM columns
+  static constexpr uint32_t TM_A = 256;
+  static constexpr uint32_t TM_T = 256 + D;
+  static constexpr uint32_t TM_COLS = 512;
+  static_assert(D == 64 || D == 128, "tensor-core path handles D = 64 or 128");
+  static_assert(USED + 1024 <= 227 * 1024, "shared memory budget");
+};
+
+// Control block in shared memory.
+template <int NS>
+struct TcCtrl {
+  uint64_t q_full;
+  uint64_t kdk_full[NS], kdk_empty[NS];
+  uint64_t vdv_full[NS], vdv_empty[NS];
+  uint64_t s_full[2], p_full[2];
+  uint64_t at_done, o_full, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+__device__ __forceinline__ void record_timeout(unsigned int* status, volatile int* abort) {
+  *abort = 1;
+  atomicOr(status, 1u);
+}
+
+// Bounded wait taken by every lane of a warp, with a warp-uniform outcome, so
+// that the warp-collective TMEM instructions after it never run diverged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          volatile int* abort) {
+  const bool got = mbar_wait(bar, parity, abort);
+  if (!got) record_timeout(status, abort);
+  return __all_sync(0xffffffffu, got);
+}
+
+// Loads the 64 mask entries of one row for the key tile starting at j0.
+// Entries at or beyond Nk are not read.  Bool: 16 words of 4 bytes.
+template <int MASK>
+struct MaskRegs {};  // no per-row mask data for none / causal
+template <>
+struct MaskRegs<kMaskBool> {
+  uint32_t w[16] = {};
+  __device__ __forceinline__ void load(const FwdParams& p, const uint8_t* row, int j0) {
+    if (p.mask_vec && j0 + 64 <= p.Nk) {
+      const uint4* src = reinterpret_cast<const uint4*>(row + j0);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 x = __ldg(src + c);
+        w[4 * c] = x.x; w[4 * c + 1] = x.y; w[4 * c + 2] = x.z; w[4 * c + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = j0 + 4 * c + e;
+          const uint32_t byte = (j < p.Nk) ? row[static_cast<long long>(j) * p.msk] : 0u;
+          word |= (byte != 0 ? 1u : 0u) << (8 * e);
+        }
+        w[c] = word;
+      }
+    }
+  }
+  __device__ __forceinline__ bool keep(int jj) const {
+    return ((w[jj >> 2] >> (8 * (jj & 3))) & 0xFFu) != 0;
+  }
+};
+template <>
+struct MaskRegs<kMaskAdditive> {
+  float a[64] = {};
+  __device__ __forceinline__ void load(const FwdParams& p, const float* row, int j0) {
+    if (p.mask_vec && j0 + 64 <= p.Nk) {
+      const float4* src = reinterpret_cast<const float4*>(row + j0);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 x = __ldg(src + c);
+        a[4 * c] = x.x; a[4 * c + 1] = x.y; a[4 * c + 2] = x.z; a[4 * c + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < 64; ++jj) {
+        const int j = j0 + jj;
+        a[jj] = (j < p.Nk) ? row[static_cast<long long>(j) * p.msk] : 0.0f;
+      }
+    }
+  }
+};
+
+template <typename T, int D, int MASK, bool TANGENT>
+__global__ void __launch_bounds__(192, 1)
+    fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
+  using L = TcLayout<D, TANGENT>;
+  constexpr int NS = L::NS;
+  constexpr int BN = L::BN;
+  constexpr bool kBF16 = ElemTraits<T>::kBF16;
+  constexpr int KSTEPS_D = D / 16;   // MMA K-steps over the head dimension
+  constexpr int KSTEPS_N = BN / 16;  // MMA K-steps over a key tile
+  constexpr uint32_t IDESC_S = idesc_f16(kBF16, 128, TANGENT ? 2 * BN : BN, false);
+  constexpr uint32_t IDESC_DS = idesc_f16(kBF16, 128, BN, false);
+  constexpr uint32_t IDESC_AT = idesc_f16(kBF16, 128, TANGENT ? 2 * D : D, true);
+  constexpr uint32_t IDESC_T = idesc_f16(kBF16, 128, D, true);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle pattern.
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  TcCtrl<NS>* ctrl = reinterpret_cast<TcCtrl<NS>*>(smem + L::OFF_CTRL);
+  volatile int* abort = &ctrl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int bh = blockIdx.x % BH;
+  int qt = blockIdx.x / BH;
+  if (MASK == kMaskCausal) qt = p.num_q_tiles - 1 - qt;  // longest tiles first
+  const int b = bh / p.H, h = bh % p.H;
+  const int q0 = qt * L::BM;
+  int n_kv = (p.Nk + BN - 1) / BN;
+  if (MASK == kMaskCausal) {
+    const int last_row = min(q0 + L::BM, p.Nq) - 1;
+    n_kv = min(n_kv, last_row / BN + 1);
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&ctrl->kdk_full[s], 1);
+      mbar_init(&ctrl->kdk_empty[s], 1);
+      mbar_init(&ctrl->vdv_full[s], 1);
+      mbar_init(&ctrl->vdv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctrl->s_full[s], 1);
+      mbar_init(&ctrl->p_full[s], 128);
+    }
+    mbar_init(&ctrl->at_done, 1);
+    mbar_init(&ctrl->o_full, 1);
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, L::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      if (TANGENT) {
+        tma_prefetch_desc(&maps.dq);
+        tma_prefetch_desc(&maps.dk);
+        tma_prefetch_desc(&maps.dv);
+      }
+      mbar_arrive_expect_tx(&ctrl->q_full, (TANGENT ? 2 : 1) * L::Q_BYTES);
+      for (int c = 0; c < L::KCH; ++c) {
+        tma_load_4d(smem + L::OFF_Q + c * L::BM * 128, &maps.q, &ctrl->q_full, c * 64, q0, h, b);
+        if (TANGENT)
+          tma_load_4d(smem + L::OFF_DQ + c * L::BM * 128, &maps.dq, &ctrl->q_full, c * 64, q0, h,
+                      b);
+      }
+      int k_fills = 0, v_fills = 0;  // ring fills issued so far
+      for (int t = 0; t < n_kv; ++t) {
+        const int s = t % NS;
+        const uint32_t ph = (t / NS) & 1;
+        const int j0 = t * BN;
+        if (!mbar_wait(&ctrl->kdk_empty[s], ph ^ 1, abort)) {
+          record_timeout(p.status, abort);
+          break;
+        }
+        uint8_t* kdk = smem + L::OFF_KDK + s * L::KDK_BYTES;
+        mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_BYTES);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_4d(kdk + c * L::KCHUNK_BYTES, &maps.k, &ctrl->kdk_full[s], c * 64, j0, h, b);
+          if (TANGENT)
+            tma_load_4d(kdk + c * L::KCHUNK_BYTES + BN * 128, &maps.dk, &ctrl->kdk_full[s], c * 64,
+                        j0, h, b);
+        }
+        ++k_fills;
+        if (!mbar_wait(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
+          record_timeout(p.status, abort);
+          break;
+        }
+        uint8_t* vdv = smem + L::OFF_VDV + s * L::VDV_BYTES;
+        mbar_arrive_expect_tx(&ctrl->vdv_full[s], L::VDV_BYTES);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_4d(vdv + c * L::VCHUNK_BYTES, &maps.v, &ctrl->vdv_full[s], c * 64, j0, h, b);
+          if (TANGENT)
+            tma_load_4d(vdv + (L::KCH + c) * L::VCHUNK_BYTES, &maps.dv, &ctrl->vdv_full[s], c * 64,
+                        j0, h, b);
+        }
+        ++v_fills;
+      }
+      if (*abort) {
+        // Let every copy already issued land before the CTA can exit.
+        const int zero = 0;
+        mbar_wait(&ctrl->q_full, 0, &zero);
+        for (int t = max(0, k_fills - NS); t < k_fills; ++t)
+          mbar_wait(&ctrl->kdk_full[t % NS], (t / NS) & 1, &zero);
+        for (int t = max(0, v_fills - NS); t < v_fills; ++t)
+          mbar_wait(&ctrl->vdv_full[t % NS], (t / NS) & 1, &zero);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort);
+      if (!ok) record_timeout(p.status, abort);
+      tc_fence_after();
+      const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+      const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
+
+      auto issue_scores = [&](int t) -> bool {
+        const int s = t % NS;
+        if (!mbar_wait(&ctrl->kdk_full[s], (t / NS) & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + L::OFF_KDK + s * L::KDK_BYTES);
+        const uint32_t d_s = tmem + (t & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS_D; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
+          mma_ss(d_s, a, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        if (TANGENT) {
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS_D; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            const uint64_t a = sdesc_sw128(sdQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
+            mma_ss(d_s + BN, a, bd, IDESC_DS, 1u);
+          }
+        }
+        mma_commit(&ctrl->kdk_empty[s]);
+        mma_commit(&ctrl->s_full[t & 1]);
+        return true;
+      };
+
+      if (ok && n_kv > 0) ok = issue_scores(0);
+      for (int t = 0; ok && t < n_kv; ++t) {
+        if (t + 1 < n_kv && !issue_scores(t + 1)) {
+          ok = false;
+          break;
+        }
+        const int buf = t & 1;
+        if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const int s = t % NS;
+        if (!mbar_wait(&ctrl->vdv_full[s], (t / NS) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sV = smem_u32(smem + L::OFF_VDV + s * L::VDV_BYTES);
+        const uint32_t p_tm = tmem + buf * 128;        // P~ (16-bit pairs)
+        const uint32_t pd_tm = tmem + buf * 128 + BN;  // P~ * dS (16-bit pairs)
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS_N; ++kk) {
+          const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
+          mma_ts(tmem + L::TM_A, p_tm + kk * 8, bd, IDESC_AT, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (TANGENT) {
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS_N; ++kk) {
+            const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
+            mma_ts(tmem + L::TM_T, pd_tm + kk * 8, bd, IDESC_T, 1u);
+          }
+        }
+        mma_commit(&ctrl->vdv_empty[s]);
+        mma_commit(&ctrl->at_done);
+      }
+      if (ok) {
+        mma_commit(&ctrl->o_full);
+      } else {
+        record_timeout(p.status, abort);
+      }
+      // Drain: every MMA this thread issued completes before TMEM is freed.
+      mma_commit(&ctrl->drain);
+      const int zero = 0;
+      mbar_wait(&ctrl->drain, 0, &zero);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int sub = warp & 3;                 // TMEM sub-partition of this warp
+    const int r = sub * 32 + lane;            // row within the tile
+    const int i = q0 + r;                     // query row
+    const bool row_ok = i < p.Nq;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    const float c = p.scale_log2;
+    const float s_scale = p.scale;
+    float m_run = -INFINITY;  // running max, log2 units of the scaled logits
+    float l_run = 0.0f;       // sum of p~
+    float mu_run = 0.0f;      // sum of p~ * dS
+    bool ok = true;
+
+    const void* mrow = nullptr;
+    if (MASK == kMaskBool || MASK == kMaskAdditive) {
+      const long long off = static_cast<long long>(b) * p.msb + static_cast<long long>(h) * p.msh +
+                            static_cast<long long>(row_ok ? i : 0) * p.msq;
+      mrow = (MASK == kMaskBool)
+                 ? static_cast<const void*>(static_cast<const uint8_t*>(p.mask) + off)
+                 : static_cast<const void*>(static_cast<const float*>(p.mask) + off);
+    }
+
+    for (int t = 0; t < n_kv; ++t) {
+      const int buf = t & 1;
+      const int j0 = t * BN;
+      MaskRegs<MASK> mreg;
+      if constexpr (MASK == kMaskBool) {
+        if (row_ok) mreg.load(p, static_cast<const uint8_t*>(mrow), j0);
+      } else if constexpr (MASK == kMaskAdditive) {
+        if (row_ok) mreg.load(p, static_cast<const float*>(mrow), j0);
+      }
+      if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sa[32], sb[32];
+      tmem_ld32x2(lane_base + buf * 128, lane_base + buf * 128 + 32, sa, sb);
+      float x[64];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        x[jj] = __uint_as_float(sa[jj]);
+        x[jj + 32] = __uint_as_float(sb[jj]);
+      }
+      // Masking (raw-score domain unless additive, which is pre-scaled).
+      if constexpr (MASK == kMaskAdditive) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) x[jj] = fmaf(x[jj], c, mreg.a[jj] * kLog2e);
+      } else if constexpr (MASK == kMaskBool) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj)
+          if (!mreg.keep(jj)) x[jj] = -INFINITY;
+      }
+      if (j0 + BN > p.Nk) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj)
+          if (j0 + jj >= p.Nk) x[jj] = -INFINITY;
+      }
+      if (MASK == kMaskCausal && j0 + BN - 1 > q0) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj)
+          if (j0 + jj > i) x[jj] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int jj = 1; jj < 64; ++jj) mx = fmaxf(mx, x[jj]);
+      const float m_tile = (MASK == kMaskAdditive) ? mx : mx * c;
+      const bool need = m_tile > m_run + kRescaleThreshold;
+      const float m_new = need ? m_tile : m_run;
+      const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+      l_run *= alpha;
+      mu_run *= alpha;
+      if (t > 0 && __any_sync(0xffffffffu, need)) {
+        // A and T hold tile t-1's contributions once its MMAs are done.
+        if (!warp_wait(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int col = 0; col < (TANGENT ? 2 * D : D); col += 32) {
+          uint32_t acc[32];
+          tmem_ld32(lane_base + L::TM_A + col, acc);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = __float_as_uint(__uint_as_float(acc[e]) * alpha);
+          tmem_st32(lane_base + L::TM_A + col, acc);
+        }
+        tmem_st_wait();
+      }
+      m_run = m_new;
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+
+      uint32_t pk[32];
+      float2 lsum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      if (MASK == kMaskAdditive) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) x[jj] = ex2_approx(x[jj] - m_use);
+      } else {
+        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
+#pragma unroll
+        for (int jj = 0; jj < 64; jj += 2) {
+          const float2 arg = fma2(make_float2(x[jj], x[jj + 1]), c2, nm2);
+          x[jj] = ex2_approx(arg.x);
+          x[jj + 1] = ex2_approx(arg.y);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 64; jj += 2) {
+        lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], make_float2(x[jj], x[jj + 1]));
+        pk[jj >> 1] = ElemTraits<T>::pack(x[jj], x[jj + 1]);
+      }
+      l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
+               (lsum[3].x + lsum[3].y);
+      tmem_st32(lane_base + buf * 128, pk);
+      if (TANGENT) {
+        uint32_t da[32], db[32];
+        tmem_ld32x2(lane_base + buf * 128 + BN, lane_base + buf * 128 + BN + 32, da, db);
+        float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        const float2 s2 = make_float2(s_scale, s_scale);
+        uint32_t pdk[32];
+#pragma unroll
+        for (int jj = 0; jj < 64; jj += 2) {
+          const float2 ds = (jj < 32) ? make_float2(__uint_as_float(da[jj]), __uint_as_float(da[jj + 1]))
+                                      : make_float2(__uint_as_float(db[jj - 32]),
+                                                    __uint_as_float(db[jj - 31]));
+          const float2 pd = mul2(make_float2(x[jj], x[jj + 1]), mul2(ds, s2));
+          msum[(jj >> 1) & 3] = add2(msum[(jj >> 1) & 3], pd);
+          pdk[jj >> 1] = ElemTraits<T>::pack(pd.x, pd.y);
+        }
+        mu_run += (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
+                  (msum[3].x + msum[3].y);
+        tmem_st32(lane_base + buf * 128 + BN, pdk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctrl->p_full[buf]);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      const float mu_row = mu_run * inv_l;
+      T* orow = static_cast<T*>(p.o) + static_cast<long long>(b) * p.so.b +
+                static_cast<long long>(h) * p.so.h + static_cast<long long>(row_ok ? i : 0) * p.so.n;
+      T* trow = TANGENT ? static_cast<T*>(p.t_o) + static_cast<long long>(b) * p.sto.b +
+                              static_cast<long long>(h) * p.sto.h +
+                              static_cast<long long>(row_ok ? i : 0) * p.sto.n
+                        : nullptr;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t a[32], tt[32];
+        if (n_kv > 0) {
+          if (TANGENT) {
+            tmem_ld32x2(lane_base + L::TM_A + col, lane_base + L::TM_T + col, a, tt);
+          } else {
+            tmem_ld32(lane_base + L::TM_A + col, a);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = tt[e] = 0u;
+        }
+        uint32_t po[16], pt[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float o0 = __uint_as_float(a[e]) * inv_l, o1 = __uint_as_float(a[e + 1]) * inv_l;
+          po[e >> 1] = ElemTraits<T>::pack(o0, o1);
+          if (TANGENT) {
+            const float t0 = __uint_as_float(tt[e]) * inv_l - mu_row * o0;
+            const float t1 = __uint_as_float(tt[e + 1]) * inv_l - mu_row * o1;
+            pt[e >> 1] = ElemTraits<T>::pack(t0, t1);
+          }
+        }
+        if (row_ok) {
+          uint4* od = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
+          if (TANGENT) {
+            uint4* td = reinterpret_cast<uint4*>(trow + col);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              td[v4] = make_uint4(pt[4 * v4], pt[4 * v4 + 1], pt[4 * v4 + 2], pt[4 * v4 + 3]);
+          }
+        }
+      }
+      if (row_ok) {
+        const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
+        if (p.lse)
+          p.lse[ridx] = (l_run > 0.0f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TM_COLS);
+  }
+}
+
+template <typename T, int D, int MASK, bool TANGENT>
+cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream_t stream) {
+  using L = TcLayout<D, TANGENT>;
+  auto kern = fwd_dual_tc_kernel<T, D, MASK, TANGENT>;
+  // The attribute is per device; setting it is idempotent, the mask only saves calls.
+  static unsigned long long attr_done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_done & (1ull << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_done |= 1ull << dev;
+  }
+  const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H;
+  kern<<<static_cast<unsigned>(grid), 192, L::SMEM_BYTES, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_tc_dispatch(int mask_kind, bool tangent, const TcMaps& maps,
+                               const FwdParams& p, cudaStream_t stream) {
+#define JVP_TC_CASE(MK)                                                      \
+  case MK:                                                                   \
+    return tangent ? launch_tc_variant<T, D, MK, true>(maps, p, stream)      \
+                   : launch_tc_variant<T, D, MK, false>(maps, p, stream);
+  switch (mask_kind) {
+    JVP_TC_CASE(kMaskNone)
+    JVP_TC_CASE(kMaskBool)
+    JVP_TC_CASE(kMaskAdditive)
+    JVP_TC_CASE(kMaskCausal)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef JVP_TC_CASE
+}
+
+}  // namespace jvp

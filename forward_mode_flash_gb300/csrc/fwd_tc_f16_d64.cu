@@ -1,0 +1,9 @@
+// Tensor-core forward + JVP kernels for f16 inputs, head dimension 64.
+#include "fwd_dual_tc.cuh"
+
+namespace jvp {
+cudaError_t launch_fwd_tc_f16_d64(int mask_kind, bool tangent, const TcMaps& maps,
+                                  const FwdParams& p, cudaStream_t stream) {
+  return launch_tc_dispatch<__half, 64>(mask_kind, tangent, maps, p, stream);
+}
+}  // namespace jvp

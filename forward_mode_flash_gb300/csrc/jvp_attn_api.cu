@@ -1,0 +1,365 @@
+// jvp_attn_api.cu -- the C ABI declared in include/jvp_attn.h: argument
+// validation, path selection (tensor-core or CUDA-core kernel), TMA tensor-map
+// encoding and the device status word.  All compute runs in the kernels; this
+// file only checks, describes and enqueues.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "jvp_attn.h"
+#include "jvp_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace jvp {
+
+// Bit 0: some bounded device wait ran out.  One word per device (each device
+// that loads the library gets its own copy of this variable).
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local int t_last_path = 0;  // 0 none, 1 tensor-core, 2 CUDA-core
+
+jvp_status_t fail(jvp_status_t s, const std::string& msg) {
+  t_last_error = msg;
+  return s;
+}
+
+jvp_status_t ok() {
+  t_last_error.clear();
+  return JVP_OK;
+}
+
+size_t elem_size(int dt) { return dt == JVP_F32 ? 4 : 2; }
+
+struct DeviceInfo {
+  bool queried = false;
+  bool sm103 = false;
+  unsigned int* status = nullptr;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+// Looks up (once per device) whether the current device is an sm_103 part
+// and where its status word lives.
+jvp_status_t current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(JVP_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(JVP_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.queried) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess)
+      return fail(JVP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    d.sm103 = (major == 10 && minor == 3);
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_device_status);
+    if (e != cudaSuccess)
+      return fail(JVP_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    d.status = static_cast<unsigned int*>(addr);
+    d.queried = true;
+  }
+  *out = &d;
+  return JVP_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 4-D tiled map over a [B, H, N, D] tensor with a {64, rows} box and the
+// 128-byte swizzle the MMA descriptors expect.  Returns false if the layout
+// cannot be described (the caller then takes the CUDA-core path).
+bool encode_map(CUtensorMap* map, int dt, const void* ptr, int64_t B, int64_t H, int64_t N,
+                int64_t D, const jvp_strides_t& st, int rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int64_t e = static_cast<int64_t>(elem_size(dt));
+  // A size-1 dimension's stride is never used; give it a well-formed value.
+  int64_t sn = st.n, sh = st.h, sb = st.b;
+  if (N == 1) sn = D;
+  if (H == 1) sh = sn * N;
+  if (B == 1) sb = sh * H;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn * e), static_cast<cuuint64_t>(sh * e),
+                           static_cast<cuuint64_t>(sb * e)};
+  for (auto s : strides)
+    if (s == 0 || s % 16 != 0 || s >= (1ull << 40)) return false;
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty =
+      dt == JVP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, ty, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool strides_aligned16(const jvp_strides_t& s, size_t e) {
+  return (s.b * static_cast<int64_t>(e)) % 16 == 0 && (s.h * static_cast<int64_t>(e)) % 16 == 0 &&
+         (s.n * static_cast<int64_t>(e)) % 16 == 0;
+}
+
+Strides to_strides(const jvp_strides_t& s) { return Strides{s.b, s.h, s.n}; }
+
+// Shared body of jvp_attn_fwd_dual and jvp_attn_fwd.
+jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* const* in,
+                     const jvp_strides_t* in_strides, const jvp_mask_t* mask, float scale,
+                     void* const* out, const jvp_strides_t* out_strides, float* lse, float* mu,
+                     void* stream_ptr, bool tangent) {
+  t_last_path = 0;
+  const int n_in = tangent ? 6 : 3, n_out = tangent ? 2 : 1;
+  if (!shape) return fail(JVP_ERR_INVALID_ARG, "shape is NULL");
+  const int64_t B = shape->B, H = shape->H, Nq = shape->Nq, Nk = shape->Nk, D = shape->D;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return fail(JVP_ERR_INVALID_ARG, "negative size");
+  if (D <= 0) return fail(JVP_ERR_INVALID_ARG, "D must be positive");
+  if (D > 128) return fail(JVP_ERR_UNSUPPORTED, "D > 128 is not supported");
+  if (dtype != JVP_F32 && dtype != JVP_F16 && dtype != JVP_BF16)
+    return fail(JVP_ERR_INVALID_ARG, "unknown dtype");
+  if (!in_strides || !out_strides) return fail(JVP_ERR_INVALID_ARG, "strides are NULL");
+  if (!std::isfinite(scale)) return fail(JVP_ERR_INVALID_ARG, "scale is not finite");
+  const int64_t lim = (1ll << 31) - 1;
+  if (Nq > lim || Nk > lim || B * H > lim || ((Nq + 127) / 128) * B * H > lim ||
+      ((Nq + 7) / 8) * B * H > lim)
+    return fail(JVP_ERR_UNSUPPORTED, "problem too large for one launch");
+  for (int t = 0; t < n_in; ++t) {
+    const jvp_strides_t& s = in_strides[t];
+    if (s.d != 1) return fail(JVP_ERR_INVALID_ARG, "innermost (d) stride must be 1");
+    if (s.b < 0 || s.h < 0 || s.n < 0) return fail(JVP_ERR_INVALID_ARG, "negative stride");
+  }
+  for (int t = 0; t < n_out; ++t) {
+    const jvp_strides_t& s = out_strides[t];
+    if (s.d != 1) return fail(JVP_ERR_INVALID_ARG, "innermost (d) stride of an output must be 1");
+    if (s.b < 0 || s.h < 0 || s.n < 0) return fail(JVP_ERR_INVALID_ARG, "negative stride");
+  }
+  int kind = JVP_MASK_NONE;
+  const void* mptr = nullptr;
+  int64_t msb = 0, msh = 0, msq = 0, msk = 0;
+  if (mask) {
+    kind = mask->kind;
+    mptr = mask->ptr;
+    msb = mask->stride_b, msh = mask->stride_h, msq = mask->stride_q, msk = mask->stride_k;
+    if (kind < JVP_MASK_NONE || kind > JVP_MASK_CAUSAL)
+      return fail(JVP_ERR_INVALID_ARG, "unknown mask kind");
+    if (kind == JVP_MASK_CAUSAL && mptr)
+      return fail(JVP_ERR_INVALID_ARG, "a causal mask cannot be combined with a mask tensor");
+    if (kind == JVP_MASK_NONE && mptr)
+      return fail(JVP_ERR_INVALID_ARG, "mask kind NONE with a mask tensor");
+    if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && B * H * Nq * Nk > 0)
+      return fail(JVP_ERR_INVALID_ARG, "mask tensor is NULL");
+    if (msb < 0 || msh < 0 || msq < 0 || msk < 0) return fail(JVP_ERR_INVALID_ARG, "negative mask stride");
+    if (kind == JVP_MASK_ADDITIVE && !aligned(mptr, 4))
+      return fail(JVP_ERR_ALIGNMENT, "additive mask is not 4-byte aligned");
+  }
+  const size_t e = elem_size(dtype);
+  const bool rows_exist = B * H * Nq > 0;
+  if (!rows_exist) {
+    t_last_path = 0;
+    return ok();  // nothing to compute
+  }
+  for (int t = 0; t < n_in; ++t) {
+    const bool is_q = (t == 0 || t == 3);
+    if (!in[t] && (is_q || Nk > 0)) return fail(JVP_ERR_INVALID_ARG, "input pointer is NULL");
+    if (!aligned(in[t], e)) return fail(JVP_ERR_ALIGNMENT, "input not aligned to its element size");
+  }
+  for (int t = 0; t < n_out; ++t) {
+    if (!out[t]) return fail(JVP_ERR_INVALID_ARG, "output pointer is NULL");
+    if (!aligned(out[t], e)) return fail(JVP_ERR_ALIGNMENT, "output not aligned to its element size");
+  }
+  if (!aligned(lse, 4) || !aligned(mu, 4)) return fail(JVP_ERR_ALIGNMENT, "lse/mu not 4-byte aligned");
+
+  DeviceInfo* dev = nullptr;
+  jvp_status_t s = current_device(&dev);
+  if (s != JVP_OK) return s;
+  if (!dev->sm103)
+    return fail(JVP_ERR_UNSUPPORTED, "the current device is not an sm_103 (GB300-class) GPU");
+
+  FwdParams p{};
+  p.B = static_cast<int>(B);
+  p.H = static_cast<int>(H);
+  p.Nq = static_cast<int>(Nq);
+  p.Nk = static_cast<int>(Nk);
+  p.D = static_cast<int>(D);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask = mptr;
+  p.msb = msb, p.msh = msh, p.msq = msq, p.msk = msk;
+  const size_t me = (kind == JVP_MASK_ADDITIVE) ? 4 : 1;
+  p.mask_vec = (mptr && msk == 1 && aligned(mptr, 16) && (msq * me) % 16 == 0 &&
+                (msh * me) % 16 == 0 && (msb * me) % 16 == 0)
+                   ? 1
+                   : 0;
+  p.q = in[0], p.k = in[1], p.v = in[2];
+  p.sq = to_strides(in_strides[0]), p.sk = to_strides(in_strides[1]), p.sv = to_strides(in_strides[2]);
+  if (tangent) {
+    p.dq = in[3], p.dk = in[4], p.dv = in[5];
+    p.sdq = to_strides(in_strides[3]), p.sdk = to_strides(in_strides[4]),
+    p.sdv = to_strides(in_strides[5]);
+    p.t_o = out[1];
+    p.sto = to_strides(out_strides[1]);
+  }
+  p.o = out[0];
+  p.so = to_strides(out_strides[0]);
+  p.lse = lse;
+  p.mu = tangent ? mu : nullptr;
+  p.status = dev->status;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  // Tensor-core path: fp16/bf16, D in {64, 128}, positive scale, at least one
+  // key, and every tensor 16-byte aligned with 16-byte-multiple strides.
+  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) && (D == 64 || D == 128) && scale > 0.f &&
+            Nk > 0;
+  for (int t = 0; tc && t < n_in; ++t)
+    tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
+  for (int t = 0; tc && t < n_out; ++t)
+    tc = aligned(out[t], 16) && strides_aligned16(out_strides[t], e);
+  TcMaps maps;
+  if (tc) {
+    const int64_t Ns[6] = {Nq, Nk, Nk, Nq, Nk, Nk};
+    CUtensorMap* dst[6] = {&maps.q, &maps.k, &maps.v, &maps.dq, &maps.dk, &maps.dv};
+    for (int t = 0; tc && t < n_in; ++t)
+      tc = encode_map(dst[t], dtype, in[t], B, H, Ns[t], D, in_strides[t],
+                      (t == 0 || t == 3) ? kTcBlockM : kTcBlockN);
+    if (tc && !tangent) {
+      maps.dq = maps.q, maps.dk = maps.k, maps.dv = maps.v;
+    }
+  }
+  cudaError_t err;
+  if (tc) {
+    p.num_q_tiles = static_cast<int>((Nq + kTcBlockM - 1) / kTcBlockM);
+    err = launch_fwd_tc(static_cast<DType>(dtype), static_cast<int>(D), kind, tangent, maps, p,
+                        stream);
+    t_last_path = 1;
+  } else {
+    p.num_q_tiles = static_cast<int>((Nq + 7) / 8);
+    err = launch_fwd_simt(static_cast<DType>(dtype), kind, tangent, p, stream);
+    t_last_path = 2;
+  }
+  if (err != cudaSuccess)
+    return fail(JVP_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(err));
+  return ok();
+}
+
+__global__ void wait_timeout_selftest_kernel(long long limit, unsigned int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_barrier_init();
+  // Nothing ever arrives on `bar`: the bounded wait must give up.
+  if (!mbar_wait(&bar, 0, &abort_flag, limit)) atomicOr(status, 1u);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(DType dt, int D, int mask_kind, bool tangent, const TcMaps& maps,
+                          const FwdParams& p, cudaStream_t stream) {
+  if (dt == kF16 && D == 64) return launch_fwd_tc_f16_d64(mask_kind, tangent, maps, p, stream);
+  if (dt == kF16 && D == 128) return launch_fwd_tc_f16_d128(mask_kind, tangent, maps, p, stream);
+  if (dt == kBF16 && D == 64) return launch_fwd_tc_bf16_d64(mask_kind, tangent, maps, p, stream);
+  if (dt == kBF16 && D == 128) return launch_fwd_tc_bf16_d128(mask_kind, tangent, maps, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace jvp
+
+extern "C" {
+
+jvp_status_t jvp_attn_fwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                               const void* k, const void* v, const void* dq, const void* dk,
+                               const void* dv, const jvp_strides_t* in_strides,
+                               const jvp_mask_t* mask, float scale, void* o, void* t_o,
+                               const jvp_strides_t* out_strides, float* lse, float* mu,
+                               void* stream) {
+  const void* in[6] = {q, k, v, dq, dk, dv};
+  void* out[2] = {o, t_o};
+  return jvp::forward(shape, dtype, in, in_strides, mask, scale, out, out_strides, lse, mu, stream,
+                      true);
+}
+
+jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                          const void* k, const void* v, const jvp_strides_t* in_strides,
+                          const jvp_mask_t* mask, float scale, void* o,
+                          const jvp_strides_t* out_strides, float* lse, void* stream) {
+  const void* in[3] = {q, k, v};
+  void* out[1] = {o};
+  return jvp::forward(shape, dtype, in, in_strides, mask, scale, out, out_strides, lse, nullptr,
+                      stream, false);
+}
+
+jvp_status_t jvp_attn_get_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return jvp::fail(JVP_ERR_CUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e));
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, jvp::g_device_status, sizeof(word));
+  if (e != cudaSuccess)
+    return jvp::fail(JVP_ERR_CUDA, std::string("reading the status word: ") + cudaGetErrorString(e));
+  if (word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(jvp::g_device_status, &zero, sizeof(zero));
+    if (e != cudaSuccess)
+      return jvp::fail(JVP_ERR_CUDA, std::string("clearing the status word: ") + cudaGetErrorString(e));
+    return jvp::fail(JVP_ERR_DEVICE_TIMEOUT, "a device-side wait ran out of time");
+  }
+  return jvp::ok();
+}
+
+const char* jvp_attn_status_string(jvp_status_t status) {
+  switch (status) {
+    case JVP_OK: return "ok";
+    case JVP_ERR_INVALID_ARG: return "invalid argument";
+    case JVP_ERR_UNSUPPORTED: return "unsupported";
+    case JVP_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case JVP_ERR_CUDA: return "CUDA error";
+    case JVP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case JVP_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* jvp_attn_last_error(void) { return jvp::t_last_error.c_str(); }
+
+int jvp_attn_version(void) { return 100; }
+
+int jvp_attn_debug_last_path(void) { return jvp::t_last_path; }
+
+jvp_status_t jvp_attn_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles >= (1ll << 31))
+    return jvp::fail(JVP_ERR_INVALID_ARG, "limit_cycles must be in [1, 2^31)");
+  jvp::DeviceInfo* dev = nullptr;
+  jvp_status_t s = jvp::current_device(&dev);
+  if (s != JVP_OK) return s;
+  if (!dev->sm103) return jvp::fail(JVP_ERR_UNSUPPORTED, "the current device is not sm_103");
+  jvp::wait_timeout_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<long long>(limit_cycles), dev->status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return jvp::fail(JVP_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
+  return jvp::ok();
+}
+
+}  // extern "C"

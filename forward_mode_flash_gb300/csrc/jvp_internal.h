@@ -1,0 +1,71 @@
+// jvp_internal.h -- launch descriptions shared by the host entry points and
+// the kernel translation units (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace jvp {
+
+enum DType { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum MaskKind { kMaskNone = 0, kMaskBool = 1, kMaskAdditive = 2, kMaskCausal = 3 };
+
+struct Strides {
+  long long b, h, n;  // element strides; d stride is 1
+};
+
+// Everything a forward kernel needs besides the tensor maps.
+struct FwdParams {
+  int B, H, Nq, Nk, D;
+  int num_q_tiles;
+  float scale;       // logit scale s
+  float scale_log2;  // s * log2(e)
+  const void* mask;  // uint8 (bool) or float (additive); nullptr otherwise
+  long long msb, msh, msq, msk;  // mask element strides
+  int mask_vec;      // 1: rows are 16-byte aligned and stride_k == 1 (vector loads)
+  // inputs (used by the CUDA-core kernel; the tensor-core kernel reads them by TMA)
+  const void *q, *k, *v, *dq, *dk, *dv;
+  Strides sq, sk, sv, sdq, sdk, sdv;
+  // outputs
+  void* o;
+  void* t_o;
+  Strides so, sto;
+  float* lse;
+  float* mu;
+  unsigned int* status;  // device status word (timeouts)
+};
+
+// Tensor maps of the tensor-core kernel: q, k, v, dq, dk, dv (tangent maps
+// are unused by the primal-only variant).
+struct TcMaps {
+  CUtensorMap q, k, v, dq, dk, dv;
+};
+
+// Tensor-core kernels (fp16/bf16, D in {64, 128}).  Return a cudaError_t.
+cudaError_t launch_fwd_tc(DType dt, int D, int mask_kind, bool tangent, const TcMaps& maps,
+                          const FwdParams& p, cudaStream_t stream);
+// Static shared-memory footprint and block size of a tensor-core variant.
+int tc_block_threads();
+constexpr int kTcBlockM = 128;
+constexpr int kTcBlockN = 64;
+
+// CUDA-core kernel (any dtype, D <= 128).
+cudaError_t launch_fwd_simt(DType dt, int mask_kind, bool tangent, const FwdParams& p,
+                            cudaStream_t stream);
+
+// Per-variant entry points of the tensor-core kernel, one translation unit per
+// (dtype, D) so that the build compiles them in parallel.
+cudaError_t launch_fwd_tc_f16_d64(int mask_kind, bool tangent, const TcMaps& maps,
+                                  const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_tc_f16_d128(int mask_kind, bool tangent, const TcMaps& maps,
+                                   const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_tc_bf16_d64(int mask_kind, bool tangent, const TcMaps& maps,
+                                   const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_tc_bf16_d128(int mask_kind, bool tangent, const TcMaps& maps,
+                                    const FwdParams& p, cudaStream_t stream);
+
+// Device status word owned by the library (bit 0: a bounded wait timed out).
+unsigned int* device_status_ptr();
+
+}  // namespace jvp

@@ -1,0 +1,163 @@
+/*
+ * jvp_attn.h -- C ABI of the GB300 attention forward + JVP library.
+ *
+ * The operation (the "JVP Flash Attention" project page, Description and Usage
+ * sections): a drop-in for scaled_dot_product_attention(q, k, v, attn_mask)
+ * whose dual forward `fwd_dual(q, k, v)`, used inside torch.func.jvp, returns
+ * the attention output together with its forward-mode tangent.  Per (b, h):
+ *
+ *   S   = scale * Q K^T + M                 M: mask (see jvp_mask_t)
+ *   P   = softmax over the kept keys of each row of S
+ *   O   = P V
+ *   dS  = scale * (dQ K^T + Q dK^T)         (M carries no tangent)
+ *   mu  = rowsum(P * dS)                    (the tangent of the log-sum-exp)
+ *   tO  = (P * dS) V - mu * O + P dV        (the directional derivative of O)
+ *   lse = log sum_j exp(S_ij)               (natural log)
+ *
+ * A row that keeps no key yields O = tO = 0, lse = -inf and mu = 0.
+ *
+ * Conventions for every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *     allocates no device memory and keeps no pointer after the call returns.
+ *   - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t
+ *     passed as void*, NULL = the legacy default stream) and the call returns
+ *     without synchronising.  Inputs must stay valid and unmodified, and outputs
+ *     must not be read, until the stream reaches the work.
+ *   - Tensors are [B, H, N, D] with element strides (jvp_strides_t); the
+ *     innermost stride (d) must be 1.  Outputs must not overlap inputs.
+ *   - Errors are reported by the returned status, never by abort or exception.
+ *     Arguments are validated before anything is enqueued; on an error nothing
+ *     is enqueued.  jvp_attn_last_error() gives a one-line reason (per thread).
+ *   - A device-side wait that exceeds its time limit (about two seconds) makes
+ *     the kernel return early and records JVP_ERR_DEVICE_TIMEOUT, which
+ *     jvp_attn_get_device_status() reports.
+ */
+#ifndef JVP_ATTN_H_
+#define JVP_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  JVP_OK = 0,
+  JVP_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad stride, bad mask */
+  JVP_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. D > 128, no sm_103 device) */
+  JVP_ERR_ALIGNMENT = 3,      /* pointer or stride not aligned to the element size */
+  JVP_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, attribute, ...) */
+  JVP_ERR_DEVICE_TIMEOUT = 5, /* a device-side wait ran out (reported asynchronously) */
+  JVP_ERR_WORKSPACE = 6       /* workspace missing or too small */
+} jvp_status_t;
+
+typedef enum { JVP_F32 = 0, JVP_F16 = 1, JVP_BF16 = 2 } jvp_dtype_t;
+
+/* Mask kinds.  BOOL: uint8 elements, nonzero = the key takes part (SDPA's
+ * boolean attn_mask).  ADDITIVE: float32 elements added to the scaled logits;
+ * an entry of -inf excludes the key.  CAUSAL: key j takes part in row i iff
+ * j <= i (top-left aligned); it uses no mask tensor, so a causal mask combined
+ * with a mask tensor is rejected (JVP_ERR_INVALID_ARG). */
+typedef enum {
+  JVP_MASK_NONE = 0,
+  JVP_MASK_BOOL = 1,
+  JVP_MASK_ADDITIVE = 2,
+  JVP_MASK_CAUSAL = 3
+} jvp_mask_kind_t;
+
+typedef struct {
+  int64_t B, H; /* batch, heads */
+  int64_t Nq;   /* query rows */
+  int64_t Nk;   /* key / value rows */
+  int64_t D;    /* head dimension, 1..128 */
+} jvp_shape_t;
+
+/* Element strides of a [B, H, N, D] tensor; d must be 1. */
+typedef struct {
+  int64_t b, h, n, d;
+} jvp_strides_t;
+
+/* Mask of logical shape [B|1, H|1, Nq, Nk]; stride 0 broadcasts a dimension
+ * (e.g. stride_h = 0 for a mask shared by all heads).  `ptr` is NULL for
+ * JVP_MASK_NONE and JVP_MASK_CAUSAL. */
+typedef struct {
+  int32_t kind; /* jvp_mask_kind_t */
+  const void* ptr;
+  int64_t stride_b, stride_h, stride_q, stride_k;
+} jvp_mask_t;
+
+/*
+ * Fused attention forward + JVP (the project page's `JVPAttn.fwd_dual`).
+ *
+ *   shape          sizes; B*H*Nq == 0 or Nk == 0 is valid (nothing to compute
+ *                  beyond writing the empty-row convention when Nk == 0).
+ *   dtype          element type shared by q, k, v, dq, dk, dv, o and t_o.
+ *   q, dq          [B,H,Nq,D];  k, v, dk, dv [B,H,Nk,D]  (device, read only).
+ *   in_strides     6 stride records, in the order q, k, v, dq, dk, dv.
+ *   mask           NULL or a mask description (see jvp_mask_t).
+ *   scale          logit scale (SDPA's default is 1/sqrt(D)); must be finite.
+ *   o, t_o         [B,H,Nq,D] outputs (device, written).
+ *   out_strides    2 stride records, for o and t_o.
+ *   lse, mu        NULL or [B,H,Nq] contiguous float32 outputs (device).
+ *   stream         cudaStream_t as void*.
+ *
+ * fp16/bf16 inputs with D in {64, 128}, 16-byte aligned base pointers and
+ * strides take the tensor-core path (TMA + tcgen05 + TMEM, fp32 accumulation);
+ * every other valid case (float32, other D) takes the CUDA-core path, which
+ * computes in fp32 FFMA.
+ */
+jvp_status_t jvp_attn_fwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                               const void* k, const void* v, const void* dq, const void* dk,
+                               const void* dv, const jvp_strides_t* in_strides,
+                               const jvp_mask_t* mask, float scale, void* o, void* t_o,
+                               const jvp_strides_t* out_strides, float* lse, float* mu,
+                               void* stream);
+
+/*
+ * Attention forward without tangents (the project page's `jvp_attention` /
+ * `attention`, Usage section): O = softmax(scale Q K^T + M) V and lse.
+ * Arguments as for jvp_attn_fwd_dual; in_strides holds 3 records (q, k, v)
+ * and out_strides 1 record (o).
+ */
+jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                          const void* k, const void* v, const jvp_strides_t* in_strides,
+                          const jvp_mask_t* mask, float scale, void* o,
+                          const jvp_strides_t* out_strides, float* lse, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side status word:
+ * JVP_ERR_DEVICE_TIMEOUT if any kernel of this library gave up on a wait since
+ * the last call, JVP_ERR_CUDA if the stream reports an error, else JVP_OK.
+ */
+jvp_status_t jvp_attn_get_device_status(void* stream);
+
+/* Static string for a status code. */
+const char* jvp_attn_status_string(jvp_status_t status);
+
+/* One-line description of the last error returned on the calling thread. */
+const char* jvp_attn_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int jvp_attn_version(void);
+
+/*
+ * Diagnostic: enqueues a one-thread kernel that waits on a device barrier
+ * that nothing completes, with a wait limit of `limit_cycles` SM clock cycles,
+ * so that the bounded-wait path runs out and records JVP_ERR_DEVICE_TIMEOUT
+ * without faulting or hanging the GPU.  limit_cycles must be in [1, 2^31).
+ */
+jvp_status_t jvp_attn_selftest_wait_timeout(int64_t limit_cycles, void* stream);
+
+/*
+ * Diagnostic: which kernel family the last successful forward call on the
+ * calling thread enqueued: 1 = tensor-core path, 2 = CUDA-core path,
+ * 0 = nothing was enqueued (empty problem or an error).
+ */
+int jvp_attn_debug_last_path(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JVP_ATTN_H_ */

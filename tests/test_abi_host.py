@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load without a device, export every function that
+``include/jvp_attn.h`` declares, and reject bad arguments with the documented
+status before it touches the device.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from forward_mode_flash_gb300 import _abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _abi.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "jvp_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(jvp_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert header_functions() == sorted(_abi.EXPORTS)
+
+
+def test_library_loads_and_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.jvp_attn_version() == 100
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.jvp_attn_status_string(code)
+    assert lib.jvp_attn_status_string(0) == b"ok"
+
+
+def _strides(n, shape):
+    B, H, N, D = shape
+    arr = (_abi.Strides * n)()
+    for i in range(n):
+        arr[i] = _abi.Strides(H * N * D, N * D, D, 1)
+    return arr
+
+
+def call_fwd_dual(lib, shape=(1, 2, 64, 64), dtype=_abi.JVP_BF16, ptrs=0x1000, mask=None,
+                  scale=0.125, in_strides=None, out_strides=None):
+    B, H, N, D = shape
+    sh = _abi.Shape(B, H, N, N, D)
+    p = ctypes.c_void_p(ptrs) if ptrs else None
+    ins = in_strides if in_strides is not None else _strides(6, shape)
+    outs = out_strides if out_strides is not None else _strides(2, shape)
+    m = ctypes.byref(mask) if mask is not None else None
+    return lib.jvp_attn_fwd_dual(ctypes.byref(sh), dtype, p, p, p, p, p, p, ins, m, scale, p, p,
+                                 outs, None, None, None)
+
+
+def test_validation_rejects_bad_arguments_without_a_device(lib):
+    assert lib.jvp_attn_fwd_dual(None, 2, None, None, None, None, None, None, None, None, 1.0,
+                                 None, None, None, None, None, None) == _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, shape=(1, 1, 8, 0)) == _abi.JVP_ERR_INVALID_ARG       # D = 0
+    assert call_fwd_dual(lib, shape=(1, 1, 8, 256)) == _abi.JVP_ERR_UNSUPPORTED     # D > 128
+    assert call_fwd_dual(lib, shape=(-1, 1, 8, 64)) == _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, dtype=7) == _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, scale=float("nan")) == _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, scale=float("inf")) == _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, ptrs=0) == _abi.JVP_ERR_INVALID_ARG                   # null inputs
+    assert call_fwd_dual(lib, ptrs=0x1001) == _abi.JVP_ERR_ALIGNMENT                # odd address
+    bad = _strides(6, (1, 2, 64, 64))
+    bad[2] = _abi.Strides(8192, 4096, 64, 2)
+    assert call_fwd_dual(lib, in_strides=bad) == _abi.JVP_ERR_INVALID_ARG           # d stride != 1
+    causal_with_tensor = _abi.Mask(_abi.JVP_MASK_CAUSAL, 0x2000, 0, 0, 64, 1)
+    assert call_fwd_dual(lib, mask=causal_with_tensor) == _abi.JVP_ERR_INVALID_ARG
+    bool_without_tensor = _abi.Mask(_abi.JVP_MASK_BOOL, None, 0, 0, 64, 1)
+    assert call_fwd_dual(lib, mask=bool_without_tensor) == _abi.JVP_ERR_INVALID_ARG
+    unknown = _abi.Mask(9, None, 0, 0, 0, 0)
+    assert call_fwd_dual(lib, mask=unknown) == _abi.JVP_ERR_INVALID_ARG
+    assert b"causal" in lib.jvp_attn_last_error() or lib.jvp_attn_last_error()
+
+
+def test_empty_problems_succeed_without_a_device(lib):
+    assert call_fwd_dual(lib, shape=(0, 2, 64, 64), ptrs=0) == _abi.JVP_OK
+    assert call_fwd_dual(lib, shape=(1, 0, 64, 64), ptrs=0) == _abi.JVP_OK
+    assert call_fwd_dual(lib, shape=(1, 2, 0, 64), ptrs=0) == _abi.JVP_OK
+    assert lib.jvp_attn_debug_last_path() == 0
+
+
+def test_selftest_rejects_bad_limits(lib):
+    assert lib.jvp_attn_selftest_wait_timeout(0, None) == _abi.JVP_ERR_INVALID_ARG
+    assert lib.jvp_attn_selftest_wait_timeout(1 << 31, None) == _abi.JVP_ERR_INVALID_ARG

@@ -1,0 +1,262 @@
+"""GPU parity: the CUDA path against the float64 oracle on the same inputs.
+
+Tolerances (max-abs on O and tO, unit-variance inputs): 1e-4 for float32
+inputs, 2e-2 for fp16/bf16 inputs.  lse is checked too (1e-5 / 1e-3).
+Boolean and causal masking must be exact in which keys contribute: perturbing
+an excluded key's K, V, dK or dV leaves every output bit-identical.
+
+The oracle runs on the dtype-rounded inputs upcast to float64, so the only
+differences are the GPU's own rounding (fp32 accumulation, 16-bit P and
+P*dS operands, 16-bit outputs).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from forward_mode_flash_gb300 import attention as A
+from forward_mode_flash_gb300 import build, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "f16": 2e-2, "bf16": 2e-2}
+LSE_TOL = {"f32": 1e-5, "f16": 1e-3, "bf16": 1e-3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def np64(t):
+    return None if t is None else t.detach().to("cpu", torch.float64).numpy()
+
+
+def mask_for_oracle(w, inp):
+    if w.mask == "bool":
+        return "bool", inp.mask.numpy()
+    if w.mask == "additive":
+        return "additive", inp.mask.double().numpy()
+    return w.mask, None
+
+
+def run_gpu(w, inp, scale=None):
+    dev = "cuda"
+    g = [x.to(dev) for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    m = inp.mask.to(dev) if inp.mask is not None else None
+    o, t_o, lse, mu = A.fwd_dual(*g, attn_mask=m, is_causal=(w.mask == "causal"), scale=scale,
+                                 return_stats=True)
+    torch.cuda.synchronize()
+    return o, t_o, lse, mu, A.last_path()
+
+
+def compare_full(w, scale=None, expect_path=None):
+    inp = synth.make_inputs(w)
+    o, t_o, lse, mu, path = run_gpu(w, inp, scale)
+    if expect_path is not None:
+        assert path == expect_path, f"expected path {expect_path}, got {path}"
+    kind, m = mask_for_oracle(w, inp)
+    ro, rt, rl, rm = oracle.fwd_dual(np64(inp.q), np64(inp.k), np64(inp.v), np64(inp.dq),
+                                     np64(inp.dk), np64(inp.dv), kind, m, scale=scale)
+    eo = np.abs(np64(o) - ro).max()
+    et = np.abs(np64(t_o) - rt).max()
+    fin = np.isfinite(rl)
+    el = np.abs(np64(lse)[fin] - rl[fin]).max() if fin.any() else 0.0
+    assert np.array_equal(np.isfinite(np64(lse)), fin)
+    tol = TOL[w.dtype]
+    assert eo <= tol and et <= tol, (w.name, eo, et)
+    assert el <= LSE_TOL[w.dtype], (w.name, el)
+    assert np.abs(np64(mu) - rm).max() <= 20 * tol, w.name
+    return eo, et
+
+
+# ------------------------------------------------------------------ small shapes
+SMALL_N = [1, 17, 63, 64, 65, 127, 128, 129, 200, 333]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("N", SMALL_N)
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_tensor_core_path_small(dtype, D, N, mask):
+    w = synth.small(dtype, 2, 3, N, D, mask, seed=N + D)
+    compare_full(w, expect_path=1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("N", [17, 64, 130, 257])
+@pytest.mark.parametrize("mask", ["bool", "additive"])
+def test_tensor_core_path_masks(dtype, D, N, mask):
+    w = synth.small(dtype, 2, 2, N, D, mask, seed=7 * N + D)
+    compare_full(w, expect_path=1)
+
+
+@pytest.mark.parametrize("D", [1, 16, 33, 64, 100, 128])
+@pytest.mark.parametrize("mask", ["none", "bool", "additive", "causal"])
+def test_cuda_core_path_f32(D, mask):
+    w = synth.small("f32", 2, 2, 45, D, mask, seed=D)
+    compare_full(w, expect_path=2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [16, 32, 80])
+def test_cuda_core_path_half_other_head_dims(dtype, D):
+    w = synth.small(dtype, 1, 2, 70, D, "causal", seed=D)
+    compare_full(w, expect_path=2)
+
+
+def test_nondefault_scale():
+    compare_full(synth.small("bf16", 1, 2, 150, 64, "none", seed=3), scale=0.05, expect_path=1)
+    compare_full(synth.small("f32", 1, 2, 40, 16, "none", seed=3), scale=0.9, expect_path=2)
+
+
+def test_fully_masked_rows_follow_the_convention():
+    w = synth.small("bf16", 1, 2, 96, 64, "bool", seed=11)
+    inp = synth.make_inputs(w)
+    inp.mask[:, :, 5, :] = False
+    inp.mask[:, :, 70, :] = False
+    o, t_o, lse, mu, _ = run_gpu(w, inp)
+    assert torch.all(o[:, :, 5] == 0) and torch.all(t_o[:, :, 70] == 0)
+    assert torch.all(lse[:, :, 5] == -math.inf) and torch.all(mu[:, :, 70] == 0)
+
+
+# ------------------------------------------------------------------ exactness
+def test_boolean_masking_is_exact_in_which_keys_contribute():
+    w = synth.small("bf16", 1, 2, 200, 128, "bool", seed=21)
+    inp = synth.make_inputs(w)
+    inp.mask[..., 37] = False
+    inp.mask[..., 150] = False
+    base = run_gpu(w, inp)
+    for t in (inp.k, inp.v, inp.dk, inp.dv):
+        t[:, :, 37] += 3.0
+        t[:, :, 150] -= 5.0
+    pert = run_gpu(w, inp)
+    for a, b in zip(base[:4], pert[:4]):
+        assert torch.equal(a, b)
+
+
+def test_causal_masking_is_exact_in_which_keys_contribute():
+    w = synth.small("f16", 1, 2, 256, 64, "causal", seed=22)
+    inp = synth.make_inputs(w)
+    base = run_gpu(w, inp)
+    for t in (inp.k, inp.v, inp.dk, inp.dv):
+        t[:, :, 200:] += 2.0
+    pert = run_gpu(w, inp)
+    for a, b in zip(base[:2], pert[:2]):
+        assert torch.equal(a[:, :, :200], b[:, :, :200])
+    assert torch.equal(base[2][:, :, :200], pert[2][:, :, :200])
+
+
+def test_keys_beyond_the_sequence_are_never_read():
+    # K/V views over a longer buffer: data past Nk must not influence anything.
+    w = synth.small("bf16", 1, 2, 100, 64, "none", seed=23)
+    inp = synth.make_inputs(w)
+    dev = "cuda"
+    big = [torch.randn(1, 2, 192, 64, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    for bt, t in zip(big, (inp.k, inp.v, inp.dk, inp.dv)):
+        bt[:, :, :100] = t.to(dev)
+    q, dq = inp.q.to(dev), inp.dq.to(dev)
+    views = [bt[:, :, :100] for bt in big]
+    r1 = A.fwd_dual(q, views[0], views[1], dq, views[2], views[3], return_stats=True)
+    for bt in big:
+        bt[:, :, 100:] = 1e4
+    r2 = A.fwd_dual(q, views[0], views[1], dq, views[2], views[3], return_stats=True)
+    torch.cuda.synchronize()
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
+
+
+def test_zero_tangents_give_exactly_zero_and_dv_only_matches_forward_of_dv():
+    w = synth.small("bf16", 2, 2, 300, 128, "none", seed=24)
+    inp = synth.make_inputs(w)
+    dev = "cuda"
+    q, k, v, dv = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.dv))
+    z = torch.zeros_like(q)
+    o, t_o, lse, mu = A.fwd_dual(q, k, v, z, z, torch.zeros_like(v), return_stats=True)
+    assert torch.all(t_o == 0) and torch.all(mu == 0)
+    o2, t_o2 = A.fwd_dual(q, k, v, z, z, dv)
+    o_dv = A.attention(q, k, dv)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+    assert (t_o2.float() - o_dv.float()).abs().max().item() <= 1e-2
+
+
+def test_forward_only_entry_point_matches_oracle():
+    for dt, D, mask in (("bf16", 128, "causal"), ("f16", 64, "additive"), ("f32", 16, "bool")):
+        w = synth.small(dt, 2, 2, 130, D, mask, seed=25)
+        inp = synth.make_inputs(w)
+        dev = "cuda"
+        m = inp.mask.to(dev) if inp.mask is not None else None
+        o, lse = A.attention(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), attn_mask=m,
+                             is_causal=(mask == "causal"), return_lse=True)
+        torch.cuda.synchronize()
+        kind, mm = mask_for_oracle(w, inp)
+        ro, _, rl, _ = oracle.fwd_dual(np64(inp.q), np64(inp.k), np64(inp.v), mask_kind=kind,
+                                       mask=mm)
+        assert np.abs(np64(o) - ro).max() <= TOL[dt]
+        assert np.abs(np64(lse) - rl).max() <= LSE_TOL[dt]
+
+
+def test_strided_inputs_from_a_bnhd_layout():
+    # q/k/v as [B, N, H, D] buffers viewed as [B, H, N, D] (non-contiguous heads).
+    w = synth.small("bf16", 2, 4, 140, 64, "none", seed=26)
+    inp = synth.make_inputs(w)
+    dev = "cuda"
+    g = [x.to(dev).transpose(1, 2).contiguous().transpose(1, 2)
+         for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    o, t_o = A.fwd_dual(*g)
+    torch.cuda.synchronize()
+    assert A.last_path() == 1
+    ro, rt, _, _ = oracle.fwd_dual(*(np64(x) for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk,
+                                                        inp.dv)))
+    assert np.abs(np64(o) - ro).max() <= 2e-2 and np.abs(np64(t_o) - rt).max() <= 2e-2
+
+
+# ------------------------------------------------------------------ specified workloads
+def test_workload_f32_b1h2n32d16_full():
+    compare_full(synth.WORKLOADS["f32_b1h2n32d16"], expect_path=2)
+
+
+def sampled_rows(w, inp, o, t_o, lse, n_rows, seed=0):
+    rng = np.random.default_rng(seed)
+    total = w.B * w.H * w.N
+    rows = np.unique(np.concatenate([rng.integers(0, total, n_rows),
+                                     [0, w.N - 1, total - 1, total - w.N]]))
+    kind, m = mask_for_oracle(w, inp)
+    ro, rt, rl, _ = oracle.fwd_dual_rows(np64(inp.q), np64(inp.k), np64(inp.v), np64(inp.dq),
+                                         np64(inp.dk), np64(inp.dv), rows, kind, m)
+    D = w.D
+    go = np64(o).reshape(-1, D)[rows]
+    gt = np64(t_o).reshape(-1, D)[rows]
+    gl = np64(lse).reshape(-1)[rows]
+    return np.abs(go - ro).max(), np.abs(gt - rt).max(), np.abs(gl - rl).max()
+
+
+@pytest.mark.parametrize("name", ["f16_b2h8n512d64", "f16_b2h8n512d64_causal",
+                                  "bf16_b2h8n1024d64_bool", "bf16_b2h8n1024d64_additive",
+                                  "bf16_b4h16n2048d128", "bf16_b4h16n2048d128_causal",
+                                  "f16_b2h8n2048d64_causal"])
+def test_specified_workloads_on_sampled_rows(name):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    o, t_o, lse, mu, path = run_gpu(w, inp)
+    assert path == 1
+    eo, et, el = sampled_rows(w, inp, o, t_o, lse, 96)
+    assert eo <= TOL[w.dtype] and et <= TOL[w.dtype], (name, eo, et)
+    assert el <= LSE_TOL[w.dtype], (name, el)
+    # properties at full size: finite outputs, |O| bounded by max |V| per head
+    assert torch.isfinite(o).all() and torch.isfinite(t_o).all()
+    vmax = inp.v.float().abs().amax(dim=(2, 3)).to(o.device)
+    assert (o.float().abs().amax(dim=(2, 3)) <= vmax * 1.01 + 1e-3).all()
+
+
+def test_device_timeout_is_reported_and_the_context_survives():
+    st = A._abi.load().jvp_attn_selftest_wait_timeout(200000, None)
+    assert st == 0
+    assert A.device_status(torch.cuda.default_stream()) == A._abi.JVP_ERR_DEVICE_TIMEOUT
+    assert A.device_status(torch.cuda.default_stream()) == 0
+    compare_full(synth.small("bf16", 1, 1, 64, 64, "none", seed=1), expect_path=1)
