@@ -207,7 +207,7 @@ def main():
     import torch
     import torch.distributed as dist
 
-    from forward_mode_flash_gb300 import attention, build, metrics, synth
+    from forward_mode_flash_gb300 import api, build, metrics, synth
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
@@ -228,12 +228,12 @@ def main():
     out = (torch.empty_like(g[0]), torch.empty_like(g[0]))
 
     def step():
-        return attention.fwd_dual(*g, attn_mask=mask, is_causal=causal, out=out)
+        return api.fwd_dual(*g, attn_mask=mask, is_causal=causal, out=out)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    if attention.last_path() != 1:
+    if api.last_path() != 1:
         raise SystemExit("the tensor-core path did not run for the benchmark workload")
     if world > 1:
         dist.barrier()
@@ -278,7 +278,7 @@ def main():
                 d.copy_(hsrc, non_blocking=True)
             if dev_mask is not None:
                 dev_mask.copy_(host_mask, non_blocking=True)
-            o, t_o = attention.fwd_dual(*dev_in, attn_mask=dev_mask, is_causal=causal, out=out)
+            o, t_o = api.fwd_dual(*dev_in, attn_mask=dev_mask, is_causal=causal, out=out)
             host_out[0].copy_(o, non_blocking=True)
             host_out[1].copy_(t_o, non_blocking=True)
 

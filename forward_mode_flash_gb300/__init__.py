@@ -7,6 +7,6 @@ this package holds the ctypes binding (``attention``), work/traffic counts
 does, and raises if it has not been built.
 """
 
-from .attention import attention, device_status, fwd_dual, last_path  # noqa: F401
+from .api import attention, device_status, fwd_dual, last_path  # noqa: F401
 
 __all__ = ["attention", "fwd_dual", "device_status", "last_path"]

@@ -31,6 +31,13 @@
 // Rescaling is conditional: the row maximum used in the exponent is only
 // moved when a tile's maximum exceeds it by more than 2^8, so A, T, l and mu~
 // are rarely touched; the final ratios are exact for any stale maximum.
+//
+// Consistent rounding: the tensor core consumes P~ and P~ * dS rounded to 16
+// bits, so l and mu~ are summed from those same rounded values.  O and tO are
+// then the exact attention output and JVP of a softmax whose weights are
+// perturbed by one 16-bit rounding each, and the rounding errors enter tO
+// multiplied by (V_j - O) rather than V_j (tO = T/l - mu O cancels).  A
+// separate fp32 sum of the unrounded p~ gives the log-sum-exp.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -50,6 +57,9 @@ struct ElemTraits<__half> {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+  static __device__ __forceinline__ float2 unpack(uint32_t x) {
+    return __half22float2(*reinterpret_cast<__half2*>(&x));
+  }
 };
 template <>
 struct ElemTraits<__nv_bfloat16> {
@@ -57,6 +67,9 @@ struct ElemTraits<__nv_bfloat16> {
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t x) {
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
   }
 };
 
@@ -386,8 +399,9 @@ __global__ void __launch_bounds__(192, 1)
     const float c = p.scale_log2;
     const float s_scale = p.scale;
     float m_run = -INFINITY;  // running max, log2 units of the scaled logits
-    float l_run = 0.0f;       // sum of p~
-    float mu_run = 0.0f;      // sum of p~ * dS
+    float l_run = 0.0f;       // sum of p~ as rounded for the MMA
+    float lx_run = 0.0f;      // sum of p~ in fp32 (for the log-sum-exp)
+    float mu_run = 0.0f;      // sum of p~ * dS as rounded for the MMA
     bool ok = true;
 
     const void* mrow = nullptr;
@@ -448,6 +462,7 @@ __global__ void __launch_bounds__(192, 1)
       const float m_new = need ? m_tile : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
       l_run *= alpha;
+      lx_run *= alpha;
       mu_run *= alpha;
       if (t > 0 && __any_sync(0xffffffffu, need)) {
         // A and T hold tile t-1's contributions once its MMAs are done.
@@ -471,6 +486,7 @@ __global__ void __launch_bounds__(192, 1)
 
       uint32_t pk[32];
       float2 lsum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      float2 xsum[2] = {{0.f, 0.f}, {0.f, 0.f}};
       if (MASK == kMaskAdditive) {
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj) x[jj] = ex2_approx(x[jj] - m_use);
@@ -485,11 +501,13 @@ __global__ void __launch_bounds__(192, 1)
       }
 #pragma unroll
       for (int jj = 0; jj < 64; jj += 2) {
-        lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], make_float2(x[jj], x[jj + 1]));
         pk[jj >> 1] = ElemTraits<T>::pack(x[jj], x[jj + 1]);
+        lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], ElemTraits<T>::unpack(pk[jj >> 1]));
+        xsum[(jj >> 1) & 1] = add2(xsum[(jj >> 1) & 1], make_float2(x[jj], x[jj + 1]));
       }
       l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
                (lsum[3].x + lsum[3].y);
+      lx_run += (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
       tmem_st32(lane_base + buf * 128, pk);
       if (TANGENT) {
         uint32_t da[32], db[32];
@@ -503,8 +521,8 @@ __global__ void __launch_bounds__(192, 1)
                                       : make_float2(__uint_as_float(db[jj - 32]),
                                                     __uint_as_float(db[jj - 31]));
           const float2 pd = mul2(make_float2(x[jj], x[jj + 1]), mul2(ds, s2));
-          msum[(jj >> 1) & 3] = add2(msum[(jj >> 1) & 3], pd);
           pdk[jj >> 1] = ElemTraits<T>::pack(pd.x, pd.y);
+          msum[(jj >> 1) & 3] = add2(msum[(jj >> 1) & 3], ElemTraits<T>::unpack(pdk[jj >> 1]));
         }
         mu_run += (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
                   (msum[3].x + msum[3].y);
@@ -567,7 +585,7 @@ __global__ void __launch_bounds__(192, 1)
       if (row_ok) {
         const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
         if (p.lse)
-          p.lse[ridx] = (l_run > 0.0f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+          p.lse[ridx] = (lx_run > 0.0f) ? (m_run + log2f(lx_run)) * kLn2 : -INFINITY;
         if (TANGENT && p.mu) p.mu[ridx] = mu_row;
       }
     }

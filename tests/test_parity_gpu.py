@@ -10,14 +10,16 @@ differences are the GPU's own rounding (fp32 accumulation, 16-bit P and
 P*dS operands, 16-bit outputs).
 """
 
+import json
 import math
+import os
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from forward_mode_flash_gb300 import attention as A
+from forward_mode_flash_gb300 import api as A
 from forward_mode_flash_gb300 import build, synth
 
 pytestmark = pytest.mark.gpu
@@ -53,6 +55,14 @@ def run_gpu(w, inp, scale=None):
     return o, t_o, lse, mu, A.last_path()
 
 
+def log_error(name, **errs):
+    """Append the measured errors to $JVP_PARITY_LOG (one JSON object per line)."""
+    path = os.environ.get("JVP_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": name, **{k: float(v) for k, v in errs.items()}}) + "\n")
+
+
 def compare_full(w, scale=None, expect_path=None):
     inp = synth.make_inputs(w)
     o, t_o, lse, mu, path = run_gpu(w, inp, scale)
@@ -67,6 +77,7 @@ def compare_full(w, scale=None, expect_path=None):
     el = np.abs(np64(lse)[fin] - rl[fin]).max() if fin.any() else 0.0
     assert np.array_equal(np.isfinite(np64(lse)), fin)
     tol = TOL[w.dtype]
+    log_error(w.name, o=eo, t_o=et, lse=el)
     assert eo <= tol and et <= tol, (w.name, eo, et)
     assert el <= LSE_TOL[w.dtype], (w.name, el)
     assert np.abs(np64(mu) - rm).max() <= 20 * tol, w.name
@@ -246,6 +257,7 @@ def test_specified_workloads_on_sampled_rows(name):
     o, t_o, lse, mu, path = run_gpu(w, inp)
     assert path == 1
     eo, et, el = sampled_rows(w, inp, o, t_o, lse, 96)
+    log_error(name + "[sampled rows]", o=eo, t_o=et, lse=el)
     assert eo <= TOL[w.dtype] and et <= TOL[w.dtype], (name, eo, et)
     assert el <= LSE_TOL[w.dtype], (name, el)
     # properties at full size: finite outputs, |O| bounded by max |V| per head
