@@ -12,12 +12,14 @@
 //   A = sum p~ V          T = sum p~ (dS V + dV)
 // (p~ = exp(S - m)), then O = A / l, mu = mu~ / l, tO = T / l - mu O.
 //
-// Work decomposition: one CTA per (128-row query tile, batch*head), six warps.
+// Work decomposition: one CTA per (128-row query tile, batch*head), ten warps.
 //   warp 0      TMA producer: Q, dQ once; then per 64-key tile the [K;dK]
 //               block and the [V|dV] block, through an NS-deep ring.
 //   warp 1      TMEM allocator and single-thread MMA issuer.
-//   warps 2..5  softmax: one query row per thread (TMEM lane = row); the
-//               epilogue writes O, tO, lse and mu.
+//   warps 2..9  softmax, two warpgroups: a thread owns one query row (its TMEM
+//               lane) and one half (32 keys) of every key tile; the two halves
+//               exchange their maxima through shared memory each tile.  The
+//               epilogue splits the output columns the same way.
 // Per key tile t (buffer b = t % 2 of the double-buffered score region):
 //   M1  [S | Q dK^T] = Q [K ; dK]^T          (N = 128, SMEM x SMEM)
 //   M2  Q dK^T      += dQ K^T                 (N = 64)
@@ -90,7 +92,7 @@ struct TcLayout {
   static constexpr int OFF_KDK = OFF_DQ + (TANGENT ? Q_BYTES : 0);
   static constexpr int OFF_VDV = OFF_KDK + NS * KDK_BYTES;
   static constexpr int OFF_CTRL = OFF_VDV + NS * VDV_BYTES;
-  static constexpr int CTRL_BYTES = 512;
+  static constexpr int CTRL_BYTES = 8192;
   static constexpr int USED = OFF_CTRL + CTRL_BYTES;
   // Padded so that only one CTA fits per SM (each CTA owns all 512 TMEM columns).
   static constexpr int SMEM_BYTES = (USED + 1024 < 120 * 1024 ? 120 * 1024 : USED + 1024);
@@ -102,16 +104,21 @@ struct TcLayout {
   static_assert(USED + 1024 <= 227 * 1024, "shared memory budget");
 };
 
+constexpr int kSoftmaxThreads = 256;           // two warpgroups
+constexpr int kTcThreads = 64 + kSoftmaxThreads;  // + producer warp + MMA warp
+
 // Control block in shared memory.
 template <int NS>
 struct TcCtrl {
   uint64_t q_full;
   uint64_t kdk_full[NS], kdk_empty[NS];
   uint64_t vdv_full[NS], vdv_empty[NS];
-  uint64_t s_full[2], p_full[2];
-  uint64_t at_done, o_full, drain;
+  uint64_t s_full[2], p_full[2], max_ready[2];
+  uint64_t at_done, o_full, drain, sums_ready;
   uint32_t tmem_base;
   int abort;
+  float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
+  float xsum[2][3][kTcBlockM];     // [warpgroup][l, lx, mu][row] final half sums
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -132,24 +139,27 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
   return __all_sync(0xffffffffu, got);
 }
 
-// Loads the 64 mask entries of one row for the key tile starting at j0.
-// Entries at or beyond Nk are not read.  Bool: 16 words of 4 bytes.
-template <int MASK>
-struct MaskRegs {};  // no per-row mask data for none / causal
-template <>
-struct MaskRegs<kMaskBool> {
-  uint32_t w[16] = {};
-  __device__ __forceinline__ void load(const FwdParams& p, const uint8_t* row, int j0) {
-    if (p.mask_vec && j0 + 64 <= p.Nk) {
+// Loads the mask entries of one row for the KN keys starting at j0; entries at
+// or beyond Nk are not read.  Bool masks pack 4 bytes per word.
+template <int MASK, int KN>
+struct MaskRegs {  // no per-row mask data for none / causal
+  __device__ __forceinline__ void load(const FwdParams&, const void*, int) {}
+};
+template <int KN>
+struct MaskRegs<kMaskBool, KN> {
+  uint32_t w[KN / 4] = {};
+  __device__ __forceinline__ void load(const FwdParams& p, const void* rowp, int j0) {
+    const uint8_t* row = static_cast<const uint8_t*>(rowp);
+    if (p.mask_vec && j0 + KN <= p.Nk) {
       const uint4* src = reinterpret_cast<const uint4*>(row + j0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < KN / 16; ++c) {
         const uint4 x = __ldg(src + c);
         w[4 * c] = x.x; w[4 * c + 1] = x.y; w[4 * c + 2] = x.z; w[4 * c + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < KN / 4; ++c) {
         uint32_t word = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -165,20 +175,21 @@ struct MaskRegs<kMaskBool> {
     return ((w[jj >> 2] >> (8 * (jj & 3))) & 0xFFu) != 0;
   }
 };
-template <>
-struct MaskRegs<kMaskAdditive> {
-  float a[64] = {};
-  __device__ __forceinline__ void load(const FwdParams& p, const float* row, int j0) {
-    if (p.mask_vec && j0 + 64 <= p.Nk) {
+template <int KN>
+struct MaskRegs<kMaskAdditive, KN> {
+  float a[KN] = {};
+  __device__ __forceinline__ void load(const FwdParams& p, const void* rowp, int j0) {
+    const float* row = static_cast<const float*>(rowp);
+    if (p.mask_vec && j0 + KN <= p.Nk) {
       const float4* src = reinterpret_cast<const float4*>(row + j0);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < KN / 4; ++c) {
         const float4 x = __ldg(src + c);
         a[4 * c] = x.x; a[4 * c + 1] = x.y; a[4 * c + 2] = x.z; a[4 * c + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int jj = 0; jj < 64; ++jj) {
+      for (int jj = 0; jj < KN; ++jj) {
         const int j = j0 + jj;
         a[jj] = (j < p.Nk) ? row[static_cast<long long>(j) * p.msk] : 0.0f;
       }
@@ -186,33 +197,59 @@ struct MaskRegs<kMaskAdditive> {
   }
 };
 
+// Maximum of n values by a pairwise tree (log2 n dependent steps).
+template <int N>
+__device__ __forceinline__ float tree_max(const float (&x)[N]) {
+  float y[N / 2];
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) y[k] = fmaxf(x[k], x[k + N / 2]);
+#pragma unroll
+  for (int w = N / 4; w >= 1; w /= 2) {
+#pragma unroll
+    for (int k = 0; k < w; ++k) y[k] = fmaxf(y[k], y[k + w]);
+  }
+  return y[0];
+}
+
 template <typename T, int D, int MASK, bool TANGENT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
   using L = TcLayout<D, TANGENT>;
   constexpr int NS = L::NS;
   constexpr int BN = L::BN;
+  constexpr int HN = BN / 2;  // key columns per softmax warpgroup
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSTEPS_D = D / 16;   // MMA K-steps over the head dimension
   constexpr int KSTEPS_N = BN / 16;  // MMA K-steps over a key tile
+  constexpr int ACC_COLS = TANGENT ? 2 * D : D;  // TMEM columns of [A | T]
   constexpr uint32_t IDESC_S = idesc_f16(kBF16, 128, TANGENT ? 2 * BN : BN, false);
   constexpr uint32_t IDESC_DS = idesc_f16(kBF16, 128, BN, false);
-  constexpr uint32_t IDESC_AT = idesc_f16(kBF16, 128, TANGENT ? 2 * D : D, true);
+  constexpr uint32_t IDESC_AT = idesc_f16(kBF16, 128, ACC_COLS, true);
   constexpr uint32_t IDESC_T = idesc_f16(kBF16, 128, D, true);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle pattern.
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  static_assert(sizeof(TcCtrl<NS>) <= L::CTRL_BYTES, "control block budget");
   TcCtrl<NS>* ctrl = reinterpret_cast<TcCtrl<NS>*>(smem + L::OFF_CTRL);
   volatile int* abort = &ctrl->abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+
+  // Work item: heads are taken in groups sized to about one wave of CTAs,
+  // with the query tiles of a group innermost, so that the K/V of the heads in
+  // flight stay in L2.  Causal problems take their longest tiles first.
   const int BH = p.B * p.H;
-  const int bh = blockIdx.x % BH;
-  int qt = blockIdx.x / BH;
-  if (MASK == kMaskCausal) qt = p.num_q_tiles - 1 - qt;  // longest tiles first
+  const int nq = p.num_q_tiles;
+  const int G = p.group_heads;
+  const int g = blockIdx.x / (G * nq);
+  const int rem = blockIdx.x - g * G * nq;
+  const int Gg = min(G, BH - g * G);
+  const int q_rank = rem / Gg;
+  const int bh = g * G + rem % Gg;
+  const int qt = (MASK == kMaskCausal) ? nq - 1 - q_rank : q_rank;
   const int b = bh / p.H, h = bh % p.H;
   const int q0 = qt * L::BM;
   int n_kv = (p.Nk + BN - 1) / BN;
@@ -231,11 +268,13 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
-      mbar_init(&ctrl->p_full[s], 128);
+      mbar_init(&ctrl->p_full[s], kSoftmaxThreads);
+      mbar_init(&ctrl->max_ready[s], kSoftmaxThreads);
     }
     mbar_init(&ctrl->at_done, 1);
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
+    mbar_init(&ctrl->sums_ready, kSoftmaxThreads);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -391,17 +430,22 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int sub = warp & 3;                 // TMEM sub-partition of this warp
-    const int r = sub * 32 + lane;            // row within the tile
-    const int i = q0 + r;                     // query row
+    // Two warpgroups; warpgroup wg owns key columns [wg*HN, wg*HN + HN) of
+    // every tile and, in the epilogue, output columns [wg*D/2, wg*D/2 + D/2).
+    // Thread (warp, lane) owns query row r = 32 * (warp % 4) + lane (its TMEM lane).
+    const int wg = (warp - 2) >> 2;
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;
+    const int i = q0 + r;
     const bool row_ok = i < p.Nq;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    const int cofs = wg * HN;
     const float c = p.scale_log2;
     const float s_scale = p.scale;
-    float m_run = -INFINITY;  // running max, log2 units of the scaled logits
-    float l_run = 0.0f;       // sum of p~ as rounded for the MMA
-    float lx_run = 0.0f;      // sum of p~ in fp32 (for the log-sum-exp)
-    float mu_run = 0.0f;      // sum of p~ * dS as rounded for the MMA
+    float m_run = -INFINITY;  // running max, log2 units of the scaled logits (whole row)
+    float l_run = 0.0f;       // this half's sum of p~ as rounded for the MMA
+    float lx_run = 0.0f;      // this half's sum of p~ in fp32 (for the log-sum-exp)
+    float mu_run = 0.0f;      // this half's sum of p~ * dS as rounded for the MMA
     bool ok = true;
 
     const void* mrow = nullptr;
@@ -415,49 +459,52 @@ __global__ void __launch_bounds__(192, 1)
 
     for (int t = 0; t < n_kv; ++t) {
       const int buf = t & 1;
-      const int j0 = t * BN;
-      MaskRegs<MASK> mreg;
-      if constexpr (MASK == kMaskBool) {
-        if (row_ok) mreg.load(p, static_cast<const uint8_t*>(mrow), j0);
-      } else if constexpr (MASK == kMaskAdditive) {
-        if (row_ok) mreg.load(p, static_cast<const float*>(mrow), j0);
-      }
+      const int j0 = t * BN + cofs;  // first key of this half tile
+      MaskRegs<MASK, HN> mreg;
+      if (row_ok) mreg.load(p, mrow, j0);
       if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sa[32], sb[32];
-      tmem_ld32x2(lane_base + buf * 128, lane_base + buf * 128 + 32, sa, sb);
-      float x[64];
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        x[jj] = __uint_as_float(sa[jj]);
-        x[jj + 32] = __uint_as_float(sb[jj]);
+      uint32_t sa[32], da[32];
+      if (TANGENT) {
+        tmem_ld32x2(lane_base + buf * 128 + cofs, lane_base + buf * 128 + BN + cofs, sa, da);
+      } else {
+        tmem_ld32(lane_base + buf * 128 + cofs, sa);
       }
+      float x[HN];
+#pragma unroll
+      for (int jj = 0; jj < HN; ++jj) x[jj] = __uint_as_float(sa[jj]);
       // Masking (raw-score domain unless additive, which is pre-scaled).
       if constexpr (MASK == kMaskAdditive) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) x[jj] = fmaf(x[jj], c, mreg.a[jj] * kLog2e);
+        for (int jj = 0; jj < HN; ++jj) x[jj] = fmaf(x[jj], c, mreg.a[jj] * kLog2e);
       } else if constexpr (MASK == kMaskBool) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj)
+        for (int jj = 0; jj < HN; ++jj)
           if (!mreg.keep(jj)) x[jj] = -INFINITY;
       }
-      if (j0 + BN > p.Nk) {
+      if (j0 + HN > p.Nk) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj)
+        for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj >= p.Nk) x[jj] = -INFINITY;
       }
-      if (MASK == kMaskCausal && j0 + BN - 1 > q0) {
+      if (MASK == kMaskCausal && j0 + HN - 1 > q0) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj)
+        for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj > i) x[jj] = -INFINITY;
       }
-      float mx = x[0];
-#pragma unroll
-      for (int jj = 1; jj < 64; ++jj) mx = fmaxf(mx, x[jj]);
-      const float m_tile = (MASK == kMaskAdditive) ? mx : mx * c;
+      const float mx = tree_max(x);
+      const float m_half = (MASK == kMaskAdditive) ? mx : mx * c;
+      // Exchange the half-row maxima between the two warpgroups.
+      ctrl->xmax[buf][wg][r] = m_half;
+      mbar_arrive(&ctrl->max_ready[buf]);
+      if (!warp_wait(&ctrl->max_ready[buf], (t >> 1) & 1, p.status, abort)) {
+        ok = false;
+        break;
+      }
+      const float m_tile = fmaxf(m_half, ctrl->xmax[buf][wg ^ 1][r]);
       const bool need = m_tile > m_run + kRescaleThreshold;
       const float m_new = need ? m_tile : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
@@ -465,14 +512,15 @@ __global__ void __launch_bounds__(192, 1)
       lx_run *= alpha;
       mu_run *= alpha;
       if (t > 0 && __any_sync(0xffffffffu, need)) {
-        // A and T hold tile t-1's contributions once its MMAs are done.
+        // A and T hold tile t-1's contributions once its MMAs are done; each
+        // warpgroup rescales half of the [A | T] columns of its rows.
         if (!warp_wait(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int col = 0; col < (TANGENT ? 2 * D : D); col += 32) {
+        for (int col = wg * (ACC_COLS / 2); col < (wg + 1) * (ACC_COLS / 2); col += 32) {
           uint32_t acc[32];
           tmem_ld32(lane_base + L::TM_A + col, acc);
 #pragma unroll
@@ -484,23 +532,23 @@ __global__ void __launch_bounds__(192, 1)
       m_run = m_new;
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
 
-      uint32_t pk[32];
-      float2 lsum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-      float2 xsum[2] = {{0.f, 0.f}, {0.f, 0.f}};
       if (MASK == kMaskAdditive) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) x[jj] = ex2_approx(x[jj] - m_use);
+        for (int jj = 0; jj < HN; ++jj) x[jj] = ex2_approx(x[jj] - m_use);
       } else {
         const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
-        for (int jj = 0; jj < 64; jj += 2) {
+        for (int jj = 0; jj < HN; jj += 2) {
           const float2 arg = fma2(make_float2(x[jj], x[jj + 1]), c2, nm2);
           x[jj] = ex2_approx(arg.x);
           x[jj + 1] = ex2_approx(arg.y);
         }
       }
+      uint32_t pk[HN / 2];
+      float2 lsum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      float2 xsum[2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-      for (int jj = 0; jj < 64; jj += 2) {
+      for (int jj = 0; jj < HN; jj += 2) {
         pk[jj >> 1] = ElemTraits<T>::pack(x[jj], x[jj + 1]);
         lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], ElemTraits<T>::unpack(pk[jj >> 1]));
         xsum[(jj >> 1) & 1] = add2(xsum[(jj >> 1) & 1], make_float2(x[jj], x[jj + 1]));
@@ -508,25 +556,21 @@ __global__ void __launch_bounds__(192, 1)
       l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
                (lsum[3].x + lsum[3].y);
       lx_run += (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
-      tmem_st32(lane_base + buf * 128, pk);
+      tmem_st16(lane_base + buf * 128 + wg * (HN / 2), pk);
       if (TANGENT) {
-        uint32_t da[32], db[32];
-        tmem_ld32x2(lane_base + buf * 128 + BN, lane_base + buf * 128 + BN + 32, da, db);
         float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         const float2 s2 = make_float2(s_scale, s_scale);
-        uint32_t pdk[32];
+        uint32_t pdk[HN / 2];
 #pragma unroll
-        for (int jj = 0; jj < 64; jj += 2) {
-          const float2 ds = (jj < 32) ? make_float2(__uint_as_float(da[jj]), __uint_as_float(da[jj + 1]))
-                                      : make_float2(__uint_as_float(db[jj - 32]),
-                                                    __uint_as_float(db[jj - 31]));
+        for (int jj = 0; jj < HN; jj += 2) {
+          const float2 ds = make_float2(__uint_as_float(da[jj]), __uint_as_float(da[jj + 1]));
           const float2 pd = mul2(make_float2(x[jj], x[jj + 1]), mul2(ds, s2));
           pdk[jj >> 1] = ElemTraits<T>::pack(pd.x, pd.y);
           msum[(jj >> 1) & 3] = add2(msum[(jj >> 1) & 3], ElemTraits<T>::unpack(pdk[jj >> 1]));
         }
         mu_run += (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
                   (msum[3].x + msum[3].y);
-        tmem_st32(lane_base + buf * 128 + BN, pdk);
+        tmem_st16(lane_base + buf * 128 + BN + wg * (HN / 2), pdk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -534,11 +578,22 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     // ------------------------------------------------------------ epilogue
+    // Combine the two halves' sums (both warpgroups hold the same m_run).
+    if (ok) {
+      ctrl->xsum[wg][0][r] = l_run;
+      ctrl->xsum[wg][1][r] = lx_run;
+      ctrl->xsum[wg][2][r] = mu_run;
+      mbar_arrive(&ctrl->sums_ready);
+      ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
+    }
     if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
     if (ok) {
       tc_fence_after();
-      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-      const float mu_row = mu_run * inv_l;
+      const float l_all = l_run + ctrl->xsum[wg ^ 1][0][r];
+      const float lx_all = lx_run + ctrl->xsum[wg ^ 1][1][r];
+      const float mu_all = mu_run + ctrl->xsum[wg ^ 1][2][r];
+      const float inv_l = (l_all > 0.0f) ? 1.0f / l_all : 0.0f;
+      const float mu_row = mu_all * inv_l;
       T* orow = static_cast<T*>(p.o) + static_cast<long long>(b) * p.so.b +
                 static_cast<long long>(h) * p.so.h + static_cast<long long>(row_ok ? i : 0) * p.so.n;
       T* trow = TANGENT ? static_cast<T*>(p.t_o) + static_cast<long long>(b) * p.sto.b +
@@ -546,7 +601,7 @@ __global__ void __launch_bounds__(192, 1)
                               static_cast<long long>(row_ok ? i : 0) * p.sto.n
                         : nullptr;
 #pragma unroll 1
-      for (int col = 0; col < D; col += 32) {
+      for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 32) {
         uint32_t a[32], tt[32];
         if (n_kv > 0) {
           if (TANGENT) {
@@ -582,10 +637,10 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      if (row_ok) {
+      if (row_ok && wg == 0) {
         const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
         if (p.lse)
-          p.lse[ridx] = (lx_run > 0.0f) ? (m_run + log2f(lx_run)) * kLn2 : -INFINITY;
+          p.lse[ridx] = (lx_all > 0.0f) ? (m_run + log2f(lx_all)) * kLn2 : -INFINITY;
         if (TANGENT && p.mu) p.mu[ridx] = mu_row;
       }
     }
@@ -614,7 +669,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     if (dev < 64) attr_done |= 1ull << dev;
   }
   const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H;
-  kern<<<static_cast<unsigned>(grid), 192, L::SMEM_BYTES, stream>>>(maps, p);
+  kern<<<static_cast<unsigned>(grid), kTcThreads, L::SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }
 

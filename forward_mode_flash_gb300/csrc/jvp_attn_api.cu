@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -41,6 +42,7 @@ size_t elem_size(int dt) { return dt == JVP_F32 ? 4 : 2; }
 struct DeviceInfo {
   bool queried = false;
   bool sm103 = false;
+  int num_sms = 0;
   unsigned int* status = nullptr;
 };
 std::mutex g_dev_mu;
@@ -62,6 +64,9 @@ jvp_status_t current_device(DeviceInfo** out) {
     if (e != cudaSuccess)
       return fail(JVP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
     d.sm103 = (major == 10 && minor == 3);
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+      return fail(JVP_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
     void* addr = nullptr;
     e = cudaGetSymbolAddress(&addr, g_device_status);
     if (e != cudaSuccess)
@@ -250,6 +255,8 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   cudaError_t err;
   if (tc) {
     p.num_q_tiles = static_cast<int>((Nq + kTcBlockM - 1) / kTcBlockM);
+    // About one wave of CTAs per group of heads (one CTA per SM).
+    p.group_heads = std::max(1, std::min(static_cast<int>(B * H), dev->num_sms / p.num_q_tiles));
     err = launch_fwd_tc(static_cast<DType>(dtype), static_cast<int>(D), kind, tangent, maps, p,
                         stream);
     t_last_path = 1;

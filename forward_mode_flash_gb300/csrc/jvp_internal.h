@@ -19,6 +19,7 @@ struct Strides {
 struct FwdParams {
   int B, H, Nq, Nk, D;
   int num_q_tiles;
+  int group_heads;   // tensor-core kernel: (batch, head) pairs per scheduling group
   float scale;       // logit scale s
   float scale_log2;  // s * log2(e)
   const void* mask;  // uint8 (bool) or float (additive); nullptr otherwise
