@@ -132,6 +132,7 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, volatile in
 
 // Bounded wait taken by every lane of a warp, with a warp-uniform outcome, so
 // that the warp-collective TMEM instructions after it never run diverged.
+// (Waiters sleep inside try_wait, so polling adds little shared-memory traffic.)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
                                           volatile int* abort) {
   const bool got = mbar_wait(bar, parity, abort);
