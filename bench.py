@@ -207,7 +207,7 @@ def main():
     import torch
     import torch.distributed as dist
 
-    from forward_mode_flash_gb300 import api, build, metrics, synth
+    from forward_mode_flash_gb300 import api, build, metrics, replicas, synth
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
@@ -251,13 +251,9 @@ def main():
     if world > 1:
         dist.barrier()
     per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(per_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replicas.max_over_ranks(sum(per_ms), device=dev)
     ms_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = replicas.aggregate_throughput(world, flops, args.steps, total_ms * 1e-3) / 1e12
     launches = args.steps  # one fwd_dual kernel per step
 
     # End to end through the public API: pinned host inputs -> device -> kernel -> host.
@@ -293,11 +289,7 @@ def main():
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / k_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = replicas.max_over_ranks(a.elapsed_time(b) / k_e2e, device=dev)
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": k_e2e}
