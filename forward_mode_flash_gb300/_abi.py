@@ -23,6 +23,8 @@ JVP_MASK_NONE, JVP_MASK_BOOL, JVP_MASK_ADDITIVE, JVP_MASK_CAUSAL = 0, 1, 2, 3
 EXPORTS = (
     "jvp_attn_fwd_dual",
     "jvp_attn_fwd",
+    "jvp_attn_bwd_dual",
+    "jvp_attn_bwd_dual_workspace_size",
     "jvp_attn_get_device_status",
     "jvp_attn_status_string",
     "jvp_attn_last_error",
@@ -77,6 +79,11 @@ def load(path: str | None = None):
         lib.jvp_attn_fwd_dual.restype = i32
         lib.jvp_attn_fwd.argtypes = [SP, i32, vp, vp, vp, STP, MP, f32, vp, STP, vp, vp]
         lib.jvp_attn_fwd.restype = i32
+        lib.jvp_attn_bwd_dual.argtypes = [SP, i32] + [vp] * 8 + [vp, vp] + [vp, vp] + [STP, MP, f32] + \
+            [vp] * 6 + [STP, vp, ctypes.c_size_t, vp]
+        lib.jvp_attn_bwd_dual.restype = i32
+        lib.jvp_attn_bwd_dual_workspace_size.argtypes = [SP, i32]
+        lib.jvp_attn_bwd_dual_workspace_size.restype = ctypes.c_size_t
         lib.jvp_attn_get_device_status.argtypes = [vp]
         lib.jvp_attn_get_device_status.restype = i32
         lib.jvp_attn_status_string.argtypes = [i32]

@@ -143,6 +143,52 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return (o, lse) if return_lse else o
 
 
+def bwd_dual_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,
+                            dtype: torch.dtype = torch.bfloat16) -> int:
+    """Bytes of device scratch jvp_attn_bwd_dual needs for this shape."""
+    shape = _abi.Shape(B, H, Nq, Nk, D)
+    return int(_abi.load().jvp_attn_bwd_dual_workspace_size(ctypes.byref(shape), _DT[dtype]))
+
+
+def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
+             attn_mask: Optional[torch.Tensor] = None, is_causal: bool = False,
+             scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None):
+    """Gradients of <g_o, O> + <g_to, tO> with respect to (q, k, v, dq, dk, dv).
+
+    o, t_o, lse, mu are the outputs of ``fwd_dual(..., return_stats=True)`` on
+    the same inputs.  ``workspace`` (uint8, on q's device) is allocated here if
+    not given; its size is ``bwd_dual_workspace_size``.
+    """
+    lib = _abi.load()
+    _check_inputs([q, k, v, dq, dk, dv, o, t_o, g_o, g_to],
+                  ["q", "k", "v", "dq", "dk", "dv", "o", "t_o", "g_o", "g_to"])
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    for t, n in ((lse, "lse"), (mu, "mu")):
+        if t.dtype != torch.float32 or tuple(t.shape) != (B, H, Nq) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 [B, H, Nq] tensor")
+    outs = [torch.empty_like(x) for x in (q, k, v, dq, dk, dv)]
+    need = bwd_dual_workspace_size(B, H, Nq, Nk, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
+    ins = (_abi.Strides * 10)(*[_strides(t) for t in (q, k, v, dq, dk, dv, o, t_o, g_o, g_to)])
+    ost = (_abi.Strides * 6)(*[_strides(t) for t in outs])
+    shape = _abi.Shape(B, H, Nq, Nk, D)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = lib.jvp_attn_bwd_dual(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(o), _ptr(t_o), _ptr(lse),
+                                   _ptr(mu), _ptr(g_o), _ptr(g_to), ins, ctypes.byref(mask),
+                                   float(scale), *[_ptr(x) for x in outs], ost, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   ctypes.c_void_p(stream))
+    _abi.check(st)
+    return tuple(outs)
+
+
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise the stream and return (and clear) the library's device status."""
     lib = _abi.load()

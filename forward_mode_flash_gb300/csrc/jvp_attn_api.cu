@@ -270,6 +270,101 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   return ok();
 }
 
+// Body of jvp_attn_bwd_dual.
+jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* const* in,
+                      const float* lse, const float* mu, const jvp_strides_t* in_strides,
+                      const jvp_mask_t* mask, float scale, void* const* out,
+                      const jvp_strides_t* out_strides, void* workspace, size_t ws_bytes,
+                      void* stream_ptr) {
+  if (!shape) return fail(JVP_ERR_INVALID_ARG, "shape is NULL");
+  const int64_t B = shape->B, H = shape->H, Nq = shape->Nq, Nk = shape->Nk, D = shape->D;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return fail(JVP_ERR_INVALID_ARG, "negative size");
+  if (D <= 0) return fail(JVP_ERR_INVALID_ARG, "D must be positive");
+  if (D > 128) return fail(JVP_ERR_UNSUPPORTED, "D > 128 is not supported");
+  if (dtype != JVP_F32 && dtype != JVP_F16 && dtype != JVP_BF16)
+    return fail(JVP_ERR_INVALID_ARG, "unknown dtype");
+  if (!in_strides || !out_strides) return fail(JVP_ERR_INVALID_ARG, "strides are NULL");
+  if (!std::isfinite(scale)) return fail(JVP_ERR_INVALID_ARG, "scale is not finite");
+  const int64_t lim = (1ll << 31) - 1;
+  if (Nq > lim || Nk > lim || B * H * Nq > lim / 32 || B * H * Nk > lim)
+    return fail(JVP_ERR_UNSUPPORTED, "problem too large for one launch");
+  for (int t = 0; t < 10; ++t) {
+    const jvp_strides_t& s = in_strides[t];
+    if (s.d != 1) return fail(JVP_ERR_INVALID_ARG, "innermost (d) stride must be 1");
+    if (s.b < 0 || s.h < 0 || s.n < 0) return fail(JVP_ERR_INVALID_ARG, "negative stride");
+  }
+  for (int t = 0; t < 6; ++t) {
+    const jvp_strides_t& s = out_strides[t];
+    if (s.d != 1) return fail(JVP_ERR_INVALID_ARG, "innermost (d) stride of an output must be 1");
+    if (s.b < 0 || s.h < 0 || s.n < 0) return fail(JVP_ERR_INVALID_ARG, "negative stride");
+  }
+  int kind = JVP_MASK_NONE;
+  const void* mptr = nullptr;
+  int64_t msb = 0, msh = 0, msq = 0, msk = 0;
+  if (mask) {
+    kind = mask->kind;
+    mptr = mask->ptr;
+    msb = mask->stride_b, msh = mask->stride_h, msq = mask->stride_q, msk = mask->stride_k;
+    if (kind < JVP_MASK_NONE || kind > JVP_MASK_CAUSAL)
+      return fail(JVP_ERR_INVALID_ARG, "unknown mask kind");
+    if ((kind == JVP_MASK_CAUSAL || kind == JVP_MASK_NONE) && mptr)
+      return fail(JVP_ERR_INVALID_ARG, "this mask kind takes no mask tensor");
+    if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && B * H * Nq * Nk > 0)
+      return fail(JVP_ERR_INVALID_ARG, "mask tensor is NULL");
+    if (msb < 0 || msh < 0 || msq < 0 || msk < 0) return fail(JVP_ERR_INVALID_ARG, "negative mask stride");
+    if (kind == JVP_MASK_ADDITIVE && !aligned(mptr, 4))
+      return fail(JVP_ERR_ALIGNMENT, "additive mask is not 4-byte aligned");
+  }
+  if (B * H * (Nq + Nk) == 0) return ok();  // nothing to compute
+  const size_t e = elem_size(dtype);
+  for (int t = 0; t < 10; ++t) {
+    const bool on_keys = (t == 1 || t == 2 || t == 4 || t == 5);
+    if (!in[t] && (!on_keys || Nk > 0) && (on_keys || Nq > 0))
+      return fail(JVP_ERR_INVALID_ARG, "input pointer is NULL");
+    if (!aligned(in[t], e)) return fail(JVP_ERR_ALIGNMENT, "input not aligned to its element size");
+  }
+  for (int t = 0; t < 6; ++t) {
+    const bool on_keys = (t == 1 || t == 2 || t == 4 || t == 5);
+    if (!out[t] && (!on_keys || Nk > 0) && (on_keys || Nq > 0))
+      return fail(JVP_ERR_INVALID_ARG, "output pointer is NULL");
+    if (!aligned(out[t], e)) return fail(JVP_ERR_ALIGNMENT, "output not aligned to its element size");
+  }
+  if (Nq > 0 && (!lse || !mu)) return fail(JVP_ERR_INVALID_ARG, "lse and mu are required");
+  if (!aligned(lse, 4) || !aligned(mu, 4)) return fail(JVP_ERR_ALIGNMENT, "lse/mu not 4-byte aligned");
+  const size_t need = bwd_workspace_bytes(B * H * Nq);
+  if (need > 0 && (!workspace || ws_bytes < need))
+    return fail(JVP_ERR_WORKSPACE, "workspace is NULL or smaller than jvp_attn_bwd_dual_workspace_size()");
+  if (!aligned(workspace, 4)) return fail(JVP_ERR_ALIGNMENT, "workspace is not 4-byte aligned");
+
+  DeviceInfo* dev = nullptr;
+  jvp_status_t s = current_device(&dev);
+  if (s != JVP_OK) return s;
+  if (!dev->sm103)
+    return fail(JVP_ERR_UNSUPPORTED, "the current device is not an sm_103 (GB300-class) GPU");
+
+  BwdParams p{};
+  p.B = static_cast<int>(B), p.H = static_cast<int>(H), p.Nq = static_cast<int>(Nq);
+  p.Nk = static_cast<int>(Nk), p.D = static_cast<int>(D);
+  p.scale = scale;
+  p.mask_kind = kind;
+  p.mask = mptr;
+  p.msb = msb, p.msh = msh, p.msq = msq, p.msk = msk;
+  p.q = in[0], p.k = in[1], p.v = in[2], p.dq = in[3], p.dk = in[4], p.dv = in[5];
+  p.o = in[6], p.t_o = in[7], p.g_o = in[8], p.g_to = in[9];
+  Strides* sin[10] = {&p.sq, &p.sk, &p.sv, &p.sdq, &p.sdk, &p.sdv, &p.so, &p.sto, &p.sgo, &p.sgto};
+  for (int t = 0; t < 10; ++t) *sin[t] = to_strides(in_strides[t]);
+  p.lse = lse, p.mu = mu;
+  p.g_q = out[0], p.g_k = out[1], p.g_v = out[2], p.g_dq = out[3], p.g_dk = out[4], p.g_dv = out[5];
+  Strides* sout[6] = {&p.sgq, &p.sgk, &p.sgv, &p.sgdq, &p.sgdk, &p.sgdv};
+  for (int t = 0; t < 6; ++t) *sout[t] = to_strides(out_strides[t]);
+  p.nu = static_cast<float*>(workspace);
+  p.delta = p.nu + B * H * Nq;
+  cudaError_t err = launch_bwd_simt(static_cast<DType>(dtype), p, static_cast<cudaStream_t>(stream_ptr));
+  if (err != cudaSuccess)
+    return fail(JVP_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(err));
+  return ok();
+}
+
 __global__ void wait_timeout_selftest_kernel(long long limit, unsigned int* status) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -315,6 +410,25 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
   void* out[1] = {o};
   return jvp::forward(shape, dtype, in, in_strides, mask, scale, out, out_strides, lse, nullptr,
                       stream, false);
+}
+
+jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                               const void* k, const void* v, const void* dq, const void* dk,
+                               const void* dv, const void* o, const void* t_o, const float* lse,
+                               const float* mu, const void* g_o, const void* g_to,
+                               const jvp_strides_t* in_strides, const jvp_mask_t* mask,
+                               float scale, void* g_q, void* g_k, void* g_v, void* g_dq,
+                               void* g_dk, void* g_dv, const jvp_strides_t* out_strides,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  const void* in[10] = {q, k, v, dq, dk, dv, o, t_o, g_o, g_to};
+  void* out[6] = {g_q, g_k, g_v, g_dq, g_dk, g_dv};
+  return jvp::backward(shape, dtype, in, lse, mu, in_strides, mask, scale, out, out_strides,
+                       workspace, workspace_bytes, stream);
+}
+
+size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t) {
+  if (!shape || shape->B < 0 || shape->H < 0 || shape->Nq < 0) return 0;
+  return jvp::bwd_workspace_bytes(shape->B * shape->H * shape->Nq);
 }
 
 jvp_status_t jvp_attn_get_device_status(void* stream) {

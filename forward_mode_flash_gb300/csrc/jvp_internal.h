@@ -66,6 +66,32 @@ cudaError_t launch_fwd_tc_bf16_d64(int mask_kind, bool tangent, const TcMaps& ma
 cudaError_t launch_fwd_tc_bf16_d128(int mask_kind, bool tangent, const TcMaps& maps,
                                     const FwdParams& p, cudaStream_t stream);
 
+// Everything the backward kernels need.  The workspace holds two float32
+// arrays [B, H, Nq]: nu = gtO . O and delta = gO . O + gtO . tO - mu * nu.
+struct BwdParams {
+  int B, H, Nq, Nk, D;
+  float scale;
+  int mask_kind;
+  const void* mask;
+  long long msb, msh, msq, msk;
+  const void *q, *k, *v, *dq, *dk, *dv, *o, *t_o, *g_o, *g_to;
+  Strides sq, sk, sv, sdq, sdk, sdv, so, sto, sgo, sgto;
+  const float* lse;
+  const float* mu;
+  void *g_q, *g_k, *g_v, *g_dq, *g_dk, *g_dv;
+  Strides sgq, sgk, sgv, sgdq, sgdk, sgdv;
+  float* nu;
+  float* delta;
+};
+
+// Workspace bytes of the backward for a problem with `rows` = B * H * Nq query rows.
+inline size_t bwd_workspace_bytes(long long rows) {
+  return static_cast<size_t>(2 * rows) * sizeof(float);
+}
+
+// Backward of the dual computation (CUDA-core kernels).  Returns a cudaError_t.
+cudaError_t launch_bwd_simt(DType dt, const BwdParams& p, cudaStream_t stream);
+
 // Device status word owned by the library (bit 0: a bounded wait timed out).
 unsigned int* device_status_ptr();
 

@@ -126,6 +126,40 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
                           const jvp_strides_t* out_strides, float* lse, void* stream);
 
 /*
+ * Reverse mode of the dual computation (the backward needed to train through
+ * `fwd_dual` or to form Hessian-vector products: the project page,
+ * Description and Results sections).  Given the cotangents g_o, g_to of
+ * Loss = <g_o, O> + <g_to, tO>, writes the gradients with respect to q, k, v,
+ * dq, dk, dv.  No gradient flows into the mask.
+ *
+ *   q, k, v, dq, dk, dv   the forward inputs (as passed to jvp_attn_fwd_dual)
+ *   o, t_o, lse, mu       that call's outputs (lse and mu are required here)
+ *   g_o, g_to             cotangents, [B,H,Nq,D]
+ *   in_strides            10 records: q, k, v, dq, dk, dv, o, t_o, g_o, g_to
+ *   g_q, g_k, g_v, g_dq, g_dk, g_dv   outputs, shapes of q, k, v, dq, dk, dv
+ *   out_strides           6 records in that order
+ *   workspace             device scratch of at least
+ *                         jvp_attn_bwd_dual_workspace_size() bytes, 4-byte
+ *                         aligned, owned by the caller; its contents on entry
+ *                         do not matter and are overwritten.
+ *
+ * Every tensor has the same dtype; mask and scale as in the forward call.  The
+ * computation runs on CUDA cores in fp32 (three kernels, enqueued on
+ * `stream`).  Returns JVP_ERR_WORKSPACE if the workspace is NULL or too small.
+ */
+jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                               const void* k, const void* v, const void* dq, const void* dk,
+                               const void* dv, const void* o, const void* t_o, const float* lse,
+                               const float* mu, const void* g_o, const void* g_to,
+                               const jvp_strides_t* in_strides, const jvp_mask_t* mask,
+                               float scale, void* g_q, void* g_k, void* g_v, void* g_dq,
+                               void* g_dk, void* g_dv, const jvp_strides_t* out_strides,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes jvp_attn_bwd_dual needs for `shape` (8 * B * H * Nq). */
+size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side status word:
  * JVP_ERR_DEVICE_TIMEOUT if any kernel of this library gave up on a wait since
  * the last call, JVP_ERR_CUDA if the stream reports an error, else JVP_OK.

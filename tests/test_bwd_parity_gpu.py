@@ -1,0 +1,89 @@
+"""GPU parity of jvp_attn_bwd_dual (reverse mode of the dual computation)
+against the float64 oracle's reverse mode on the same inputs.
+
+Tolerance: max-abs error <= tol * max(1, max |reference|) per gradient, with
+tol = 1e-4 for float32 inputs and 2e-2 for fp16/bf16.  The GPU computes in
+fp32 from its own 16-bit O and tO (which enter delta and nu) and rounds the
+gradients to 16 bits, so relative errors of a few 2^-9 are expected there.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from forward_mode_flash_gb300 import api as A
+from forward_mode_flash_gb300 import build, synth
+
+pytestmark = pytest.mark.gpu
+TOL = {"f32": 1e-4, "f16": 2e-2, "bf16": 2e-2}
+NAMES = ["g_q", "g_k", "g_v", "g_dq", "g_dk", "g_dv"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def np64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def run(w, heads=None):
+    inp = synth.make_inputs(w, with_cotangents=True)
+    dev = "cuda"
+    g = [x.to(dev) for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    m = inp.mask.to(dev) if inp.mask is not None else None
+    causal = w.mask == "causal"
+    o, t_o, lse, mu = A.fwd_dual(*g, attn_mask=m, is_causal=causal, return_stats=True)
+    grads = A.bwd_dual(*g, o, t_o, lse, mu, inp.g_o.to(dev), inp.g_to.to(dev), attn_mask=m,
+                       is_causal=causal)
+    torch.cuda.synchronize()
+    assert A.device_status() == 0
+    sel = slice(None) if heads is None else heads
+    xs = [np64(x)[sel] for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv, inp.g_o, inp.g_to)]
+    mm = None
+    if w.mask == "bool":
+        mm = inp.mask.numpy()[sel]
+    elif w.mask == "additive":
+        mm = inp.mask.double().numpy()[sel]
+    ref = oracle.bwd_dual(*xs, w.mask, mm)
+    errs = {}
+    for name, gg, r in zip(NAMES, grads, ref):
+        gv = np64(gg)[sel]
+        errs[name] = (np.abs(gv - r).max(), np.abs(r).max())
+    return errs
+
+
+def check(w, errs):
+    tol = TOL[w.dtype]
+    for name, (e, scale) in errs.items():
+        assert e <= tol * max(1.0, scale), (w.name, name, e, scale)
+
+
+@pytest.mark.parametrize("mask", ["none", "causal", "bool", "additive"])
+@pytest.mark.parametrize("dtype,D", [("f32", 16), ("f32", 40), ("bf16", 64), ("f16", 64),
+                                     ("bf16", 128), ("f16", 32)])
+@pytest.mark.parametrize("N", [1, 33, 130])
+def test_bwd_small(mask, dtype, D, N):
+    w = synth.small(dtype, 2, 2, N, D, mask, seed=N + D)
+    check(w, run(w))
+
+
+def test_bwd_workspace_is_required_and_sized():
+    assert A.bwd_dual_workspace_size(2, 8, 2048, 2048, 64) == 8 * 2 * 8 * 2048
+    w = synth.small("bf16", 1, 1, 64, 64, "none")
+    inp = synth.make_inputs(w, with_cotangents=True)
+    g = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    o, t_o, lse, mu = A.fwd_dual(*g, return_stats=True)
+    small_ws = torch.empty(8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(A._abi.JvpAttnError) as ei:
+        A.bwd_dual(*g, o, t_o, lse, mu, inp.g_o.cuda(), inp.g_to.cuda(), workspace=small_ws)
+    assert ei.value.status == A._abi.JVP_ERR_WORKSPACE
+
+
+def test_bwd_specified_workload_f16_b2h8n2048d64_causal_two_heads():
+    # Full-size launch; the oracle checks two whole heads (every gradient entry).
+    w = synth.WORKLOADS["f16_b2h8n2048d64_causal"]
+    errs = run(w, heads=(slice(0, 2), slice(3, 4)))
+    check(w, errs)
