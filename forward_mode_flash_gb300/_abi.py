@@ -25,6 +25,7 @@ EXPORTS = (
     "jvp_attn_fwd",
     "jvp_attn_bwd_dual",
     "jvp_attn_bwd_dual_workspace_size",
+    "jvp_attn_bwd_dual_noalloc",
     "jvp_attn_get_device_status",
     "jvp_attn_status_string",
     "jvp_attn_last_error",
@@ -82,6 +83,8 @@ def load(path: str | None = None):
         lib.jvp_attn_bwd_dual.argtypes = [SP, i32] + [vp] * 8 + [vp, vp] + [vp, vp] + [STP, MP, f32] + \
             [vp] * 6 + [STP, vp, ctypes.c_size_t, vp]
         lib.jvp_attn_bwd_dual.restype = i32
+        lib.jvp_attn_bwd_dual_noalloc.argtypes = lib.jvp_attn_bwd_dual.argtypes[:-3] + [vp]
+        lib.jvp_attn_bwd_dual_noalloc.restype = i32
         lib.jvp_attn_bwd_dual_workspace_size.argtypes = [SP, i32]
         lib.jvp_attn_bwd_dual_workspace_size.restype = ctypes.c_size_t
         lib.jvp_attn_get_device_status.argtypes = [vp]

@@ -484,3 +484,62 @@ jvp_status_t jvp_attn_selftest_wait_timeout(int64_t limit_cycles, void* stream) 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without allocation (jvp_attn_bwd_dual_noalloc).
+//
+// Some callers cannot allocate device memory (plugins living in another
+// framework's memory pool, code that must not call the allocator after
+// start-up).  For them the backward's per-row scratch (nu and delta) lives in
+// this fixed device array instead of a caller workspace.  Host code may not
+// use the symbol itself as an address (it is a host-side stand-in); the real
+// device address is looked up once per device and passed to the kernels.
+
+static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[JVP_BWD_NOALLOC_SCRATCH_BYTES];
+
+namespace jvp {
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};  // device address of the array, per device
+
+// Device address of the scratch array on the current device (first call per
+// device: cudaGetSymbolAddress with that device current).
+jvp_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(JVP_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(JVP_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_bwd_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+      return fail(JVP_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return JVP_OK;
+}
+}  // namespace
+}  // namespace jvp
+
+extern "C" jvp_status_t jvp_attn_bwd_dual_noalloc(
+    const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q, const void* k, const void* v,
+    const void* dq, const void* dk, const void* dv, const void* o, const void* t_o,
+    const float* lse, const float* mu, const void* g_o, const void* g_to,
+    const jvp_strides_t* in_strides, const jvp_mask_t* mask, float scale, void* g_q, void* g_k,
+    void* g_v, void* g_dq, void* g_dk, void* g_dv, const jvp_strides_t* out_strides,
+    void* stream) {
+  if (!shape) return jvp::fail(JVP_ERR_INVALID_ARG, "shape is NULL");
+  if (shape->B > 0 && shape->H > 0 && shape->Nq > 0 &&
+      jvp_attn_bwd_dual_workspace_size(shape, dtype) > JVP_BWD_NOALLOC_SCRATCH_BYTES)
+    return jvp::fail(JVP_ERR_WORKSPACE,
+                     "problem needs more than the 4 MiB fixed scratch of "
+                     "jvp_attn_bwd_dual_noalloc (8 * B * H * Nq bytes); use jvp_attn_bwd_dual");
+  void* scratch = nullptr;
+  jvp_status_t s = jvp::noalloc_scratch(&scratch);
+  if (s != JVP_OK) return s;
+  return jvp_attn_bwd_dual(shape, dtype, q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
+                           in_strides, mask, scale, g_q, g_k, g_v, g_dq, g_dk, g_dv, out_strides,
+                           scratch, JVP_BWD_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -160,6 +160,39 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
 size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
 
 /*
+ * jvp_attn_bwd_dual for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this entry point; it exists for callers such
+ * as plugins that run inside someone else's process or memory pool, code
+ * paths that must not touch the allocator after start-up, and callers without
+ * access to cudaMalloc.  It allocates nothing: instead of a caller-provided
+ * workspace it uses a fixed scratch array that the library itself places in
+ * device memory (4 MiB, JVP_BWD_NOALLOC_SCRATCH_BYTES; every device that loads
+ * the library holds it until the process exits).  Arguments are those of
+ * jvp_attn_bwd_dual without the workspace.
+ *
+ *   - Size limit: the problem may need at most 4 MiB of scratch, i.e.
+ *     8 * B * H * Nq <= 4 MiB (B * H * Nq <= 524288 query rows in total).
+ *     Larger problems return JVP_ERR_WORKSPACE with a message naming the limit.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - Sharing: every call uses the same array.  Nothing in it needs to start
+ *     at zero (each call overwrites the part it reads), but calls whose work
+ *     overlaps on the GPU (different streams, no ordering between them) race
+ *     on it; order them, e.g. issue them on one stream.
+ */
+#define JVP_BWD_NOALLOC_SCRATCH_BYTES (4u << 20)
+jvp_status_t jvp_attn_bwd_dual_noalloc(const jvp_shape_t* shape, jvp_dtype_t dtype,
+                                       const void* q, const void* k, const void* v,
+                                       const void* dq, const void* dk, const void* dv,
+                                       const void* o, const void* t_o, const float* lse,
+                                       const float* mu, const void* g_o, const void* g_to,
+                                       const jvp_strides_t* in_strides, const jvp_mask_t* mask,
+                                       float scale, void* g_q, void* g_k, void* g_v, void* g_dq,
+                                       void* g_dk, void* g_dv, const jvp_strides_t* out_strides,
+                                       void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side status word:
  * JVP_ERR_DEVICE_TIMEOUT if any kernel of this library gave up on a wait since
  * the last call, JVP_ERR_CUDA if the stream reports an error, else JVP_OK.
