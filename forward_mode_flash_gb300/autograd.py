@@ -28,6 +28,22 @@ def _zeros_if_none(t, like):
     return torch.zeros_like(like) if t is None else t
 
 
+def _plain(t):
+    """The storage-backed tensor under torch.func's wrappers.
+
+    Under torch.func.jvp the tangents handed to a Function's jvp rule are
+    wrapper tensors without storage; the kernels need the underlying device
+    buffers, so the rule unwraps them and returns a plain tensor, which
+    torch.func accepts as the output tangent.
+    """
+    if t is None:
+        return None
+    ft = torch._C._functorch
+    while ft.is_functorch_wrapped_tensor(t):
+        t = ft.get_unwrapped(t)
+    return t
+
+
 class JVPAttn(torch.autograd.Function):
     """Attention with a forward-mode rule backed by the fused fwd_dual kernel."""
 
@@ -47,8 +63,8 @@ class JVPAttn(torch.autograd.Function):
 
     @staticmethod
     def jvp(ctx, dq, dk, dv, *_):
-        q, k, v, _o, lse = ctx.saved_tensors
-        dq, dk, dv = (_zeros_if_none(t, x) for t, x in ((dq, q), (dk, k), (dv, v)))
+        q, k, v, _o, lse = (_plain(t) for t in ctx.saved_tensors)
+        dq, dk, dv = (_zeros_if_none(_plain(t), x) for t, x in ((dq, q), (dk, k), (dv, v)))
         _, t_o, _, mu = api.fwd_dual(q, k, v, dq, dk, dv, attn_mask=ctx.attn_mask,
                                      is_causal=ctx.is_causal, scale=ctx.scale, return_stats=True)
         return t_o, mu  # mu is the tangent of lse
