@@ -63,10 +63,14 @@ class JVPAttn(torch.autograd.Function):
 
     @staticmethod
     def jvp(ctx, dq, dk, dv, *_):
-        q, k, v, _o, lse = (_plain(t) for t in ctx.saved_tensors)
-        dq, dk, dv = (_zeros_if_none(_plain(t), x) for t, x in ((dq, q), (dk, k), (dv, v)))
-        _, t_o, _, mu = api.fwd_dual(q, k, v, dq, dk, dv, attn_mask=ctx.attn_mask,
-                                     is_causal=ctx.is_causal, scale=ctx.scale, return_stats=True)
+        # Outside torch.func's dispatch, so that the output buffers the binding
+        # allocates are plain device tensors too.
+        with torch._C._DisableFuncTorch():
+            q, k, v, _o, lse = (_plain(t) for t in ctx.saved_tensors)
+            dq, dk, dv = (_zeros_if_none(_plain(t), x) for t, x in ((dq, q), (dk, k), (dv, v)))
+            _, t_o, _, mu = api.fwd_dual(q, k, v, dq, dk, dv, attn_mask=_plain(ctx.attn_mask),
+                                         is_causal=ctx.is_causal, scale=ctx.scale,
+                                         return_stats=True)
         return t_o, mu  # mu is the tangent of lse
 
     @staticmethod
