@@ -13,27 +13,22 @@
 // (p~ = exp(S - m)), then O = A / l, mu = mu~ / l, tO = T / l - mu O.
 //
 // Work decomposition: one CTA per (128-row query tile, batch*head), ten warps.
-//   warp 0      TMA producer: Q, dQ once; then per 64-key tile the [dK | K]
+//   warp 0      TMA producer: Q, dQ once; then per 64-key tile the [K;dK]
 //               block and the [V|dV] block, through an NS-deep ring.
 //   warp 1      TMEM allocator and single-thread MMA issuer.
 //   warps 2..9  softmax, two warpgroups: a thread owns one query row (its TMEM
-//               lane); both warpgroups read all 64 scores of a tile (so both
-//               know the tile maximum without exchanging it) and each turns
-//               its own 32 keys into P~ and P~ * dS.  The epilogue splits the
-//               output columns the same way.
+//               lane) and one half (32 keys) of every key tile; the two halves
+//               exchange their maxima through shared memory each tile.  The
+//               epilogue splits the output columns the same way.
 // Per key tile t (buffer b = t % 2 of the double-buffered score region):
-//   M1  [Q dK^T | S]  = Q [dK ; K]^T          (N = 128, SMEM x SMEM)
-//   M2  [dQ K^T | 0] += dQ [K ; 0]^T          (N = 128; the zero rows keep
-//                                               every MMA at N >= 128)
+//   M1  [S | Q dK^T] = Q [K ; dK]^T          (N = 128, SMEM x SMEM)
+//   M2  Q dK^T      += dQ K^T                 (N = 64)
 //   softmax: p~ and p~ * s * dS_raw, written back to TMEM as 16-bit values
-//            into the dS columns of its own 32 keys (which only it reads)
-//   M3  [A | T]      += P~ [V | dV]           (N = 2D, A operand from TMEM)
-//   M4  T            += (P~ * dS) V           (N = D)
+//            over the S / dS columns they came from
+//   M3  [A | T]     += P~ [V | dV]            (N = 2D, A operand from TMEM)
+//   M4  T           += (P~ * dS) V            (N = D)
 // The MMA warp issues M1/M2 of tile t+1 before M3/M4 of tile t, so the
-// tensor core computes the next scores while the softmax warps work.  One
-// thread can issue an MMA only every ~46 cycles, so every MMA is at least
-// N = 128 (>= 64 tensor cycles): the issue queue then stays ahead of the
-// tensor core and the issuing thread's barrier waits do not starve it.
+// tensor core computes the next scores while the softmax warps work.
 //
 // Rescaling is conditional: the row maximum used in the exponent is only
 // moved when a tile's maximum exceeds it by more than 2^8, so A, T, l and mu~
@@ -87,15 +82,9 @@ struct TcLayout {
   static constexpr int KCH = D / 64;                // 128-byte chunks along D
   static constexpr int NS = (D == 128) ? 2 : 4;     // pipeline depth
   static constexpr int Q_BYTES = KCH * BM * 128;
-  // One 64-column chunk of the key block: rows [dK (64) | K (64) | zeros (64)]
-  // with the tangent, [K (64)] without.
-  static constexpr int KROWS = TANGENT ? 3 * BN : BN;
-  static constexpr int KCHUNK_BYTES = KROWS * 128;
-  static constexpr int DK_OFF = 0;                          // within a chunk
-  static constexpr int K_OFF = TANGENT ? BN * 128 : 0;
-  static constexpr int Z_OFF = 2 * BN * 128;
+  static constexpr int KROWS = TANGENT ? 2 * BN : BN;  // rows of the [K;dK] block
+  static constexpr int KCHUNK_BYTES = KROWS * 128;     // one 64-column chunk of it
   static constexpr int KDK_BYTES = KCH * KCHUNK_BYTES;
-  static constexpr int KDK_TMA_BYTES = KCH * (TANGENT ? 2 : 1) * BN * 128;
   static constexpr int VCHUNK_BYTES = BN * 128;        // one 64-column chunk of V
   static constexpr int VDV_BYTES = (TANGENT ? 2 : 1) * KCH * VCHUNK_BYTES;
   static constexpr int OFF_Q = 0;
@@ -103,25 +92,14 @@ struct TcLayout {
   static constexpr int OFF_KDK = OFF_DQ + (TANGENT ? Q_BYTES : 0);
   static constexpr int OFF_VDV = OFF_KDK + NS * KDK_BYTES;
   static constexpr int OFF_CTRL = OFF_VDV + NS * VDV_BYTES;
-  static constexpr int CTRL_BYTES = 512;
+  static constexpr int CTRL_BYTES = 8192;
   static constexpr int USED = OFF_CTRL + CTRL_BYTES;
   // Padded so that only one CTA fits per SM (each CTA owns all 512 TMEM columns).
   static constexpr int SMEM_BYTES = (USED + 1024 < 120 * 1024 ? 120 * 1024 : USED + 1024);
-  // TMEM columns of a 128-column score buffer: with the tangent, dS in [0, 64)
-  // and S in [64, 128); without, S in [0, 64).  Softmax warpgroup w writes its
-  // 32 keys' P~ (16 columns of packed pairs) and P~ * dS (16 columns) into
-  // [w*32, w*32+32) (the dS columns of its own keys, which only it reads);
-  // without the tangent, P~ goes to [64 + w*16, 64 + w*16 + 16).
-  static constexpr uint32_t S_COL = TANGENT ? BN : 0;
+  // TMEM columns
   static constexpr uint32_t TM_A = 256;
   static constexpr uint32_t TM_T = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
-  static __host__ __device__ constexpr uint32_t p_col(int w) {
-    return TANGENT ? static_cast<uint32_t>(w * 32) : static_cast<uint32_t>(64 + w * 16);
-  }
-  static __host__ __device__ constexpr uint32_t pd_col(int w) {
-    return static_cast<uint32_t>(w * 32 + 16);
-  }
   static_assert(D == 64 || D == 128, "tensor-core path handles D = 64 or 128");
   static_assert(USED + 1024 <= 227 * 1024, "shared memory budget");
 };
@@ -135,10 +113,12 @@ struct TcCtrl {
   uint64_t q_full;
   uint64_t kdk_full[NS], kdk_empty[NS];
   uint64_t vdv_full[NS], vdv_empty[NS];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[2], p_full[2], max_ready[2];
   uint64_t at_done, o_full, drain, sums_ready;
   uint32_t tmem_base;
   int abort;
+  float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
+  float xsum[2][3][kTcBlockM];     // [warpgroup][l, lx, mu][row] final half sums
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -238,12 +218,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using L = TcLayout<D, TANGENT>;
   constexpr int NS = L::NS;
   constexpr int BN = L::BN;
-  constexpr int HN = BN / 2;  // keys per softmax warpgroup
+  constexpr int HN = BN / 2;  // key columns per softmax warpgroup
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSTEPS_D = D / 16;   // MMA K-steps over the head dimension
   constexpr int KSTEPS_N = BN / 16;  // MMA K-steps over a key tile
   constexpr int ACC_COLS = TANGENT ? 2 * D : D;  // TMEM columns of [A | T]
   constexpr uint32_t IDESC_S = idesc_f16(kBF16, 128, TANGENT ? 2 * BN : BN, false);
+  constexpr uint32_t IDESC_DS = idesc_f16(kBF16, 128, BN, false);
   constexpr uint32_t IDESC_AT = idesc_f16(kBF16, 128, ACC_COLS, true);
   constexpr uint32_t IDESC_T = idesc_f16(kBF16, 128, D, true);
 
@@ -278,16 +259,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     n_kv = min(n_kv, last_row / BN + 1);
   }
 
-  if (TANGENT) {
-    // Zero rows of every key block (never written by TMA).
-    for (int x = threadIdx.x; x < NS * L::KCH * (BN * 128 / 16); x += blockDim.x) {
-      const int per_chunk = BN * 128 / 16;
-      const int chunk = x / per_chunk, e = x % per_chunk;
-      uint4* z = reinterpret_cast<uint4*>(smem + L::OFF_KDK + chunk * L::KCHUNK_BYTES + L::Z_OFF);
-      z[e] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
     for (int s = 0; s < NS; ++s) {
@@ -299,6 +270,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
       mbar_init(&ctrl->p_full[s], kSoftmaxThreads);
+      mbar_init(&ctrl->max_ready[s], kSoftmaxThreads);
     }
     mbar_init(&ctrl->at_done, 1);
     mbar_init(&ctrl->o_full, 1);
@@ -344,13 +316,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         uint8_t* kdk = smem + L::OFF_KDK + s * L::KDK_BYTES;
-        mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_TMA_BYTES);
+        mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_BYTES);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(kdk + c * L::KCHUNK_BYTES + L::K_OFF, &maps.k, &ctrl->kdk_full[s], c * 64,
-                      j0, h, b);
+          tma_load_4d(kdk + c * L::KCHUNK_BYTES, &maps.k, &ctrl->kdk_full[s], c * 64, j0, h, b);
           if (TANGENT)
-            tma_load_4d(kdk + c * L::KCHUNK_BYTES + L::DK_OFF, &maps.dk, &ctrl->kdk_full[s],
-                        c * 64, j0, h, b);
+            tma_load_4d(kdk + c * L::KCHUNK_BYTES + BN * 128, &maps.dk, &ctrl->kdk_full[s], c * 64,
+                        j0, h, b);
         }
         ++k_fills;
         if (!mbar_wait(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
@@ -383,32 +354,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = mbar_wait(&ctrl->q_full, 0, abort);
       if (!ok) record_timeout(p.status, abort);
       tc_fence_after();
-      // Descriptors are precomputed: a K-step only adds a constant to the
-      // start-address field (addresses < 256 KB, so the 14-bit field never carries).
-      const uint64_t dq0 = sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
-      const uint64_t ddq0 = sdesc_sw128(smem_u32(smem + L::OFF_DQ), 16, 1024);
-      const uint64_t dk0 = sdesc_sw128(smem_u32(smem + L::OFF_KDK), 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(smem_u32(smem + L::OFF_VDV), L::VCHUNK_BYTES, 1024);
-      auto step_off = [](int kk, int chunk_bytes) -> uint64_t {
-        return static_cast<uint64_t>(((kk >> 2) * chunk_bytes + (kk & 3) * 32) >> 4);
-      };
+      const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+      const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
 
       auto issue_scores = [&](int t) -> bool {
         const int s = t % NS;
         if (!mbar_wait(&ctrl->kdk_full[s], (t / NS) & 1, abort)) return false;
         tc_fence_after();
-        const uint64_t kb = dk0 + static_cast<uint64_t>((s * L::KDK_BYTES) >> 4);
+        const uint32_t sK = smem_u32(smem + L::OFF_KDK + s * L::KDK_BYTES);
         const uint32_t d_s = tmem + (t & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS_D; ++kk)  // [Q dK^T | S] = Q [dK ; K]^T
-          mma_ss(d_s, dq0 + step_off(kk, L::BM * 128), kb + step_off(kk, L::KCHUNK_BYTES),
-                 IDESC_S, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < KSTEPS_D; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
+          mma_ss(d_s, a, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
         if (TANGENT) {
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS_D; ++kk)  // [dQ K^T | 0] += dQ [K ; 0]^T
-            mma_ss(d_s, ddq0 + step_off(kk, L::BM * 128),
-                   kb + static_cast<uint64_t>(L::K_OFF >> 4) + step_off(kk, L::KCHUNK_BYTES),
-                   IDESC_S, 1u);
+          for (int kk = 0; kk < KSTEPS_D; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            const uint64_t a = sdesc_sw128(sdQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
+            mma_ss(d_s + BN, a, bd, IDESC_DS, 1u);
+          }
         }
         mma_commit(&ctrl->kdk_empty[s]);
         mma_commit(&ctrl->s_full[t & 1]);
@@ -422,28 +391,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         const int buf = t & 1;
+        if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
         const int s = t % NS;
         if (!mbar_wait(&ctrl->vdv_full[s], (t / NS) & 1, abort)) {
           ok = false;
           break;
         }
-        if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
-        const uint64_t vb = dv0 + static_cast<uint64_t>((s * L::VDV_BYTES) >> 4);
-        const uint32_t sb = tmem + buf * 128;
+        const uint32_t sV = smem_u32(smem + L::OFF_VDV + s * L::VDV_BYTES);
+        const uint32_t p_tm = tmem + buf * 128;        // P~ (16-bit pairs)
+        const uint32_t pd_tm = tmem + buf * 128 + BN;  // P~ * dS (16-bit pairs)
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS_N; ++kk)  // [A | T] += P~ [V | dV]
-          mma_ts(tmem + L::TM_A, sb + L::p_col(kk >> 1) + (kk & 1) * 8,
-                 vb + static_cast<uint64_t>((kk * 16 * 128) >> 4), IDESC_AT,
-                 (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < KSTEPS_N; ++kk) {
+          const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
+          mma_ts(tmem + L::TM_A, p_tm + kk * 8, bd, IDESC_AT, (t > 0 || kk > 0) ? 1u : 0u);
+        }
         if (TANGENT) {
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS_N; ++kk)  // T += (P~ * dS) V
-            mma_ts(tmem + L::TM_T, sb + L::pd_col(kk >> 1) + (kk & 1) * 8,
-                   vb + static_cast<uint64_t>((kk * 16 * 128) >> 4), IDESC_T, 1u);
+          for (int kk = 0; kk < KSTEPS_N; ++kk) {
+            const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
+            mma_ts(tmem + L::TM_T, pd_tm + kk * 8, bd, IDESC_T, 1u);
+          }
         }
         mma_commit(&ctrl->vdv_empty[s]);
         mma_commit(&ctrl->at_done);
@@ -460,11 +431,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Two warpgroups; both read the 64 scores of every tile (each computes the
-    // same tile maximum), and warpgroup wg turns keys [wg*32, wg*32 + 32) into
-    // P~ and P~ * dS.  In the epilogue it owns output columns
-    // [wg*D/2, wg*D/2 + D/2).  Thread (warp, lane) owns query row
-    // r = 32 * (warp % 4) + lane (its TMEM lane).
+    // Two warpgroups; warpgroup wg owns key columns [wg*HN, wg*HN + HN) of
+    // every tile and, in the epilogue, output columns [wg*D/2, wg*D/2 + D/2).
+    // Thread (warp, lane) owns query row r = 32 * (warp % 4) + lane (its TMEM lane).
     const int wg = (warp - 2) >> 2;
     const int sub = warp & 3;
     const int r = sub * 32 + lane;
@@ -491,48 +460,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     for (int t = 0; t < n_kv; ++t) {
       const int buf = t & 1;
-      const int j0 = t * BN;  // first key of the tile
-      MaskRegs<MASK, BN> mreg;
+      const int j0 = t * BN + cofs;  // first key of this half tile
+      MaskRegs<MASK, HN> mreg;
       if (row_ok) mreg.load(p, mrow, j0);
       if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sbuf = lane_base + buf * 128;
-      uint32_t sa[32], sb[32], da[32];
+      uint32_t sa[32], da[32];
       if (TANGENT) {
-        tmem_ld32x3(sbuf + L::S_COL, sbuf + L::S_COL + 32, sbuf + cofs, sa, sb, da);
+        tmem_ld32x2(lane_base + buf * 128 + cofs, lane_base + buf * 128 + BN + cofs, sa, da);
       } else {
-        tmem_ld32x2(sbuf + L::S_COL, sbuf + L::S_COL + 32, sa, sb);
+        tmem_ld32(lane_base + buf * 128 + cofs, sa);
       }
-      float x[BN];
+      float x[HN];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        x[jj] = __uint_as_float(sa[jj]);
-        x[jj + 32] = __uint_as_float(sb[jj]);
-      }
+      for (int jj = 0; jj < HN; ++jj) x[jj] = __uint_as_float(sa[jj]);
       // Masking (raw-score domain unless additive, which is pre-scaled).
       if constexpr (MASK == kMaskAdditive) {
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) x[jj] = fmaf(x[jj], c, mreg.a[jj] * kLog2e);
+        for (int jj = 0; jj < HN; ++jj) x[jj] = fmaf(x[jj], c, mreg.a[jj] * kLog2e);
       } else if constexpr (MASK == kMaskBool) {
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj)
+        for (int jj = 0; jj < HN; ++jj)
           if (!mreg.keep(jj)) x[jj] = -INFINITY;
       }
-      if (j0 + BN > p.Nk) {
+      if (j0 + HN > p.Nk) {
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj)
+        for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj >= p.Nk) x[jj] = -INFINITY;
       }
-      if (MASK == kMaskCausal && j0 + BN - 1 > q0) {
+      if (MASK == kMaskCausal && j0 + HN - 1 > q0) {
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj)
+        for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj > i) x[jj] = -INFINITY;
       }
       const float mx = tree_max(x);
-      const float m_tile = (MASK == kMaskAdditive) ? mx : mx * c;
+      const float m_half = (MASK == kMaskAdditive) ? mx : mx * c;
+      // Exchange the half-row maxima between the two warpgroups.
+      ctrl->xmax[buf][wg][r] = m_half;
+      mbar_arrive(&ctrl->max_ready[buf]);
+      if (!warp_wait(&ctrl->max_ready[buf], (t >> 1) & 1, p.status, abort)) {
+        ok = false;
+        break;
+      }
+      const float m_tile = fmaxf(m_half, ctrl->xmax[buf][wg ^ 1][r]);
       const bool need = m_tile > m_run + kRescaleThreshold;
       const float m_new = need ? m_tile : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
@@ -560,21 +533,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       m_run = m_new;
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
 
-      // This warpgroup's 32 keys (selected with constant indices so that x
-      // stays in registers).
-      float pv[HN];
-#pragma unroll
-      for (int jj = 0; jj < HN; ++jj) pv[jj] = (wg == 0) ? x[jj] : x[jj + HN];
       if (MASK == kMaskAdditive) {
 #pragma unroll
-        for (int jj = 0; jj < HN; ++jj) pv[jj] = ex2_approx(pv[jj] - m_use);
+        for (int jj = 0; jj < HN; ++jj) x[jj] = ex2_approx(x[jj] - m_use);
       } else {
         const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
         for (int jj = 0; jj < HN; jj += 2) {
-          const float2 arg = fma2(make_float2(pv[jj], pv[jj + 1]), c2, nm2);
-          pv[jj] = ex2_approx(arg.x);
-          pv[jj + 1] = ex2_approx(arg.y);
+          const float2 arg = fma2(make_float2(x[jj], x[jj + 1]), c2, nm2);
+          x[jj] = ex2_approx(arg.x);
+          x[jj + 1] = ex2_approx(arg.y);
         }
       }
       uint32_t pk[HN / 2];
@@ -582,14 +550,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float2 xsum[2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
       for (int jj = 0; jj < HN; jj += 2) {
-        pk[jj >> 1] = ElemTraits<T>::pack(pv[jj], pv[jj + 1]);
+        pk[jj >> 1] = ElemTraits<T>::pack(x[jj], x[jj + 1]);
         lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], ElemTraits<T>::unpack(pk[jj >> 1]));
-        xsum[(jj >> 1) & 1] = add2(xsum[(jj >> 1) & 1], make_float2(pv[jj], pv[jj + 1]));
+        xsum[(jj >> 1) & 1] = add2(xsum[(jj >> 1) & 1], make_float2(x[jj], x[jj + 1]));
       }
       l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
                (lsum[3].x + lsum[3].y);
       lx_run += (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
-      tmem_st16(sbuf + L::p_col(wg), pk);
+      tmem_st16(lane_base + buf * 128 + wg * (HN / 2), pk);
       if (TANGENT) {
         float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         const float2 s2 = make_float2(s_scale, s_scale);
@@ -597,13 +565,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < HN; jj += 2) {
           const float2 ds = make_float2(__uint_as_float(da[jj]), __uint_as_float(da[jj + 1]));
-          const float2 pd = mul2(make_float2(pv[jj], pv[jj + 1]), mul2(ds, s2));
+          const float2 pd = mul2(make_float2(x[jj], x[jj + 1]), mul2(ds, s2));
           pdk[jj >> 1] = ElemTraits<T>::pack(pd.x, pd.y);
           msum[(jj >> 1) & 3] = add2(msum[(jj >> 1) & 3], ElemTraits<T>::unpack(pdk[jj >> 1]));
         }
         mu_run += (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
                   (msum[3].x + msum[3].y);
-        tmem_st16(sbuf + L::pd_col(wg), pdk);
+        tmem_st16(lane_base + buf * 128 + BN + wg * (HN / 2), pdk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -611,23 +579,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
-    // Combine the two halves' sums (both warpgroups hold the same m_run)
-    // through shared memory of the key ring, idle once every MMA is done.
-    float* xs = reinterpret_cast<float*>(smem + L::OFF_KDK);  // [2][3][128]
+    // Combine the two halves' sums (both warpgroups hold the same m_run).
     if (ok) {
-      xs[(wg * 3 + 0) * L::BM + r] = l_run;
-      xs[(wg * 3 + 1) * L::BM + r] = lx_run;
-      xs[(wg * 3 + 2) * L::BM + r] = mu_run;
+      ctrl->xsum[wg][0][r] = l_run;
+      ctrl->xsum[wg][1][r] = lx_run;
+      ctrl->xsum[wg][2][r] = mu_run;
       mbar_arrive(&ctrl->sums_ready);
       ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
     }
+    if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
     if (ok) {
       tc_fence_after();
-      const int o = wg ^ 1;
-      const float l_all = l_run + xs[(o * 3 + 0) * L::BM + r];
-      const float lx_all = lx_run + xs[(o * 3 + 1) * L::BM + r];
-      const float mu_all = mu_run + xs[(o * 3 + 2) * L::BM + r];
+      const float l_all = l_run + ctrl->xsum[wg ^ 1][0][r];
+      const float lx_all = lx_run + ctrl->xsum[wg ^ 1][1][r];
+      const float mu_all = mu_run + ctrl->xsum[wg ^ 1][2][r];
       const float inv_l = (l_all > 0.0f) ? 1.0f / l_all : 0.0f;
       const float mu_row = mu_all * inv_l;
       T* orow = static_cast<T*>(p.o) + static_cast<long long>(b) * p.so.b +

@@ -194,26 +194,6 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr_a, uint32_t taddr_b,
       : "r"(taddr_a), "r"(taddr_b)
       : "memory");
 }
-// Three 32-column loads under one wait.
-__device__ __forceinline__ void tmem_ld32x3(uint32_t ta, uint32_t tb, uint32_t tc,
-                                            uint32_t (&a)[32], uint32_t (&b)[32],
-                                            uint32_t (&c)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%96];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%97];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
-      "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%98];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : JVP_R8(a, 0), JVP_R8(a, 8), JVP_R8(a, 16), JVP_R8(a, 24), JVP_R8(b, 0), JVP_R8(b, 8),
-        JVP_R8(b, 16), JVP_R8(b, 24), JVP_R8(c, 0), JVP_R8(c, 8), JVP_R8(c, 16), JVP_R8(c, 24)
-      : "r"(ta), "r"(tb), "r"(tc)
-      : "memory");
-}
 #undef JVP_R8
 
 #define JVP_W8(a, i) "r"(a[i]), "r"(a[i + 1]), "r"(a[i + 2]), "r"(a[i + 3]), "r"(a[i + 4]), \
