@@ -28,9 +28,7 @@
 //   M3  [A | T]     += P~ [V | dV]            (N = 2D, A operand from TMEM)
 //   M4  T           += (P~ * dS) V            (N = D)
 // The MMA warp issues M1/M2 of tile t+1 before M3/M4 of tile t, so the
-// tensor core computes the next scores while the softmax warps work.  The
-// softmax publishes P~ and P~ * dS through separate barriers, so M3 starts as
-// soon as P~ is in TMEM.
+// tensor core computes the next scores while the softmax warps work.
 //
 // Rescaling is conditional: the row maximum used in the exponent is only
 // moved when a tile's maximum exceeds it by more than 2^8, so A, T, l and mu~
@@ -115,7 +113,7 @@ struct TcCtrl {
   uint64_t q_full;
   uint64_t kdk_full[NS], kdk_empty[NS];
   uint64_t vdv_full[NS], vdv_empty[NS];
-  uint64_t s_full[2], p_full[2], pd_full[2], max_ready[2];
+  uint64_t s_full[2], p_full[2], max_ready[2];
   uint64_t at_done, o_full, drain, sums_ready;
   uint32_t tmem_base;
   int abort;
@@ -272,7 +270,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
       mbar_init(&ctrl->p_full[s], kSoftmaxThreads);
-      mbar_init(&ctrl->pd_full[s], kSoftmaxThreads);
       mbar_init(&ctrl->max_ready[s], kSoftmaxThreads);
     }
     mbar_init(&ctrl->at_done, 1);
@@ -394,14 +391,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         const int buf = t & 1;
-        const int s = t % NS;
-        // The V tile has normally landed long ago; checking it first, while the
-        // queue still holds the score MMAs, keeps the check off the critical path.
-        if (!mbar_wait(&ctrl->vdv_full[s], (t / NS) & 1, abort)) {
+        if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
           ok = false;
           break;
         }
-        if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+        const int s = t % NS;
+        if (!mbar_wait(&ctrl->vdv_full[s], (t / NS) & 1, abort)) {
           ok = false;
           break;
         }
@@ -415,13 +410,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_ts(tmem + L::TM_A, p_tm + kk * 8, bd, IDESC_AT, (t > 0 || kk > 0) ? 1u : 0u);
         }
         if (TANGENT) {
-          // P~ * dS is published separately: M3 above runs while the softmax
-          // warps are still forming it.
-          if (!mbar_wait(&ctrl->pd_full[buf], (t >> 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < KSTEPS_N; ++kk) {
             const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
@@ -570,9 +558,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                (lsum[3].x + lsum[3].y);
       lx_run += (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
       tmem_st16(lane_base + buf * 128 + wg * (HN / 2), pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&ctrl->p_full[buf]);  // P~ ready: [A | T] += P~ [V | dV] can start
       if (TANGENT) {
         float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         const float2 s2 = make_float2(s_scale, s_scale);
@@ -587,10 +572,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mu_run += (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
                   (msum[3].x + msum[3].y);
         tmem_st16(lane_base + buf * 128 + BN + wg * (HN / 2), pdk);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&ctrl->pd_full[buf]);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctrl->p_full[buf]);
     }
 
     // ------------------------------------------------------------ epilogue
