@@ -189,6 +189,83 @@ def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
     return tuple(outs)
 
 
+def fwd_dual_host(q, k, v, dq, dk, dv, attn_mask: Optional[torch.Tensor] = None,
+                  is_causal: bool = False, scale: Optional[float] = None, chunks: int = 8,
+                  device=None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """fwd_dual for host-resident tensors, with copies overlapped with compute.
+
+    q, k, v, dq, dk, dv are CPU tensors [B, H, N, D] (pinned memory lets the
+    copies run asynchronously).  The batch*head pairs are split into
+    ``chunks`` groups; while the kernel runs on group c, group c+1 is copied
+    to the device and group c-1's outputs are copied back, on three streams
+    with two device staging slots.  Returns CPU tensors (O, tO), or fills
+    ``out``.  A mask must broadcast over batch and heads ([1, 1, Nq, Nk]).
+    """
+    dev = torch.device(device) if device is not None else torch.device("cuda",
+                                                                        torch.cuda.current_device())
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    for t in (q, k, v, dq, dk, dv):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("fwd_dual_host takes contiguous CPU tensors")
+    if attn_mask is not None and attn_mask.dim() == 4 and (attn_mask.shape[0] != 1 or
+                                                           attn_mask.shape[1] != 1):
+        raise ValueError("fwd_dual_host needs a mask shared by all batches and heads")
+    BH = B * H
+    chunks = max(1, min(int(chunks), BH))
+    size = (BH + chunks - 1) // chunks
+    ins = [t.view(BH, t.shape[2], D) for t in (q, k, v, dq, dk, dv)]
+    if out is None:
+        pin = q.is_pinned()
+        o_h = torch.empty((B, H, Nq, D), dtype=q.dtype, pin_memory=pin)
+        t_h = torch.empty((B, H, Nq, D), dtype=q.dtype, pin_memory=pin)
+    else:
+        o_h, t_h = out
+    outs = [o_h.view(BH, Nq, D), t_h.view(BH, Nq, D)]
+    mask_d = attn_mask.to(dev, non_blocking=True) if attn_mask is not None else None
+
+    main = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_in.wait_stream(main)
+    slots = [([torch.empty((1, size, x.shape[1], D), dtype=q.dtype, device=dev) for x in ins],
+              [torch.empty((1, size, Nq, D), dtype=q.dtype, device=dev) for _ in range(2)])
+             for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    for c in range(chunks):
+        lo, hi = c * size, min(BH, (c + 1) * size)
+        if lo >= hi:
+            break
+        n = hi - lo
+        sl = c % 2
+        dev_in, dev_out = slots[sl]
+        with torch.cuda.stream(s_in):
+            if c >= 2:
+                s_in.wait_event(computed[sl])  # the kernel of chunk c-2 has read this slot
+            for d_t, h_t in zip(dev_in, ins):
+                d_t[0, :n].copy_(h_t[lo:hi], non_blocking=True)
+            in_ready[sl].record(s_in)
+        main.wait_event(in_ready[sl])
+        if c >= 2:
+            main.wait_event(out_done[sl])  # chunk c-2's outputs have left this slot
+        with torch.cuda.stream(main):
+            args = [x[:, :n] for x in dev_in]
+            fwd_dual(*args, attn_mask=mask_d, is_causal=is_causal, scale=scale,
+                     out=(dev_out[0][:, :n], dev_out[1][:, :n]))
+            computed[sl].record(main)
+        s_out.wait_event(computed[sl])
+        with torch.cuda.stream(s_out):
+            for h_t, d_t in zip(outs, dev_out):
+                h_t[lo:hi].copy_(d_t[0, :n], non_blocking=True)
+            out_done[sl].record(s_out)
+    main.wait_stream(s_out)
+    for x in slots:  # keep the staging buffers alive until the streams are done
+        for t in x[0] + x[1]:
+            t.record_stream(main)
+    return o_h, t_h
+
+
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise the stream and return (and clear) the library's device status."""
     lib = _abi.load()

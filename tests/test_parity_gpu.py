@@ -272,3 +272,16 @@ def test_device_timeout_is_reported_and_the_context_survives():
     assert A.device_status(torch.cuda.default_stream()) == A._abi.JVP_ERR_DEVICE_TIMEOUT
     assert A.device_status(torch.cuda.default_stream()) == 0
     compare_full(synth.small("bf16", 1, 1, 64, 64, "none", seed=1), expect_path=1)
+
+
+def test_host_pipeline_matches_device_call():
+    # fwd_dual_host splits batch*heads into chunks and overlaps copies with compute;
+    # every (b, h) problem is computed by the same kernel, so results are bit-identical.
+    w = synth.small("bf16", 3, 5, 200, 128, "causal", seed=27)
+    inp = synth.make_inputs(w)
+    host = [x.pin_memory() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    o_h, t_h = A.fwd_dual_host(*host, is_causal=True, chunks=4)
+    torch.cuda.synchronize()
+    o_d, t_d = A.fwd_dual(*[x.cuda() for x in host], is_causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(t_h, t_d.cpu())
