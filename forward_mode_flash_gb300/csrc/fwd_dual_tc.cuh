@@ -114,7 +114,7 @@ struct TcCtrl {
   uint64_t kdk_full[NS], kdk_empty[NS];
   uint64_t vdv_full[NS], vdv_empty[NS];
   uint64_t s_full[2], p_full[2], max_ready[2];
-  uint64_t at_done, o_full, drain, sums_ready, q_empty, acc_free;
+  uint64_t at_done, o_full, drain, sums_ready;
   uint32_t tmem_base;
   int abort;
   float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
@@ -239,42 +239,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work items: heads are taken in groups sized to about one wave of CTAs,
+  // Work item: heads are taken in groups sized to about one wave of CTAs,
   // with the query tiles of a group innermost, so that the K/V of the heads in
-  // flight stay in L2.  Causal problems take their longest tiles first.  The
-  // CTAs are persistent: CTA c takes item r * gridDim.x + c in even rounds r
-  // and r * gridDim.x + (gridDim.x - 1 - c) in odd ones (a snake, so that
-  // causal tiles of different lengths even out across CTAs).
+  // flight stay in L2.  Causal problems take their longest tiles first.
   const int BH = p.B * p.H;
   const int nq = p.num_q_tiles;
   const int G = p.group_heads;
-  const int n_items = nq * BH;
-  struct Item {
-    int b, h, q0, n_kv;
-  };
-  auto item_at = [&](int round, Item* it) -> bool {
-    const int c = (round & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                              : static_cast<int>(blockIdx.x);
-    const long long idx = static_cast<long long>(round) * gridDim.x + c;
-    if (idx >= n_items) return false;
-    const int item = static_cast<int>(idx);
-    const int g = item / (G * nq);
-    const int rem = item - g * G * nq;
-    const int Gg = min(G, BH - g * G);
-    const int q_rank = rem / Gg;
-    const int bh = g * G + rem % Gg;
-    const int qt = (MASK == kMaskCausal) ? nq - 1 - q_rank : q_rank;
-    it->b = bh / p.H;
-    it->h = bh % p.H;
-    it->q0 = qt * L::BM;
-    int n_kv = (p.Nk + BN - 1) / BN;
-    if (MASK == kMaskCausal) {
-      const int last_row = min(it->q0 + L::BM, p.Nq) - 1;
-      n_kv = min(n_kv, last_row / BN + 1);
-    }
-    it->n_kv = n_kv;
-    return true;
-  };
+  const int g = blockIdx.x / (G * nq);
+  const int rem = blockIdx.x - g * G * nq;
+  const int Gg = min(G, BH - g * G);
+  const int q_rank = rem / Gg;
+  const int bh = g * G + rem % Gg;
+  const int qt = (MASK == kMaskCausal) ? nq - 1 - q_rank : q_rank;
+  const int b = bh / p.H, h = bh % p.H;
+  const int q0 = qt * L::BM;
+  int n_kv = (p.Nk + BN - 1) / BN;
+  if (MASK == kMaskCausal) {
+    const int last_row = min(q0 + L::BM, p.Nq) - 1;
+    n_kv = min(n_kv, last_row / BN + 1);
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
@@ -293,8 +276,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
     mbar_init(&ctrl->sums_ready, kSoftmaxThreads);
-    mbar_init(&ctrl->q_empty, 1);
-    mbar_init(&ctrl->acc_free, kSoftmaxThreads);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -318,62 +299,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&maps.dk);
         tma_prefetch_desc(&maps.dv);
       }
-      int k_fills = 0, v_fills = 0, q_fills = 0;  // fills issued so far (whole kernel)
-      Item it;
-      for (int round = 0; !*abort && item_at(round, &it); ++round) {
-        // Q and dQ of this item replace the previous item's once its last
-        // score MMAs are done.
-        if (round > 0 && !mbar_wait(&ctrl->q_empty, (round - 1) & 1, abort)) {
+      mbar_arrive_expect_tx(&ctrl->q_full, (TANGENT ? 2 : 1) * L::Q_BYTES);
+      for (int c = 0; c < L::KCH; ++c) {
+        tma_load_4d(smem + L::OFF_Q + c * L::BM * 128, &maps.q, &ctrl->q_full, c * 64, q0, h, b);
+        if (TANGENT)
+          tma_load_4d(smem + L::OFF_DQ + c * L::BM * 128, &maps.dq, &ctrl->q_full, c * 64, q0, h,
+                      b);
+      }
+      int k_fills = 0, v_fills = 0;  // ring fills issued so far
+      for (int t = 0; t < n_kv; ++t) {
+        const int s = t % NS;
+        const uint32_t ph = (t / NS) & 1;
+        const int j0 = t * BN;
+        if (!mbar_wait(&ctrl->kdk_empty[s], ph ^ 1, abort)) {
           record_timeout(p.status, abort);
           break;
         }
-        mbar_arrive_expect_tx(&ctrl->q_full, (TANGENT ? 2 : 1) * L::Q_BYTES);
+        uint8_t* kdk = smem + L::OFF_KDK + s * L::KDK_BYTES;
+        mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_BYTES);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(smem + L::OFF_Q + c * L::BM * 128, &maps.q, &ctrl->q_full, c * 64, it.q0,
-                      it.h, it.b);
+          tma_load_4d(kdk + c * L::KCHUNK_BYTES, &maps.k, &ctrl->kdk_full[s], c * 64, j0, h, b);
           if (TANGENT)
-            tma_load_4d(smem + L::OFF_DQ + c * L::BM * 128, &maps.dq, &ctrl->q_full, c * 64, it.q0,
-                        it.h, it.b);
+            tma_load_4d(kdk + c * L::KCHUNK_BYTES + BN * 128, &maps.dk, &ctrl->kdk_full[s], c * 64,
+                        j0, h, b);
         }
-        ++q_fills;
-        for (int t = 0; t < it.n_kv; ++t) {
-          const int s = k_fills % NS;
-          const uint32_t ph = (k_fills / NS) & 1;
-          const int j0 = t * BN;
-          if (!mbar_wait(&ctrl->kdk_empty[s], ph ^ 1, abort)) {
-            record_timeout(p.status, abort);
-            break;
-          }
-          uint8_t* kdk = smem + L::OFF_KDK + s * L::KDK_BYTES;
-          mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_BYTES);
-          for (int c = 0; c < L::KCH; ++c) {
-            tma_load_4d(kdk + c * L::KCHUNK_BYTES, &maps.k, &ctrl->kdk_full[s], c * 64, j0, it.h,
-                        it.b);
-            if (TANGENT)
-              tma_load_4d(kdk + c * L::KCHUNK_BYTES + BN * 128, &maps.dk, &ctrl->kdk_full[s],
-                          c * 64, j0, it.h, it.b);
-          }
-          ++k_fills;
-          if (!mbar_wait(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
-            record_timeout(p.status, abort);
-            break;
-          }
-          uint8_t* vdv = smem + L::OFF_VDV + s * L::VDV_BYTES;
-          mbar_arrive_expect_tx(&ctrl->vdv_full[s], L::VDV_BYTES);
-          for (int c = 0; c < L::KCH; ++c) {
-            tma_load_4d(vdv + c * L::VCHUNK_BYTES, &maps.v, &ctrl->vdv_full[s], c * 64, j0, it.h,
-                        it.b);
-            if (TANGENT)
-              tma_load_4d(vdv + (L::KCH + c) * L::VCHUNK_BYTES, &maps.dv, &ctrl->vdv_full[s],
-                          c * 64, j0, it.h, it.b);
-          }
-          ++v_fills;
+        ++k_fills;
+        if (!mbar_wait(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
+          record_timeout(p.status, abort);
+          break;
         }
+        uint8_t* vdv = smem + L::OFF_VDV + s * L::VDV_BYTES;
+        mbar_arrive_expect_tx(&ctrl->vdv_full[s], L::VDV_BYTES);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_4d(vdv + c * L::VCHUNK_BYTES, &maps.v, &ctrl->vdv_full[s], c * 64, j0, h, b);
+          if (TANGENT)
+            tma_load_4d(vdv + (L::KCH + c) * L::VCHUNK_BYTES, &maps.dv, &ctrl->vdv_full[s], c * 64,
+                        j0, h, b);
+        }
+        ++v_fills;
       }
       if (*abort) {
         // Let every copy already issued land before the CTA can exit.
         const int zero = 0;
-        if (q_fills > 0) mbar_wait(&ctrl->q_full, (q_fills - 1) & 1, &zero);
+        mbar_wait(&ctrl->q_full, 0, &zero);
         for (int t = max(0, k_fills - NS); t < k_fills; ++t)
           mbar_wait(&ctrl->kdk_full[t % NS], (t / NS) & 1, &zero);
         for (int t = max(0, v_fills - NS); t < v_fills; ++t)
@@ -383,17 +351,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = true;
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort);
+      if (!ok) record_timeout(p.status, abort);
+      tc_fence_after();
       const uint32_t sQ = smem_u32(smem + L::OFF_Q);
       const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
-      int gt = 0;  // tiles of earlier items (global tile index = gt + local t)
 
-      auto issue_scores = [&](int g) -> bool {
-        const int s = g % NS;
-        if (!mbar_wait(&ctrl->kdk_full[s], (g / NS) & 1, abort)) return false;
+      auto issue_scores = [&](int t) -> bool {
+        const int s = t % NS;
+        if (!mbar_wait(&ctrl->kdk_full[s], (t / NS) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t sK = smem_u32(smem + L::OFF_KDK + s * L::KDK_BYTES);
-        const uint32_t d_s = tmem + (g & 1) * 128;
+        const uint32_t d_s = tmem + (t & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS_D; ++kk) {
           const uint32_t off = (kk & 3) * 32;
@@ -411,72 +380,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         mma_commit(&ctrl->kdk_empty[s]);
-        mma_commit(&ctrl->s_full[g & 1]);
+        mma_commit(&ctrl->s_full[t & 1]);
         return true;
       };
 
-      Item it;
-      for (int round = 0; ok && item_at(round, &it); ++round) {
-        const int n_kv = it.n_kv;
-        if (!mbar_wait(&ctrl->q_full, round & 1, abort)) {
+      if (ok && n_kv > 0) ok = issue_scores(0);
+      for (int t = 0; ok && t < n_kv; ++t) {
+        if (t + 1 < n_kv && !issue_scores(t + 1)) {
+          ok = false;
+          break;
+        }
+        const int buf = t & 1;
+        if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const int s = t % NS;
+        if (!mbar_wait(&ctrl->vdv_full[s], (t / NS) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (!issue_scores(gt)) {
-          ok = false;
-          break;
+        const uint32_t sV = smem_u32(smem + L::OFF_VDV + s * L::VDV_BYTES);
+        const uint32_t p_tm = tmem + buf * 128;        // P~ (16-bit pairs)
+        const uint32_t pd_tm = tmem + buf * 128 + BN;  // P~ * dS (16-bit pairs)
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS_N; ++kk) {
+          const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
+          mma_ts(tmem + L::TM_A, p_tm + kk * 8, bd, IDESC_AT, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        if (n_kv == 1) mma_commit(&ctrl->q_empty);  // Q, dQ no longer read
-        for (int t = 0; t < n_kv; ++t) {
-          const int g = gt + t;
-          if (t + 1 < n_kv) {
-            if (!issue_scores(g + 1)) {
-              ok = false;
-              break;
-            }
-            if (t + 2 == n_kv) mma_commit(&ctrl->q_empty);
-          }
-          const int buf = g & 1;
-          if (!mbar_wait(&ctrl->p_full[buf], (g >> 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          const int s = g % NS;
-          if (!mbar_wait(&ctrl->vdv_full[s], (g / NS) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          // The first accumulator MMA of an item overwrites A and T: the
-          // previous item's epilogue must have read them.
-          if (t == 0 && round > 0 && !mbar_wait(&ctrl->acc_free, (round - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sV = smem_u32(smem + L::OFF_VDV + s * L::VDV_BYTES);
-          const uint32_t p_tm = tmem + buf * 128;        // P~ (16-bit pairs)
-          const uint32_t pd_tm = tmem + buf * 128 + BN;  // P~ * dS (16-bit pairs)
+        if (TANGENT) {
 #pragma unroll
           for (int kk = 0; kk < KSTEPS_N; ++kk) {
             const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
-            mma_ts(tmem + L::TM_A, p_tm + kk * 8, bd, IDESC_AT, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + L::TM_T, pd_tm + kk * 8, bd, IDESC_T, 1u);
           }
-          if (TANGENT) {
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS_N; ++kk) {
-              const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
-              mma_ts(tmem + L::TM_T, pd_tm + kk * 8, bd, IDESC_T, 1u);
-            }
-          }
-          mma_commit(&ctrl->vdv_empty[s]);
-          mma_commit(&ctrl->at_done);
         }
-        if (!ok) break;
-        mma_commit(&ctrl->o_full);  // this item's A and T are complete
-        gt += n_kv;
+        mma_commit(&ctrl->vdv_empty[s]);
+        mma_commit(&ctrl->at_done);
       }
-      if (!ok) record_timeout(p.status, abort);
+      if (ok) {
+        mma_commit(&ctrl->o_full);
+      } else {
+        record_timeout(p.status, abort);
+      }
       // Drain: every MMA this thread issued completes before TMEM is freed.
       mma_commit(&ctrl->drain);
       const int zero = 0;
@@ -490,21 +437,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int wg = (warp - 2) >> 2;
     const int sub = warp & 3;
     const int r = sub * 32 + lane;
+    const int i = q0 + r;
+    const bool row_ok = i < p.Nq;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
     const int cofs = wg * HN;
     const float c = p.scale_log2;
     const float s_scale = p.scale;
-    bool ok = true;
-    int gt = 0;  // tiles of earlier items
-    Item item;
-    for (int round = 0; ok && item_at(round, &item); ++round) {
-    const int b = item.b, h = item.h, q0 = item.q0, n_kv = item.n_kv;
-    const int i = q0 + r;                     // query row
-    const bool row_ok = i < p.Nq;
     float m_run = -INFINITY;  // running max, log2 units of the scaled logits (whole row)
     float l_run = 0.0f;       // this half's sum of p~ as rounded for the MMA
     float lx_run = 0.0f;      // this half's sum of p~ in fp32 (for the log-sum-exp)
     float mu_run = 0.0f;      // this half's sum of p~ * dS as rounded for the MMA
+    bool ok = true;
 
     const void* mrow = nullptr;
     if (MASK == kMaskBool || MASK == kMaskAdditive) {
@@ -516,12 +459,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     for (int t = 0; t < n_kv; ++t) {
-      const int g = gt + t;  // global tile index (barrier phases)
-      const int buf = g & 1;
+      const int buf = t & 1;
       const int j0 = t * BN + cofs;  // first key of this half tile
       MaskRegs<MASK, HN> mreg;
       if (row_ok) mreg.load(p, mrow, j0);
-      if (!warp_wait(&ctrl->s_full[buf], (g >> 1) & 1, p.status, abort)) {
+      if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
         ok = false;
         break;
       }
@@ -559,7 +501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Exchange the half-row maxima between the two warpgroups.
       ctrl->xmax[buf][wg][r] = m_half;
       mbar_arrive(&ctrl->max_ready[buf]);
-      if (!warp_wait(&ctrl->max_ready[buf], (g >> 1) & 1, p.status, abort)) {
+      if (!warp_wait(&ctrl->max_ready[buf], (t >> 1) & 1, p.status, abort)) {
         ok = false;
         break;
       }
@@ -573,7 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (t > 0 && __any_sync(0xffffffffu, need)) {
         // A and T hold tile t-1's contributions once its MMAs are done; each
         // warpgroup rescales half of the [A | T] columns of its rows.
-        if (!warp_wait(&ctrl->at_done, (g - 1) & 1, p.status, abort)) {
+        if (!warp_wait(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
           ok = false;
           break;
         }
@@ -638,16 +580,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ------------------------------------------------------------ epilogue
     // Combine the two halves' sums (both warpgroups hold the same m_run).
-    if (!ok) break;
-    gt += n_kv;
     if (ok) {
       ctrl->xsum[wg][0][r] = l_run;
       ctrl->xsum[wg][1][r] = lx_run;
       ctrl->xsum[wg][2][r] = mu_run;
       mbar_arrive(&ctrl->sums_ready);
-      ok = warp_wait(&ctrl->sums_ready, round & 1, p.status, abort);
+      ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
     }
-    if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, round & 1, p.status, abort);
+    if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
     if (ok) {
       tc_fence_after();
       const float l_all = l_run + ctrl->xsum[wg ^ 1][0][r];
@@ -704,11 +644,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           p.lse[ridx] = (lx_all > 0.0f) ? (m_run + log2f(lx_all)) * kLn2 : -INFINITY;
         if (TANGENT && p.mu) p.mu[ridx] = mu_row;
       }
-      // A and T have been read: the next item's first accumulator MMA may go.
-      tc_fence_before();
-      mbar_arrive(&ctrl->acc_free);
     }
-    }  // items
     tc_fence_before();
   }
 
@@ -733,8 +669,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done |= 1ull << dev;
   }
-  const long long items = static_cast<long long>(p.num_q_tiles) * p.B * p.H;
-  const long long grid = items < p.num_ctas ? items : p.num_ctas;  // persistent CTAs
+  const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H;
   kern<<<static_cast<unsigned>(grid), kTcThreads, L::SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }

@@ -257,7 +257,6 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     p.num_q_tiles = static_cast<int>((Nq + kTcBlockM - 1) / kTcBlockM);
     // About one wave of CTAs per group of heads (one CTA per SM).
     p.group_heads = std::max(1, std::min(static_cast<int>(B * H), dev->num_sms / p.num_q_tiles));
-    p.num_ctas = dev->num_sms;
     err = launch_fwd_tc(static_cast<DType>(dtype), static_cast<int>(D), kind, tangent, maps, p,
                         stream);
     t_last_path = 1;

@@ -20,7 +20,6 @@ struct FwdParams {
   int B, H, Nq, Nk, D;
   int num_q_tiles;
   int group_heads;   // tensor-core kernel: (batch, head) pairs per scheduling group
-  int num_ctas;      // tensor-core kernel: persistent CTAs (at most one per SM)
   float scale;       // logit scale s
   float scale_log2;  // s * log2(e)
   const void* mask;  // uint8 (bool) or float (additive); nullptr otherwise
