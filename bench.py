@@ -46,6 +46,8 @@ def parse():
                     help="target length of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mode", default="fwd_dual", choices=["fwd_dual", "bwd_dual"],
+                    help="fwd_dual (the headline) or the backward of the dual computation")
     return ap.parse_args()
 
 
@@ -196,6 +198,92 @@ def run_reference(args, rank, world):
     return 0
 
 
+FP32_LANES_PER_SM = 128  # CUDA-core fp32 FMA lanes per SM (4 partitions x 32)
+
+
+def run_bwd(args, rank, world, local):
+    """Times jvp_attn_bwd_dual (three CUDA-core kernels) on one workload."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from forward_mode_flash_gb300 import api, build, replicas, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    name = args.workload if args.workload != DEFAULT_WORKLOAD else "f16_b2h8n2048d64_causal"
+    w = synth.WORKLOADS[name]
+    causal = w.mask == "causal"
+    inp = synth.make_inputs(w, with_cotangents=True, device=str(dev))
+    g = [inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv]
+    o, t_o, lse, mu = api.fwd_dual(*g, attn_mask=inp.mask, is_causal=causal, return_stats=True)
+    ws = torch.empty(max(1, api.bwd_dual_workspace_size(w.B, w.H, w.N, w.N, w.D)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        return api.bwd_dual(*g, o, t_o, lse, mu, inp.g_o, inp.g_to, attn_mask=inp.mask,
+                            is_causal=causal, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        for s in range(args.steps):
+            flush.fill_(float(s))
+            starts[s].record(stream)
+            step()
+            ends[s].record(stream)
+        torch.cuda.synchronize()
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = replicas.max_over_ranks(sum(per_ms), device=dev)
+    ms_step = total_ms / args.steps
+    half = 0.5 if causal else 1.0
+    bhnnd = w.B * w.H * w.N * w.N * w.D * half
+    alg_flops = 30.0 * bhnnd       # the 15 N x N x D products of the reverse mode
+    exec_flops = 42.0 * bhnnd      # the 21 products these kernels execute (scores recomputed)
+    value = replicas.aggregate_throughput(world, alg_flops, args.steps, total_ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+    clk = pk.get("sm_max_mhz", 2070.0) * 1e6
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = n_sms * FP32_LANES_PER_SM * 2 * clk / 1e12
+    achieved = exec_flops / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": "bwd_dual (reverse mode of fwd+JVP attention) TFLOP/s", "mode": "bwd_dual",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "mask": w.mask,
+                   "input_dtype": w.dtype, "algorithmic_flops_per_step": alg_flops,
+                   "executed_flops_per_step": exec_flops,
+                   "l2": "flushed: 256 MiB written between timed steps (outside the events)"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": achieved / alu_peak, "traffic": None,
+                     "peak_source": f"{n_sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 x "
+                                    f"{clk / 1e6:.0f} MHz (CUDA-core fp32)",
+                     "kernel": "bwd_keys_kernel + bwd_queries_kernel + bwd_rows_kernel"},
+        "clocks": clocks.summary(), "gpu_launches": 3 * args.steps, "e2e": None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # The float64 oracle's reverse mode on one whole head of the same workload.
+        x = [t[:1, :1].double().cpu().numpy() for t in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv,
+                                                         inp.g_o, inp.g_to)]
+        t0 = time.perf_counter()
+        oracle.bwd_dual(*x, w.mask, None)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 30.0 * w.N * w.N * w.D * half / dt / 1e12,
+                                "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                "sample": f"one (b, h) head of {name}, float64 reverse mode, "
+                                          f"{dt:.1f} s wall (the oracle threads over heads)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -215,6 +303,12 @@ def main():
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
+    if args.mode == "bwd_dual":
+        rc = run_bwd(args, rank, world, local)
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return rc
     build.build()
 
     w = synth.WORKLOADS[args.workload]
