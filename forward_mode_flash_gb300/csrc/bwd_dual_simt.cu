@@ -406,7 +406,28 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t stream) {
   return e;
 }
 
+template <typename T>
+cudaError_t launch_rows_only(const BwdParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
+  const long long row_blocks = (rows * 32 + kThreads - 1) / kThreads;
+  if (row_blocks == 0) return cudaSuccess;
+  bwd_rows_kernel<T><<<static_cast<unsigned>(row_blocks), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_rows(DType dt, const BwdParams& p, cudaStream_t stream) {
+  switch (dt) {
+    case kF32:
+      return launch_rows_only<float>(p, stream);
+    case kF16:
+      return launch_rows_only<__half>(p, stream);
+    case kBF16:
+      return launch_rows_only<__nv_bfloat16>(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_bwd_simt(DType dt, const BwdParams& p, cudaStream_t stream) {
   switch (dt) {

@@ -1,0 +1,844 @@
+// bwd_dual_tc.cuh -- tensor-core kernels (tcgen05 + TMEM + TMA) for the
+// reverse mode of the dual computation, fp16/bf16 inputs, fp32 accumulation.
+//
+// With P = exp(S - lse) recomputed from the saved log-sum-exp, the backward
+// needs no online softmax: every (row, key) term is independent once the
+// per-row scalars lse, mu, nu = gtO.O and delta = gO.O + gtO.tO - mu*nu are
+// known.  Per (b, h):
+//   dS  = s (dQ K^T + Q dK^T)     G = gtO V^T     gP1 = gO V^T + gtO dV^T
+//   gP  = gP1 + G (dS - mu) - nu dS
+//   gS  = P (gP - delta)          g_dS = P (G - nu)          dP = P (dS - mu)
+//   gQ  = s (gS K + g_dS dK)      g_dQ = s g_dS K
+//   gK  = s (gS^T Q + g_dS^T dQ)  g_dK = s g_dS^T Q
+//   gV  = P^T gO + dP^T gtO       g_dV = P^T gtO
+//
+// Query-major kernel (gQ, g_dQ): one CTA per 128-row query tile, looping over
+// 64-key tiles; like the forward, the score products take their A operands
+// (Q, dQ, gO, gtO) from shared memory:
+//   [S | Q dK^T]      = Q   [K ; dK]^T      then  Q dK^T += dQ K^T
+//   [G | gtO dV^T]    = gtO [V ; dV]^T      then  gtO dV^T += gO V^T   (= gP1)
+// the elementwise warps turn each 64-key tile into gS and g_dS (16-bit, in
+// TMEM over the S columns they read), and
+//   [g_dQ | gQ] += g_dS [K | dK]            then  gQ += gS K
+// with the same shared-memory K/dK tile read as an MN-major operand.
+//
+// Key-major kernel (gK, g_dK, gV, g_dV): one CTA per 128-key tile, looping over
+// 64-row query tiles, with the transposed scores (TMEM lanes = keys):
+//   [S^T | K dQ^T]    = K [Q ; dQ]^T        then  K dQ^T += dK Q^T
+//   [G^T | V gO^T]    = V [gtO ; gO]^T      then  V gO^T += dV gtO^T   (= gP1^T)
+//   [g_dV | gV] += P^T [gtO | gO],  gV += dP^T gtO
+//   [g_dK | gK] += g_dS^T [Q | dQ], gK += gS^T Q
+// At D = 128 the four key-side accumulators do not fit TMEM next to the
+// scores, so the key-major kernel runs twice (value part, key part).
+//
+// Each kernel: warp 0 TMA producer, warp 1 TMEM allocator + single-thread MMA
+// issuer, warps 2..9 two elementwise warpgroups (each owns half of the 64
+// columns of a tile, a thread owns a TMEM lane).  Every wait is bounded.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "fwd_dual_tc.cuh"
+
+namespace jvp {
+
+constexpr int kBwdThreads = 64 + 256;
+
+// ----------------------------------------------------------------------------
+// Query-major kernel.
+template <int D>
+struct BqLayout {
+  static constexpr int BM = 128;  // query rows per CTA
+  static constexpr int BN = 64;   // keys per tile
+  static constexpr int KCH = D / 64;
+  static constexpr int NS = (D == 64) ? 3 : 1;
+  static constexpr int QT_BYTES = KCH * BM * 128;  // one [128 x D] query-side tile
+  static constexpr int KCHUNK = 2 * BN * 128;      // [K rows | dK rows] of one 64-column chunk
+  static constexpr int KBLK = KCH * KCHUNK;        // [K ; dK] block of one stage
+  static constexpr int OFF_Q = 0, OFF_DQ = QT_BYTES, OFF_GO = 2 * QT_BYTES, OFF_GTO = 3 * QT_BYTES;
+  static constexpr int OFF_K = 4 * QT_BYTES;
+  static constexpr int OFF_V = OFF_K + NS * KBLK;
+  static constexpr int OFF_CTRL = OFF_V + NS * KBLK;
+  static constexpr int CTRL_BYTES = 512;
+  static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
+  // TMEM columns
+  static constexpr uint32_t TM_S = 0, TM_DS = 64, TM_G = 128, TM_GP = 192, TM_ACC = 256;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+template <int NS>
+struct BwdCtrl {
+  uint64_t q_full;
+  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t s_full, p_full, o_full, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Per-(row, key) backward terms from the score-side values.  keep = false
+// gives all-zero terms (masked key, or a row that keeps no key).
+struct BwdTerms {
+  float gS, gdS, P, dP;
+};
+__device__ __forceinline__ BwdTerms bwd_terms(bool keep, float x_log2, float lse2, float ds_raw,
+                                              float g, float gp1, float s, float mu, float nu,
+                                              float delta) {
+  BwdTerms r;
+  const float P = keep ? ex2_approx(x_log2 - lse2) : 0.0f;
+  const float dS = s * ds_raw;
+  const float gP = fmaf(g, dS - mu, gp1) - nu * dS;
+  r.P = P;
+  r.dP = P * (dS - mu);
+  r.gS = P * (gP - delta);
+  r.gdS = P * (g - nu);
+  return r;
+}
+
+template <typename T, int D, int MASK>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_q_tc_kernel(const __grid_constant__ BwdTcMaps maps, const BwdParams p, int group_heads,
+                    unsigned int* status) {
+  using L = BqLayout<D>;
+  constexpr int NS = L::NS, BN = L::BN, BM = L::BM;
+  constexpr bool kBF16 = ElemTraits<T>::kBF16;
+  constexpr int KSD = D / 16;   // K-steps over the head dimension
+  constexpr int KSN = BN / 16;  // K-steps over a key tile
+  constexpr uint32_t I_N128 = idesc_f16(kBF16, 128, 128, false);
+  constexpr uint32_t I_N64 = idesc_f16(kBF16, 128, 64, false);
+  constexpr uint32_t I_ACC2 = idesc_f16(kBF16, 128, 2 * D, true);  // D = 64: [g_dQ | gQ]
+  constexpr uint32_t I_ACC1 = idesc_f16(kBF16, 128, D, true);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  static_assert(sizeof(BwdCtrl<NS>) <= L::CTRL_BYTES, "control block budget");
+  BwdCtrl<NS>* ctrl = reinterpret_cast<BwdCtrl<NS>*>(smem + L::OFF_CTRL);
+  volatile int* abort = &ctrl->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int BH = p.B * p.H;
+  const int nq = (p.Nq + BM - 1) / BM;
+  const int G = group_heads;
+  const int g = blockIdx.x / (G * nq);
+  const int rem = blockIdx.x - g * G * nq;
+  const int Gg = min(G, BH - g * G);
+  const int q_rank = rem / Gg;
+  const int bh = g * G + rem % Gg;
+  const int qt = (MASK == kMaskCausal) ? nq - 1 - q_rank : q_rank;
+  const int b = bh / p.H, h = bh % p.H;
+  const int q0 = qt * BM;
+  int n_kv = (p.Nk + BN - 1) / BN;
+  if (MASK == kMaskCausal) n_kv = min(n_kv, (min(q0 + BM, p.Nq) - 1) / BN + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&ctrl->k_full[s], 1);
+      mbar_init(&ctrl->k_empty[s], 1);
+      mbar_init(&ctrl->v_full[s], 1);
+      mbar_init(&ctrl->v_empty[s], 1);
+    }
+    mbar_init(&ctrl->s_full, 1);
+    mbar_init(&ctrl->p_full, 256);
+    mbar_init(&ctrl->o_full, 1);
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&ctrl->q_full, 4 * L::QT_BYTES);
+      for (int c = 0; c < L::KCH; ++c) {
+        const int o = c * BM * 128;
+        tma_load_4d(smem + L::OFF_Q + o, &maps.q, &ctrl->q_full, c * 64, q0, h, b);
+        tma_load_4d(smem + L::OFF_DQ + o, &maps.dq, &ctrl->q_full, c * 64, q0, h, b);
+        tma_load_4d(smem + L::OFF_GO + o, &maps.go, &ctrl->q_full, c * 64, q0, h, b);
+        tma_load_4d(smem + L::OFF_GTO + o, &maps.gto, &ctrl->q_full, c * 64, q0, h, b);
+      }
+      int kf = 0, vf = 0;
+      for (int t = 0; t < n_kv; ++t) {
+        const int s = t % NS;
+        const uint32_t ph = (t / NS) & 1;
+        const int j0 = t * BN;
+        if (!mbar_wait(&ctrl->k_empty[s], ph ^ 1, abort)) {
+          record_timeout(status, abort);
+          break;
+        }
+        uint8_t* kb = smem + L::OFF_K + s * L::KBLK;
+        mbar_arrive_expect_tx(&ctrl->k_full[s], L::KBLK);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_4d(kb + c * L::KCHUNK, &maps.k, &ctrl->k_full[s], c * 64, j0, h, b);
+          tma_load_4d(kb + c * L::KCHUNK + BN * 128, &maps.dk, &ctrl->k_full[s], c * 64, j0, h, b);
+        }
+        ++kf;
+        if (!mbar_wait(&ctrl->v_empty[s], ph ^ 1, abort)) {
+          record_timeout(status, abort);
+          break;
+        }
+        uint8_t* vb = smem + L::OFF_V + s * L::KBLK;
+        mbar_arrive_expect_tx(&ctrl->v_full[s], L::KBLK);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_4d(vb + c * L::KCHUNK, &maps.v, &ctrl->v_full[s], c * 64, j0, h, b);
+          tma_load_4d(vb + c * L::KCHUNK + BN * 128, &maps.dv, &ctrl->v_full[s], c * 64, j0, h, b);
+        }
+        ++vf;
+      }
+      if (*abort) {
+        const int zero = 0;
+        mbar_wait(&ctrl->q_full, 0, &zero);
+        for (int t = max(0, kf - NS); t < kf; ++t)
+          mbar_wait(&ctrl->k_full[t % NS], (t / NS) & 1, &zero);
+        for (int t = max(0, vf - NS); t < vf; ++t)
+          mbar_wait(&ctrl->v_full[t % NS], (t / NS) & 1, &zero);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort);
+      tc_fence_after();
+      const uint32_t aQ = smem_u32(smem + L::OFF_Q), adQ = smem_u32(smem + L::OFF_DQ);
+      const uint32_t aGO = smem_u32(smem + L::OFF_GO), aGTO = smem_u32(smem + L::OFF_GTO);
+      for (int t = 0; ok && t < n_kv; ++t) {
+        const int s = t % NS;
+        const uint32_t ph = (t / NS) & 1;
+        if (!mbar_wait(&ctrl->k_full[s], ph, abort) || !mbar_wait(&ctrl->v_full[s], ph, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + L::OFF_K + s * L::KBLK);
+        const uint32_t vb = smem_u32(smem + L::OFF_V + s * L::KBLK);
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // [S | Q dK^T] = Q [K ; dK]^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_S, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + off, 16, 1024),
+                 sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N128, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // Q dK^T += dQ K^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_DS, sdesc_sw128(adQ + (kk >> 2) * BM * 128 + off, 16, 1024),
+                 sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // [G | gtO dV^T] = gtO [V ; dV]^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_G, sdesc_sw128(aGTO + (kk >> 2) * BM * 128 + off, 16, 1024),
+                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N128, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // gtO dV^T += gO V^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_GP, sdesc_sw128(aGO + (kk >> 2) * BM * 128 + off, 16, 1024),
+                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
+        }
+        mma_commit(&ctrl->v_empty[s]);
+        mma_commit(&ctrl->s_full);
+        if (!mbar_wait(&ctrl->p_full, t & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // gS and g_dS of keys [16 kk, 16 kk + 16): written by warpgroup kk / 2.
+#pragma unroll
+        for (int kk = 0; kk < KSN; ++kk) {
+          const uint32_t a_gs = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+          const uint32_t a_gds = a_gs + 16;
+          const uint32_t kx = kb + kk * 16 * 128;  // MN-major: 16 keys per K-step
+          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+          if (D == 64) {
+            // [g_dQ | gQ] += g_dS [K | dK]  (K and dK chunks 8 KB apart)
+            mma_ts(tmem + L::TM_ACC, a_gds, sdesc_sw128(kx, BN * 128, 1024), I_ACC2, acc);
+          } else {
+            // g_dQ += g_dS K ; gQ += g_dS dK  (chunks of one tensor 16 KB apart)
+            mma_ts(tmem + L::TM_ACC, a_gds, sdesc_sw128(kx, L::KCHUNK, 1024), I_ACC1, acc);
+            mma_ts(tmem + L::TM_ACC + D, a_gds, sdesc_sw128(kx + BN * 128, L::KCHUNK, 1024),
+                   I_ACC1, acc);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSN; ++kk) {  // gQ += gS K
+          const uint32_t a_gs = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+          mma_ts(tmem + L::TM_ACC + D, a_gs,
+                 sdesc_sw128(kb + kk * 16 * 128, D == 64 ? BN * 128 : L::KCHUNK, 1024), I_ACC1,
+                 1u);
+        }
+        mma_commit(&ctrl->k_empty[s]);
+      }
+      if (ok) mma_commit(&ctrl->o_full);
+      if (!ok) record_timeout(status, abort);
+      mma_commit(&ctrl->drain);
+      const int zero = 0;
+      mbar_wait(&ctrl->drain, 0, &zero);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int wg = (warp - 2) >> 2;
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;
+    const int i = q0 + r;
+    const bool row_ok = i < p.Nq;
+    const uint32_t lb = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    const long long ridx = static_cast<long long>(bh) * p.Nq + (row_ok ? i : 0);
+    const float lse = row_ok ? p.lse[ridx] : -INFINITY;
+    const float lse2 = lse * kLog2e;
+    const bool live = row_ok && lse != -INFINITY;
+    const float mu = row_ok ? p.mu[ridx] : 0.f;
+    const float nu = row_ok ? p.nu[ridx] : 0.f;
+    const float delta = row_ok ? p.delta[ridx] : 0.f;
+    const float c = p.scale * kLog2e;
+    const float s = p.scale;
+    bool ok = true;
+    const void* mrow = nullptr;
+    if (MASK == kMaskBool || MASK == kMaskAdditive) {
+      const long long off = static_cast<long long>(b) * p.msb + static_cast<long long>(h) * p.msh +
+                            static_cast<long long>(row_ok ? i : 0) * p.msq;
+      mrow = (MASK == kMaskBool)
+                 ? static_cast<const void*>(static_cast<const uint8_t*>(p.mask) + off)
+                 : static_cast<const void*>(static_cast<const float*>(p.mask) + off);
+    }
+    // The row-scalar loads above are plain global reads of the workspace and
+    // outputs of earlier kernels on this stream.
+    FwdParams mp{};  // only the mask fields are used by MaskRegs
+    mp.Nk = p.Nk;
+    mp.msk = p.msk;
+    mp.mask_vec = 0;
+    for (int t = 0; t < n_kv; ++t) {
+      const int j0 = t * BN + wg * 32;
+      MaskRegs<MASK, 32> mreg;
+      if (row_ok) mreg.load(mp, mrow, j0);
+      if (!warp_wait(&ctrl->s_full, t & 1, status, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t rs[32], rds[32], rg[32], rgp[32];
+      tmem_ld32x2(lb + L::TM_S + wg * 32, lb + L::TM_DS + wg * 32, rs, rds);
+      tmem_ld32x2(lb + L::TM_G + wg * 32, lb + L::TM_GP + wg * 32, rg, rgp);
+      uint32_t pgs[16], pgds[16];
+#pragma unroll
+      for (int jj = 0; jj < 32; jj += 2) {
+        float gs[2], gds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = j0 + jj + e;
+          bool keep = live && j < p.Nk;
+          float x = __uint_as_float(rs[jj + e]) * c;
+          if constexpr (MASK == kMaskCausal) keep = keep && j <= i;
+          if constexpr (MASK == kMaskBool) keep = keep && mreg.keep(jj + e);
+          if constexpr (MASK == kMaskAdditive) {
+            x = fmaf(mreg.a[jj + e], kLog2e, x);
+            keep = keep && x != -INFINITY;
+          }
+          const BwdTerms bt =
+              bwd_terms(keep, x, lse2, __uint_as_float(rds[jj + e]), __uint_as_float(rg[jj + e]),
+                        __uint_as_float(rgp[jj + e]), s, mu, nu, delta);
+          gs[e] = bt.gS;
+          gds[e] = bt.gdS;
+        }
+        pgs[jj >> 1] = ElemTraits<T>::pack(gs[0], gs[1]);
+        pgds[jj >> 1] = ElemTraits<T>::pack(gds[0], gds[1]);
+      }
+      tmem_st16(lb + wg * 32, pgs);        // gS over this warpgroup's S columns
+      tmem_st16(lb + wg * 32 + 16, pgds);  // g_dS next to it
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctrl->p_full);
+    }
+    if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, status, abort);
+    if (ok) {
+      tc_fence_after();
+      // Warpgroup 0 writes g_dQ, warpgroup 1 writes gQ (both scaled by s).
+      void* dst = wg == 0 ? p.g_dq : p.g_q;
+      const Strides& ds = wg == 0 ? p.sgdq : p.sgq;
+      T* row = static_cast<T*>(dst) + static_cast<long long>(b) * ds.b +
+               static_cast<long long>(h) * ds.h + static_cast<long long>(row_ok ? i : 0) * ds.n;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t a[32];
+        if (n_kv > 0) {
+          tmem_ld32(lb + L::TM_ACC + wg * D + col, a);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = 0u;
+        }
+        uint32_t po[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          po[e >> 1] = ElemTraits<T>::pack(__uint_as_float(a[e]) * s, __uint_as_float(a[e + 1]) * s);
+        if (row_ok) {
+          uint4* od = reinterpret_cast<uint4*>(row + col);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Key-major kernel.  PART: 3 = all four key-side gradients (D = 64),
+// 1 = value part (gV, g_dV), 2 = key part (gK, g_dK).
+template <int D, int PART>
+struct BkLayout {
+  static constexpr bool kV = (PART & 1) != 0;
+  static constexpr bool kK = (PART & 2) != 0;
+  static constexpr int BK = 128;  // keys per CTA
+  static constexpr int BQ = 64;   // query rows per tile
+  static constexpr int KCH = D / 64;
+  static constexpr int KT_BYTES = KCH * BK * 128;  // one [128 x D] key-side tile
+  static constexpr int QCHUNK = 2 * BQ * 128;      // [X rows | Y rows] of one 64-column chunk
+  static constexpr int QBLK = KCH * QCHUNK;        // a [X ; Y] block of one stage
+  // key-side tiles resident for the whole CTA: K and dK always, V and dV for the key part
+  static constexpr int OFF_K = 0, OFF_DK = KT_BYTES;
+  static constexpr int OFF_V = 2 * KT_BYTES, OFF_DV = 3 * KT_BYTES;
+  static constexpr int KSIDE = (kK ? 4 : 2) * KT_BYTES;
+  // per stage: [Q ; dQ], [gtO ; gO] and the row scalars (lse, mu, nu, delta) x 64 rows
+  static constexpr int STAGE = 2 * QBLK + 1024;
+  static constexpr int NS = (227 * 1024 - KSIDE - 2048) / STAGE >= 3 ? 3
+                            : (227 * 1024 - KSIDE - 2048) / STAGE;
+  static constexpr int OFF_ST = KSIDE;
+  static constexpr int OFF_CTRL = OFF_ST + NS * STAGE;
+  static constexpr int CTRL_BYTES = 512;
+  static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
+  // TMEM columns: transposed scores, then the accumulators
+  static constexpr uint32_t TM_S = 0, TM_DS = 64, TM_G = 128, TM_GP = 192, TM_ACC = 256;
+  static_assert(NS >= 1, "at least one stage");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(D == 64 || PART != 3, "the four accumulators fit TMEM only at D = 64");
+};
+
+template <int NS>
+struct BwdKCtrl {
+  uint64_t k_full;
+  uint64_t q_full[NS], q_empty[NS];
+  uint64_t s_full, p_full, o_full, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <typename T, int D, int MASK, int PART>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_k_tc_kernel(const __grid_constant__ BwdTcMaps maps, const BwdParams p, int group_heads,
+                    unsigned int* status) {
+  using L = BkLayout<D, PART>;
+  constexpr int NS = L::NS, BK = L::BK, BQ = L::BQ;
+  constexpr bool kBF16 = ElemTraits<T>::kBF16;
+  constexpr int KSD = D / 16;
+  constexpr int KSQ = BQ / 16;
+  constexpr uint32_t I_N128 = idesc_f16(kBF16, 128, 128, false);
+  constexpr uint32_t I_N64 = idesc_f16(kBF16, 128, 64, false);
+  constexpr uint32_t I_ACC2 = idesc_f16(kBF16, 128, 2 * D, true);
+  constexpr uint32_t I_ACC1 = idesc_f16(kBF16, 128, D, true);
+  // Accumulator columns (relative to TM_ACC)
+  constexpr uint32_t A_GDV = 0, A_GV = D;                        // value part
+  constexpr uint32_t A_GDK = L::kV ? 2 * D : 0, A_GK = A_GDK + D;  // key part
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  static_assert(sizeof(BwdKCtrl<NS>) <= L::CTRL_BYTES, "control block budget");
+  BwdKCtrl<NS>* ctrl = reinterpret_cast<BwdKCtrl<NS>*>(smem + L::OFF_CTRL);
+  volatile int* abort = &ctrl->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int BH = p.B * p.H;
+  const int nk = (p.Nk + BK - 1) / BK;
+  const int G = group_heads;
+  const int g = blockIdx.x / (G * nk);
+  const int rem = blockIdx.x - g * G * nk;
+  const int Gg = min(G, BH - g * G);
+  const int k_rank = rem / Gg;
+  const int bh = g * G + rem % Gg;
+  const int kt = k_rank;  // causal: the first key tiles see the most query rows
+  const int b = bh / p.H, h = bh % p.H;
+  const int j0 = kt * BK;
+  const int nqt = (p.Nq + BQ - 1) / BQ;
+  const int t_begin = (MASK == kMaskCausal) ? min(j0 / BQ, nqt) : 0;  // rows i >= j0 only
+  const int n_t = nqt - t_begin;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->k_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&ctrl->q_full[s], 1);
+      mbar_init(&ctrl->q_empty[s], 1);
+    }
+    mbar_init(&ctrl->s_full, 1);
+    mbar_init(&ctrl->p_full, 256);
+    mbar_init(&ctrl->o_full, 1);
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+  const long long rbase = static_cast<long long>(bh) * p.Nq;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&ctrl->k_full, (L::kK ? 4 : 2) * L::KT_BYTES);
+      for (int c = 0; c < L::KCH; ++c) {
+        const int o = c * BK * 128;
+        tma_load_4d(smem + L::OFF_K + o, &maps.k, &ctrl->k_full, c * 64, j0, h, b);
+        tma_load_4d(smem + L::OFF_DK + o, &maps.dk, &ctrl->k_full, c * 64, j0, h, b);
+        if (L::kK) {
+          tma_load_4d(smem + L::OFF_V + o, &maps.v, &ctrl->k_full, c * 64, j0, h, b);
+          tma_load_4d(smem + L::OFF_DV + o, &maps.dv, &ctrl->k_full, c * 64, j0, h, b);
+        }
+      }
+      int fills = 0;
+      for (int t = 0; t < n_t; ++t) {
+        const int s = t % NS;
+        const uint32_t ph = (t / NS) & 1;
+        const int i0 = (t_begin + t) * BQ;
+        if (!mbar_wait(&ctrl->q_empty[s], ph ^ 1, abort)) {
+          record_timeout(status, abort);
+          break;
+        }
+        uint8_t* st = smem + L::OFF_ST + s * L::STAGE;
+        mbar_arrive_expect_tx(&ctrl->q_full[s], 2 * L::QBLK);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_4d(st + c * L::QCHUNK, &maps.q, &ctrl->q_full[s], c * 64, i0, h, b);
+          tma_load_4d(st + c * L::QCHUNK + BQ * 128, &maps.dq, &ctrl->q_full[s], c * 64, i0, h, b);
+          tma_load_4d(st + L::QBLK + c * L::QCHUNK, &maps.gto, &ctrl->q_full[s], c * 64, i0, h, b);
+          tma_load_4d(st + L::QBLK + c * L::QCHUNK + BQ * 128, &maps.go, &ctrl->q_full[s], c * 64,
+                      i0, h, b);
+        }
+        ++fills;
+      }
+      if (*abort) {
+        const int zero = 0;
+        mbar_wait(&ctrl->k_full, 0, &zero);
+        for (int t = max(0, fills - NS); t < fills; ++t)
+          mbar_wait(&ctrl->q_full[t % NS], (t / NS) & 1, &zero);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(&ctrl->k_full, 0, abort);
+      tc_fence_after();
+      const uint32_t aK = smem_u32(smem + L::OFF_K), adK = smem_u32(smem + L::OFF_DK);
+      const uint32_t aV = smem_u32(smem + L::OFF_V), adV = smem_u32(smem + L::OFF_DV);
+      for (int t = 0; ok && t < n_t; ++t) {
+        const int s = t % NS;
+        if (!mbar_wait(&ctrl->q_full[s], (t / NS) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t qb = smem_u32(smem + L::OFF_ST + s * L::STAGE);  // [Q ; dQ]
+        const uint32_t ob = qb + L::QBLK;                               // [gtO ; gO]
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // [S^T | K dQ^T] = K [Q ; dQ]^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_S, sdesc_sw128(aK + (kk >> 2) * BK * 128 + off, 16, 1024),
+                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N128, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // K dQ^T += dK Q^T  (= dS_raw^T)
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_DS, sdesc_sw128(adK + (kk >> 2) * BK * 128 + off, 16, 1024),
+                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N64, 1u);
+        }
+        if (L::kK) {
+#pragma unroll
+          for (int kk = 0; kk < KSD; ++kk) {  // [G^T | V gO^T] = V [gtO ; gO]^T
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(tmem + L::TM_G, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N128, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < KSD; ++kk) {  // V gO^T += dV gtO^T  (= gP1^T)
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(tmem + L::TM_GP, sdesc_sw128(adV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N64, 1u);
+          }
+        }
+        mma_commit(&ctrl->s_full);
+        if (!mbar_wait(&ctrl->p_full, t & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // A operands of query rows [16 kk, 16 kk + 16): warpgroup kk / 2 wrote
+        // P^T, dP^T at its columns [w*32, w*32+32) and gS^T, g_dS^T at
+        // [64 + w*32, 64 + w*32 + 32).
+#pragma unroll
+        for (int kk = 0; kk < KSQ; ++kk) {
+          const uint32_t a0 = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+          const uint32_t xq = qb + kk * 16 * 128;  // MN-major: 16 query rows per K-step
+          const uint32_t xo = ob + kk * 16 * 128;
+          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+          if (L::kV) {
+            if (D == 64) {  // [g_dV | gV] += P^T [gtO | gO]
+              mma_ts(tmem + L::TM_ACC + A_GDV, a0, sdesc_sw128(xo, BQ * 128, 1024), I_ACC2, acc);
+            } else {
+              mma_ts(tmem + L::TM_ACC + A_GDV, a0, sdesc_sw128(xo, L::QCHUNK, 1024), I_ACC1, acc);
+              mma_ts(tmem + L::TM_ACC + A_GV, a0, sdesc_sw128(xo + BQ * 128, L::QCHUNK, 1024),
+                     I_ACC1, acc);
+            }
+          }
+          if (L::kK) {
+            if (D == 64) {  // [g_dK | gK] += g_dS^T [Q | dQ]
+              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 16, sdesc_sw128(xq, BQ * 128, 1024),
+                     I_ACC2, acc);
+            } else {
+              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 16, sdesc_sw128(xq, L::QCHUNK, 1024),
+                     I_ACC1, acc);
+              mma_ts(tmem + L::TM_ACC + A_GK, a0 + 64 + 16,
+                     sdesc_sw128(xq + BQ * 128, L::QCHUNK, 1024), I_ACC1, acc);
+            }
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSQ; ++kk) {
+          const uint32_t a0 = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+          if (L::kV)  // gV += dP^T gtO
+            mma_ts(tmem + L::TM_ACC + A_GV, a0 + 16,
+                   sdesc_sw128(ob + kk * 16 * 128, D == 64 ? BQ * 128 : L::QCHUNK, 1024), I_ACC1, 1u);
+          if (L::kK)  // gK += gS^T Q
+            mma_ts(tmem + L::TM_ACC + A_GK, a0 + 64,
+                   sdesc_sw128(qb + kk * 16 * 128, D == 64 ? BQ * 128 : L::QCHUNK, 1024), I_ACC1, 1u);
+        }
+        mma_commit(&ctrl->q_empty[s]);
+      }
+      if (ok && n_t > 0) mma_commit(&ctrl->o_full);
+      if (!ok) record_timeout(status, abort);
+      mma_commit(&ctrl->drain);
+      const int zero = 0;
+      mbar_wait(&ctrl->drain, 0, &zero);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    // Thread = key (TMEM lane); warpgroup wg owns query rows [wg*32, wg*32+32)
+    // of every tile.
+    const int wg = (warp - 2) >> 2;
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;
+    const int j = j0 + r;
+    const bool key_ok = j < p.Nk;
+    const uint32_t lb = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    const float c = p.scale * kLog2e;
+    const float s = p.scale;
+    bool ok = true;
+    for (int t = 0; t < n_t; ++t) {
+      const int st_i = t % NS;
+      const int i0 = (t_begin + t) * BQ + wg * 32;  // first query row of this half tile
+      if (!warp_wait(&ctrl->s_full, t & 1, status, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // Two halves of 16 query rows keep the register footprint small.
+#pragma unroll 1
+      for (int hq = 0; hq < 2; ++hq) {
+        const uint32_t col = wg * 32 + hq * 16;
+        uint32_t rs[16], rds[16], rg[16], rgp[16];
+        tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_DS + col, rs, rds);
+        if (L::kK) tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
+        uint32_t pa[8], pb[8], pc[8], pd[8];  // P^T, dP^T, gS^T, g_dS^T (packed pairs)
+#pragma unroll
+        for (int qq = 0; qq < 16; qq += 2) {
+          float P2[2], dP2[2], gS2[2], gdS2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = i0 + hq * 16 + qq + e;
+            const bool row_ok = i < p.Nq;
+            const long long ridx = rbase + (row_ok ? i : 0);
+            // Row scalars: plain cached loads (every lane reads the same row).
+            const float lse = row_ok ? __ldg(p.lse + ridx) : -INFINITY;
+            bool keep = key_ok && row_ok && lse != -INFINITY;
+            float x = __uint_as_float(rs[qq + e]) * c;
+            if constexpr (MASK == kMaskCausal) keep = keep && j <= i;
+            if constexpr (MASK == kMaskBool) {
+              if (keep)
+                keep = static_cast<const uint8_t*>(p.mask)[b * p.msb + h * p.msh +
+                                                           static_cast<long long>(i) * p.msq +
+                                                           static_cast<long long>(j) * p.msk] != 0;
+            }
+            if constexpr (MASK == kMaskAdditive) {
+              const float m = keep ? static_cast<const float*>(p.mask)[b * p.msb + h * p.msh +
+                                                                       static_cast<long long>(i) * p.msq +
+                                                                       static_cast<long long>(j) * p.msk]
+                                   : 0.f;
+              x = fmaf(m, kLog2e, x);
+              keep = keep && x != -INFINITY;
+            }
+            const float mu = row_ok ? __ldg(p.mu + ridx) : 0.f;
+            const float nu = (L::kK && row_ok) ? __ldg(p.nu + ridx) : 0.f;
+            const float delta = (L::kK && row_ok) ? __ldg(p.delta + ridx) : 0.f;
+            const float gv = L::kK ? __uint_as_float(rg[qq + e]) : 0.f;
+            const float gp = L::kK ? __uint_as_float(rgp[qq + e]) : 0.f;
+            const BwdTerms bt = bwd_terms(keep, x, lse * kLog2e, __uint_as_float(rds[qq + e]), gv,
+                                          gp, s, mu, nu, delta);
+            P2[e] = bt.P;
+            dP2[e] = bt.dP;
+            gS2[e] = bt.gS;
+            gdS2[e] = bt.gdS;
+          }
+          pa[qq >> 1] = ElemTraits<T>::pack(P2[0], P2[1]);
+          pb[qq >> 1] = ElemTraits<T>::pack(dP2[0], dP2[1]);
+          pc[qq >> 1] = ElemTraits<T>::pack(gS2[0], gS2[1]);
+          pd[qq >> 1] = ElemTraits<T>::pack(gdS2[0], gdS2[1]);
+        }
+        // packed column of query pair (hq*16 + qq)/2 within this warpgroup's 16
+        if (L::kV) {
+          tmem_st8(lb + wg * 32 + hq * 8, pa);
+          tmem_st8(lb + wg * 32 + 16 + hq * 8, pb);
+        }
+        if (L::kK) {
+          tmem_st8(lb + 64 + wg * 32 + hq * 8, pc);
+          tmem_st8(lb + 64 + wg * 32 + 16 + hq * 8, pd);
+        }
+      }
+      (void)st_i;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctrl->p_full);
+    }
+    if (ok && n_t > 0) ok = warp_wait(&ctrl->o_full, 0, status, abort);
+    if (ok) {
+      tc_fence_after();
+      // Output tensors of this kernel, split between the two warpgroups.
+      constexpr int NOUT = (L::kV ? 2 : 0) + (L::kK ? 2 : 0);
+#pragma unroll 1
+      for (int oi = wg; oi < NOUT; oi += 2) {
+        // oi enumerates g_dV, gV (value part) then g_dK, gK (key part)
+        const int which = L::kV ? oi : oi + 2;
+        void* dst = which == 0 ? p.g_dv : which == 1 ? p.g_v : which == 2 ? p.g_dk : p.g_k;
+        const Strides& ds = which == 0 ? p.sgdv : which == 1 ? p.sgv : which == 2 ? p.sgdk : p.sgk;
+        const uint32_t acol = which == 0 ? A_GDV : which == 1 ? A_GV : which == 2 ? A_GDK : A_GK;
+        const float scl = which >= 2 ? s : 1.0f;
+        T* row = static_cast<T*>(dst) + static_cast<long long>(b) * ds.b +
+                 static_cast<long long>(h) * ds.h + static_cast<long long>(key_ok ? j : 0) * ds.n;
+#pragma unroll 1
+        for (int col = 0; col < D; col += 32) {
+          uint32_t a[32];
+          if (n_t > 0) {
+            tmem_ld32(lb + L::TM_ACC + acol + col, a);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = 0u;
+          }
+          uint32_t po[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            po[e >> 1] =
+                ElemTraits<T>::pack(__uint_as_float(a[e]) * scl, __uint_as_float(a[e + 1]) * scl);
+          if (key_ok) {
+            uint4* od = reinterpret_cast<uint4*>(row + col);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Launch of the tensor-core backward (after the row pre-pass).
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+  static unsigned long long done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && (done & (1ull << dev))) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) done |= 1ull << dev;
+  return e;
+}
+
+template <typename T, int D, int MASK>
+cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
+                                  const BwdParams& p, int num_sms, unsigned int* status,
+                                  cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  {
+    using L = BqLayout<D>;
+    auto kern = bwd_q_tc_kernel<T, D, MASK>;
+    cudaError_t e = set_smem(kern, L::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int nq = (p.Nq + L::BM - 1) / L::BM;
+    const int G = max(1, min(BH, num_sms / max(1, nq)));
+    kern<<<static_cast<unsigned>(static_cast<long long>(nq) * BH), kBwdThreads, L::SMEM_BYTES,
+           stream>>>(qmaps, p, G, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto key_side = [&](auto part_tag) -> cudaError_t {
+    constexpr int PART = decltype(part_tag)::value;
+    using L = BkLayout<D, PART>;
+    auto kern = bwd_k_tc_kernel<T, D, MASK, PART>;
+    cudaError_t e = set_smem(kern, L::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int nk = (p.Nk + L::BK - 1) / L::BK;
+    const int G = max(1, min(BH, num_sms / max(1, nk)));
+    kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BH), kBwdThreads, L::SMEM_BYTES,
+           stream>>>(kmaps, p, G, status);
+    return cudaGetLastError();
+  };
+  if constexpr (D == 64) {
+    return key_side(std::integral_constant<int, 3>{});
+  } else {
+    cudaError_t e = key_side(std::integral_constant<int, 1>{});
+    if (e != cudaSuccess) return e;
+    return key_side(std::integral_constant<int, 2>{});
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_bwd_tc_dispatch(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
+                                   const BwdParams& p, int num_sms, unsigned int* status,
+                                   cudaStream_t stream) {
+  switch (mask_kind) {
+    case kMaskNone:
+      return launch_bwd_tc_variant<T, D, kMaskNone>(qmaps, kmaps, p, num_sms, status, stream);
+    case kMaskBool:
+      return launch_bwd_tc_variant<T, D, kMaskBool>(qmaps, kmaps, p, num_sms, status, stream);
+    case kMaskAdditive:
+      return launch_bwd_tc_variant<T, D, kMaskAdditive>(qmaps, kmaps, p, num_sms, status, stream);
+    case kMaskCausal:
+      return launch_bwd_tc_variant<T, D, kMaskCausal>(qmaps, kmaps, p, num_sms, status, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace jvp

@@ -276,6 +276,7 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
                       const jvp_mask_t* mask, float scale, void* const* out,
                       const jvp_strides_t* out_strides, void* workspace, size_t ws_bytes,
                       void* stream_ptr) {
+  t_last_path = 0;
   if (!shape) return fail(JVP_ERR_INVALID_ARG, "shape is NULL");
   const int64_t B = shape->B, H = shape->H, Nq = shape->Nq, Nk = shape->Nk, D = shape->D;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return fail(JVP_ERR_INVALID_ARG, "negative size");
@@ -359,7 +360,41 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   for (int t = 0; t < 6; ++t) *sout[t] = to_strides(out_strides[t]);
   p.nu = static_cast<float*>(workspace);
   p.delta = p.nu + B * H * Nq;
-  cudaError_t err = launch_bwd_simt(static_cast<DType>(dtype), p, static_cast<cudaStream_t>(stream_ptr));
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  // Tensor-core path: fp16/bf16, D in {64, 128}, at least one row and one key,
+  // every tensor 16-byte aligned with 16-byte-multiple strides.
+  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) && (D == 64 || D == 128) && Nq > 0 && Nk > 0;
+  for (int t = 0; tc && t < 10; ++t) tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
+  for (int t = 0; tc && t < 6; ++t) tc = aligned(out[t], 16) && strides_aligned16(out_strides[t], e);
+  BwdTcMaps qm, km;
+  if (tc) {
+    // in order: q k v dq dk dv o t_o g_o g_to
+    const int64_t Ns[10] = {Nq, Nk, Nk, Nq, Nk, Nk, Nq, Nq, Nq, Nq};
+    const int qidx[4] = {0, 3, 8, 9}, kidx[4] = {1, 4, 2, 5};
+    CUtensorMap* qdst_q[4] = {&qm.q, &qm.dq, &qm.go, &qm.gto};
+    CUtensorMap* qdst_k[4] = {&qm.k, &qm.dk, &qm.v, &qm.dv};
+    CUtensorMap* kdst_q[4] = {&km.q, &km.dq, &km.go, &km.gto};
+    CUtensorMap* kdst_k[4] = {&km.k, &km.dk, &km.v, &km.dv};
+    for (int u = 0; tc && u < 4; ++u) {
+      const int a = qidx[u], c = kidx[u];
+      tc = encode_map(qdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 128) &&
+           encode_map(kdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 64) &&
+           encode_map(qdst_k[u], dtype, in[c], B, H, Ns[c], D, in_strides[c], 64) &&
+           encode_map(kdst_k[u], dtype, in[c], B, H, Ns[c], D, in_strides[c], 128);
+    }
+  }
+  cudaError_t err;
+  if (tc) {
+    err = launch_bwd_rows(static_cast<DType>(dtype), p, stream);
+    if (err == cudaSuccess)
+      err = launch_bwd_tc(static_cast<DType>(dtype), static_cast<int>(D), kind, qm, km, p,
+                          dev->num_sms, dev->status, stream);
+    t_last_path = 1;
+  } else {
+    err = launch_bwd_simt(static_cast<DType>(dtype), p, stream);
+    t_last_path = 2;
+  }
   if (err != cudaSuccess)
     return fail(JVP_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(err));
   return ok();

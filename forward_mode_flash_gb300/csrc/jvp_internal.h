@@ -91,6 +91,31 @@ inline size_t bwd_workspace_bytes(long long rows) {
 
 // Backward of the dual computation (CUDA-core kernels).  Returns a cudaError_t.
 cudaError_t launch_bwd_simt(DType dt, const BwdParams& p, cudaStream_t stream);
+// Only the per-row pre-pass (nu and delta into the workspace).
+cudaError_t launch_bwd_rows(DType dt, const BwdParams& p, cudaStream_t stream);
+
+// Tensor maps of the tensor-core backward kernels (query-side and key-side
+// tensors; each kernel gets its own set, the box heights differ).
+struct BwdTcMaps {
+  CUtensorMap q, dq, go, gto, k, dk, v, dv;
+};
+// Tensor-core backward (fp16/bf16, D in {64, 128}); the row pre-pass must
+// have been enqueued before.
+cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, const BwdTcMaps& qmaps,
+                          const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
+                          unsigned int* status, cudaStream_t stream);
+cudaError_t launch_bwd_tc_f16_d64(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
+                                  const BwdParams& p, int num_sms, unsigned int* status,
+                                  cudaStream_t stream);
+cudaError_t launch_bwd_tc_f16_d128(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
+                                   const BwdParams& p, int num_sms, unsigned int* status,
+                                   cudaStream_t stream);
+cudaError_t launch_bwd_tc_bf16_d64(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
+                                   const BwdParams& p, int num_sms, unsigned int* status,
+                                   cudaStream_t stream);
+cudaError_t launch_bwd_tc_bf16_d128(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
+                                    const BwdParams& p, int num_sms, unsigned int* status,
+                                    cudaStream_t stream);
 
 // Device status word owned by the library (bit 0: a bounded wait timed out).
 unsigned int* device_status_ptr();

@@ -194,10 +194,30 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr_a, uint32_t taddr_b,
       : "r"(taddr_a), "r"(taddr_b)
       : "memory");
 }
+// Two 16-column loads under one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (&a)[16],
+                                            uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : JVP_R8(a, 0), JVP_R8(a, 8), JVP_R8(b, 0), JVP_R8(b, 8)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
 #undef JVP_R8
 
 #define JVP_W8(a, i) "r"(a[i]), "r"(a[i + 1]), "r"(a[i + 2]), "r"(a[i + 3]), "r"(a[i + 4]), \
                      "r"(a[i + 5]), "r"(a[i + 6]), "r"(a[i + 7])
+// registers -> TMEM: 32 lanes x 8 columns.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
 // registers -> TMEM: 32 lanes x 16 columns.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
