@@ -421,6 +421,20 @@ cudaError_t launch_fwd_tc(DType dt, int D, int mask_kind, bool tangent, const Tc
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, const BwdTcMaps& qmaps,
+                          const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
+                          unsigned int* status, cudaStream_t stream) {
+  if (dt == kF16 && D == 64)
+    return launch_bwd_tc_f16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+  if (dt == kF16 && D == 128)
+    return launch_bwd_tc_f16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+  if (dt == kBF16 && D == 64)
+    return launch_bwd_tc_bf16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+  if (dt == kBF16 && D == 128)
+    return launch_bwd_tc_bf16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace jvp
 
 extern "C" {
