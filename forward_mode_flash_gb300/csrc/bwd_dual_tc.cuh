@@ -774,8 +774,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ----------------------------------------------------------------------------
 // Launch of the tensor-core backward (after the row pre-pass).
-template <typename K>
-cudaError_t set_smem(K kern, int bytes) {
+// Keyed on the kernel itself (all backward kernels share one signature), so
+// each kernel gets its own per-device record of the attribute being set.
+template <auto kern>
+cudaError_t set_smem(int bytes) {
   static unsigned long long done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -793,8 +795,8 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
   const int BH = p.B * p.H;
   {
     using L = BqLayout<D>;
-    auto kern = bwd_q_tc_kernel<T, D, MASK>;
-    cudaError_t e = set_smem(kern, L::SMEM_BYTES);
+    constexpr auto kern = bwd_q_tc_kernel<T, D, MASK>;
+    cudaError_t e = set_smem<kern>(L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int nq = (p.Nq + L::BM - 1) / L::BM;
     const int G = max(1, min(BH, num_sms / max(1, nq)));
@@ -806,8 +808,8 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
   auto key_side = [&](auto part_tag) -> cudaError_t {
     constexpr int PART = decltype(part_tag)::value;
     using L = BkLayout<D, PART>;
-    auto kern = bwd_k_tc_kernel<T, D, MASK, PART>;
-    cudaError_t e = set_smem(kern, L::SMEM_BYTES);
+    constexpr auto kern = bwd_k_tc_kernel<T, D, MASK, PART>;
+    cudaError_t e = set_smem<kern>(L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int nk = (p.Nk + L::BK - 1) / L::BK;
     const int G = max(1, min(BH, num_sms / max(1, nk)));
