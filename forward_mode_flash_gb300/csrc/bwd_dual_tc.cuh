@@ -589,12 +589,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tc_fence_after();
-        // A operands of query rows [16 kk, 16 kk + 16): warpgroup kk / 2 wrote
-        // P^T, dP^T at its columns [w*32, w*32+32) and gS^T, g_dS^T at
-        // [64 + w*32, 64 + w*32 + 32).
+        // A operands of query rows [16 kk, 16 kk + 16) (written by warpgroup
+        // kk / 2, half kk % 2): P^T at columns 16 kk, dP^T at 16 kk + 8, gS^T and
+        // g_dS^T 64 columns further.
 #pragma unroll
         for (int kk = 0; kk < KSQ; ++kk) {
-          const uint32_t a0 = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+          const uint32_t a0 = tmem + kk * 16;
           const uint32_t xq = qb + kk * 16 * 128;  // MN-major: 16 query rows per K-step
           const uint32_t xo = ob + kk * 16 * 128;
           const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
@@ -609,21 +609,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           if (L::kK) {
             if (D == 64) {  // [g_dK | gK] += g_dS^T [Q | dQ]
-              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 16, sdesc_sw128(xq, BQ * 128, 1024),
+              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 8, sdesc_sw128(xq, BQ * 128, 1024),
                      I_ACC2, acc);
             } else {
-              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 16, sdesc_sw128(xq, L::QCHUNK, 1024),
+              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 8, sdesc_sw128(xq, L::QCHUNK, 1024),
                      I_ACC1, acc);
-              mma_ts(tmem + L::TM_ACC + A_GK, a0 + 64 + 16,
+              mma_ts(tmem + L::TM_ACC + A_GK, a0 + 64 + 8,
                      sdesc_sw128(xq + BQ * 128, L::QCHUNK, 1024), I_ACC1, acc);
             }
           }
         }
 #pragma unroll
         for (int kk = 0; kk < KSQ; ++kk) {
-          const uint32_t a0 = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+          const uint32_t a0 = tmem + kk * 16;
           if (L::kV)  // gV += dP^T gtO
-            mma_ts(tmem + L::TM_ACC + A_GV, a0 + 16,
+            mma_ts(tmem + L::TM_ACC + A_GV, a0 + 8,
                    sdesc_sw128(ob + kk * 16 * 128, D == 64 ? BQ * 128 : L::QCHUNK, 1024), I_ACC1, 1u);
           if (L::kK)  // gK += gS^T Q
             mma_ts(tmem + L::TM_ACC + A_GK, a0 + 64,
@@ -710,14 +710,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pc[qq >> 1] = ElemTraits<T>::pack(gS2[0], gS2[1]);
           pd[qq >> 1] = ElemTraits<T>::pack(gdS2[0], gdS2[1]);
         }
-        // packed column of query pair (hq*16 + qq)/2 within this warpgroup's 16
+        // The 16-bit results go only into the 16 columns this half has just
+        // read (S at col, dS at 64 + col), so the other half's inputs stay intact.
         if (L::kV) {
-          tmem_st8(lb + wg * 32 + hq * 8, pa);
-          tmem_st8(lb + wg * 32 + 16 + hq * 8, pb);
+          tmem_st8(lb + col, pa);
+          tmem_st8(lb + col + 8, pb);
         }
         if (L::kK) {
-          tmem_st8(lb + 64 + wg * 32 + hq * 8, pc);
-          tmem_st8(lb + 64 + wg * 32 + 16 + hq * 8, pd);
+          tmem_st8(lb + 64 + col, pc);
+          tmem_st8(lb + 64 + col + 8, pd);
         }
       }
       (void)st_i;
