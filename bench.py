@@ -202,7 +202,11 @@ FP32_LANES_PER_SM = 128  # CUDA-core fp32 FMA lanes per SM (4 partitions x 32)
 
 
 def run_bwd(args, rank, world, local):
-    """Times jvp_attn_bwd_dual (three CUDA-core kernels) on one workload."""
+    """Times jvp_attn_bwd_dual on one workload.
+
+    fp16/bf16 inputs with D in {64, 128} run the row pre-pass and the tcgen05
+    kernels (query-major, then key-major: one launch at D = 64, value and key
+    parts at D = 128); other shapes run three CUDA-core kernels."""
     import numpy as np
     import torch
 
@@ -229,6 +233,7 @@ def run_bwd(args, rank, world, local):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    tensor_core = api.last_path() == 1
     stream = torch.cuda.current_stream()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -245,28 +250,43 @@ def run_bwd(args, rank, world, local):
     half = 0.5 if causal else 1.0
     bhnnd = w.B * w.H * w.N * w.N * w.D * half
     alg_flops = 30.0 * bhnnd       # the 15 N x N x D products of the reverse mode
-    exec_flops = 42.0 * bhnnd      # the 21 products these kernels execute (scores recomputed)
+    # Products executed (scores recomputed): 21 per (row, key, d) in the
+    # CUDA-core kernels and in the tensor-core kernels at D = 64; the D = 128
+    # key-major split recomputes the three score products once more (24).
+    exec_flops = (48.0 if (tensor_core and w.D == 128) else 42.0) * bhnnd
     value = replicas.aggregate_throughput(world, alg_flops, args.steps, total_ms * 1e-3) / 1e12
     pk, pk_src = peaks()
     clk = pk.get("sm_max_mhz", 2070.0) * 1e6
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = n_sms * FP32_LANES_PER_SM * 2 * clk / 1e12
     achieved = exec_flops / (ms_step * 1e-3) / 1e12
+    if tensor_core:
+        tc_peak = float(pk.get("bf16_tflops", 1900.0))  # fp16 and bf16 share the dense rate
+        launches = 3 if w.D == 64 else 4
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tc_peak, "traffic": None,
+                    "peak_source": f"{pk_src} bf16 dense (cuBLAS burst)",
+                    "kernel": "whole step: bwd_rows_kernel + bwd_q_tc_kernel + bwd_k_tc_kernel"
+                              + (" x2 (value, key parts)" if w.D == 128 else "")}
+    else:
+        alu_peak = n_sms * FP32_LANES_PER_SM * 2 * clk / 1e12
+        launches = 3
+        roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                    "frac": achieved / alu_peak, "traffic": None,
+                    "peak_source": f"{n_sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 x "
+                                   f"{clk / 1e6:.0f} MHz (CUDA-core fp32)",
+                    "kernel": "bwd_keys_kernel + bwd_queries_kernel + bwd_rows_kernel"}
     line = {
         "metric": "bwd_dual (reverse mode of fwd+JVP attention) TFLOP/s", "mode": "bwd_dual",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{w.dtype} (fp32 accumulate)" if tensor_core else "f32", "data": "synthetic",
         "config": {"workload": name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "mask": w.mask,
                    "input_dtype": w.dtype, "algorithmic_flops_per_step": alg_flops,
                    "executed_flops_per_step": exec_flops,
                    "l2": "flushed: 256 MiB written between timed steps (outside the events)"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": achieved / alu_peak, "traffic": None,
-                     "peak_source": f"{n_sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 x "
-                                    f"{clk / 1e6:.0f} MHz (CUDA-core fp32)",
-                     "kernel": "bwd_keys_kernel + bwd_queries_kernel + bwd_rows_kernel"},
-        "clocks": clocks.summary(), "gpu_launches": 3 * args.steps, "e2e": None,
+        "roofline": roofline,
+        "clocks": clocks.summary(), "gpu_launches": launches * args.steps, "e2e": None,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # The float64 oracle's reverse mode on one whole head of the same workload.

@@ -38,10 +38,15 @@ class Workload:
     seed: int = 0
     keep_p: float = 0.9
     extra: dict = field(default_factory=dict)
+    Nk: Optional[int] = None  # key/value length; None means equal to N
 
     @property
     def torch_dtype(self) -> torch.dtype:
         return DTYPES[self.dtype]
+
+    @property
+    def n_keys(self) -> int:
+        return self.N if self.Nk is None else self.Nk
 
 
 # The five workloads the method is specified on (sizes, dtypes and masks),
@@ -77,15 +82,18 @@ def make_inputs(w: Workload, with_cotangents: bool = False, device: str = "cpu")
     """Draw the inputs of workload ``w`` on the CPU, then move them to ``device``."""
     g = torch.Generator().manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.D)
-    draws = [torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(6)]
+    kshape = (w.B, w.H, w.n_keys, w.D)
+    # draw order: Q, K, V, dQ, dK, dV
+    draws = [torch.randn(sh, generator=g, dtype=torch.float32)
+             for sh in (shape, kshape, kshape, shape, kshape, kshape)]
     mask = None
     if w.mask == "bool":
-        keep = torch.rand((w.B, 1, w.N, w.N), generator=g, dtype=torch.float32) < w.keep_p
-        idx = torch.arange(w.N)
+        keep = torch.rand((w.B, 1, w.N, w.n_keys), generator=g, dtype=torch.float32) < w.keep_p
+        idx = torch.arange(min(w.N, w.n_keys))
         keep[:, :, idx, idx] = True
         mask = keep
     elif w.mask == "additive":
-        mask = torch.randn((w.B, 1, w.N, w.N), generator=g, dtype=torch.float32)
+        mask = torch.randn((w.B, 1, w.N, w.n_keys), generator=g, dtype=torch.float32)
     g_o = g_to = None
     if with_cotangents:
         g_o = torch.randn(shape, generator=g, dtype=torch.float32)
@@ -101,7 +109,10 @@ def make_inputs(w: Workload, with_cotangents: bool = False, device: str = "cpu")
 
 
 def small(dtype: str, B: int, H: int, N: int, D: int, mask: str = "none", seed: int = 0,
-          keep_p: float = 0.9) -> Workload:
-    """An ad-hoc workload for parity cases at sizes the oracle finishes quickly."""
-    return Workload(f"{dtype}_b{B}h{H}n{N}d{D}_{mask}_s{seed}", dtype, B, H, N, D, mask, seed,
-                    keep_p)
+          keep_p: float = 0.9, Nk: Optional[int] = None) -> Workload:
+    """An ad-hoc workload for parity cases at sizes the oracle finishes quickly.
+
+    ``Nk`` gives keys/values a length of their own (queries keep ``N``)."""
+    kv = "" if Nk is None else f"k{Nk}"
+    return Workload(f"{dtype}_b{B}h{H}n{N}{kv}d{D}_{mask}_s{seed}", dtype, B, H, N, D, mask, seed,
+                    keep_p, Nk=Nk)

@@ -90,3 +90,20 @@ def test_bwd_specified_workload_f16_b2h8n2048d64_causal_two_heads():
     w = synth.WORKLOADS["f16_b2h8n2048d64_causal"]
     errs = run(w, heads=(slice(0, 2), slice(3, 4)))
     check(w, errs)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("f32", 40)])
+@pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 77), (1, 129), (130, 1)])
+@pytest.mark.parametrize("mask", ["none", "causal", "bool", "additive"])
+def test_bwd_query_and_key_lengths_differ(dtype, D, Nq, Nk, mask):
+    w = synth.small(dtype, 1, 2, Nq, D, mask, seed=Nq + 3 * Nk, Nk=Nk)
+    check(w, run(w))
+
+
+@pytest.mark.parametrize("name,heads", [("bf16_b4h16n2048d128", (slice(3, 4), slice(14, 16))),
+                                        ("bf16_b4h16n2048d128_causal", (slice(0, 1), slice(5, 6)))])
+def test_bwd_specified_workload_d128_whole_heads(name, heads):
+    # Full-size launch (value and key parts of the key-major kernel); the oracle
+    # checks every gradient entry of the selected heads.
+    w = synth.WORKLOADS[name]
+    check(w, run(w, heads=heads))

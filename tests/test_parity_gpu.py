@@ -106,6 +106,15 @@ def test_tensor_core_path_masks(dtype, D, N, mask):
     compare_full(w, expect_path=1)
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("f32", 40)])
+@pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 77), (1, 129), (130, 1)])
+@pytest.mark.parametrize("mask", ["none", "causal", "bool", "additive"])
+def test_query_and_key_lengths_differ(dtype, D, Nq, Nk, mask):
+    # causal keeps key j for query i when j <= i (top-left aligned)
+    w = synth.small(dtype, 1, 2, Nq, D, mask, seed=Nq + 3 * Nk, Nk=Nk)
+    compare_full(w, expect_path=2 if dtype == "f32" else 1)
+
+
 @pytest.mark.parametrize("D", [1, 16, 33, 64, 100, 128])
 @pytest.mark.parametrize("mask", ["none", "bool", "additive", "causal"])
 def test_cuda_core_path_f32(D, mask):
