@@ -216,7 +216,7 @@ def run_bwd(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    name = args.workload if args.workload != DEFAULT_WORKLOAD else "f16_b2h8n2048d64_causal"
+    name = args.workload
     w = synth.WORKLOADS[name]
     causal = w.mask == "causal"
     inp = synth.make_inputs(w, with_cotangents=True, device=str(dev))
