@@ -78,16 +78,17 @@ struct BwdCtrl {
   int abort;
 };
 
-// Per-(row, key) backward terms from the score-side values.  keep = false
-// gives all-zero terms (masked key, or a row that keeps no key).
+// Per-(row, key) backward terms from the score-side values; xm is the
+// base-2 logit minus the row's base-2 log-sum-exp.  keep = false gives
+// all-zero terms (masked key, or a row that keeps no key).
 struct BwdTerms {
   float gS, gdS, P, dP;
 };
-__device__ __forceinline__ BwdTerms bwd_terms(bool keep, float x_log2, float lse2, float ds_raw,
-                                              float g, float gp1, float s, float mu, float nu,
+__device__ __forceinline__ BwdTerms bwd_terms(bool keep, float xm, float ds_raw, float g,
+                                              float gp1, float s, float mu, float nu,
                                               float delta) {
   BwdTerms r;
-  const float P = keep ? ex2_approx(x_log2 - lse2) : 0.0f;
+  const float P = keep ? ex2_approx(xm) : 0.0f;
   const float dS = s * ds_raw;
   const float gP = fmaf(g, dS - mu, gp1) - nu * dS;
   r.P = P;
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < 2; ++e) {
           const int j = j0 + jj + e;
           bool keep = live && j < p.Nk;
-          float x = __uint_as_float(rs[jj + e]) * c;
+          float x = fmaf(__uint_as_float(rs[jj + e]), c, -lse2);
           if constexpr (MASK == kMaskCausal) keep = keep && j <= i;
           if constexpr (MASK == kMaskBool) keep = keep && mreg.keep(jj + e);
           if constexpr (MASK == kMaskAdditive) {
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             keep = keep && x != -INFINITY;
           }
           const BwdTerms bt =
-              bwd_terms(keep, x, lse2, __uint_as_float(rds[jj + e]), __uint_as_float(rg[jj + e]),
+              bwd_terms(keep, x, __uint_as_float(rds[jj + e]), __uint_as_float(rg[jj + e]),
                         __uint_as_float(rgp[jj + e]), s, mu, nu, delta);
           gs[e] = bt.gS;
           gds[e] = bt.gdS;
@@ -481,7 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->k_full, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&ctrl->q_full[s], 1);
+      mbar_init(&ctrl->q_full[s], 2);  // TMA bytes + the row scalars written by warp 0
       mbar_init(&ctrl->q_empty[s], 1);
     }
     mbar_init(&ctrl->s_full, 1);
@@ -503,6 +504,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 issues the TMA copies; all 32 lanes then write the stage's row
+    // scalars (lse * log2 e, mu, nu, delta per query row; rows past Nq get
+    // lse = -inf) and lane 0 adds the second arrival on q_full.
     if (lane == 0) {
       mbar_arrive_expect_tx(&ctrl->k_full, (L::kK ? 4 : 2) * L::KT_BYTES);
       for (int c = 0; c < L::KCH; ++c) {
@@ -514,16 +518,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_4d(smem + L::OFF_DV + o, &maps.dv, &ctrl->k_full, c * 64, j0, h, b);
         }
       }
-      int fills = 0;
-      for (int t = 0; t < n_t; ++t) {
-        const int s = t % NS;
-        const uint32_t ph = (t / NS) & 1;
-        const int i0 = (t_begin + t) * BQ;
-        if (!mbar_wait(&ctrl->q_empty[s], ph ^ 1, abort)) {
-          record_timeout(status, abort);
-          break;
-        }
-        uint8_t* st = smem + L::OFF_ST + s * L::STAGE;
+    }
+    int fills = 0;
+    for (int t = 0; t < n_t; ++t) {
+      const int s = t % NS;
+      const uint32_t ph = (t / NS) & 1;
+      const int i0 = (t_begin + t) * BQ;
+      bool got = true;
+      if (lane == 0) got = mbar_wait(&ctrl->q_empty[s], ph ^ 1, abort);
+      if (!__shfl_sync(0xffffffffu, got, 0)) {
+        if (lane == 0) record_timeout(status, abort);
+        break;
+      }
+      uint8_t* st = smem + L::OFF_ST + s * L::STAGE;
+      if (lane == 0) {
         mbar_arrive_expect_tx(&ctrl->q_full[s], 2 * L::QBLK);
         for (int c = 0; c < L::KCH; ++c) {
           tma_load_4d(st + c * L::QCHUNK, &maps.q, &ctrl->q_full[s], c * 64, i0, h, b);
@@ -532,14 +540,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_4d(st + L::QBLK + c * L::QCHUNK + BQ * 128, &maps.go, &ctrl->q_full[s], c * 64,
                       i0, h, b);
         }
-        ++fills;
       }
-      if (*abort) {
-        const int zero = 0;
-        mbar_wait(&ctrl->k_full, 0, &zero);
-        for (int t = max(0, fills - NS); t < fills; ++t)
-          mbar_wait(&ctrl->q_full[t % NS], (t / NS) & 1, &zero);
+      float4* rsc = reinterpret_cast<float4*>(st + 2 * L::QBLK);
+#pragma unroll
+      for (int rr = lane; rr < BQ; rr += 32) {
+        const int i = i0 + rr;
+        float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        if (i < p.Nq) {
+          const long long idx = rbase + i;
+          v.x = p.lse[idx] * kLog2e;
+          v.y = p.mu[idx];
+          if (L::kK) {
+            v.z = p.nu[idx];
+            v.w = p.delta[idx];
+          }
+        }
+        rsc[rr] = v;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctrl->q_full[s]);
+      ++fills;
+    }
+    if (lane == 0 && *abort) {
+      const int zero = 0;
+      mbar_wait(&ctrl->k_full, 0, &zero);
+      for (int t = max(0, fills - NS); t < fills; ++t)
+        mbar_wait(&ctrl->q_full[t % NS], (t / NS) & 1, &zero);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -653,11 +679,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int t = 0; t < n_t; ++t) {
       const int st_i = t % NS;
       const int i0 = (t_begin + t) * BQ + wg * 32;  // first query row of this half tile
-      if (!warp_wait(&ctrl->s_full, t & 1, status, abort)) {
+      if (!warp_wait(&ctrl->s_full, t & 1, status, abort) ||
+          !warp_wait(&ctrl->q_full[st_i], (t / NS) & 1, status, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const float4* rsc =
+          reinterpret_cast<const float4*>(smem + L::OFF_ST + st_i * L::STAGE + 2 * L::QBLK) + wg * 32;
       // Two halves of 16 query rows keep the register footprint small.
 #pragma unroll 1
       for (int hq = 0; hq < 2; ++hq) {
@@ -672,12 +701,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int i = i0 + hq * 16 + qq + e;
-            const bool row_ok = i < p.Nq;
-            const long long ridx = rbase + (row_ok ? i : 0);
-            // Row scalars: plain cached loads (every lane reads the same row).
-            const float lse = row_ok ? __ldg(p.lse + ridx) : -INFINITY;
-            bool keep = key_ok && row_ok && lse != -INFINITY;
-            float x = __uint_as_float(rs[qq + e]) * c;
+            const float4 rv = rsc[hq * 16 + qq + e];  // lse2, mu, nu, delta (one broadcast read)
+            bool keep = key_ok && rv.x != -INFINITY;  // false for rows past Nq
+            float x = fmaf(__uint_as_float(rs[qq + e]), c, -rv.x);
             if constexpr (MASK == kMaskCausal) keep = keep && j <= i;
             if constexpr (MASK == kMaskBool) {
               if (keep)
@@ -693,13 +719,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               x = fmaf(m, kLog2e, x);
               keep = keep && x != -INFINITY;
             }
-            const float mu = row_ok ? __ldg(p.mu + ridx) : 0.f;
-            const float nu = (L::kK && row_ok) ? __ldg(p.nu + ridx) : 0.f;
-            const float delta = (L::kK && row_ok) ? __ldg(p.delta + ridx) : 0.f;
             const float gv = L::kK ? __uint_as_float(rg[qq + e]) : 0.f;
             const float gp = L::kK ? __uint_as_float(rgp[qq + e]) : 0.f;
-            const BwdTerms bt = bwd_terms(keep, x, lse * kLog2e, __uint_as_float(rds[qq + e]), gv,
-                                          gp, s, mu, nu, delta);
+            const BwdTerms bt =
+                bwd_terms(keep, x, __uint_as_float(rds[qq + e]), gv, gp, s, rv.y, rv.z, rv.w);
             P2[e] = bt.P;
             dP2[e] = bt.dP;
             gS2[e] = bt.gS;
