@@ -46,8 +46,12 @@ def parse():
                     help="target length of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--mode", default="fwd_dual", choices=["fwd_dual", "bwd_dual"],
-                    help="fwd_dual (the headline) or the backward of the dual computation")
+    ap.add_argument("--mode", default="fwd_dual",
+                    choices=["fwd_dual", "bwd_dual", "sweep", "memory"],
+                    help="fwd_dual (the headline), the backward of the dual computation, the "
+                         "sequence-length sweep (one JSON line per configuration) or the "
+                         "memory-scaling report (one JSON line per N)")
+    ap.add_argument("--sweep-dtypes", default="bf16,f16")
     return ap.parse_args()
 
 
@@ -304,6 +308,28 @@ def run_bwd(args, rank, world, local):
     return 0
 
 
+def run_report(args, rank, world, local):
+    """The sequence-length sweep or the memory-scaling report (rank 0 only)."""
+    import torch
+
+    from forward_mode_flash_gb300 import build, report
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    build.build()
+    pk, pk_src = peaks()
+    if args.mode == "sweep":
+        for row in report.sweep(dtypes=tuple(args.sweep_dtypes.split(",")),
+                                peak_tflops=float(pk.get("bf16_tflops", 1900.0)),
+                                peak_gbs=float(pk.get("hbm_gbs", 6800.0))):
+            print(json.dumps({"mode": "sweep", "peaks": pk_src, **row}), flush=True)
+    else:
+        for row in report.memory_scaling():
+            print(json.dumps({"mode": "memory", **row}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -323,6 +349,8 @@ def main():
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
+    if args.mode in ("sweep", "memory"):
+        return run_report(args, rank, world, local)
     if args.mode == "bwd_dual":
         rc = run_bwd(args, rank, world, local)
         if world > 1:

@@ -75,11 +75,13 @@ def _ptr(t: Optional[torch.Tensor]):
 def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor,
              dk: torch.Tensor, dv: torch.Tensor, attn_mask: Optional[torch.Tensor] = None,
              is_causal: bool = False, scale: Optional[float] = None, return_stats: bool = False,
-             out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+             out: Optional[Tuple[torch.Tensor, ...]] = None):
     """Attention forward and its JVP in one fused pass.
 
     Returns (o, t_o), or (o, t_o, lse, mu) with ``return_stats``: lse is the
     natural-log log-sum-exp per row and mu its tangent, both float32 [B,H,Nq].
+    ``out`` = (o, t_o) or (o, t_o, lse, mu) gives preallocated outputs (the
+    four-tuple implies ``return_stats``).
     """
     lib = _abi.load()
     _check_inputs([q, k, v, dq, dk, dv], ["q", "k", "v", "dq", "dk", "dv"])
@@ -96,9 +98,17 @@ def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor
         o = torch.empty((B, H, Nq, D), dtype=q.dtype, device=q.device)
         t_o = torch.empty_like(o)
     else:
-        o, t_o = out
-    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if return_stats else None
-    mu = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if return_stats else None
+        o, t_o = out[0], out[1]
+    if out is not None and len(out) == 4:
+        lse, mu = out[2], out[3]
+        for t, n in ((lse, "lse"), (mu, "mu")):
+            if (t.dtype != torch.float32 or tuple(t.shape) != (B, H, Nq) or not t.is_contiguous()
+                    or t.device != q.device):
+                raise ValueError(f"out {n} must be a contiguous float32 [B, H, Nq] device tensor")
+        return_stats = True
+    else:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if return_stats else None
+        mu = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if return_stats else None
     mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
     ins = (_abi.Strides * 6)(*[_strides(t) for t in (q, k, v, dq, dk, dv)])
     outs = (_abi.Strides * 2)(_strides(o), _strides(t_o))

@@ -1,0 +1,48 @@
+"""GPU checks of the memory-scaling report and a tiny sequence-length sweep.
+
+The kernels allocate no device memory, so the bytes one call adds on top of
+its inputs are exactly its outputs (fwd_dual: O, tO and the float32 lse, mu;
+bwd_dual: six gradients plus the 8 B*H*Nq byte workspace), linear in N.  The
+sizes below are multiples of the caching allocator's 512-byte rounding, so the
+counts are exact.
+"""
+
+import pytest
+import torch
+
+from forward_mode_flash_gb300 import build, report
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_calls_add_exactly_their_outputs(mask):
+    B, H, D = 2, 8, 64
+    rows = list(report.memory_scaling(Ns=(256, 512, 1024), B=B, H=H, D=D, mask=mask))
+    for r in rows:
+        N = r["N"]
+        elem = 2  # bf16
+        fwd = 2 * B * H * N * D * elem + 2 * B * H * N * 4
+        bwd = 6 * B * H * N * D * elem + 8 * B * H * N
+        assert r["fwd_dual_added_mb"] * 2**20 == fwd, r
+        assert r["bwd_dual_added_mb"] * 2**20 == bwd, r
+    # reverse-over-forward through JVPAttn.fwd_dual: the same bytes per token at every N
+    per_token = [r["reverse_over_forward_added_bytes_per_token"] for r in rows]
+    assert max(per_token) <= 1.05 * min(per_token), per_token
+
+
+def test_sweep_rows_are_well_formed():
+    rows = list(report.sweep(dtypes=("bf16",), Ns=(64, 512), masks=("none", "bool"),
+                             graph_max_n=64))
+    assert [(r["N"], r["mask"]) for r in rows] == [(64, "none"), (64, "bool"), (512, "none"),
+                                                   (512, "bool")]
+    for r in rows:
+        assert r["path"] == "tensor-core"
+        assert r["ms_hot"] > 0 and r["ms_cold_l2"] > 0
+        assert (r["ms_graph_batch100"] is not None) == (r["N"] <= 64)
+    assert torch.cuda.memory_allocated() < 2**30
