@@ -18,6 +18,7 @@ JVP_OK, JVP_ERR_INVALID_ARG, JVP_ERR_UNSUPPORTED, JVP_ERR_ALIGNMENT = 0, 1, 2, 3
 JVP_ERR_CUDA, JVP_ERR_DEVICE_TIMEOUT, JVP_ERR_WORKSPACE = 4, 5, 6
 JVP_F32, JVP_F16, JVP_BF16 = 0, 1, 2
 JVP_MASK_NONE, JVP_MASK_BOOL, JVP_MASK_ADDITIVE, JVP_MASK_CAUSAL = 0, 1, 2, 3
+JVP_MASK_BOOL_CAUSAL, JVP_MASK_ADDITIVE_CAUSAL = 4, 5
 
 # Every function the header declares (checked against the library's exports).
 EXPORTS = (
@@ -36,8 +37,9 @@ EXPORTS = (
 
 
 class Shape(ctypes.Structure):
+    # Hkv = 0 means Hkv = H (no grouped-query attention)
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Nq", ctypes.c_int64),
-                ("Nk", ctypes.c_int64), ("D", ctypes.c_int64)]
+                ("Nk", ctypes.c_int64), ("D", ctypes.c_int64), ("Hkv", ctypes.c_int64)]
 
 
 class Strides(ctypes.Structure):

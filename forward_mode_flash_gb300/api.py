@@ -28,7 +28,15 @@ def _strides(t: torch.Tensor) -> _abi.Strides:
     return _abi.Strides(sb, sh, sn, sd)
 
 
-def _check_inputs(tensors, names):
+_KV_NAMES = frozenset(("k", "v", "dk", "dv"))
+
+
+def _check_inputs(tensors, names) -> int:
+    """Checks dtype, device, rank and sizes; returns the key/value head count.
+
+    Key-side tensors (k, v, dk, dv) may have fewer heads than the queries
+    (grouped-query attention) as long as the query heads are a multiple.
+    """
     ref = tensors[0]
     if ref.dim() != 4:
         raise ValueError(f"{names[0]} must be [B, H, N, D], got {tuple(ref.shape)}")
@@ -36,29 +44,40 @@ def _check_inputs(tensors, names):
         raise TypeError(f"unsupported dtype {ref.dtype}")
     if ref.device.type != "cuda":
         raise ValueError("tensors must be on a CUDA device")
+    H = ref.shape[1]
+    hkv = next((t.shape[1] for t, n in zip(tensors, names) if n in _KV_NAMES and t.dim() == 4), H)
+    if hkv <= 0 and H > 0 or (hkv > 0 and H % hkv != 0):
+        raise ValueError(f"query heads ({H}) must be a multiple of key/value heads ({hkv})")
     for t, n in zip(tensors, names):
         if t.dtype != ref.dtype or t.device != ref.device or t.dim() != 4:
             raise ValueError(f"{n} must be a 4-D {ref.dtype} tensor on {ref.device}")
-        if t.shape[-1] != ref.shape[-1] or t.shape[0] != ref.shape[0] or t.shape[1] != ref.shape[1]:
+        heads = hkv if n in _KV_NAMES else H
+        if t.shape[-1] != ref.shape[-1] or t.shape[0] != ref.shape[0] or t.shape[1] != heads:
             raise ValueError(f"{n} has shape {tuple(t.shape)}, inconsistent with {tuple(ref.shape)}")
         if t.stride(-1) != 1 and t.numel() > 0:
             raise ValueError(f"{n} must have a unit innermost stride")
+    return hkv
 
 
 def _mask_desc(attn_mask: Optional[torch.Tensor], is_causal: bool, B, H, Nq, Nk, device):
-    """Mask description (and the tensor it points into, kept alive by the caller)."""
-    if is_causal:
-        if attn_mask is not None:
-            raise ValueError("is_causal cannot be combined with attn_mask")
-        return _abi.Mask(_abi.JVP_MASK_CAUSAL, None, 0, 0, 0, 0), None
+    """Mask description (and the tensor it points into, kept alive by the caller).
+
+    ``is_causal`` together with ``attn_mask`` keeps a key only where both do
+    (an extension: scaled_dot_product_attention rejects the combination).
+    """
     if attn_mask is None:
-        return _abi.Mask(_abi.JVP_MASK_NONE, None, 0, 0, 0, 0), None
+        kind = _abi.JVP_MASK_CAUSAL if is_causal else _abi.JVP_MASK_NONE
+        return _abi.Mask(kind, None, 0, 0, 0, 0), None
     if attn_mask.device != device:
         raise ValueError("attn_mask must be on the same device as q")
     if attn_mask.dtype == torch.bool:
         kind, m = _abi.JVP_MASK_BOOL, attn_mask.view(torch.uint8)
+        if is_causal:
+            kind = _abi.JVP_MASK_BOOL_CAUSAL
     elif attn_mask.dtype == torch.float32:
         kind, m = _abi.JVP_MASK_ADDITIVE, attn_mask
+        if is_causal:
+            kind = _abi.JVP_MASK_ADDITIVE_CAUSAL
     else:
         raise TypeError("attn_mask must be torch.bool (keep-mask) or torch.float32 (additive)")
     while m.dim() < 4:
@@ -84,7 +103,7 @@ def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor
     four-tuple implies ``return_stats``).
     """
     lib = _abi.load()
-    _check_inputs([q, k, v, dq, dk, dv], ["q", "k", "v", "dq", "dk", "dv"])
+    hkv = _check_inputs([q, k, v, dq, dk, dv], ["q", "k", "v", "dq", "dk", "dv"])
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
     for t, n in ((v, "v"), (dk, "dk"), (dv, "dv")):
@@ -112,7 +131,7 @@ def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor
     mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
     ins = (_abi.Strides * 6)(*[_strides(t) for t in (q, k, v, dq, dk, dv)])
     outs = (_abi.Strides * 2)(_strides(o), _strides(t_o))
-    shape = _abi.Shape(B, H, Nq, Nk, D)
+    shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
     stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
         st = lib.jvp_attn_fwd_dual(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v),
@@ -131,7 +150,7 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
               out: Optional[torch.Tensor] = None):
     """Attention forward only (no tangents): o, or (o, lse) with ``return_lse``."""
     lib = _abi.load()
-    _check_inputs([q, k, v], ["q", "k", "v"])
+    hkv = _check_inputs([q, k, v], ["q", "k", "v"])
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
     if v.shape[2] != Nk:
@@ -143,7 +162,7 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
     ins = (_abi.Strides * 3)(*[_strides(t) for t in (q, k, v)])
     outs = (_abi.Strides * 1)(_strides(o))
-    shape = _abi.Shape(B, H, Nq, Nk, D)
+    shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
     stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
         st = lib.jvp_attn_fwd(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), ins,
@@ -170,8 +189,8 @@ def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
     not given; its size is ``bwd_dual_workspace_size``.
     """
     lib = _abi.load()
-    _check_inputs([q, k, v, dq, dk, dv, o, t_o, g_o, g_to],
-                  ["q", "k", "v", "dq", "dk", "dv", "o", "t_o", "g_o", "g_to"])
+    hkv = _check_inputs([q, k, v, dq, dk, dv, o, t_o, g_o, g_to],
+                        ["q", "k", "v", "dq", "dk", "dv", "o", "t_o", "g_o", "g_to"])
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
     if scale is None:
@@ -186,7 +205,7 @@ def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
     mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
     ins = (_abi.Strides * 10)(*[_strides(t) for t in (q, k, v, dq, dk, dv, o, t_o, g_o, g_to)])
     ost = (_abi.Strides * 6)(*[_strides(t) for t in outs])
-    shape = _abi.Shape(B, H, Nq, Nk, D)
+    shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
     stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
         st = lib.jvp_attn_bwd_dual(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v),
@@ -218,6 +237,8 @@ def fwd_dual_host(q, k, v, dq, dk, dv, attn_mask: Optional[torch.Tensor] = None,
     for t in (q, k, v, dq, dk, dv):
         if t.device.type != "cpu" or not t.is_contiguous():
             raise ValueError("fwd_dual_host takes contiguous CPU tensors")
+    if k.shape[1] != H:
+        raise ValueError("fwd_dual_host needs as many key/value heads as query heads")
     if attn_mask is not None and attn_mask.dim() == 4 and (attn_mask.shape[0] != 1 or
                                                            attn_mask.shape[1] != 1):
         raise ValueError("fwd_dual_host needs a mask shared by all batches and heads")

@@ -70,10 +70,16 @@ __device__ __forceinline__ float group_sum(float x, int width) {
   return x;
 }
 
+// Causal alone, or on top of a bool / additive mask.
+__device__ __forceinline__ bool is_causal(const BwdParams& p) {
+  return p.mask_kind == kMaskCausal || p.causal != 0;
+}
+
 // Whether key j takes part in row i, and the additive bias.
 __device__ __forceinline__ bool keep_ij(const BwdParams& p, int b, int h, int i, int j,
                                         float* bias) {
   *bias = 0.f;
+  if (p.causal && j > i) return false;
   switch (p.mask_kind) {
     case kMaskCausal:
       return j <= i;
@@ -163,9 +169,10 @@ __global__ void __launch_bounds__(kThreads) bwd_keys_kernel(BwdParams p, int par
 
   const int keys_per_block = kThreads / parts;
   const int n_blocks = (p.Nk + keys_per_block - 1) / keys_per_block;
-  const int bh = blockIdx.x / n_blocks;
+  const int Hkv = p.H / p.kv_group;
+  const int bhk = blockIdx.x / n_blocks;  // (batch, key/value head)
   const int kb = blockIdx.x % n_blocks;
-  const int b = bh / p.H, h = bh % p.H;
+  const int b = bhk / Hkv, hk = bhk % Hkv;
   const int part = threadIdx.x % parts;
   const int j = kb * keys_per_block + threadIdx.x / parts;
   const bool key_ok = j < p.Nk;
@@ -177,16 +184,19 @@ __global__ void __launch_bounds__(kThreads) bwd_keys_kernel(BwdParams p, int par
   for (int e = 0; e < kPart; ++e) {
     const int d = part * kPart + e;
     const bool in = key_ok && d < D;
-    k_[e] = in ? ld(row_ptr<T>(p.k, p.sk, b, h, j) + d) : 0.f;
-    dk_[e] = in ? ld(row_ptr<T>(p.dk, p.sdk, b, h, j) + d) : 0.f;
-    v_[e] = in ? ld(row_ptr<T>(p.v, p.sv, b, h, j) + d) : 0.f;
-    dv_[e] = in ? ld(row_ptr<T>(p.dv, p.sdv, b, h, j) + d) : 0.f;
+    k_[e] = in ? ld(row_ptr<T>(p.k, p.sk, b, hk, j) + d) : 0.f;
+    dk_[e] = in ? ld(row_ptr<T>(p.dk, p.sdk, b, hk, j) + d) : 0.f;
+    v_[e] = in ? ld(row_ptr<T>(p.v, p.sv, b, hk, j) + d) : 0.f;
+    dv_[e] = in ? ld(row_ptr<T>(p.dv, p.sdv, b, hk, j) + d) : 0.f;
     gk[e] = gdk[e] = gv[e] = gdv[e] = 0.f;
   }
 
   // Causal: rows before the block's first key keep none of its keys.
-  const int i_begin = (p.mask_kind == kMaskCausal) ? kb * keys_per_block : 0;
-  const long long rbase = static_cast<long long>(bh) * p.Nq;
+  const int i_begin = is_causal(p) ? kb * keys_per_block : 0;
+  // Grouped-query attention: the key/value head serves kv_group query heads,
+  // whose contributions all add into its gradients.
+  for (int h = hk * p.kv_group; h < (hk + 1) * p.kv_group; ++h) {
+  const long long rbase = (static_cast<long long>(b) * p.H + h) * p.Nq;
   for (int i0 = i_begin; i0 < p.Nq; i0 += kChunk) {
     const int ni = min(kChunk, p.Nq - i0);
     __syncthreads();
@@ -254,15 +264,16 @@ __global__ void __launch_bounds__(kThreads) bwd_keys_kernel(BwdParams p, int par
       }
     }
   }
+  }  // query heads of the group
   if (!key_ok) return;
 #pragma unroll
   for (int e = 0; e < kPart; ++e) {
     const int d = part * kPart + e;
     if (d < D) {
-      st(static_cast<T*>(p.g_k) + b * p.sgk.b + h * p.sgk.h + static_cast<long long>(j) * p.sgk.n + d, gk[e]);
-      st(static_cast<T*>(p.g_dk) + b * p.sgdk.b + h * p.sgdk.h + static_cast<long long>(j) * p.sgdk.n + d, gdk[e]);
-      st(static_cast<T*>(p.g_v) + b * p.sgv.b + h * p.sgv.h + static_cast<long long>(j) * p.sgv.n + d, gv[e]);
-      st(static_cast<T*>(p.g_dv) + b * p.sgdv.b + h * p.sgdv.h + static_cast<long long>(j) * p.sgdv.n + d, gdv[e]);
+      st(static_cast<T*>(p.g_k) + b * p.sgk.b + hk * p.sgk.h + static_cast<long long>(j) * p.sgk.n + d, gk[e]);
+      st(static_cast<T*>(p.g_dk) + b * p.sgdk.b + hk * p.sgdk.h + static_cast<long long>(j) * p.sgdk.n + d, gdk[e]);
+      st(static_cast<T*>(p.g_v) + b * p.sgv.b + hk * p.sgv.h + static_cast<long long>(j) * p.sgv.n + d, gv[e]);
+      st(static_cast<T*>(p.g_dv) + b * p.sgdv.b + hk * p.sgdv.h + static_cast<long long>(j) * p.sgdv.n + d, gdv[e]);
     }
   }
 }
@@ -283,6 +294,7 @@ __global__ void __launch_bounds__(kThreads) bwd_queries_kernel(BwdParams p, int 
   const int bh = blockIdx.x / n_blocks;
   const int qb = blockIdx.x % n_blocks;
   const int b = bh / p.H, h = bh % p.H;
+  const int hk = h / p.kv_group;  // key/value head (grouped-query attention)
   const int part = threadIdx.x % parts;
   const int i = qb * rows_per_block + threadIdx.x / parts;
   const bool row_ok = i < p.Nq;
@@ -306,16 +318,16 @@ __global__ void __launch_bounds__(kThreads) bwd_queries_kernel(BwdParams p, int 
   }
 
   int j_end = p.Nk;
-  if (p.mask_kind == kMaskCausal) j_end = min(j_end, min(p.Nq, (qb + 1) * rows_per_block));
+  if (is_causal(p)) j_end = min(j_end, min(p.Nq, (qb + 1) * rows_per_block));
   for (int j0 = 0; j0 < j_end; j0 += kChunk) {
     const int nj = min(kChunk, j_end - j0);
     __syncthreads();
     for (int x = threadIdx.x; x < nj * D; x += blockDim.x) {
       const int r = x / D, d = x % D, at = r * stride + sm_pos(d, parts);
-      sK[at] = ld(row_ptr<T>(p.k, p.sk, b, h, j0 + r) + d);
-      sdK[at] = ld(row_ptr<T>(p.dk, p.sdk, b, h, j0 + r) + d);
-      sV[at] = ld(row_ptr<T>(p.v, p.sv, b, h, j0 + r) + d);
-      sdV[at] = ld(row_ptr<T>(p.dv, p.sdv, b, h, j0 + r) + d);
+      sK[at] = ld(row_ptr<T>(p.k, p.sk, b, hk, j0 + r) + d);
+      sdK[at] = ld(row_ptr<T>(p.dk, p.sdk, b, hk, j0 + r) + d);
+      sV[at] = ld(row_ptr<T>(p.v, p.sv, b, hk, j0 + r) + d);
+      sdV[at] = ld(row_ptr<T>(p.dv, p.sdv, b, hk, j0 + r) + d);
     }
     for (int x = threadIdx.x; x < stride * kChunk; x += blockDim.x) {
       const int q = x % stride;
@@ -392,7 +404,8 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t stream) {
                            static_cast<int>(smem_q));
   if (e != cudaSuccess) return e;
   const long long per_block = kThreads / parts;
-  const long long kblocks = static_cast<long long>(p.B) * p.H * ((p.Nk + per_block - 1) / per_block);
+  const long long kblocks =
+      static_cast<long long>(p.B) * (p.H / p.kv_group) * ((p.Nk + per_block - 1) / per_block);
   const long long qblocks = static_cast<long long>(p.B) * p.H * ((p.Nq + per_block - 1) / per_block);
   if (kblocks > 0) {
     bwd_keys_kernel<T><<<static_cast<unsigned>(kblocks), kThreads, smem_k, stream>>>(p, parts);

@@ -128,11 +128,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int Gg = min(G, BH - g * G);
   const int q_rank = rem / Gg;
   const int bh = g * G + rem % Gg;
-  const int qt = (MASK == kMaskCausal) ? nq - 1 - q_rank : q_rank;
+  // Causal alone, or on top of a bool / additive mask (runtime flag).
+  const bool causal =
+      (MASK == kMaskCausal) || ((MASK == kMaskBool || MASK == kMaskAdditive) && p.causal != 0);
+  const int qt = causal ? nq - 1 - q_rank : q_rank;
   const int b = bh / p.H, h = bh % p.H;
+  const int hk = h / p.kv_group;  // key/value head (grouped-query attention)
   const int q0 = qt * BM;
   int n_kv = (p.Nk + BN - 1) / BN;
-  if (MASK == kMaskCausal) n_kv = min(n_kv, (min(q0 + BM, p.Nq) - 1) / BN + 1);
+  if (causal) n_kv = min(n_kv, (min(q0 + BM, p.Nq) - 1) / BN + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
@@ -181,8 +185,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint8_t* kb = smem + L::OFF_K + s * L::KBLK;
         mbar_arrive_expect_tx(&ctrl->k_full[s], L::KBLK);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(kb + c * L::KCHUNK, &maps.k, &ctrl->k_full[s], c * 64, j0, h, b);
-          tma_load_4d(kb + c * L::KCHUNK + BN * 128, &maps.dk, &ctrl->k_full[s], c * 64, j0, h, b);
+          tma_load_4d(kb + c * L::KCHUNK, &maps.k, &ctrl->k_full[s], c * 64, j0, hk, b);
+          tma_load_4d(kb + c * L::KCHUNK + BN * 128, &maps.dk, &ctrl->k_full[s], c * 64, j0, hk, b);
         }
         ++kf;
         if (!mbar_wait(&ctrl->v_empty[s], ph ^ 1, abort)) {
@@ -192,8 +196,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint8_t* vb = smem + L::OFF_V + s * L::KBLK;
         mbar_arrive_expect_tx(&ctrl->v_full[s], L::KBLK);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(vb + c * L::KCHUNK, &maps.v, &ctrl->v_full[s], c * 64, j0, h, b);
-          tma_load_4d(vb + c * L::KCHUNK + BN * 128, &maps.dv, &ctrl->v_full[s], c * 64, j0, h, b);
+          tma_load_4d(vb + c * L::KCHUNK, &maps.v, &ctrl->v_full[s], c * 64, j0, hk, b);
+          tma_load_4d(vb + c * L::KCHUNK + BN * 128, &maps.dv, &ctrl->v_full[s], c * 64, j0, hk, b);
         }
         ++vf;
       }
@@ -254,11 +258,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tc_fence_after();
-        // gS and g_dS of keys [16 kk, 16 kk + 16): written by warpgroup kk / 2.
+        // gS and g_dS of keys [16 kk, 16 kk + 16) (warpgroup kk / 2, half
+        // kk % 2): gS at columns 16 kk, g_dS at 16 kk + 8.
 #pragma unroll
         for (int kk = 0; kk < KSN; ++kk) {
-          const uint32_t a_gs = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
-          const uint32_t a_gds = a_gs + 16;
+          const uint32_t a_gs = tmem + kk * 16;
+          const uint32_t a_gds = a_gs + 8;
           const uint32_t kx = kb + kk * 16 * 128;  // MN-major: 16 keys per K-step
           const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
           if (D == 64) {
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
 #pragma unroll
         for (int kk = 0; kk < KSN; ++kk) {  // gQ += gS K
-          const uint32_t a_gs = tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+          const uint32_t a_gs = tmem + kk * 16;
           mma_ts(tmem + L::TM_ACC + D, a_gs,
                  sdesc_sw128(kb + kk * 16 * 128, D == 64 ? BN * 128 : L::KCHUNK, 1024), I_ACC1,
                  1u);
@@ -318,28 +323,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mp.Nk = p.Nk;
     mp.msk = p.msk;
     mp.mask_vec = 0;
-    for (int t = 0; t < n_kv; ++t) {
-      const int j0 = t * BN + wg * 32;
-      MaskRegs<MASK, 32> mreg;
-      if (row_ok) mreg.load(mp, mrow, j0);
-      if (!warp_wait(&ctrl->s_full, t & 1, status, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t rs[32], rds[32], rg[32], rgp[32];
-      tmem_ld32x2(lb + L::TM_S + wg * 32, lb + L::TM_DS + wg * 32, rs, rds);
-      tmem_ld32x2(lb + L::TM_G + wg * 32, lb + L::TM_GP + wg * 32, rg, rgp);
-      uint32_t pgs[16], pgds[16];
+    // One half of this warpgroup's 32 keys of a tile: gS and g_dS go into
+    // the 16 columns of S the half has just read (gS first, g_dS next), so
+    // the other half's inputs stay intact.
+    auto half = [&](int j0h, uint32_t col, const MaskRegs<MASK, 16>& mreg) {
+      uint32_t rs[16], rds[16], rg[16], rgp[16];
+      tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_DS + col, rs, rds);
+      tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
+      uint32_t pgs[8], pgds[8];
 #pragma unroll
-      for (int jj = 0; jj < 32; jj += 2) {
+      for (int jj = 0; jj < 16; jj += 2) {
         float gs[2], gds[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int j = j0 + jj + e;
+          const int j = j0h + jj + e;
           bool keep = live && j < p.Nk;
           float x = fmaf(__uint_as_float(rs[jj + e]), c, -lse2);
-          if constexpr (MASK == kMaskCausal) keep = keep && j <= i;
+          if (causal) keep = keep && j <= i;
           if constexpr (MASK == kMaskBool) keep = keep && mreg.keep(jj + e);
           if constexpr (MASK == kMaskAdditive) {
             x = fmaf(mreg.a[jj + e], kLog2e, x);
@@ -354,8 +354,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pgs[jj >> 1] = ElemTraits<T>::pack(gs[0], gs[1]);
         pgds[jj >> 1] = ElemTraits<T>::pack(gds[0], gds[1]);
       }
-      tmem_st16(lb + wg * 32, pgs);        // gS over this warpgroup's S columns
-      tmem_st16(lb + wg * 32 + 16, pgds);  // g_dS next to it
+      tmem_st8(lb + col, pgs);
+      tmem_st8(lb + col + 8, pgds);
+    };
+    for (int t = 0; t < n_kv; ++t) {
+      const int j0 = t * BN + wg * 32;
+      MaskRegs<MASK, 16> m0, m1;
+      if (row_ok) m0.load(mp, mrow, j0);
+      if (!warp_wait(&ctrl->s_full, t & 1, status, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (row_ok) m1.load(mp, mrow, j0 + 16);
+      half(j0, wg * 32, m0);
+      half(j0 + 16, wg * 32 + 16, m1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctrl->p_full);
@@ -464,20 +477,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort = &ctrl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int BH = p.B * p.H;
+  // One CTA per (batch, key/value head, key tile); with grouped-query
+  // attention it visits the query tiles of every query head of its group.
+  const int Hkv = p.H / p.kv_group;
+  const int BH = p.B * Hkv;
   const int nk = (p.Nk + BK - 1) / BK;
   const int G = group_heads;
   const int g = blockIdx.x / (G * nk);
   const int rem = blockIdx.x - g * G * nk;
   const int Gg = min(G, BH - g * G);
   const int k_rank = rem / Gg;
-  const int bh = g * G + rem % Gg;
+  const int bhk = g * G + rem % Gg;
   const int kt = k_rank;  // causal: the first key tiles see the most query rows
-  const int b = bh / p.H, h = bh % p.H;
+  const int b = bhk / Hkv, hk = bhk % Hkv;
   const int j0 = kt * BK;
   const int nqt = (p.Nq + BQ - 1) / BQ;
-  const int t_begin = (MASK == kMaskCausal) ? min(j0 / BQ, nqt) : 0;  // rows i >= j0 only
-  const int n_t = nqt - t_begin;
+  const bool causal =
+      (MASK == kMaskCausal) || ((MASK == kMaskBool || MASK == kMaskAdditive) && p.causal != 0);
+  const int t_begin = causal ? min(j0 / BQ, nqt) : 0;  // rows i >= j0 only
+  const int n_th = nqt - t_begin;                       // query tiles per query head
+  const int n_t = n_th * p.kv_group;                    // tiles over the whole group
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->k_full, 1);
@@ -500,7 +519,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
-  const long long rbase = static_cast<long long>(bh) * p.Nq;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -511,11 +529,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(&ctrl->k_full, (L::kK ? 4 : 2) * L::KT_BYTES);
       for (int c = 0; c < L::KCH; ++c) {
         const int o = c * BK * 128;
-        tma_load_4d(smem + L::OFF_K + o, &maps.k, &ctrl->k_full, c * 64, j0, h, b);
-        tma_load_4d(smem + L::OFF_DK + o, &maps.dk, &ctrl->k_full, c * 64, j0, h, b);
+        tma_load_4d(smem + L::OFF_K + o, &maps.k, &ctrl->k_full, c * 64, j0, hk, b);
+        tma_load_4d(smem + L::OFF_DK + o, &maps.dk, &ctrl->k_full, c * 64, j0, hk, b);
         if (L::kK) {
-          tma_load_4d(smem + L::OFF_V + o, &maps.v, &ctrl->k_full, c * 64, j0, h, b);
-          tma_load_4d(smem + L::OFF_DV + o, &maps.dv, &ctrl->k_full, c * 64, j0, h, b);
+          tma_load_4d(smem + L::OFF_V + o, &maps.v, &ctrl->k_full, c * 64, j0, hk, b);
+          tma_load_4d(smem + L::OFF_DV + o, &maps.dv, &ctrl->k_full, c * 64, j0, hk, b);
         }
       }
     }
@@ -523,7 +541,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int t = 0; t < n_t; ++t) {
       const int s = t % NS;
       const uint32_t ph = (t / NS) & 1;
-      const int i0 = (t_begin + t) * BQ;
+      const int h = hk * p.kv_group + t / n_th;  // query head of this tile
+      const int i0 = (t_begin + t % n_th) * BQ;
+      const long long rbase = (static_cast<long long>(b) * p.H + h) * p.Nq;
       bool got = true;
       if (lane == 0) got = mbar_wait(&ctrl->q_empty[s], ph ^ 1, abort);
       if (!__shfl_sync(0xffffffffu, got, 0)) {
@@ -678,7 +698,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
       const int st_i = t % NS;
-      const int i0 = (t_begin + t) * BQ + wg * 32;  // first query row of this half tile
+      const int h = hk * p.kv_group + t / n_th;                  // query head of this tile
+      const int i0 = (t_begin + t % n_th) * BQ + wg * 32;  // first query row of this half tile
       if (!warp_wait(&ctrl->s_full, t & 1, status, abort) ||
           !warp_wait(&ctrl->q_full[st_i], (t / NS) & 1, status, abort)) {
         ok = false;
@@ -687,6 +708,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const float4* rsc =
           reinterpret_cast<const float4*>(smem + L::OFF_ST + st_i * L::STAGE + 2 * L::QBLK) + wg * 32;
+      // Mask entries of this thread's key for the tile's rows: base + i * msq.
+      const long long mcol = static_cast<long long>(b) * p.msb + static_cast<long long>(h) * p.msh +
+                             static_cast<long long>(key_ok ? j : 0) * p.msk;
       // Two halves of 16 query rows keep the register footprint small.
 #pragma unroll 1
       for (int hq = 0; hq < 2; ++hq) {
@@ -704,18 +728,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float4 rv = rsc[hq * 16 + qq + e];  // lse2, mu, nu, delta (one broadcast read)
             bool keep = key_ok && rv.x != -INFINITY;  // false for rows past Nq
             float x = fmaf(__uint_as_float(rs[qq + e]), c, -rv.x);
-            if constexpr (MASK == kMaskCausal) keep = keep && j <= i;
+            if (causal) keep = keep && j <= i;
             if constexpr (MASK == kMaskBool) {
               if (keep)
-                keep = static_cast<const uint8_t*>(p.mask)[b * p.msb + h * p.msh +
-                                                           static_cast<long long>(i) * p.msq +
-                                                           static_cast<long long>(j) * p.msk] != 0;
+                keep = static_cast<const uint8_t*>(p.mask)[mcol + static_cast<long long>(i) * p.msq] != 0;
             }
             if constexpr (MASK == kMaskAdditive) {
-              const float m = keep ? static_cast<const float*>(p.mask)[b * p.msb + h * p.msh +
-                                                                       static_cast<long long>(i) * p.msq +
-                                                                       static_cast<long long>(j) * p.msk]
-                                   : 0.f;
+              const float m =
+                  keep ? static_cast<const float*>(p.mask)[mcol + static_cast<long long>(i) * p.msq]
+                       : 0.f;
               x = fmaf(m, kLog2e, x);
               keep = keep && x != -INFINITY;
             }
@@ -763,7 +784,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t acol = which == 0 ? A_GDV : which == 1 ? A_GV : which == 2 ? A_GDK : A_GK;
         const float scl = which >= 2 ? s : 1.0f;
         T* row = static_cast<T*>(dst) + static_cast<long long>(b) * ds.b +
-                 static_cast<long long>(h) * ds.h + static_cast<long long>(key_ok ? j : 0) * ds.n;
+                 static_cast<long long>(hk) * ds.h + static_cast<long long>(key_ok ? j : 0) * ds.n;
 #pragma unroll 1
         for (int col = 0; col < D; col += 32) {
           uint32_t a[32];
@@ -836,8 +857,9 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
     cudaError_t e = set_smem<kern>(L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int nk = (p.Nk + L::BK - 1) / L::BK;
-    const int G = max(1, min(BH, num_sms / max(1, nk)));
-    kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BH), kBwdThreads, L::SMEM_BYTES,
+    const int BHk = p.B * (p.H / p.kv_group);
+    const int G = max(1, min(BHk, num_sms / max(1, nk)));
+    kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk), kBwdThreads, L::SMEM_BYTES,
            stream>>>(kmaps, p, G, status);
     return cudaGetLastError();
   };

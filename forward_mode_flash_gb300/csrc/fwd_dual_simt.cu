@@ -76,17 +76,21 @@ __global__ void __launch_bounds__(kRows * 32)
   const int n_row_blocks = (p.Nq + kRows - 1) / kRows;
   const int bh = blockIdx.x % (p.B * p.H);
   int rb = blockIdx.x / (p.B * p.H);
-  if (MASK == kMaskCausal) rb = n_row_blocks - 1 - rb;
+  // Causal alone, or on top of a bool / additive mask (runtime flag).
+  const bool causal =
+      (MASK == kMaskCausal) || ((MASK == kMaskBool || MASK == kMaskAdditive) && p.causal != 0);
+  if (causal) rb = n_row_blocks - 1 - rb;
   const int b = bh / p.H, h = bh % p.H;
+  const int hk = h / p.kv_group;  // key/value head (grouped-query attention)
   const int i = rb * kRows + warp;
   const bool row_ok = i < p.Nq;
 
   const T* q = static_cast<const T*>(p.q) + b * p.sq.b + h * p.sq.h;
-  const T* k = static_cast<const T*>(p.k) + b * p.sk.b + h * p.sk.h;
-  const T* v = static_cast<const T*>(p.v) + b * p.sv.b + h * p.sv.h;
+  const T* k = static_cast<const T*>(p.k) + b * p.sk.b + hk * p.sk.h;
+  const T* v = static_cast<const T*>(p.v) + b * p.sv.b + hk * p.sv.h;
   const T* dq = TANGENT ? static_cast<const T*>(p.dq) + b * p.sdq.b + h * p.sdq.h : nullptr;
-  const T* dk = TANGENT ? static_cast<const T*>(p.dk) + b * p.sdk.b + h * p.sdk.h : nullptr;
-  const T* dv = TANGENT ? static_cast<const T*>(p.dv) + b * p.sdv.b + h * p.sdv.h : nullptr;
+  const T* dk = TANGENT ? static_cast<const T*>(p.dk) + b * p.sdk.b + hk * p.sdk.h : nullptr;
+  const T* dv = TANGENT ? static_cast<const T*>(p.dv) + b * p.sdv.b + hk * p.sdv.h : nullptr;
 
   for (int d = lane; d < D; d += 32) {
     sQ[warp * D + d] = row_ok ? to_f32(q[static_cast<long long>(i) * p.sq.n + d]) : 0.f;
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(kRows * 32)
   }
 
   int n_keys = p.Nk;
-  if (MASK == kMaskCausal) n_keys = min(n_keys, min(rb * kRows + kRows, p.Nq));
+  if (causal) n_keys = min(n_keys, min(rb * kRows + kRows, p.Nq));
   const float* mrow_f = nullptr;
   const uint8_t* mrow_b = nullptr;
   if (row_ok) {
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(kRows * 32)
         bias = mrow_f[static_cast<long long>(j) * p.msk];
         keep = !(isinf(bias) && bias < 0.f);
       }
+      if (MASK != kMaskCausal && causal) keep = keep && j <= i;
     }
     float s_qk = 0.f, s_t = 0.f;
     if (keep) {

@@ -250,11 +250,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int Gg = min(G, BH - g * G);
   const int q_rank = rem / Gg;
   const int bh = g * G + rem % Gg;
-  const int qt = (MASK == kMaskCausal) ? nq - 1 - q_rank : q_rank;
+  // Causal alone, or on top of a bool / additive mask (runtime flag).
+  const bool causal =
+      (MASK == kMaskCausal) || ((MASK == kMaskBool || MASK == kMaskAdditive) && p.causal != 0);
+  const int qt = causal ? nq - 1 - q_rank : q_rank;
   const int b = bh / p.H, h = bh % p.H;
+  const int hk = h / p.kv_group;  // key/value head (grouped-query attention)
   const int q0 = qt * L::BM;
   int n_kv = (p.Nk + BN - 1) / BN;
-  if (MASK == kMaskCausal) {
+  if (causal) {
     const int last_row = min(q0 + L::BM, p.Nq) - 1;
     n_kv = min(n_kv, last_row / BN + 1);
   }
@@ -318,10 +322,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t* kdk = smem + L::OFF_KDK + s * L::KDK_BYTES;
         mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_BYTES);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(kdk + c * L::KCHUNK_BYTES, &maps.k, &ctrl->kdk_full[s], c * 64, j0, h, b);
+          tma_load_4d(kdk + c * L::KCHUNK_BYTES, &maps.k, &ctrl->kdk_full[s], c * 64, j0, hk, b);
           if (TANGENT)
             tma_load_4d(kdk + c * L::KCHUNK_BYTES + BN * 128, &maps.dk, &ctrl->kdk_full[s], c * 64,
-                        j0, h, b);
+                        j0, hk, b);
         }
         ++k_fills;
         if (!mbar_wait(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
@@ -331,10 +335,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t* vdv = smem + L::OFF_VDV + s * L::VDV_BYTES;
         mbar_arrive_expect_tx(&ctrl->vdv_full[s], L::VDV_BYTES);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(vdv + c * L::VCHUNK_BYTES, &maps.v, &ctrl->vdv_full[s], c * 64, j0, h, b);
+          tma_load_4d(vdv + c * L::VCHUNK_BYTES, &maps.v, &ctrl->vdv_full[s], c * 64, j0, hk, b);
           if (TANGENT)
             tma_load_4d(vdv + (L::KCH + c) * L::VCHUNK_BYTES, &maps.dv, &ctrl->vdv_full[s], c * 64,
-                        j0, h, b);
+                        j0, hk, b);
         }
         ++v_fills;
       }
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj >= p.Nk) x[jj] = -INFINITY;
       }
-      if (MASK == kMaskCausal && j0 + HN - 1 > q0) {
+      if (causal && j0 + HN - 1 > q0) {
 #pragma unroll
         for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj > i) x[jj] = -INFINITY;

@@ -130,6 +130,25 @@ bool strides_aligned16(const jvp_strides_t& s, size_t e) {
 
 Strides to_strides(const jvp_strides_t& s) { return Strides{s.b, s.h, s.n}; }
 
+// Key/value head count (0 = H) and its check: H must be a multiple of it.
+jvp_status_t kv_heads(const jvp_shape_t* shape, int64_t* hkv) {
+  const int64_t H = shape->H;
+  *hkv = shape->Hkv == 0 ? H : shape->Hkv;
+  if (shape->Hkv < 0) return fail(JVP_ERR_INVALID_ARG, "negative Hkv");
+  if (H > 0 && H % *hkv != 0)
+    return fail(JVP_ERR_INVALID_ARG, "H must be a multiple of Hkv (grouped-query attention)");
+  return JVP_OK;
+}
+
+// Mask kind as the kernels see it: the combined kinds become a bool or
+// additive mask plus the causal flag.
+void split_mask_kind(int kind, int* base, int* causal) {
+  *causal = (kind == JVP_MASK_BOOL_CAUSAL || kind == JVP_MASK_ADDITIVE_CAUSAL) ? 1 : 0;
+  *base = kind == JVP_MASK_BOOL_CAUSAL ? JVP_MASK_BOOL
+          : kind == JVP_MASK_ADDITIVE_CAUSAL ? JVP_MASK_ADDITIVE
+                                             : kind;
+}
+
 // Shared body of jvp_attn_fwd_dual and jvp_attn_fwd.
 jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* const* in,
                      const jvp_strides_t* in_strides, const jvp_mask_t* mask, float scale,
@@ -160,17 +179,21 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     if (s.d != 1) return fail(JVP_ERR_INVALID_ARG, "innermost (d) stride of an output must be 1");
     if (s.b < 0 || s.h < 0 || s.n < 0) return fail(JVP_ERR_INVALID_ARG, "negative stride");
   }
-  int kind = JVP_MASK_NONE;
+  int64_t Hkv = 0;
+  if (kv_heads(shape, &Hkv) != JVP_OK) return JVP_ERR_INVALID_ARG;
+  int kind = JVP_MASK_NONE, causal_flag = 0;
   const void* mptr = nullptr;
   int64_t msb = 0, msh = 0, msq = 0, msk = 0;
   if (mask) {
-    kind = mask->kind;
     mptr = mask->ptr;
     msb = mask->stride_b, msh = mask->stride_h, msq = mask->stride_q, msk = mask->stride_k;
-    if (kind < JVP_MASK_NONE || kind > JVP_MASK_CAUSAL)
+    if (mask->kind < JVP_MASK_NONE || mask->kind > JVP_MASK_ADDITIVE_CAUSAL)
       return fail(JVP_ERR_INVALID_ARG, "unknown mask kind");
+    split_mask_kind(mask->kind, &kind, &causal_flag);
     if (kind == JVP_MASK_CAUSAL && mptr)
-      return fail(JVP_ERR_INVALID_ARG, "a causal mask cannot be combined with a mask tensor");
+      return fail(JVP_ERR_INVALID_ARG,
+                  "JVP_MASK_CAUSAL takes no mask tensor (use JVP_MASK_BOOL_CAUSAL or "
+                  "JVP_MASK_ADDITIVE_CAUSAL)");
     if (kind == JVP_MASK_NONE && mptr)
       return fail(JVP_ERR_INVALID_ARG, "mask kind NONE with a mask tensor");
     if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && B * H * Nq * Nk > 0)
@@ -212,6 +235,8 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask = mptr;
   p.msb = msb, p.msh = msh, p.msq = msq, p.msk = msk;
+  p.causal = causal_flag;
+  p.kv_group = static_cast<int>(H / Hkv);
   const size_t me = (kind == JVP_MASK_ADDITIVE) ? 4 : 1;
   p.mask_vec = (mptr && msk == 1 && aligned(mptr, 16) && (msq * me) % 16 == 0 &&
                 (msh * me) % 16 == 0 && (msb * me) % 16 == 0)
@@ -245,9 +270,11 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   if (tc) {
     const int64_t Ns[6] = {Nq, Nk, Nk, Nq, Nk, Nk};
     CUtensorMap* dst[6] = {&maps.q, &maps.k, &maps.v, &maps.dq, &maps.dk, &maps.dv};
-    for (int t = 0; tc && t < n_in; ++t)
-      tc = encode_map(dst[t], dtype, in[t], B, H, Ns[t], D, in_strides[t],
-                      (t == 0 || t == 3) ? kTcBlockM : kTcBlockN);
+    for (int t = 0; tc && t < n_in; ++t) {
+      const bool on_q = (t == 0 || t == 3);
+      tc = encode_map(dst[t], dtype, in[t], B, on_q ? H : Hkv, Ns[t], D, in_strides[t],
+                      on_q ? kTcBlockM : kTcBlockN);
+    }
     if (tc && !tangent) {
       maps.dq = maps.q, maps.dk = maps.k, maps.dv = maps.v;
     }
@@ -299,15 +326,17 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
     if (s.d != 1) return fail(JVP_ERR_INVALID_ARG, "innermost (d) stride of an output must be 1");
     if (s.b < 0 || s.h < 0 || s.n < 0) return fail(JVP_ERR_INVALID_ARG, "negative stride");
   }
-  int kind = JVP_MASK_NONE;
+  int64_t Hkv = 0;
+  if (kv_heads(shape, &Hkv) != JVP_OK) return JVP_ERR_INVALID_ARG;
+  int kind = JVP_MASK_NONE, causal_flag = 0;
   const void* mptr = nullptr;
   int64_t msb = 0, msh = 0, msq = 0, msk = 0;
   if (mask) {
-    kind = mask->kind;
     mptr = mask->ptr;
     msb = mask->stride_b, msh = mask->stride_h, msq = mask->stride_q, msk = mask->stride_k;
-    if (kind < JVP_MASK_NONE || kind > JVP_MASK_CAUSAL)
+    if (mask->kind < JVP_MASK_NONE || mask->kind > JVP_MASK_ADDITIVE_CAUSAL)
       return fail(JVP_ERR_INVALID_ARG, "unknown mask kind");
+    split_mask_kind(mask->kind, &kind, &causal_flag);
     if ((kind == JVP_MASK_CAUSAL || kind == JVP_MASK_NONE) && mptr)
       return fail(JVP_ERR_INVALID_ARG, "this mask kind takes no mask tensor");
     if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && B * H * Nq * Nk > 0)
@@ -348,6 +377,8 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   p.Nk = static_cast<int>(Nk), p.D = static_cast<int>(D);
   p.scale = scale;
   p.mask_kind = kind;
+  p.causal = causal_flag;
+  p.kv_group = static_cast<int>(H / Hkv);
   p.mask = mptr;
   p.msb = msb, p.msh = msh, p.msq = msq, p.msk = msk;
   p.q = in[0], p.k = in[1], p.v = in[2], p.dq = in[3], p.dk = in[4], p.dv = in[5];
@@ -380,8 +411,8 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
       const int a = qidx[u], c = kidx[u];
       tc = encode_map(qdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 128) &&
            encode_map(kdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 64) &&
-           encode_map(qdst_k[u], dtype, in[c], B, H, Ns[c], D, in_strides[c], 64) &&
-           encode_map(kdst_k[u], dtype, in[c], B, H, Ns[c], D, in_strides[c], 128);
+           encode_map(qdst_k[u], dtype, in[c], B, Hkv, Ns[c], D, in_strides[c], 64) &&
+           encode_map(kdst_k[u], dtype, in[c], B, Hkv, Ns[c], D, in_strides[c], 128);
     }
   }
   cudaError_t err;
@@ -513,7 +544,7 @@ const char* jvp_attn_status_string(jvp_status_t status) {
 
 const char* jvp_attn_last_error(void) { return jvp::t_last_error.c_str(); }
 
-int jvp_attn_version(void) { return 100; }
+int jvp_attn_version(void) { return 200; }
 
 int jvp_attn_debug_last_path(void) { return jvp::t_last_path; }
 

@@ -25,6 +25,8 @@ struct FwdParams {
   const void* mask;  // uint8 (bool) or float (additive); nullptr otherwise
   long long msb, msh, msq, msk;  // mask element strides
   int mask_vec;      // 1: rows are 16-byte aligned and stride_k == 1 (vector loads)
+  int causal;        // 1: a bool / additive mask also keeps only keys j <= i
+  int kv_group;      // query heads per key/value head (grouped-query attention; 1 = none)
   // inputs (used by the CUDA-core kernel; the tensor-core kernel reads them by TMA)
   const void *q, *k, *v, *dq, *dk, *dv;
   Strides sq, sk, sv, sdq, sdk, sdv;
@@ -72,6 +74,8 @@ struct BwdParams {
   int B, H, Nq, Nk, D;
   float scale;
   int mask_kind;
+  int causal;    // 1: a bool / additive mask also keeps only keys j <= i
+  int kv_group;  // query heads per key/value head (grouped-query attention; 1 = none)
   const void* mask;
   long long msb, msh, msq, msk;
   const void *q, *k, *v, *dq, *dk, *dv, *o, *t_o, *g_o, *g_to;

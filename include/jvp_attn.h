@@ -57,20 +57,28 @@ typedef enum { JVP_F32 = 0, JVP_F16 = 1, JVP_BF16 = 2 } jvp_dtype_t;
 /* Mask kinds.  BOOL: uint8 elements, nonzero = the key takes part (SDPA's
  * boolean attn_mask).  ADDITIVE: float32 elements added to the scaled logits;
  * an entry of -inf excludes the key.  CAUSAL: key j takes part in row i iff
- * j <= i (top-left aligned); it uses no mask tensor, so a causal mask combined
- * with a mask tensor is rejected (JVP_ERR_INVALID_ARG). */
+ * j <= i (top-left aligned); it uses no mask tensor (CAUSAL with a mask tensor
+ * is rejected with JVP_ERR_INVALID_ARG).  BOOL_CAUSAL / ADDITIVE_CAUSAL: a
+ * BOOL / ADDITIVE mask tensor and, in addition, the causal rule (SDPA rejects
+ * is_causal together with attn_mask; these kinds are an extension, equal to
+ * the mask tensor with the entries j > i excluded). */
 typedef enum {
   JVP_MASK_NONE = 0,
   JVP_MASK_BOOL = 1,
   JVP_MASK_ADDITIVE = 2,
-  JVP_MASK_CAUSAL = 3
+  JVP_MASK_CAUSAL = 3,
+  JVP_MASK_BOOL_CAUSAL = 4,
+  JVP_MASK_ADDITIVE_CAUSAL = 5
 } jvp_mask_kind_t;
 
 typedef struct {
-  int64_t B, H; /* batch, heads */
+  int64_t B, H; /* batch, query heads */
   int64_t Nq;   /* query rows */
   int64_t Nk;   /* key / value rows */
   int64_t D;    /* head dimension, 1..128 */
+  int64_t Hkv;  /* key / value heads: 0 means H.  Otherwise H must be a multiple
+                   of Hkv and query head h reads key / value head
+                   h / (H / Hkv) (grouped-query attention). */
 } jvp_shape_t;
 
 /* Element strides of a [B, H, N, D] tensor; d must be 1. */
@@ -93,7 +101,7 @@ typedef struct {
  *   shape          sizes; B*H*Nq == 0 or Nk == 0 is valid (nothing to compute
  *                  beyond writing the empty-row convention when Nk == 0).
  *   dtype          element type shared by q, k, v, dq, dk, dv, o and t_o.
- *   q, dq          [B,H,Nq,D];  k, v, dk, dv [B,H,Nk,D]  (device, read only).
+ *   q, dq          [B,H,Nq,D];  k, v, dk, dv [B,Hkv,Nk,D]  (device, read only).
  *   in_strides     6 stride records, in the order q, k, v, dq, dk, dv.
  *   mask           NULL or a mask description (see jvp_mask_t).
  *   scale          logit scale (SDPA's default is 1/sqrt(D)); must be finite.
@@ -137,15 +145,21 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
  *   g_o, g_to             cotangents, [B,H,Nq,D]
  *   in_strides            10 records: q, k, v, dq, dk, dv, o, t_o, g_o, g_to
  *   g_q, g_k, g_v, g_dq, g_dk, g_dv   outputs, shapes of q, k, v, dq, dk, dv
+ *                         (with grouped-query attention g_k, g_v, g_dk, g_dv
+ *                         sum the contributions of every query head of the
+ *                         group)
  *   out_strides           6 records in that order
  *   workspace             device scratch of at least
  *                         jvp_attn_bwd_dual_workspace_size() bytes, 4-byte
  *                         aligned, owned by the caller; its contents on entry
  *                         do not matter and are overwritten.
  *
- * Every tensor has the same dtype; mask and scale as in the forward call.  The
- * computation runs on CUDA cores in fp32 (three kernels, enqueued on
- * `stream`).  Returns JVP_ERR_WORKSPACE if the workspace is NULL or too small.
+ * Every tensor has the same dtype; mask and scale as in the forward call.
+ * fp16/bf16 with D in {64, 128} and 16-byte aligned tensors run a row pass
+ * and tcgen05 kernels (query-major for g_q, g_dq; key-major for g_k, g_dk,
+ * g_v, g_dv), fp32 accumulation; every other case runs three CUDA-core
+ * kernels in fp32.  All are enqueued on `stream`.  Returns JVP_ERR_WORKSPACE
+ * if the workspace is NULL or too small.
  */
 jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
                                const void* k, const void* v, const void* dq, const void* dk,

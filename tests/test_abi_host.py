@@ -37,7 +37,7 @@ def test_library_loads_and_exports_every_declared_symbol(lib):
     assert len(names) >= 8
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.jvp_attn_version() == 100
+    assert lib.jvp_attn_version() == 200
 
 
 def test_status_strings(lib):
@@ -55,9 +55,9 @@ def _strides(n, shape):
 
 
 def call_fwd_dual(lib, shape=(1, 2, 64, 64), dtype=_abi.JVP_BF16, ptrs=0x1000, mask=None,
-                  scale=0.125, in_strides=None, out_strides=None):
+                  scale=0.125, in_strides=None, out_strides=None, hkv=0):
     B, H, N, D = shape
-    sh = _abi.Shape(B, H, N, N, D)
+    sh = _abi.Shape(B, H, N, N, D, hkv)
     p = ctypes.c_void_p(ptrs) if ptrs else None
     ins = in_strides if in_strides is not None else _strides(6, shape)
     outs = out_strides if out_strides is not None else _strides(2, shape)
@@ -99,3 +99,21 @@ def test_empty_problems_succeed_without_a_device(lib):
 def test_selftest_rejects_bad_limits(lib):
     assert lib.jvp_attn_selftest_wait_timeout(0, None) == _abi.JVP_ERR_INVALID_ARG
     assert lib.jvp_attn_selftest_wait_timeout(1 << 31, None) == _abi.JVP_ERR_INVALID_ARG
+
+
+def test_grouped_heads_and_combined_masks_are_validated_without_a_device(lib):
+    # H must be a multiple of Hkv; Hkv = 0 means H
+    assert call_fwd_dual(lib, shape=(1, 8, 64, 64), hkv=3) == _abi.JVP_ERR_INVALID_ARG
+    assert b"multiple of Hkv" in lib.jvp_attn_last_error()
+    assert call_fwd_dual(lib, shape=(1, 8, 64, 64), hkv=-2) == _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, shape=(0, 8, 64, 64), hkv=2, ptrs=0) == _abi.JVP_OK
+    assert call_fwd_dual(lib, shape=(0, 8, 64, 64), hkv=8, ptrs=0) == _abi.JVP_OK
+    # the combined kinds need a mask tensor; CAUSAL alone takes none
+    for kind in (_abi.JVP_MASK_BOOL_CAUSAL, _abi.JVP_MASK_ADDITIVE_CAUSAL):
+        assert call_fwd_dual(lib, mask=_abi.Mask(kind, None, 0, 0, 64, 1)) == \
+            _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, mask=_abi.Mask(6, 0x2000, 0, 0, 64, 1)) == _abi.JVP_ERR_INVALID_ARG
+    assert call_fwd_dual(lib, mask=_abi.Mask(_abi.JVP_MASK_CAUSAL, 0x2000, 0, 0, 64, 1)) == \
+        _abi.JVP_ERR_INVALID_ARG
+    assert b"BOOL_CAUSAL" in lib.jvp_attn_last_error()
+
