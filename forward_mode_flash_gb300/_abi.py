@@ -23,6 +23,8 @@ JVP_MASK_BOOL_CAUSAL, JVP_MASK_ADDITIVE_CAUSAL = 4, 5
 # Every function the header declares (checked against the library's exports).
 EXPORTS = (
     "jvp_attn_fwd_dual",
+    "jvp_attn_fwd_dual_ws",
+    "jvp_attn_fwd_dual_workspace_size",
     "jvp_attn_fwd",
     "jvp_attn_bwd_dual",
     "jvp_attn_bwd_dual_workspace_size",
@@ -80,6 +82,11 @@ def load(path: str | None = None):
         lib.jvp_attn_fwd_dual.argtypes = [SP, i32, vp, vp, vp, vp, vp, vp, STP, MP, f32, vp, vp,
                                           STP, vp, vp, vp]
         lib.jvp_attn_fwd_dual.restype = i32
+        lib.jvp_attn_fwd_dual_ws.argtypes = lib.jvp_attn_fwd_dual.argtypes[:-1] + \
+            [vp, ctypes.c_size_t, vp]
+        lib.jvp_attn_fwd_dual_ws.restype = i32
+        lib.jvp_attn_fwd_dual_workspace_size.argtypes = [SP, i32]
+        lib.jvp_attn_fwd_dual_workspace_size.restype = ctypes.c_size_t
         lib.jvp_attn_fwd.argtypes = [SP, i32, vp, vp, vp, STP, MP, f32, vp, STP, vp, vp]
         lib.jvp_attn_fwd.restype = i32
         lib.jvp_attn_bwd_dual.argtypes = [SP, i32] + [vp] * 8 + [vp, vp] + [vp, vp] + [STP, MP, f32] + \

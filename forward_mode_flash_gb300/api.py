@@ -94,13 +94,18 @@ def _ptr(t: Optional[torch.Tensor]):
 def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor,
              dk: torch.Tensor, dv: torch.Tensor, attn_mask: Optional[torch.Tensor] = None,
              is_causal: bool = False, scale: Optional[float] = None, return_stats: bool = False,
-             out: Optional[Tuple[torch.Tensor, ...]] = None):
+             out: Optional[Tuple[torch.Tensor, ...]] = None, split_kv: bool = True,
+             workspace: Optional[torch.Tensor] = None):
     """Attention forward and its JVP in one fused pass.
 
     Returns (o, t_o), or (o, t_o, lse, mu) with ``return_stats``: lse is the
     natural-log log-sum-exp per row and mu its tangent, both float32 [B,H,Nq].
     ``out`` = (o, t_o) or (o, t_o, lse, mu) gives preallocated outputs (the
-    four-tuple implies ``return_stats``).
+    four-tuple implies ``return_stats``).  With ``split_kv`` (the default),
+    problems with fewer query tiles than SMs split their key range over
+    several CTAs through ``jvp_attn_fwd_dual_ws``; the scratch it needs
+    (``fwd_dual_workspace_size``) is allocated here unless ``workspace`` (a
+    16-byte-aligned uint8 device tensor) is given.
     """
     lib = _abi.load()
     hkv = _check_inputs([q, k, v, dq, dk, dv], ["q", "k", "v", "dq", "dk", "dv"])
@@ -134,14 +139,33 @@ def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor
     shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
     stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        st = lib.jvp_attn_fwd_dual(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v),
-                                   _ptr(dq), _ptr(dk), _ptr(dv), ins, ctypes.byref(mask),
-                                   float(scale), _ptr(o), _ptr(t_o), outs, _ptr(lse), _ptr(mu),
-                                   ctypes.c_void_p(stream))
+        need = lib.jvp_attn_fwd_dual_workspace_size(ctypes.byref(shape), _DT[q.dtype]) \
+            if split_kv else 0
+        if need > 0:
+            if workspace is None:
+                workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            st = lib.jvp_attn_fwd_dual_ws(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k),
+                                          _ptr(v), _ptr(dq), _ptr(dk), _ptr(dv), ins,
+                                          ctypes.byref(mask), float(scale), _ptr(o), _ptr(t_o),
+                                          outs, _ptr(lse), _ptr(mu), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          ctypes.c_void_p(stream))
+        else:
+            st = lib.jvp_attn_fwd_dual(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(dq), _ptr(dk), _ptr(dv), ins,
+                                       ctypes.byref(mask), float(scale), _ptr(o), _ptr(t_o),
+                                       outs, _ptr(lse), _ptr(mu), ctypes.c_void_p(stream))
     _abi.check(st)
     if return_stats:
         return o, t_o, lse, mu
     return o, t_o
+
+
+def fwd_dual_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,
+                            dtype: torch.dtype = torch.bfloat16, Hkv: int = 0) -> int:
+    """Bytes of scratch with which fwd_dual splits the key range (0: no split)."""
+    shape = _abi.Shape(B, H, Nq, Nk, D, Hkv)
+    return int(_abi.load().jvp_attn_fwd_dual_workspace_size(ctypes.byref(shape), _DT[dtype]))
 
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -283,7 +307,7 @@ def fwd_dual_host(q, k, v, dq, dk, dv, attn_mask: Optional[torch.Tensor] = None,
         with torch.cuda.stream(main):
             args = [x[:, :n] for x in dev_in]
             fwd_dual(*args, attn_mask=mask_d, is_causal=is_causal, scale=scale,
-                     out=(dev_out[0][:, :n], dev_out[1][:, :n]))
+                     out=(dev_out[0][:, :n], dev_out[1][:, :n]), split_kv=False)
             computed[sl].record(main)
         s_out.wait_event(computed[sl])
         with torch.cuda.stream(s_out):

@@ -245,8 +245,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int BH = p.B * p.H;
   const int nq = p.num_q_tiles;
   const int G = p.group_heads;
-  const int g = blockIdx.x / (G * nq);
-  const int rem = blockIdx.x - g * G * nq;
+  // Split-KV: the p.splits CTAs of one (query tile, head) are adjacent.
+  const int split = blockIdx.x % p.splits;
+  const int item = blockIdx.x / p.splits;
+  const int g = item / (G * nq);
+  const int rem = item - g * G * nq;
   const int Gg = min(G, BH - g * G);
   const int q_rank = rem / Gg;
   const int bh = g * G + rem % Gg;
@@ -262,6 +265,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int last_row = min(q0 + L::BM, p.Nq) - 1;
     n_kv = min(n_kv, last_row / BN + 1);
   }
+  // This CTA's key tiles: [kv0, kv0 + n_kv) (the whole range unless split).
+  const int per_split = (n_kv + p.splits - 1) / p.splits;
+  const int kv0 = min(n_kv, split * per_split);
+  n_kv = min(n_kv, kv0 + per_split) - kv0;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int t = 0; t < n_kv; ++t) {
         const int s = t % NS;
         const uint32_t ph = (t / NS) & 1;
-        const int j0 = t * BN;
+        const int j0 = (kv0 + t) * BN;
         if (!mbar_wait(&ctrl->kdk_empty[s], ph ^ 1, abort)) {
           record_timeout(p.status, abort);
           break;
@@ -464,7 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     for (int t = 0; t < n_kv; ++t) {
       const int buf = t & 1;
-      const int j0 = t * BN + cofs;  // first key of this half tile
+      const int j0 = (kv0 + t) * BN + cofs;  // first key of this half tile
       MaskRegs<MASK, HN> mreg;
       if (row_ok) mreg.load(p, mrow, j0);
       if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
@@ -592,7 +599,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
     }
     if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
-    if (ok) {
+    if (ok && p.split_ws != nullptr) {
+      // Split-KV: store this key range's unnormalised state (m, l, lx, mu~,
+      // A, T) for the combine kernel.
+      tc_fence_after();
+      const long long rows = static_cast<long long>(BH) * p.Nq;
+      const long long R = static_cast<long long>(split) * rows +
+                          (static_cast<long long>(b) * p.H + h) * p.Nq + (row_ok ? i : 0);
+      if (row_ok && wg == 0) {
+        reinterpret_cast<float4*>(p.split_ws)[R] =
+            make_float4(m_run, l_run + ctrl->xsum[1][0][r], lx_run + ctrl->xsum[1][1][r],
+                        mu_run + ctrl->xsum[1][2][r]);
+      }
+      float* acc = p.split_ws + static_cast<long long>(p.splits) * rows * 4 + R * (2 * D);
+#pragma unroll 1
+      for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 32) {
+        uint32_t a[32], tt[32];
+        if (n_kv > 0) {
+          if (TANGENT) {
+            tmem_ld32x2(lane_base + L::TM_A + col, lane_base + L::TM_T + col, a, tt);
+          } else {
+            tmem_ld32(lane_base + L::TM_A + col, a);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = tt[e] = 0u;
+        }
+        if (row_ok) {
+          uint4* ad = reinterpret_cast<uint4*>(acc + col);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            ad[v4] = make_uint4(a[4 * v4], a[4 * v4 + 1], a[4 * v4 + 2], a[4 * v4 + 3]);
+          if (TANGENT) {
+            uint4* td = reinterpret_cast<uint4*>(acc + D + col);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              td[v4] = make_uint4(tt[4 * v4], tt[4 * v4 + 1], tt[4 * v4 + 2], tt[4 * v4 + 3]);
+          }
+        }
+      }
+    } else if (ok) {
       tc_fence_after();
       const float l_all = l_run + ctrl->xsum[wg ^ 1][0][r];
       const float lx_all = lx_run + ctrl->xsum[wg ^ 1][1][r];
@@ -673,7 +719,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done |= 1ull << dev;
   }
-  const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H;
+  const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H * p.splits;
   kern<<<static_cast<unsigned>(grid), kTcThreads, L::SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }

@@ -25,7 +25,7 @@ __device__ unsigned int g_device_status = 0;
 namespace {
 
 thread_local std::string t_last_error;
-thread_local int t_last_path = 0;  // 0 none, 1 tensor-core, 2 CUDA-core
+thread_local int t_last_path = 0;  // 0 none, 1 tensor-core, 2 CUDA-core, 3 tensor-core split-KV
 
 jvp_status_t fail(jvp_status_t s, const std::string& msg) {
   t_last_error = msg;
@@ -149,11 +149,23 @@ void split_mask_kind(int kind, int* base, int* causal) {
                                              : kind;
 }
 
-// Shared body of jvp_attn_fwd_dual and jvp_attn_fwd.
+// Split-KV heuristic of the tensor-core forward: split the key range only
+// when the query tiles alone give fewer CTAs than SMs, into at most 16
+// ranges of at least 4 key tiles (256 keys) each.
+int choose_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_sms) {
+  const int64_t base = ((Nq + kTcBlockM - 1) / kTcBlockM) * B * H;
+  if (base <= 0 || base >= num_sms) return 1;
+  const int64_t by_sms = (num_sms + base - 1) / base;
+  const int64_t by_keys = ((Nk + kTcBlockN - 1) / kTcBlockN) / 4;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({by_sms, by_keys, 16})));
+}
+
+// Shared body of jvp_attn_fwd_dual(_ws) and jvp_attn_fwd.
 jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* const* in,
                      const jvp_strides_t* in_strides, const jvp_mask_t* mask, float scale,
                      void* const* out, const jvp_strides_t* out_strides, float* lse, float* mu,
-                     void* stream_ptr, bool tangent) {
+                     void* stream_ptr, bool tangent, void* workspace = nullptr,
+                     size_t ws_bytes = 0) {
   t_last_path = 0;
   const int n_in = tangent ? 6 : 3, n_out = tangent ? 2 : 1;
   if (!shape) return fail(JVP_ERR_INVALID_ARG, "shape is NULL");
@@ -218,6 +230,8 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     if (!aligned(out[t], e)) return fail(JVP_ERR_ALIGNMENT, "output not aligned to its element size");
   }
   if (!aligned(lse, 4) || !aligned(mu, 4)) return fail(JVP_ERR_ALIGNMENT, "lse/mu not 4-byte aligned");
+  if (workspace && !aligned(workspace, 16))
+    return fail(JVP_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
 
   DeviceInfo* dev = nullptr;
   jvp_status_t s = current_device(&dev);
@@ -226,6 +240,8 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     return fail(JVP_ERR_UNSUPPORTED, "the current device is not an sm_103 (GB300-class) GPU");
 
   FwdParams p{};
+  p.splits = 1;
+  p.split_ws = nullptr;
   p.B = static_cast<int>(B);
   p.H = static_cast<int>(H);
   p.Nq = static_cast<int>(Nq);
@@ -284,9 +300,18 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     p.num_q_tiles = static_cast<int>((Nq + kTcBlockM - 1) / kTcBlockM);
     // About one wave of CTAs per group of heads (one CTA per SM).
     p.group_heads = std::max(1, std::min(static_cast<int>(B * H), dev->num_sms / p.num_q_tiles));
+    // Split-KV when the caller gave a large enough workspace and it pays.
+    const int splits = choose_splits(B, H, Nq, Nk, dev->num_sms);
+    if (workspace && splits > 1 &&
+        ws_bytes >= SplitLayout::bytes(B * H * Nq, static_cast<int>(D), splits)) {
+      p.splits = splits;
+      p.split_ws = static_cast<float*>(workspace);
+    }
     err = launch_fwd_tc(static_cast<DType>(dtype), static_cast<int>(D), kind, tangent, maps, p,
                         stream);
-    t_last_path = 1;
+    if (err == cudaSuccess && p.splits > 1)
+      err = launch_fwd_combine(static_cast<DType>(dtype), tangent, p, stream);
+    t_last_path = p.splits > 1 ? 3 : 1;
   } else {
     p.num_q_tiles = static_cast<int>((Nq + 7) / 8);
     err = launch_fwd_simt(static_cast<DType>(dtype), kind, tangent, p, stream);
@@ -480,6 +505,33 @@ jvp_status_t jvp_attn_fwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
   void* out[2] = {o, t_o};
   return jvp::forward(shape, dtype, in, in_strides, mask, scale, out, out_strides, lse, mu, stream,
                       true);
+}
+
+jvp_status_t jvp_attn_fwd_dual_ws(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                                  const void* k, const void* v, const void* dq, const void* dk,
+                                  const void* dv, const jvp_strides_t* in_strides,
+                                  const jvp_mask_t* mask, float scale, void* o, void* t_o,
+                                  const jvp_strides_t* out_strides, float* lse, float* mu,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  const void* in[6] = {q, k, v, dq, dk, dv};
+  void* out[2] = {o, t_o};
+  return jvp::forward(shape, dtype, in, in_strides, mask, scale, out, out_strides, lse, mu, stream,
+                      true, workspace, workspace_bytes);
+}
+
+size_t jvp_attn_fwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype) {
+  if (!shape || shape->B <= 0 || shape->H <= 0 || shape->Nq <= 0 || shape->Nk <= 0) return 0;
+  if ((dtype != JVP_F16 && dtype != JVP_BF16) || (shape->D != 64 && shape->D != 128)) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();  // no device: no split, no workspace
+    return 0;
+  }
+  const int splits = jvp::choose_splits(shape->B, shape->H, shape->Nq, shape->Nk, sms);
+  if (splits <= 1) return 0;
+  return jvp::SplitLayout::bytes(shape->B * shape->H * shape->Nq, static_cast<int>(shape->D),
+                                 splits);
 }
 
 jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,

@@ -27,6 +27,12 @@ struct FwdParams {
   int mask_vec;      // 1: rows are 16-byte aligned and stride_k == 1 (vector loads)
   int causal;        // 1: a bool / additive mask also keeps only keys j <= i
   int kv_group;      // query heads per key/value head (grouped-query attention; 1 = none)
+  // Split-KV (tensor-core kernel): `splits` CTAs share a query tile, each over
+  // a contiguous range of key tiles, and write partial states to `split_ws`
+  // (see SplitLayout) for fwd_combine_kernel; splits == 1 and split_ws ==
+  // nullptr for the ordinary single-pass kernel.
+  int splits;
+  float* split_ws;
   // inputs (used by the CUDA-core kernel; the tensor-core kernel reads them by TMA)
   const void *q, *k, *v, *dq, *dk, *dv;
   Strides sq, sk, sv, sdq, sdk, sdv;
@@ -38,6 +44,21 @@ struct FwdParams {
   float* mu;
   unsigned int* status;  // device status word (timeouts)
 };
+
+// Workspace of the split-KV forward: for split sp and query row R =
+// (b*H + h)*Nq + i, a float4 {m (log2 units), l (rounded p~ sum), lx (fp32 p~
+// sum), mu~} at stats[sp*rows + R], then fp32 A[D] and T[D] at
+// acc[(sp*rows + R) * 2D].  Every entry is written before it is read.
+struct SplitLayout {
+  long long rows;  // B * H * Nq
+  int D;
+  __host__ __device__ size_t stats_floats() const { return static_cast<size_t>(rows) * 4; }
+  __host__ __device__ static size_t bytes(long long rows, int D, int splits) {
+    return static_cast<size_t>(splits) * static_cast<size_t>(rows) * (4 + 2 * D) * sizeof(float);
+  }
+};
+// Merge of the split-KV partial states into O, tO, lse and mu (any dtype).
+cudaError_t launch_fwd_combine(DType dt, bool tangent, const FwdParams& p, cudaStream_t stream);
 
 // Tensor maps of the tensor-core kernel: q, k, v, dq, dk, dv (tangent maps
 // are unused by the primal-only variant).

@@ -123,6 +123,35 @@ jvp_status_t jvp_attn_fwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
                                void* stream);
 
 /*
+ * jvp_attn_fwd_dual with a caller-provided workspace, which lets the
+ * tensor-core path split the key range of small problems (fewer query tiles
+ * than SMs) over several CTAs and merge their partial softmax states in a
+ * second kernel (split-KV; the associative merge of (max, sums, A, T) states).
+ * Results equal jvp_attn_fwd_dual's up to floating-point rounding order.
+ *
+ *   workspace        NULL, or device scratch of workspace_bytes bytes, 16-byte
+ *                    aligned, owned by the caller; contents on entry do not
+ *                    matter.  The split runs only if workspace_bytes is at
+ *                    least jvp_attn_fwd_dual_workspace_size(shape, dtype);
+ *                    otherwise (or with NULL) the call is jvp_attn_fwd_dual.
+ *   other arguments  as for jvp_attn_fwd_dual.
+ *
+ * Calls that share a workspace and overlap on the GPU race on it.
+ */
+jvp_status_t jvp_attn_fwd_dual_ws(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                                  const void* k, const void* v, const void* dq, const void* dk,
+                                  const void* dv, const jvp_strides_t* in_strides,
+                                  const jvp_mask_t* mask, float scale, void* o, void* t_o,
+                                  const jvp_strides_t* out_strides, float* lse, float* mu,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes with which jvp_attn_fwd_dual_ws splits the key range of
+ * `shape` on the current device: splits * B*H*Nq * (16 + 8 D) bytes, or 0 when
+ * the problem is not split (enough query tiles to fill the SMs, too few keys,
+ * a shape the tensor-core path does not take, or no device). */
+size_t jvp_attn_fwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
+
+/*
  * Attention forward without tangents (the project page's `jvp_attention` /
  * `attention`, Usage section): O = softmax(scale Q K^T + M) V and lse.
  * Arguments as for jvp_attn_fwd_dual; in_strides holds 3 records (q, k, v)
@@ -231,9 +260,10 @@ int jvp_attn_version(void);
 jvp_status_t jvp_attn_selftest_wait_timeout(int64_t limit_cycles, void* stream);
 
 /*
- * Diagnostic: which kernel family the last successful forward call on the
- * calling thread enqueued: 1 = tensor-core path, 2 = CUDA-core path,
- * 0 = nothing was enqueued (empty problem or an error).
+ * Diagnostic: which kernel family the last successful call on the calling
+ * thread enqueued: 1 = tensor-core path, 2 = CUDA-core path, 3 = tensor-core
+ * path with split-KV and the merge kernel, 0 = nothing was enqueued (empty
+ * problem or an error).
  */
 int jvp_attn_debug_last_path(void);
 

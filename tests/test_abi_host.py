@@ -117,3 +117,11 @@ def test_grouped_heads_and_combined_masks_are_validated_without_a_device(lib):
         _abi.JVP_ERR_INVALID_ARG
     assert b"BOOL_CAUSAL" in lib.jvp_attn_last_error()
 
+
+def test_split_workspace_size_is_zero_without_a_device_or_for_other_shapes(lib):
+    sh = _abi.Shape(1, 2, 1000, 1000, 64, 0)
+    assert lib.jvp_attn_fwd_dual_workspace_size(ctypes.byref(sh), _abi.JVP_BF16) == 0  # no GPU here
+    sh32 = _abi.Shape(1, 2, 1000, 1000, 40, 0)
+    assert lib.jvp_attn_fwd_dual_workspace_size(ctypes.byref(sh32), _abi.JVP_BF16) == 0
+    assert lib.jvp_attn_fwd_dual_workspace_size(None, _abi.JVP_BF16) == 0
+

