@@ -139,8 +139,7 @@ def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor
     shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
     stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        need = lib.jvp_attn_fwd_dual_workspace_size(ctypes.byref(shape), _DT[q.dtype]) \
-            if split_kv else 0
+        need = _split_ws_bytes(lib, shape, q) if split_kv else 0
         if need > 0:
             if workspace is None:
                 workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -159,6 +158,19 @@ def fwd_dual(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dq: torch.Tensor
     if return_stats:
         return o, t_o, lse, mu
     return o, t_o
+
+
+_split_ws_cache = {}
+
+
+def _split_ws_bytes(lib, shape, q) -> int:
+    """jvp_attn_fwd_dual_workspace_size, cached per device and shape."""
+    key = (q.device.index, shape.B, shape.H, shape.Nq, shape.Nk, shape.D, q.dtype)
+    need = _split_ws_cache.get(key)
+    if need is None:
+        need = int(lib.jvp_attn_fwd_dual_workspace_size(ctypes.byref(shape), _DT[q.dtype]))
+        _split_ws_cache[key] = need
+    return need
 
 
 def fwd_dual_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,

@@ -150,13 +150,16 @@ void split_mask_kind(int kind, int* base, int* causal) {
 }
 
 // Split-KV heuristic of the tensor-core forward: split the key range only
-// when the query tiles alone give fewer CTAs than SMs, into at most 16
-// ranges of at least 4 key tiles (256 keys) each.
+// when the query tiles alone would keep at most half of the SMs busy, into at
+// most 16 ranges of at least 16 key tiles (1024 keys) each.  Shorter ranges
+// do not pay: a CTA's fixed cost (Q load, TMEM set-up, epilogue) and the merge
+// kernel then outweigh the shorter loop (measured at N = 512 and 1024 with
+// B*H = 16: split runs were slower).
 int choose_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_sms) {
   const int64_t base = ((Nq + kTcBlockM - 1) / kTcBlockM) * B * H;
-  if (base <= 0 || base >= num_sms) return 1;
+  if (base <= 0 || 2 * base > num_sms) return 1;
   const int64_t by_sms = (num_sms + base - 1) / base;
-  const int64_t by_keys = ((Nk + kTcBlockN - 1) / kTcBlockN) / 4;
+  const int64_t by_keys = ((Nk + kTcBlockN - 1) / kTcBlockN) / 16;
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({by_sms, by_keys, 16})));
 }
 
@@ -522,13 +525,12 @@ jvp_status_t jvp_attn_fwd_dual_ws(const jvp_shape_t* shape, jvp_dtype_t dtype, c
 size_t jvp_attn_fwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype) {
   if (!shape || shape->B <= 0 || shape->H <= 0 || shape->Nq <= 0 || shape->Nk <= 0) return 0;
   if ((dtype != JVP_F16 && dtype != JVP_BF16) || (shape->D != 64 && shape->D != 128)) return 0;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();  // no device: no split, no workspace
+  jvp::DeviceInfo* dev = nullptr;
+  if (jvp::current_device(&dev) != JVP_OK || !dev->sm103) {
+    cudaGetLastError();  // no usable device: no split, no workspace
     return 0;
   }
-  const int splits = jvp::choose_splits(shape->B, shape->H, shape->Nq, shape->Nk, sms);
+  const int splits = jvp::choose_splits(shape->B, shape->H, shape->Nq, shape->Nk, dev->num_sms);
   if (splits <= 1) return 0;
   return jvp::SplitLayout::bytes(shape->B * shape->H * shape->Nq, static_cast<int>(shape->D),
                                  splits);
