@@ -212,7 +212,9 @@ __device__ __forceinline__ float tree_max(const float (&x)[N]) {
   return y[0];
 }
 
-template <typename T, int D, int MASK, bool TANGENT>
+// SPLIT: split-KV variant (p.splits CTAs per query tile, partial states to
+// p.split_ws); the single-pass variant compiles without any of it.
+template <typename T, int D, int MASK, bool TANGENT, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
   using L = TcLayout<D, TANGENT>;
@@ -246,8 +248,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nq = p.num_q_tiles;
   const int G = p.group_heads;
   // Split-KV: the p.splits CTAs of one (query tile, head) are adjacent.
-  const int split = blockIdx.x % p.splits;
-  const int item = blockIdx.x / p.splits;
+  const int split = SPLIT ? static_cast<int>(blockIdx.x % p.splits) : 0;
+  const int item = SPLIT ? static_cast<int>(blockIdx.x / p.splits) : static_cast<int>(blockIdx.x);
   const int g = item / (G * nq);
   const int rem = item - g * G * nq;
   const int Gg = min(G, BH - g * G);
@@ -266,9 +268,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     n_kv = min(n_kv, last_row / BN + 1);
   }
   // This CTA's key tiles: [kv0, kv0 + n_kv) (the whole range unless split).
-  const int per_split = (n_kv + p.splits - 1) / p.splits;
-  const int kv0 = min(n_kv, split * per_split);
-  n_kv = min(n_kv, kv0 + per_split) - kv0;
+  int kv0 = 0;
+  if constexpr (SPLIT) {
+    const int per_split = (n_kv + p.splits - 1) / p.splits;
+    kv0 = min(n_kv, split * per_split);
+    n_kv = min(n_kv, kv0 + per_split) - kv0;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
@@ -599,7 +604,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
     }
     if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
-    if (ok && p.split_ws != nullptr) {
+    if (SPLIT && ok) {
       // Split-KV: store this key range's unnormalised state (m, l, lx, mu~,
       // A, T) for the combine kernel.
       tc_fence_after();
@@ -705,10 +710,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <typename T, int D, int MASK, bool TANGENT>
+template <typename T, int D, int MASK, bool TANGENT, bool SPLIT>
 cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream_t stream) {
   using L = TcLayout<D, TANGENT>;
-  auto kern = fwd_dual_tc_kernel<T, D, MASK, TANGENT>;
+  auto kern = fwd_dual_tc_kernel<T, D, MASK, TANGENT, SPLIT>;
   // The attribute is per device; setting it is idempotent, the mask only saves calls.
   static unsigned long long attr_done = 0;
   int dev = 0;
@@ -719,7 +724,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done |= 1ull << dev;
   }
-  const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H * p.splits;
+  const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H * (SPLIT ? p.splits : 1);
   kern<<<static_cast<unsigned>(grid), kTcThreads, L::SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }
@@ -727,10 +732,11 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
 template <typename T, int D>
 cudaError_t launch_tc_dispatch(int mask_kind, bool tangent, const TcMaps& maps,
                                const FwdParams& p, cudaStream_t stream) {
-#define JVP_TC_CASE(MK)                                                      \
-  case MK:                                                                   \
-    return tangent ? launch_tc_variant<T, D, MK, true>(maps, p, stream)      \
-                   : launch_tc_variant<T, D, MK, false>(maps, p, stream);
+#define JVP_TC_CASE(MK)                                                                  \
+  case MK:                                                                               \
+    if (!tangent) return launch_tc_variant<T, D, MK, false, false>(maps, p, stream);     \
+    return p.splits > 1 ? launch_tc_variant<T, D, MK, true, true>(maps, p, stream)       \
+                        : launch_tc_variant<T, D, MK, true, false>(maps, p, stream);
   switch (mask_kind) {
     JVP_TC_CASE(kMaskNone)
     JVP_TC_CASE(kMaskBool)

@@ -305,7 +305,7 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     p.group_heads = std::max(1, std::min(static_cast<int>(B * H), dev->num_sms / p.num_q_tiles));
     // Split-KV when the caller gave a large enough workspace and it pays.
     const int splits = choose_splits(B, H, Nq, Nk, dev->num_sms);
-    if (workspace && splits > 1 &&
+    if (tangent && workspace && splits > 1 &&
         ws_bytes >= SplitLayout::bytes(B * H * Nq, static_cast<int>(D), splits)) {
       p.splits = splits;
       p.split_ws = static_cast<float*>(workspace);
