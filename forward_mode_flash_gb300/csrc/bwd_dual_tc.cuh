@@ -414,12 +414,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ----------------------------------------------------------------------------
 // Key-major kernel.  PART: 3 = all four key-side gradients (D = 64),
 // 1 = value part (gV, g_dV), 2 = key part (gK, g_dK).
+//
+// TMEM: two score buffers of 128 columns (tile t uses buffer t & 1), each
+// [S^T | dS^T] (value part, query tiles of BQ = 64 rows) or
+// [S^T | dS^T | G^T | GP^T] (BQ = 32), then the accumulators from column 256.
+// While the elementwise warps work on tile t, the score MMAs of tile t + 1
+// fill the other buffer.  Shared memory: the resident key-side tiles, NS
+// stages of query-side tiles, the stages' row scalars, the control block.
 template <int D, int PART>
 struct BkLayout {
   static constexpr bool kV = (PART & 1) != 0;
   static constexpr bool kK = (PART & 2) != 0;
-  static constexpr int BK = 128;  // keys per CTA
-  static constexpr int BQ = 64;   // query rows per tile
+  static constexpr int BK = 128;          // keys per CTA
+  static constexpr int NSC = kK ? 4 : 2;  // score matrices per tile
+  static constexpr int BQ = 128 / NSC;    // query rows per tile (a buffer is 128 columns)
   static constexpr int KCH = D / 64;
   static constexpr int KT_BYTES = KCH * BK * 128;  // one [128 x D] key-side tile
   static constexpr int QCHUNK = 2 * BQ * 128;      // [X rows | Y rows] of one 64-column chunk
@@ -428,17 +436,22 @@ struct BkLayout {
   static constexpr int OFF_K = 0, OFF_DK = KT_BYTES;
   static constexpr int OFF_V = 2 * KT_BYTES, OFF_DV = 3 * KT_BYTES;
   static constexpr int KSIDE = (kK ? 4 : 2) * KT_BYTES;
-  // per stage: [Q ; dQ], [gtO ; gO] and the row scalars (lse, mu, nu, delta) x 64 rows
-  static constexpr int STAGE = 2 * QBLK + 1024;
-  static constexpr int NS = (227 * 1024 - KSIDE - 2048) / STAGE >= 3 ? 3
-                            : (227 * 1024 - KSIDE - 2048) / STAGE;
+  // per stage: [Q ; dQ] and [gtO ; gO]; the row scalars (a float4 per query
+  // row) of each stage live in a separate array so stages stay 1 KB aligned
+  static constexpr int STAGE = 2 * QBLK;
+  static constexpr int SCAL_BYTES = BQ * 16;
+  static constexpr int CTRL_BYTES = 256;
+  static constexpr int NS_FIT =
+      (227 * 1024 - KSIDE - CTRL_BYTES - 1024) / (STAGE + SCAL_BYTES);
+  static constexpr int NS = NS_FIT >= 4 ? 4 : NS_FIT;
   static constexpr int OFF_ST = KSIDE;
-  static constexpr int OFF_CTRL = OFF_ST + NS * STAGE;
-  static constexpr int CTRL_BYTES = 512;
+  static constexpr int OFF_SC = OFF_ST + NS * STAGE;
+  static constexpr int OFF_CTRL = OFF_SC + NS * SCAL_BYTES;
   static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
-  // TMEM columns: transposed scores, then the accumulators
-  static constexpr uint32_t TM_S = 0, TM_DS = 64, TM_G = 128, TM_GP = 192, TM_ACC = 256;
-  static_assert(NS >= 1, "at least one stage");
+  static constexpr uint32_t TM_BUF = 128, TM_ACC = 256;
+  static constexpr uint32_t S_OFF = 0, DS_OFF = BQ, G_OFF = 2 * BQ, GP_OFF = 3 * BQ;
+  static_assert(NS >= 3 || D == 64 || !kK, "three stages for the key part");
+  static_assert(NS >= 2, "two stages at least");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(D == 64 || PART != 3, "the four accumulators fit TMEM only at D = 64");
 };
@@ -447,7 +460,7 @@ template <int NS>
 struct BwdKCtrl {
   uint64_t k_full;
   uint64_t q_full[NS], q_empty[NS];
-  uint64_t s_full, p_full, o_full, drain;
+  uint64_t s_full[2], p_full[2], o_full, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -461,8 +474,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSD = D / 16;
   constexpr int KSQ = BQ / 16;
-  constexpr uint32_t I_N128 = idesc_f16(kBF16, 128, 128, false);
-  constexpr uint32_t I_N64 = idesc_f16(kBF16, 128, 64, false);
+  constexpr uint32_t I_N2Q = idesc_f16(kBF16, 128, 2 * BQ, false);  // [X ; Y]^T score pairs
+  constexpr uint32_t I_NQ = idesc_f16(kBF16, 128, BQ, false);
   constexpr uint32_t I_ACC2 = idesc_f16(kBF16, 128, 2 * D, true);
   constexpr uint32_t I_ACC1 = idesc_f16(kBF16, 128, D, true);
   // Accumulator columns (relative to TM_ACC)
@@ -504,8 +517,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&ctrl->q_full[s], 2);  // TMA bytes + the row scalars written by warp 0
       mbar_init(&ctrl->q_empty[s], 1);
     }
-    mbar_init(&ctrl->s_full, 1);
-    mbar_init(&ctrl->p_full, 256);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&ctrl->s_full[u], 1);
+      mbar_init(&ctrl->p_full[u], 256);
+    }
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
     ctrl->abort = 0;
@@ -537,13 +552,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
+    // Row scalars of tile t for this lane's rows (lane + 32 u): the loads for
+    // tile t + 1 are issued right after tile t's are published, so their
+    // latency overlaps the wait for the next free stage.
+    constexpr int RPL = BQ / 32;  // query rows per producer lane
+    const CUtensorMap* mq = BQ == 64 ? &maps.q64 : &maps.q;
+    const CUtensorMap* mdq = BQ == 64 ? &maps.dq64 : &maps.dq;
+    const CUtensorMap* mgo = BQ == 64 ? &maps.go64 : &maps.go;
+    const CUtensorMap* mgto = BQ == 64 ? &maps.gto64 : &maps.gto;
+    float4 next[RPL];
+    auto load_scalars = [&](int t) {
+      const int h = hk * p.kv_group + t / n_th;
+#pragma unroll
+      for (int u = 0; u < RPL; ++u) {
+        const int i = (t_begin + t % n_th) * BQ + lane + 32 * u;
+        float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        if (i < p.Nq) {
+          const long long idx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
+          v.x = p.lse[idx] * kLog2e;
+          v.y = p.mu[idx];
+          if (L::kK) {
+            v.z = p.nu[idx];
+            v.w = p.delta[idx];
+          }
+        }
+        next[u] = v;
+      }
+    };
+    if (n_t > 0) load_scalars(0);
     int fills = 0;
     for (int t = 0; t < n_t; ++t) {
       const int s = t % NS;
       const uint32_t ph = (t / NS) & 1;
       const int h = hk * p.kv_group + t / n_th;  // query head of this tile
       const int i0 = (t_begin + t % n_th) * BQ;
-      const long long rbase = (static_cast<long long>(b) * p.H + h) * p.Nq;
       bool got = true;
       if (lane == 0) got = mbar_wait(&ctrl->q_empty[s], ph ^ 1, abort);
       if (!__shfl_sync(0xffffffffu, got, 0)) {
@@ -554,32 +596,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(&ctrl->q_full[s], 2 * L::QBLK);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(st + c * L::QCHUNK, &maps.q, &ctrl->q_full[s], c * 64, i0, h, b);
-          tma_load_4d(st + c * L::QCHUNK + BQ * 128, &maps.dq, &ctrl->q_full[s], c * 64, i0, h, b);
-          tma_load_4d(st + L::QBLK + c * L::QCHUNK, &maps.gto, &ctrl->q_full[s], c * 64, i0, h, b);
-          tma_load_4d(st + L::QBLK + c * L::QCHUNK + BQ * 128, &maps.go, &ctrl->q_full[s], c * 64,
-                      i0, h, b);
+          tma_load_4d(st + c * L::QCHUNK, mq, &ctrl->q_full[s], c * 64, i0, h, b);
+          tma_load_4d(st + c * L::QCHUNK + BQ * 128, mdq, &ctrl->q_full[s], c * 64, i0, h, b);
+          tma_load_4d(st + L::QBLK + c * L::QCHUNK, mgto, &ctrl->q_full[s], c * 64, i0, h, b);
+          tma_load_4d(st + L::QBLK + c * L::QCHUNK + BQ * 128, mgo, &ctrl->q_full[s], c * 64, i0,
+                      h, b);
         }
       }
-      float4* rsc = reinterpret_cast<float4*>(st + 2 * L::QBLK);
 #pragma unroll
-      for (int rr = lane; rr < BQ; rr += 32) {
-        const int i = i0 + rr;
-        float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        if (i < p.Nq) {
-          const long long idx = rbase + i;
-          v.x = p.lse[idx] * kLog2e;
-          v.y = p.mu[idx];
-          if (L::kK) {
-            v.z = p.nu[idx];
-            v.w = p.delta[idx];
-          }
-        }
-        rsc[rr] = v;
-      }
+      for (int u = 0; u < RPL; ++u)
+        reinterpret_cast<float4*>(smem + L::OFF_SC + s * L::SCAL_BYTES)[lane + 32 * u] = next[u];
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->q_full[s]);
       ++fills;
+      if (t + 1 < n_t) load_scalars(t + 1);
     }
     if (lane == 0 && *abort) {
       const int zero = 0;
@@ -594,53 +624,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const uint32_t aK = smem_u32(smem + L::OFF_K), adK = smem_u32(smem + L::OFF_DK);
       const uint32_t aV = smem_u32(smem + L::OFF_V), adV = smem_u32(smem + L::OFF_DV);
-      for (int t = 0; ok && t < n_t; ++t) {
+
+      // Score products of tile t into buffer t & 1.
+      auto issue_scores = [&](int t) -> bool {
         const int s = t % NS;
-        if (!mbar_wait(&ctrl->q_full[s], (t / NS) & 1, abort)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&ctrl->q_full[s], (t / NS) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t qb = smem_u32(smem + L::OFF_ST + s * L::STAGE);  // [Q ; dQ]
         const uint32_t ob = qb + L::QBLK;                               // [gtO ; gO]
+        const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
 #pragma unroll
         for (int kk = 0; kk < KSD; ++kk) {  // [S^T | K dQ^T] = K [Q ; dQ]^T
           const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_S, sdesc_sw128(aK + (kk >> 2) * BK * 128 + off, 16, 1024),
-                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N128, kk > 0);
+          mma_ss(buf + L::S_OFF, sdesc_sw128(aK + (kk >> 2) * BK * 128 + off, 16, 1024),
+                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N2Q, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < KSD; ++kk) {  // K dQ^T += dK Q^T  (= dS_raw^T)
           const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_DS, sdesc_sw128(adK + (kk >> 2) * BK * 128 + off, 16, 1024),
-                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N64, 1u);
+          mma_ss(buf + L::DS_OFF, sdesc_sw128(adK + (kk >> 2) * BK * 128 + off, 16, 1024),
+                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
         }
         if (L::kK) {
 #pragma unroll
           for (int kk = 0; kk < KSD; ++kk) {  // [G^T | V gO^T] = V [gtO ; gO]^T
             const uint32_t off = (kk & 3) * 32;
-            mma_ss(tmem + L::TM_G, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
-                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N128, kk > 0);
+            mma_ss(buf + L::G_OFF, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N2Q, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < KSD; ++kk) {  // V gO^T += dV gtO^T  (= gP1^T)
             const uint32_t off = (kk & 3) * 32;
-            mma_ss(tmem + L::TM_GP, sdesc_sw128(adV + (kk >> 2) * BK * 128 + off, 16, 1024),
-                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N64, 1u);
+            mma_ss(buf + L::GP_OFF, sdesc_sw128(adV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
           }
         }
-        mma_commit(&ctrl->s_full);
-        if (!mbar_wait(&ctrl->p_full, t & 1, abort)) {
+        mma_commit(&ctrl->s_full[t & 1]);
+        return true;
+      };
+
+      if (ok && n_t > 0) ok = issue_scores(0);
+      for (int t = 0; ok && t < n_t; ++t) {
+        // Tile t + 1's scores go first only if its stage has already landed;
+        // otherwise tile t's accumulate MMAs (which free a stage) go first.
+        const bool early = t + 1 < n_t &&
+                           mbar_test(&ctrl->q_full[(t + 1) % NS], ((t + 1) / NS) & 1);
+        if (early && !issue_scores(t + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&ctrl->p_full[t & 1], (t >> 1) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // A operands of query rows [16 kk, 16 kk + 16) (written by warpgroup
-        // kk / 2, half kk % 2): P^T at columns 16 kk, dP^T at 16 kk + 8, gS^T and
-        // g_dS^T 64 columns further.
+        const int s = t % NS;
+        const uint32_t qb = smem_u32(smem + L::OFF_ST + s * L::STAGE);
+        const uint32_t ob = qb + L::QBLK;
+        const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
+        // A operands of query rows [16 kk, 16 kk + 16) of the tile: P^T at
+        // buffer column 16 kk (dP^T at + 8), gS^T at DS_OFF + 16 kk (g_dS^T at + 8).
 #pragma unroll
         for (int kk = 0; kk < KSQ; ++kk) {
-          const uint32_t a0 = tmem + kk * 16;
+          const uint32_t a0 = buf + kk * 16;
+          const uint32_t ag = buf + L::DS_OFF + kk * 16;
           const uint32_t xq = qb + kk * 16 * 128;  // MN-major: 16 query rows per K-step
           const uint32_t xo = ob + kk * 16 * 128;
           const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
@@ -655,27 +702,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           if (L::kK) {
             if (D == 64) {  // [g_dK | gK] += g_dS^T [Q | dQ]
-              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 8, sdesc_sw128(xq, BQ * 128, 1024),
-                     I_ACC2, acc);
+              mma_ts(tmem + L::TM_ACC + A_GDK, ag + 8, sdesc_sw128(xq, BQ * 128, 1024), I_ACC2,
+                     acc);
             } else {
-              mma_ts(tmem + L::TM_ACC + A_GDK, a0 + 64 + 8, sdesc_sw128(xq, L::QCHUNK, 1024),
+              mma_ts(tmem + L::TM_ACC + A_GDK, ag + 8, sdesc_sw128(xq, L::QCHUNK, 1024), I_ACC1,
+                     acc);
+              mma_ts(tmem + L::TM_ACC + A_GK, ag + 8, sdesc_sw128(xq + BQ * 128, L::QCHUNK, 1024),
                      I_ACC1, acc);
-              mma_ts(tmem + L::TM_ACC + A_GK, a0 + 64 + 8,
-                     sdesc_sw128(xq + BQ * 128, L::QCHUNK, 1024), I_ACC1, acc);
             }
           }
         }
 #pragma unroll
         for (int kk = 0; kk < KSQ; ++kk) {
-          const uint32_t a0 = tmem + kk * 16;
+          const uint32_t a0 = buf + kk * 16;
+          const uint32_t ag = buf + L::DS_OFF + kk * 16;
           if (L::kV)  // gV += dP^T gtO
             mma_ts(tmem + L::TM_ACC + A_GV, a0 + 8,
-                   sdesc_sw128(ob + kk * 16 * 128, D == 64 ? BQ * 128 : L::QCHUNK, 1024), I_ACC1, 1u);
+                   sdesc_sw128(ob + kk * 16 * 128, D == 64 ? BQ * 128 : L::QCHUNK, 1024), I_ACC1,
+                   1u);
           if (L::kK)  // gK += gS^T Q
-            mma_ts(tmem + L::TM_ACC + A_GK, a0 + 64,
-                   sdesc_sw128(qb + kk * 16 * 128, D == 64 ? BQ * 128 : L::QCHUNK, 1024), I_ACC1, 1u);
+            mma_ts(tmem + L::TM_ACC + A_GK, ag,
+                   sdesc_sw128(qb + kk * 16 * 128, D == 64 ? BQ * 128 : L::QCHUNK, 1024), I_ACC1,
+                   1u);
         }
         mma_commit(&ctrl->q_empty[s]);
+        if (t + 1 < n_t && !early && !issue_scores(t + 1)) {
+          ok = false;
+          break;
+        }
       }
       if (ok && n_t > 0) mma_commit(&ctrl->o_full);
       if (!ok) record_timeout(status, abort);
@@ -685,8 +739,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise
-    // Thread = key (TMEM lane); warpgroup wg owns query rows [wg*32, wg*32+32)
-    // of every tile.
+    // Thread = key (TMEM lane); warpgroup wg owns query rows [wg*QW, wg*QW + QW)
+    // of every tile, taken 16 at a time.
+    constexpr int QW = BQ / 2;
     const int wg = (warp - 2) >> 2;
     const int sub = warp & 3;
     const int r = sub * 32 + lane;
@@ -698,26 +753,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
       const int st_i = t % NS;
-      const int h = hk * p.kv_group + t / n_th;                  // query head of this tile
-      const int i0 = (t_begin + t % n_th) * BQ + wg * 32;  // first query row of this half tile
-      if (!warp_wait(&ctrl->s_full, t & 1, status, abort) ||
+      const int h = hk * p.kv_group + t / n_th;            // query head of this tile
+      const int i0 = (t_begin + t % n_th) * BQ + wg * QW;  // first query row of this warpgroup
+      if (!warp_wait(&ctrl->s_full[t & 1], (t >> 1) & 1, status, abort) ||
           !warp_wait(&ctrl->q_full[st_i], (t / NS) & 1, status, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const float4* rsc =
-          reinterpret_cast<const float4*>(smem + L::OFF_ST + st_i * L::STAGE + 2 * L::QBLK) + wg * 32;
+          reinterpret_cast<const float4*>(smem + L::OFF_SC + st_i * L::SCAL_BYTES) + wg * QW;
       // Mask entries of this thread's key for the tile's rows: base + i * msq.
       const long long mcol = static_cast<long long>(b) * p.msb + static_cast<long long>(h) * p.msh +
                              static_cast<long long>(key_ok ? j : 0) * p.msk;
-      // Two halves of 16 query rows keep the register footprint small.
+      const uint32_t bcol = (t & 1) * L::TM_BUF + wg * QW;
 #pragma unroll 1
-      for (int hq = 0; hq < 2; ++hq) {
-        const uint32_t col = wg * 32 + hq * 16;
+      for (int hq = 0; hq < QW / 16; ++hq) {
+        // The 16-bit results go only into the 16 columns this half has just
+        // read (S^T at col, dS^T at DS_OFF + col), so the other halves' inputs stay intact.
+        const uint32_t col = bcol + hq * 16;
         uint32_t rs[16], rds[16], rg[16], rgp[16];
-        tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_DS + col, rs, rds);
-        if (L::kK) tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
+        tmem_ld16x2(lb + col + L::S_OFF, lb + col + L::DS_OFF, rs, rds);
+        if (L::kK) tmem_ld16x2(lb + col + L::G_OFF, lb + col + L::GP_OFF, rg, rgp);
         uint32_t pa[8], pb[8], pc[8], pd[8];  // P^T, dP^T, gS^T, g_dS^T (packed pairs)
 #pragma unroll
         for (int qq = 0; qq < 16; qq += 2) {
@@ -754,21 +811,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pc[qq >> 1] = ElemTraits<T>::pack(gS2[0], gS2[1]);
           pd[qq >> 1] = ElemTraits<T>::pack(gdS2[0], gdS2[1]);
         }
-        // The 16-bit results go only into the 16 columns this half has just
-        // read (S at col, dS at 64 + col), so the other half's inputs stay intact.
         if (L::kV) {
-          tmem_st8(lb + col, pa);
-          tmem_st8(lb + col + 8, pb);
+          tmem_st8(lb + col + L::S_OFF, pa);
+          tmem_st8(lb + col + L::S_OFF + 8, pb);
         }
         if (L::kK) {
-          tmem_st8(lb + 64 + col, pc);
-          tmem_st8(lb + 64 + col + 8, pd);
+          tmem_st8(lb + col + L::DS_OFF, pc);
+          tmem_st8(lb + col + L::DS_OFF + 8, pd);
         }
       }
-      (void)st_i;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ctrl->p_full);
+      mbar_arrive(&ctrl->p_full[t & 1]);
     }
     if (ok && n_t > 0) ok = warp_wait(&ctrl->o_full, 0, status, abort);
     if (ok) {
@@ -833,6 +887,8 @@ cudaError_t set_smem(int bytes) {
   return e;
 }
 
+// qmaps: query-major kernel (query side 128-row boxes, key side 64); kmaps:
+// key-major kernel (key side 128-row boxes, query side 32, and 64 in q64 ...).
 template <typename T, int D, int MASK>
 cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
                                   const BwdParams& p, int num_sms, unsigned int* status,
@@ -859,6 +915,7 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
     const int nk = (p.Nk + L::BK - 1) / L::BK;
     const int BHk = p.B * (p.H / p.kv_group);
     const int G = max(1, min(BHk, num_sms / max(1, nk)));
+    static_assert(L::BQ == 32 || L::BQ == 64, "query-side box heights of kmaps");
     kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk), kBwdThreads, L::SMEM_BYTES,
            stream>>>(kmaps, p, G, status);
     return cudaGetLastError();

@@ -426,6 +426,9 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) && (D == 64 || D == 128) && Nq > 0 && Nk > 0;
   for (int t = 0; tc && t < 10; ++t) tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
   for (int t = 0; tc && t < 6; ++t) tc = aligned(out[t], 16) && strides_aligned16(out_strides[t], e);
+  // Tensor maps: qm for the query-major kernel (query side 128 rows, key side
+  // 64); km for the key-major kernel (key side 128 rows, query side 32, and 64
+  // for its value part at D = 128).
   BwdTcMaps qm, km;
   if (tc) {
     // in order: q k v dq dk dv o t_o g_o g_to
@@ -434,12 +437,14 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
     CUtensorMap* qdst_q[4] = {&qm.q, &qm.dq, &qm.go, &qm.gto};
     CUtensorMap* qdst_k[4] = {&qm.k, &qm.dk, &qm.v, &qm.dv};
     CUtensorMap* kdst_q[4] = {&km.q, &km.dq, &km.go, &km.gto};
+    CUtensorMap* kdst_q64[4] = {&km.q64, &km.dq64, &km.go64, &km.gto64};
     CUtensorMap* kdst_k[4] = {&km.k, &km.dk, &km.v, &km.dv};
     for (int u = 0; tc && u < 4; ++u) {
       const int a = qidx[u], c = kidx[u];
       tc = encode_map(qdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 128) &&
-           encode_map(kdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 64) &&
            encode_map(qdst_k[u], dtype, in[c], B, Hkv, Ns[c], D, in_strides[c], 64) &&
+           encode_map(kdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 32) &&
+           encode_map(kdst_q64[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 64) &&
            encode_map(kdst_k[u], dtype, in[c], B, Hkv, Ns[c], D, in_strides[c], 128);
     }
   }

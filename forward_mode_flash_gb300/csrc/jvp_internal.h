@@ -123,24 +123,25 @@ cudaError_t launch_bwd_rows(DType dt, const BwdParams& p, cudaStream_t stream);
 // tensors; each kernel gets its own set, the box heights differ).
 struct BwdTcMaps {
   CUtensorMap q, dq, go, gto, k, dk, v, dv;
+  // query-side maps with a second box height (key-major kernel: 64 rows for
+  // its value part; the maps above have 32)
+  CUtensorMap q64, dq64, go64, gto64;
 };
 // Tensor-core backward (fp16/bf16, D in {64, 128}); the row pre-pass must
-// have been enqueued before.
+// have been enqueued before.  qmaps: query-major kernel (query-side boxes of
+// 128 rows, key side 64); kmaps: key-major kernel (key side 128, query side 32).
 cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, const BwdTcMaps& qmaps,
                           const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
                           unsigned int* status, cudaStream_t stream);
-cudaError_t launch_bwd_tc_f16_d64(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
-                                  const BwdParams& p, int num_sms, unsigned int* status,
-                                  cudaStream_t stream);
-cudaError_t launch_bwd_tc_f16_d128(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
-                                   const BwdParams& p, int num_sms, unsigned int* status,
-                                   cudaStream_t stream);
-cudaError_t launch_bwd_tc_bf16_d64(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
-                                   const BwdParams& p, int num_sms, unsigned int* status,
-                                   cudaStream_t stream);
-cudaError_t launch_bwd_tc_bf16_d128(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
-                                    const BwdParams& p, int num_sms, unsigned int* status,
-                                    cudaStream_t stream);
+#define JVP_BWD_TC_DECL(NAME)                                                            \
+  cudaError_t NAME(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,        \
+                   const BwdParams& p, int num_sms, unsigned int* status,               \
+                   cudaStream_t stream);
+JVP_BWD_TC_DECL(launch_bwd_tc_f16_d64)
+JVP_BWD_TC_DECL(launch_bwd_tc_f16_d128)
+JVP_BWD_TC_DECL(launch_bwd_tc_bf16_d64)
+JVP_BWD_TC_DECL(launch_bwd_tc_bf16_d128)
+#undef JVP_BWD_TC_DECL
 
 // Device status word owned by the library (bit 0: a bounded wait timed out).
 unsigned int* device_status_ptr();
