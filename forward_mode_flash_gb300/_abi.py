@@ -25,6 +25,8 @@ EXPORTS = (
     "jvp_attn_fwd_dual",
     "jvp_attn_fwd_dual_ws",
     "jvp_attn_fwd_dual_workspace_size",
+    "jvp_attn_fwd_dual_host",
+    "jvp_attn_fwd_dual_host_workspace_size",
     "jvp_attn_fwd",
     "jvp_attn_bwd_dual",
     "jvp_attn_bwd_dual_workspace_size",
@@ -87,6 +89,12 @@ def load(path: str | None = None):
         lib.jvp_attn_fwd_dual_ws.restype = i32
         lib.jvp_attn_fwd_dual_workspace_size.argtypes = [SP, i32]
         lib.jvp_attn_fwd_dual_workspace_size.restype = ctypes.c_size_t
+        lib.jvp_attn_fwd_dual_host.argtypes = [SP, i32] + [vp] * 6 + [MP, f32, vp, vp, vp, vp,
+                                                                        i32, vp, ctypes.c_size_t,
+                                                                        vp]
+        lib.jvp_attn_fwd_dual_host.restype = i32
+        lib.jvp_attn_fwd_dual_host_workspace_size.argtypes = [SP, i32, i32]
+        lib.jvp_attn_fwd_dual_host_workspace_size.restype = ctypes.c_size_t
         lib.jvp_attn_fwd.argtypes = [SP, i32, vp, vp, vp, STP, MP, f32, vp, STP, vp, vp]
         lib.jvp_attn_fwd.restype = i32
         lib.jvp_attn_bwd_dual.argtypes = [SP, i32] + [vp] * 8 + [vp, vp] + [vp, vp] + [STP, MP, f32] + \

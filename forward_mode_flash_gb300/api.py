@@ -180,6 +180,14 @@ def fwd_dual_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,
     return int(_abi.load().jvp_attn_fwd_dual_workspace_size(ctypes.byref(shape), _DT[dtype]))
 
 
+def fwd_dual_host_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,
+                                 dtype: torch.dtype = torch.bfloat16, chunks: int = 4) -> int:
+    """Device staging bytes of fwd_dual_host for this shape and chunk count."""
+    shape = _abi.Shape(B, H, Nq, Nk, D, 0)
+    return int(_abi.load().jvp_attn_fwd_dual_host_workspace_size(ctypes.byref(shape),
+                                                                 _DT[dtype], int(chunks)))
+
+
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
               attn_mask: Optional[torch.Tensor] = None, is_causal: bool = False,
               scale: Optional[float] = None, return_lse: bool = False,
@@ -255,81 +263,71 @@ def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
 
 
 def fwd_dual_host(q, k, v, dq, dk, dv, attn_mask: Optional[torch.Tensor] = None,
-                  is_causal: bool = False, scale: Optional[float] = None, chunks: int = 8,
-                  device=None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
-    """fwd_dual for host-resident tensors, with copies overlapped with compute.
+                  is_causal: bool = False, scale: Optional[float] = None, chunks: int = 4,
+                  device=None, out: Optional[Tuple[torch.Tensor, ...]] = None,
+                  return_stats: bool = False, workspace: Optional[torch.Tensor] = None):
+    """fwd_dual for host-resident tensors through ``jvp_attn_fwd_dual_host``.
 
-    q, k, v, dq, dk, dv are CPU tensors [B, H, N, D] (pinned memory lets the
-    copies run asynchronously).  The batch*head pairs are split into
-    ``chunks`` groups; while the kernel runs on group c, group c+1 is copied
-    to the device and group c-1's outputs are copied back, on three streams
-    with two device staging slots.  Returns CPU tensors (O, tO), or fills
-    ``out``.  A mask must broadcast over batch and heads ([1, 1, Nq, Nk]).
+    q, k, v, dq, dk, dv are contiguous CPU tensors [B, H, N, D] (pinned memory
+    lets the copies overlap the kernels).  The library pipelines the copies in,
+    the fused kernel and the copies out over ``chunks`` groups of (batch,
+    head) pairs.  Returns CPU tensors (O, tO) (plus lse, mu with
+    ``return_stats``), or fills ``out``.  A mask must be shared by every
+    (batch, head): [Nq, Nk] or [1, 1, Nq, Nk]; it is copied to the device.
     """
+    lib = _abi.load()
     dev = torch.device(device) if device is not None else torch.device("cuda",
                                                                         torch.cuda.current_device())
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
     for t in (q, k, v, dq, dk, dv):
-        if t.device.type != "cpu" or not t.is_contiguous():
-            raise ValueError("fwd_dual_host takes contiguous CPU tensors")
+        if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("fwd_dual_host takes contiguous CPU tensors of one dtype")
     if k.shape[1] != H:
         raise ValueError("fwd_dual_host needs as many key/value heads as query heads")
-    if attn_mask is not None and attn_mask.dim() == 4 and (attn_mask.shape[0] != 1 or
-                                                           attn_mask.shape[1] != 1):
-        raise ValueError("fwd_dual_host needs a mask shared by all batches and heads")
-    BH = B * H
-    chunks = max(1, min(int(chunks), BH))
-    size = (BH + chunks - 1) // chunks
-    ins = [t.view(BH, t.shape[2], D) for t in (q, k, v, dq, dk, dv)]
+    if q.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    mask_d = None
+    if attn_mask is not None:
+        m = attn_mask
+        while m.dim() > 2 and m.shape[0] == 1:
+            m = m[0]
+        if m.dim() != 2:
+            raise ValueError("fwd_dual_host needs a mask shared by all batches and heads")
+        mask_d = m.to(dev, non_blocking=True)
+    mask, _keep = _mask_desc(mask_d, is_causal, 1, 1, Nq, Nk, dev)
+    mask.stride_b = mask.stride_h = 0
+    pin = q.is_pinned()
     if out is None:
-        pin = q.is_pinned()
         o_h = torch.empty((B, H, Nq, D), dtype=q.dtype, pin_memory=pin)
         t_h = torch.empty((B, H, Nq, D), dtype=q.dtype, pin_memory=pin)
+        lse_h = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=pin) if return_stats else None
+        mu_h = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=pin) if return_stats else None
     else:
-        o_h, t_h = out
-    outs = [o_h.view(BH, Nq, D), t_h.view(BH, Nq, D)]
-    mask_d = attn_mask.to(dev, non_blocking=True) if attn_mask is not None else None
-
-    main = torch.cuda.current_stream(dev)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    s_in.wait_stream(main)
-    slots = [([torch.empty((1, size, x.shape[1], D), dtype=q.dtype, device=dev) for x in ins],
-              [torch.empty((1, size, Nq, D), dtype=q.dtype, device=dev) for _ in range(2)])
-             for _ in range(2)]
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    computed = [torch.cuda.Event() for _ in range(2)]
-    out_done = [torch.cuda.Event() for _ in range(2)]
-    for c in range(chunks):
-        lo, hi = c * size, min(BH, (c + 1) * size)
-        if lo >= hi:
-            break
-        n = hi - lo
-        sl = c % 2
-        dev_in, dev_out = slots[sl]
-        with torch.cuda.stream(s_in):
-            if c >= 2:
-                s_in.wait_event(computed[sl])  # the kernel of chunk c-2 has read this slot
-            for d_t, h_t in zip(dev_in, ins):
-                d_t[0, :n].copy_(h_t[lo:hi], non_blocking=True)
-            in_ready[sl].record(s_in)
-        main.wait_event(in_ready[sl])
-        if c >= 2:
-            main.wait_event(out_done[sl])  # chunk c-2's outputs have left this slot
-        with torch.cuda.stream(main):
-            args = [x[:, :n] for x in dev_in]
-            fwd_dual(*args, attn_mask=mask_d, is_causal=is_causal, scale=scale,
-                     out=(dev_out[0][:, :n], dev_out[1][:, :n]), split_kv=False)
-            computed[sl].record(main)
-        s_out.wait_event(computed[sl])
-        with torch.cuda.stream(s_out):
-            for h_t, d_t in zip(outs, dev_out):
-                h_t[lo:hi].copy_(d_t[0, :n], non_blocking=True)
-            out_done[sl].record(s_out)
-    main.wait_stream(s_out)
-    for x in slots:  # keep the staging buffers alive until the streams are done
-        for t in x[0] + x[1]:
-            t.record_stream(main)
+        o_h, t_h = out[0], out[1]
+        lse_h, mu_h = (out[2], out[3]) if len(out) == 4 else (None, None)
+    shape = _abi.Shape(B, H, Nq, Nk, D, 0)
+    need = int(lib.jvp_attn_fwd_dual_host_workspace_size(ctypes.byref(shape), _DT[q.dtype],
+                                                         int(chunks)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = lib.jvp_attn_fwd_dual_host(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k),
+                                        _ptr(v), _ptr(dq), _ptr(dk), _ptr(dv), ctypes.byref(mask),
+                                        float(scale), _ptr(o_h), _ptr(t_h), _ptr(lse_h),
+                                        _ptr(mu_h), int(chunks), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        ctypes.c_void_p(stream))
+    _abi.check(st)
+    # keep the staging area and the device mask alive until the stream is done
+    workspace.record_stream(torch.cuda.current_stream(dev))
+    if mask_d is not None:
+        mask_d.record_stream(torch.cuda.current_stream(dev))
+    if return_stats or (out is not None and len(out) == 4):
+        return o_h, t_h, lse_h, mu_h
     return o_h, t_h
 
 

@@ -625,6 +625,185 @@ jvp_status_t jvp_attn_selftest_wait_timeout(int64_t limit_cycles, void* stream) 
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// Host-buffer forward (jvp_attn_fwd_dual_host): the inputs and outputs live in
+// host memory; chunks of (batch, head) pairs go through a two-slot device
+// staging area with their host->device copies, the fused kernel and the
+// device->host copies of the previous chunk overlapped on three streams.
+
+namespace jvp {
+namespace {
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;  // copy streams of this device
+  cudaEvent_t entry = nullptr, in_ready[2] = {}, computed[2] = {}, out_done[2] = {};
+};
+std::mutex g_pipe_mu;  // held for the whole enqueue of a call
+HostPipe g_pipe[64];
+
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Byte offsets of one staging slot for chunks of `n` (batch, head) pairs.
+struct SlotLayout {
+  size_t q, k, v, dq, dk, dv, o, t_o, lse, mu, bytes;
+  SlotLayout(int64_t n, int64_t Nq, int64_t Nk, int64_t D, size_t e) {
+    const size_t qb = up256(static_cast<size_t>(n * Nq * D) * e);
+    const size_t kb = up256(static_cast<size_t>(n * Nk * D) * e);
+    const size_t sb = up256(static_cast<size_t>(n * Nq) * sizeof(float));
+    q = 0, dq = qb, o = 2 * qb, t_o = 3 * qb;
+    k = 4 * qb, v = k + kb, dk = v + kb, dv = dk + kb;
+    lse = dv + kb, mu = lse + sb;
+    bytes = mu + sb;
+  }
+};
+
+int64_t chunk_pairs(int64_t BH, int chunks) {
+  const int64_t c = std::max<int64_t>(1, std::min<int64_t>(chunks, BH));
+  return (BH + c - 1) / c;
+}
+
+jvp_status_t host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(JVP_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(JVP_ERR_UNSUPPORTED, "device index out of range");
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming);
+    for (int u = 0; u < 2 && e == cudaSuccess; ++u) {
+      e = cudaEventCreateWithFlags(&hp.in_ready[u], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.computed[u], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.out_done[u], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess)
+      return fail(JVP_ERR_CUDA, std::string("stream/event set-up: ") + cudaGetErrorString(e));
+    hp.ready = true;
+  }
+  *out = &hp;
+  return JVP_OK;
+}
+}  // namespace
+}  // namespace jvp
+
+extern "C" size_t jvp_attn_fwd_dual_host_workspace_size(const jvp_shape_t* shape,
+                                                        jvp_dtype_t dtype, int chunks) {
+  if (!shape || shape->B <= 0 || shape->H <= 0 || shape->Nq <= 0 || shape->D <= 0 ||
+      shape->Nk < 0 || chunks < 1)
+    return 0;
+  const int64_t n = jvp::chunk_pairs(shape->B * shape->H, chunks);
+  return 2 * jvp::SlotLayout(n, shape->Nq, shape->Nk, shape->D, jvp::elem_size(dtype)).bytes;
+}
+
+extern "C" jvp_status_t jvp_attn_fwd_dual_host(
+    const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q, const void* k, const void* v,
+    const void* dq, const void* dk, const void* dv, const jvp_mask_t* mask, float scale, void* o,
+    void* t_o, float* lse, float* mu, int chunks, void* workspace, size_t workspace_bytes,
+    void* stream_ptr) {
+  using namespace jvp;
+  t_last_path = 0;
+  if (!shape) return fail(JVP_ERR_INVALID_ARG, "shape is NULL");
+  const int64_t B = shape->B, H = shape->H, Nq = shape->Nq, Nk = shape->Nk, D = shape->D;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return fail(JVP_ERR_INVALID_ARG, "bad sizes");
+  if (D > 128) return fail(JVP_ERR_UNSUPPORTED, "D > 128 is not supported");
+  if (dtype != JVP_F32 && dtype != JVP_F16 && dtype != JVP_BF16)
+    return fail(JVP_ERR_INVALID_ARG, "unknown dtype");
+  if (!std::isfinite(scale)) return fail(JVP_ERR_INVALID_ARG, "scale is not finite");
+  if (shape->Hkv != 0 && shape->Hkv != H)
+    return fail(JVP_ERR_UNSUPPORTED, "the host-buffer entry point takes Hkv == H only");
+  if (chunks < 1) return fail(JVP_ERR_INVALID_ARG, "chunks must be >= 1");
+  if (mask && (mask->stride_b != 0 || mask->stride_h != 0) && mask->ptr)
+    return fail(JVP_ERR_INVALID_ARG,
+                "the host-buffer entry point needs a mask shared by every (batch, head) "
+                "(stride_b = stride_h = 0)");
+  if (B * H * Nq == 0) return ok();
+  if (!q || !dq || !o || !t_o || (Nk > 0 && (!k || !v || !dk || !dv)))
+    return fail(JVP_ERR_INVALID_ARG, "input or output pointer is NULL");
+  const size_t need = jvp_attn_fwd_dual_host_workspace_size(shape, dtype, chunks);
+  if (!workspace || workspace_bytes < need)
+    return fail(JVP_ERR_WORKSPACE,
+                "workspace is NULL or smaller than jvp_attn_fwd_dual_host_workspace_size()");
+  if (!aligned(workspace, 256)) return fail(JVP_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
+
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  jvp_status_t s = host_pipe(&hp);
+  if (s != JVP_OK) return s;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const size_t e = elem_size(dtype);
+  const int64_t BH = B * H, per = chunk_pairs(BH, chunks);
+  const SlotLayout L(per, Nq, Nk, D, e);
+  auto cu = [&](cudaError_t err, const char* what) -> jvp_status_t {
+    if (err == cudaSuccess) return JVP_OK;
+    return fail(JVP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(err));
+  };
+  // Everything starts after the work already on `stream` (a previous call may
+  // still be reading the same staging area).
+  if ((s = cu(cudaEventRecord(hp->entry, stream), "cudaEventRecord")) != JVP_OK) return s;
+  if ((s = cu(cudaStreamWaitEvent(hp->in, hp->entry, 0), "cudaStreamWaitEvent")) != JVP_OK) return s;
+  if ((s = cu(cudaStreamWaitEvent(hp->out, hp->entry, 0), "cudaStreamWaitEvent")) != JVP_OK) return s;
+  int last_path = 0;
+  int last_slot = 0;
+  for (int64_t lo = 0, c = 0; lo < BH; lo += per, ++c) {
+    const int64_t n = std::min(per, BH - lo);
+    const int sl = static_cast<int>(c & 1);
+    last_slot = sl;
+    uint8_t* base = static_cast<uint8_t*>(workspace) + sl * L.bytes;
+    const size_t qbytes = static_cast<size_t>(n * Nq * D) * e, kbytes = static_cast<size_t>(n * Nk * D) * e;
+    const size_t qoff = static_cast<size_t>(lo * Nq * D) * e, koff = static_cast<size_t>(lo * Nk * D) * e;
+    // host -> device (after the kernel of chunk c-2 has read this slot)
+    if (c >= 2 && (s = cu(cudaStreamWaitEvent(hp->in, hp->computed[sl], 0), "cudaStreamWaitEvent")) != JVP_OK)
+      return s;
+    struct { size_t dst; const void* src; size_t off, bytes; } cp[6] = {
+        {L.q, q, qoff, qbytes}, {L.k, k, koff, kbytes}, {L.v, v, koff, kbytes},
+        {L.dq, dq, qoff, qbytes}, {L.dk, dk, koff, kbytes}, {L.dv, dv, koff, kbytes}};
+    for (auto& x : cp) {
+      if (x.bytes == 0) continue;
+      s = cu(cudaMemcpyAsync(base + x.dst, static_cast<const uint8_t*>(x.src) + x.off, x.bytes,
+                             cudaMemcpyHostToDevice, hp->in),
+             "cudaMemcpyAsync (host to device)");
+      if (s != JVP_OK) return s;
+    }
+    if ((s = cu(cudaEventRecord(hp->in_ready[sl], hp->in), "cudaEventRecord")) != JVP_OK) return s;
+    // the kernel on `stream` (after chunk c-2's outputs have left this slot)
+    if ((s = cu(cudaStreamWaitEvent(stream, hp->in_ready[sl], 0), "cudaStreamWaitEvent")) != JVP_OK)
+      return s;
+    if (c >= 2 && (s = cu(cudaStreamWaitEvent(stream, hp->out_done[sl], 0), "cudaStreamWaitEvent")) != JVP_OK)
+      return s;
+    const jvp_shape_t cs{1, n, Nq, Nk, D, 0};
+    const jvp_strides_t sq{n * Nq * D, Nq * D, D, 1}, sk{n * Nk * D, Nk * D, D, 1};
+    const jvp_strides_t ins[6] = {sq, sk, sk, sq, sk, sk}, outs[2] = {sq, sq};
+    s = jvp_attn_fwd_dual(&cs, dtype, base + L.q, base + L.k, base + L.v, base + L.dq, base + L.dk,
+                          base + L.dv, ins, mask, scale, base + L.o, base + L.t_o, outs,
+                          lse ? reinterpret_cast<float*>(base + L.lse) : nullptr,
+                          mu ? reinterpret_cast<float*>(base + L.mu) : nullptr, stream);
+    if (s != JVP_OK) return s;
+    last_path = t_last_path;
+    if ((s = cu(cudaEventRecord(hp->computed[sl], stream), "cudaEventRecord")) != JVP_OK) return s;
+    // device -> host
+    if ((s = cu(cudaStreamWaitEvent(hp->out, hp->computed[sl], 0), "cudaStreamWaitEvent")) != JVP_OK)
+      return s;
+    struct { void* dst; size_t src, off, bytes; } back[4] = {
+        {o, L.o, qoff, qbytes}, {t_o, L.t_o, qoff, qbytes},
+        {lse, L.lse, static_cast<size_t>(lo * Nq) * sizeof(float), static_cast<size_t>(n * Nq) * sizeof(float)},
+        {mu, L.mu, static_cast<size_t>(lo * Nq) * sizeof(float), static_cast<size_t>(n * Nq) * sizeof(float)}};
+    for (auto& x : back) {
+      if (!x.dst || x.bytes == 0) continue;
+      s = cu(cudaMemcpyAsync(static_cast<uint8_t*>(x.dst) + x.off, base + x.src, x.bytes,
+                             cudaMemcpyDeviceToHost, hp->out),
+             "cudaMemcpyAsync (device to host)");
+      if (s != JVP_OK) return s;
+    }
+    if ((s = cu(cudaEventRecord(hp->out_done[sl], hp->out), "cudaEventRecord")) != JVP_OK) return s;
+  }
+  // `stream` reaches this point only once every output is back on the host.
+  if ((s = cu(cudaStreamWaitEvent(stream, hp->out_done[last_slot], 0), "cudaStreamWaitEvent")) != JVP_OK)
+    return s;
+  t_last_path = last_path;
+  return ok();
+}
+
+// ---------------------------------------------------------------------------
 // Backward without allocation (jvp_attn_bwd_dual_noalloc).
 //
 // Some callers cannot allocate device memory (plugins living in another

@@ -152,6 +152,48 @@ jvp_status_t jvp_attn_fwd_dual_ws(const jvp_shape_t* shape, jvp_dtype_t dtype, c
 size_t jvp_attn_fwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
 
 /*
+ * jvp_attn_fwd_dual for inputs and outputs in HOST memory (the end-to-end
+ * form of the call: copies included).  The B*H (batch, head) pairs are split
+ * into `chunks` groups; each group's inputs are copied into one of two device
+ * staging slots (in `workspace`) on a copy stream of the library, the fused
+ * kernel runs on `stream`, and the outputs go back on a second copy stream,
+ * so one group's copies overlap the neighbouring groups' kernels.
+ *
+ *   q, k, v, dq, dk, dv   HOST pointers to contiguous [B,H,Nq|Nk,D] tensors;
+ *                         page-locked (pinned) memory lets the copies run
+ *                         asynchronously and overlap.
+ *   o, t_o                HOST pointers to contiguous [B,H,Nq,D] outputs.
+ *   lse, mu               NULL or HOST pointers to [B,H,Nq] float32 outputs.
+ *   mask                  as for jvp_attn_fwd_dual, but a mask tensor must be
+ *                         a DEVICE tensor shared by every (batch, head)
+ *                         (stride_b = stride_h = 0).
+ *   chunks                number of groups (>= 1; more groups overlap more but
+ *                         launch smaller kernels).
+ *   workspace             DEVICE scratch of at least
+ *                         jvp_attn_fwd_dual_host_workspace_size(shape, dtype,
+ *                         chunks) bytes, 256-byte aligned, owned by the caller.
+ *   stream                the call is ordered after the work already on
+ *                         `stream`, and `stream` reaches its end only when
+ *                         every output is in host memory: synchronise
+ *                         `stream` before reading them.  Inputs must stay
+ *                         unchanged until then.
+ *
+ * Grouped-query attention (Hkv != H) is not taken here.  Calls from several
+ * host threads are serialised while they enqueue; calls that share a
+ * workspace must be ordered (e.g. on one stream).
+ */
+jvp_status_t jvp_attn_fwd_dual_host(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                                    const void* k, const void* v, const void* dq, const void* dk,
+                                    const void* dv, const jvp_mask_t* mask, float scale, void* o,
+                                    void* t_o, float* lse, float* mu, int chunks,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device staging bytes jvp_attn_fwd_dual_host needs: two slots, each holding
+ * one group's six inputs, two outputs, lse and mu (0 for an invalid shape). */
+size_t jvp_attn_fwd_dual_host_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype,
+                                             int chunks);
+
+/*
  * Attention forward without tangents (the project page's `jvp_attention` /
  * `attention`, Usage section): O = softmax(scale Q K^T + M) V and lse.
  * Arguments as for jvp_attn_fwd_dual; in_strides holds 3 records (q, k, v)

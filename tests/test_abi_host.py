@@ -125,3 +125,24 @@ def test_split_workspace_size_is_zero_without_a_device_or_for_other_shapes(lib):
     assert lib.jvp_attn_fwd_dual_workspace_size(ctypes.byref(sh32), _abi.JVP_BF16) == 0
     assert lib.jvp_attn_fwd_dual_workspace_size(None, _abi.JVP_BF16) == 0
 
+
+def test_host_buffer_entry_point_validates_before_touching_a_device(lib):
+    sh = _abi.Shape(2, 4, 256, 256, 64, 0)
+    need = lib.jvp_attn_fwd_dual_host_workspace_size(ctypes.byref(sh), _abi.JVP_BF16, 4)
+    # two slots of 2 (b, h) pairs: q, dq, o, t_o, k, v, dk, dv of 2*256*64 bf16, lse and mu
+    assert need == 2 * (8 * 2 * 256 * 64 * 2 + 2 * 2 * 256 * 4)
+    p = ctypes.c_void_p(0x10000)
+
+    def call(shape=sh, chunks=4, ws=0x100000, ws_bytes=need, mask=None):
+        m = ctypes.byref(mask) if mask is not None else None
+        return lib.jvp_attn_fwd_dual_host(ctypes.byref(shape), _abi.JVP_BF16, p, p, p, p, p, p,
+                                          m, 0.125, p, p, None, None, chunks,
+                                          ctypes.c_void_p(ws), ws_bytes, None)
+    assert call(chunks=0) == _abi.JVP_ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == _abi.JVP_ERR_WORKSPACE
+    assert call(ws=0x100010) == _abi.JVP_ERR_ALIGNMENT
+    assert call(shape=_abi.Shape(2, 4, 256, 256, 64, 2)) == _abi.JVP_ERR_UNSUPPORTED
+    per_head = _abi.Mask(_abi.JVP_MASK_BOOL, 0x2000, 0, 256 * 256, 256, 1)
+    assert call(mask=per_head) == _abi.JVP_ERR_INVALID_ARG
+    assert b"shared by every" in lib.jvp_attn_last_error()
+

@@ -352,3 +352,32 @@ def test_split_kv_fully_masked_rows_and_empty_ranges():
     assert np.abs(np64(o) - ro).max() <= TOL["bf16"]
     assert np.abs(np64(t_o) - rt).max() <= TOL["bf16"]
 
+
+@pytest.mark.parametrize("dtype,D,mask,chunks", [("bf16", 128, "causal", 3), ("f16", 64, "bool", 5),
+                                                 ("bf16", 64, "additive", 1),
+                                                 ("f32", 40, "none", 4), ("bf16", 64, "none", 64)])
+def test_host_buffer_entry_point_matches_oracle(dtype, D, mask, chunks):
+    # jvp_attn_fwd_dual_host: host tensors in and out, copies pipelined over
+    # `chunks` groups of (batch, head) pairs (more groups than pairs is allowed).
+    w = synth.small(dtype, 3, 5, 150, D, mask, seed=70 + D)
+    inp = synth.make_inputs(w)
+    if inp.mask is not None:
+        inp.mask = inp.mask[:1]  # one mask shared by every (batch, head)
+    host = [x.pin_memory() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    o, t_o, lse, mu = A.fwd_dual_host(*host, attn_mask=inp.mask, is_causal=(mask == "causal"),
+                                      chunks=chunks, return_stats=True)
+    torch.cuda.synchronize()
+    assert o.device.type == "cpu" and lse.device.type == "cpu"
+    assert A.last_path() == (2 if dtype == "f32" else 1)
+    m = None
+    if mask == "bool":
+        m = np.broadcast_to(inp.mask.numpy(), (3, 1, 150, 150))
+    elif mask == "additive":
+        m = np.broadcast_to(inp.mask.double().numpy(), (3, 1, 150, 150))
+    ro, rt, rl, rm = oracle.fwd_dual(*(np64(x) for x in host), mask, m)
+    tol = TOL[dtype]
+    assert np.abs(np64(o) - ro).max() <= tol
+    assert np.abs(np64(t_o) - rt).max() <= tol
+    assert np.abs(np64(lse) - rl).max() <= LSE_TOL[dtype]
+    assert np.abs(np64(mu) - rm).max() <= 20 * tol
+
