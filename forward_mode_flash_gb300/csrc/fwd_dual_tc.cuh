@@ -96,7 +96,12 @@ struct TcLayout {
   static constexpr int USED = OFF_CTRL + CTRL_BYTES;
   // Padded so that only one CTA fits per SM (each CTA owns all 512 TMEM columns).
   static constexpr int SMEM_BYTES = (USED + 1024 < 120 * 1024 ? 120 * 1024 : USED + 1024);
-  // TMEM columns
+  // TMEM columns.  At D = 64 each softmax warpgroup keeps its own running
+  // max, sums and [A | T] accumulator for its half of every key tile (the two
+  // accumulators fit next to the score buffers), so no per-tile exchange of
+  // half-row maxima is needed; the halves are merged in the epilogue.
+  static constexpr bool kHalfAcc = (D == 64);
+  static constexpr uint32_t ACC_STRIDE = kHalfAcc ? 128 : 0;  // warpgroup w: TM_A + w * stride
   static constexpr uint32_t TM_A = 256;
   static constexpr uint32_t TM_T = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
@@ -118,7 +123,7 @@ struct TcCtrl {
   uint32_t tmem_base;
   int abort;
   float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
-  float xsum[2][3][kTcBlockM];     // [warpgroup][l, lx, mu][row] final half sums
+  float xsum[2][4][kTcBlockM];     // [warpgroup][l, lx, mu, m][row] final half sums
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -418,18 +423,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + L::OFF_VDV + s * L::VDV_BYTES);
-        const uint32_t p_tm = tmem + buf * 128;        // P~ (16-bit pairs)
-        const uint32_t pd_tm = tmem + buf * 128 + BN;  // P~ * dS (16-bit pairs)
+        // P~ (16-bit pairs) of keys [16 kk, 16 kk + 16), P~ * dS BN columns
+        // further: with per-warpgroup accumulators warpgroup kk / 2 stored them
+        // at the start of its own S columns, otherwise they are packed.
+        const uint32_t p_tm = tmem + buf * 128;
+        const uint32_t pd_tm = tmem + buf * 128 + BN;
+        auto pcol = [](int kk) -> uint32_t {
+          return L::kHalfAcc
+                     ? static_cast<uint32_t>((kk / (HN / 16)) * HN + (kk % (HN / 16)) * 8)
+                     : static_cast<uint32_t>(kk * 8);
+        };
+        // With per-warpgroup accumulators, K-steps [w * KH, w * KH + KH) (the
+        // keys of warpgroup w) go to warpgroup w's [A | T].
+        constexpr int KH = L::kHalfAcc ? KSTEPS_N / 2 : KSTEPS_N;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS_N; ++kk) {
           const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
-          mma_ts(tmem + L::TM_A, p_tm + kk * 8, bd, IDESC_AT, (t > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t acc_base = tmem + L::TM_A + (kk / KH) * L::ACC_STRIDE;
+          mma_ts(acc_base, p_tm + pcol(kk), bd, IDESC_AT, (t > 0 || kk % KH > 0) ? 1u : 0u);
         }
         if (TANGENT) {
 #pragma unroll
           for (int kk = 0; kk < KSTEPS_N; ++kk) {
             const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
-            mma_ts(tmem + L::TM_T, pd_tm + kk * 8, bd, IDESC_T, 1u);
+            mma_ts(tmem + L::TM_T + (kk / KH) * L::ACC_STRIDE, pd_tm + pcol(kk), bd, IDESC_T, 1u);
           }
         }
         mma_commit(&ctrl->vdv_empty[s]);
@@ -514,14 +531,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const float mx = tree_max(x);
       const float m_half = (MASK == kMaskAdditive) ? mx : mx * c;
-      // Exchange the half-row maxima between the two warpgroups.
-      ctrl->xmax[buf][wg][r] = m_half;
-      mbar_arrive(&ctrl->max_ready[buf]);
-      if (!warp_wait(&ctrl->max_ready[buf], (t >> 1) & 1, p.status, abort)) {
-        ok = false;
-        break;
+      float m_tile = m_half;
+      if constexpr (!L::kHalfAcc) {
+        // Exchange the half-row maxima between the two warpgroups.
+        ctrl->xmax[buf][wg][r] = m_half;
+        mbar_arrive(&ctrl->max_ready[buf]);
+        if (!warp_wait(&ctrl->max_ready[buf], (t >> 1) & 1, p.status, abort)) {
+          ok = false;
+          break;
+        }
+        m_tile = fmaxf(m_half, ctrl->xmax[buf][wg ^ 1][r]);
       }
-      const float m_tile = fmaxf(m_half, ctrl->xmax[buf][wg ^ 1][r]);
       const bool need = m_tile > m_run + kRescaleThreshold;
       const float m_new = need ? m_tile : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
@@ -536,13 +556,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
+        // Shared accumulator: each warpgroup rescales half of its columns;
+        // per-warpgroup accumulators: each rescales its own.
+        const int c_lo = L::kHalfAcc ? 0 : wg * (ACC_COLS / 2);
+        const int c_hi = L::kHalfAcc ? ACC_COLS : (wg + 1) * (ACC_COLS / 2);
+        const uint32_t a_base = lane_base + L::TM_A + wg * L::ACC_STRIDE;
 #pragma unroll 1
-        for (int col = wg * (ACC_COLS / 2); col < (wg + 1) * (ACC_COLS / 2); col += 32) {
+        for (int col = c_lo; col < c_hi; col += 32) {
           uint32_t acc[32];
-          tmem_ld32(lane_base + L::TM_A + col, acc);
+          tmem_ld32(a_base + col, acc);
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc[e] = __float_as_uint(__uint_as_float(acc[e]) * alpha);
-          tmem_st32(lane_base + L::TM_A + col, acc);
+          tmem_st32(a_base + col, acc);
         }
         tmem_st_wait();
       }
@@ -573,7 +598,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
                (lsum[3].x + lsum[3].y);
       lx_run += (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
-      tmem_st16(lane_base + buf * 128 + wg * (HN / 2), pk);
+      // Where P~ goes: with per-warpgroup accumulators (no per-tile exchange)
+      // into this warpgroup's own S columns, already read, since the other
+      // warpgroup may still be reading its scores; otherwise the exchange has
+      // ordered both warpgroups' reads first and the two halves are packed
+      // side by side.
+      const uint32_t pofs = L::kHalfAcc ? cofs : wg * (HN / 2);
+      tmem_st16(lane_base + buf * 128 + pofs, pk);
       if (TANGENT) {
         float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         const float2 s2 = make_float2(s_scale, s_scale);
@@ -587,7 +618,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mu_run += (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
                   (msum[3].x + msum[3].y);
-        tmem_st16(lane_base + buf * 128 + BN + wg * (HN / 2), pdk);
+        tmem_st16(lane_base + buf * 128 + BN + pofs, pdk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -600,11 +631,100 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ctrl->xsum[wg][0][r] = l_run;
       ctrl->xsum[wg][1][r] = lx_run;
       ctrl->xsum[wg][2][r] = mu_run;
+      ctrl->xsum[wg][3][r] = m_run;
       mbar_arrive(&ctrl->sums_ready);
       ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
     }
     if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
-    if (SPLIT && ok) {
+    if (L::kHalfAcc && ok) {
+      // Merge of the two warpgroups' states (each relative to its own max):
+      // with M = max(m_0, m_1) and a_w = 2^(m_w - M), l = sum a_w l_w (so for
+      // lx, mu~) and A = sum a_w A_w, T = sum a_w T_w, then the usual epilogue
+      // (or, split-KV, the merged partial state).
+      tc_fence_after();
+      const float m_oth = ctrl->xsum[wg ^ 1][3][r];
+      const float m_all = fmaxf(m_run, m_oth);
+      const float a_own = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_all);
+      const float a_oth = (m_oth == -INFINITY) ? 0.0f : exp2f(m_oth - m_all);
+      const float l_all = a_own * l_run + a_oth * ctrl->xsum[wg ^ 1][0][r];
+      const float lx_all = a_own * lx_run + a_oth * ctrl->xsum[wg ^ 1][1][r];
+      const float mu_all = a_own * mu_run + a_oth * ctrl->xsum[wg ^ 1][2][r];
+      const float inv_l = (l_all > 0.0f) ? 1.0f / l_all : 0.0f;
+      const float mu_row = mu_all * inv_l;
+      const uint32_t own = lane_base + L::TM_A + wg * L::ACC_STRIDE;
+      const uint32_t oth = lane_base + L::TM_A + (wg ^ 1) * L::ACC_STRIDE;
+      const long long rows = static_cast<long long>(BH) * p.Nq;
+      const long long R = static_cast<long long>(split) * rows +
+                          (static_cast<long long>(b) * p.H + h) * p.Nq + (row_ok ? i : 0);
+      float* acc = SPLIT ? p.split_ws + static_cast<long long>(p.splits) * rows * 4 + R * (2 * D)
+                         : nullptr;
+      if (SPLIT && row_ok && wg == 0)
+        reinterpret_cast<float4*>(p.split_ws)[R] = make_float4(m_all, l_all, lx_all, mu_all);
+      T* orow = static_cast<T*>(p.o) + static_cast<long long>(b) * p.so.b +
+                static_cast<long long>(h) * p.so.h + static_cast<long long>(row_ok ? i : 0) * p.so.n;
+      T* trow = TANGENT ? static_cast<T*>(p.t_o) + static_cast<long long>(b) * p.sto.b +
+                              static_cast<long long>(h) * p.sto.h +
+                              static_cast<long long>(row_ok ? i : 0) * p.sto.n
+                        : nullptr;
+#pragma unroll 1
+      for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 16) {
+        float fa[16], ft[16];
+        if (n_kv > 0) {
+          uint32_t a0[16], t0[16], a1[16], t1[16];
+          if (TANGENT) {
+            tmem_ld16x2(own + col, own + D + col, a0, t0);
+            tmem_ld16x2(oth + col, oth + D + col, a1, t1);
+          } else {
+            tmem_ld16x2(own + col, oth + col, a0, a1);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            fa[e] = a_own * __uint_as_float(a0[e]) + a_oth * __uint_as_float(a1[e]);
+            ft[e] = TANGENT ? a_own * __uint_as_float(t0[e]) + a_oth * __uint_as_float(t1[e]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) fa[e] = ft[e] = 0.f;
+        }
+        if (SPLIT) {
+          if (row_ok) {
+            float4* ad = reinterpret_cast<float4*>(acc + col);
+            float4* td = reinterpret_cast<float4*>(acc + D + col);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              ad[v4] = make_float4(fa[4 * v4], fa[4 * v4 + 1], fa[4 * v4 + 2], fa[4 * v4 + 3]);
+              if (TANGENT)
+                td[v4] = make_float4(ft[4 * v4], ft[4 * v4 + 1], ft[4 * v4 + 2], ft[4 * v4 + 3]);
+            }
+          }
+        } else {
+          uint32_t po[8], pt[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float o0 = fa[e] * inv_l, o1 = fa[e + 1] * inv_l;
+            po[e >> 1] = ElemTraits<T>::pack(o0, o1);
+            if (TANGENT)
+              pt[e >> 1] = ElemTraits<T>::pack(ft[e] * inv_l - mu_row * o0,
+                                               ft[e + 1] * inv_l - mu_row * o1);
+          }
+          if (row_ok) {
+            uint4* od = reinterpret_cast<uint4*>(orow + col);
+            od[0] = make_uint4(po[0], po[1], po[2], po[3]);
+            od[1] = make_uint4(po[4], po[5], po[6], po[7]);
+            if (TANGENT) {
+              uint4* td = reinterpret_cast<uint4*>(trow + col);
+              td[0] = make_uint4(pt[0], pt[1], pt[2], pt[3]);
+              td[1] = make_uint4(pt[4], pt[5], pt[6], pt[7]);
+            }
+          }
+        }
+      }
+      if (!SPLIT && row_ok && wg == 0) {
+        const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
+        if (p.lse) p.lse[ridx] = (lx_all > 0.0f) ? (m_all + log2f(lx_all)) * kLn2 : -INFINITY;
+        if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+      }
+    } else if (SPLIT && ok) {
       // Split-KV: store this key range's unnormalised state (m, l, lx, mu~,
       // A, T) for the combine kernel.
       tc_fence_after();
