@@ -109,8 +109,10 @@ struct TcLayout {
   static_assert(USED + 1024 <= 227 * 1024, "shared memory budget");
 };
 
-constexpr int kSoftmaxThreads = 256;           // two warpgroups
-constexpr int kTcThreads = 64 + kSoftmaxThreads;  // + producer warp + MMA warp
+constexpr int kSoftmaxThreads = 256;           // two warpgroups (warps 2..9)
+// + producer warp (0), score-MMA warp (1) and P~V-MMA warp (10)
+constexpr int kTcThreads = 96 + kSoftmaxThreads;
+constexpr int kPvWarp = 10;
 
 // Control block in shared memory.
 template <int NS>
@@ -119,7 +121,8 @@ struct TcCtrl {
   uint64_t kdk_full[NS], kdk_empty[NS];
   uint64_t vdv_full[NS], vdv_empty[NS];
   uint64_t s_full[2], p_full[2], max_ready[2];
-  uint64_t at_done, o_full, drain, sums_ready;
+  uint64_t at_done, o_full, drain, drain_pv, sums_ready;
+  uint64_t pv_done[2];  // P~V MMAs of the tile in each score buffer are complete
   uint32_t tmem_base;
   int abort;
   float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
@@ -294,6 +297,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&ctrl->max_ready[s], kSoftmaxThreads);
     }
     mbar_init(&ctrl->at_done, 1);
+    mbar_init(&ctrl->pv_done[0], 1);
+    mbar_init(&ctrl->pv_done[1], 1);
+    mbar_init(&ctrl->drain_pv, 1);
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
     mbar_init(&ctrl->sums_ready, kSoftmaxThreads);
@@ -370,17 +376,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score MMAs
+    // Tile t's score products go into buffer t & 1 once its K tile has landed
+    // and the P~V MMAs of tile t - 2 (the buffer's previous user) are done.
+    // Two issuing threads (this one and the P~V warp) keep the tensor pipe fed
+    // while either waits, and interleave the narrow dQ K^T products.
     if (lane == 0) {
       bool ok = mbar_wait(&ctrl->q_full, 0, abort);
-      if (!ok) record_timeout(p.status, abort);
       tc_fence_after();
       const uint32_t sQ = smem_u32(smem + L::OFF_Q);
       const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
-
-      auto issue_scores = [&](int t) -> bool {
+      for (int t = 0; ok && t < n_kv; ++t) {
         const int s = t % NS;
-        if (!mbar_wait(&ctrl->kdk_full[s], (t / NS) & 1, abort)) return false;
+        if (t >= 2 && !mbar_wait(&ctrl->pv_done[t & 1], ((t - 2) >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&ctrl->kdk_full[s], (t / NS) & 1, abort)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t sK = smem_u32(smem + L::OFF_KDK + s * L::KDK_BYTES);
         const uint32_t d_s = tmem + (t & 1) * 128;
@@ -402,15 +417,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mma_commit(&ctrl->kdk_empty[s]);
         mma_commit(&ctrl->s_full[t & 1]);
-        return true;
-      };
-
-      if (ok && n_kv > 0) ok = issue_scores(0);
+      }
+      if (!ok) record_timeout(p.status, abort);
+      // Drain: every MMA this thread issued completes before TMEM is freed.
+      mma_commit(&ctrl->drain);
+      const int zero = 0;
+      mbar_wait(&ctrl->drain, 0, &zero);
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ P~V MMAs
+    if (lane == 0) {
+      bool ok = true;
       for (int t = 0; ok && t < n_kv; ++t) {
-        if (t + 1 < n_kv && !issue_scores(t + 1)) {
-          ok = false;
-          break;
-        }
         const int buf = t & 1;
         if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
           ok = false;
@@ -451,18 +469,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mma_commit(&ctrl->vdv_empty[s]);
         mma_commit(&ctrl->at_done);
+        mma_commit(&ctrl->pv_done[buf]);
       }
       if (ok) {
         mma_commit(&ctrl->o_full);
       } else {
         record_timeout(p.status, abort);
       }
-      // Drain: every MMA this thread issued completes before TMEM is freed.
-      mma_commit(&ctrl->drain);
+      mma_commit(&ctrl->drain_pv);
       const int zero = 0;
-      mbar_wait(&ctrl->drain, 0, &zero);
+      mbar_wait(&ctrl->drain_pv, 0, &zero);
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kSoftmaxThreads / 32) {
     // ------------------------------------------------------------ softmax
     // Two warpgroups; warpgroup wg owns key columns [wg*HN, wg*HN + HN) of
     // every tile and, in the epilogue, output columns [wg*D/2, wg*D/2 + D/2).

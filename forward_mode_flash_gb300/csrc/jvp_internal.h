@@ -69,8 +69,6 @@ struct TcMaps {
 // Tensor-core kernels (fp16/bf16, D in {64, 128}).  Return a cudaError_t.
 cudaError_t launch_fwd_tc(DType dt, int D, int mask_kind, bool tangent, const TcMaps& maps,
                           const FwdParams& p, cudaStream_t stream);
-// Static shared-memory footprint and block size of a tensor-core variant.
-int tc_block_threads();
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockN = 64;
 
