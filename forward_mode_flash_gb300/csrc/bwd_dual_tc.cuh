@@ -46,6 +46,10 @@
 namespace jvp {
 
 constexpr int kBwdThreads = 64 + 256;
+// The key-major kernel adds a warp (10) that issues the accumulate MMAs while
+// warp 1 issues the score products.
+constexpr int kBwdThreadsK = 96 + 256;
+constexpr int kBwdAccWarp = 10;
 
 // ----------------------------------------------------------------------------
 // Query-major kernel.
@@ -461,12 +465,13 @@ struct BwdKCtrl {
   uint64_t k_full;
   uint64_t q_full[NS], q_empty[NS];
   uint64_t s_full[2], p_full[2], o_full, drain;
+  uint64_t acc_done[2], drain_acc;  // accumulate MMAs of the tile in each buffer are complete
   uint32_t tmem_base;
   int abort;
 };
 
 template <typename T, int D, int MASK, int PART>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdThreadsK, 1)
     bwd_k_tc_kernel(const __grid_constant__ BwdTcMaps maps, const BwdParams p, int group_heads,
                     unsigned int* status) {
   using L = BkLayout<D, PART>;
@@ -520,9 +525,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int u = 0; u < 2; ++u) {
       mbar_init(&ctrl->s_full[u], 1);
       mbar_init(&ctrl->p_full[u], 256);
+      mbar_init(&ctrl->acc_done[u], 1);
     }
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
+    mbar_init(&ctrl->drain_acc, 1);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -618,7 +625,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait(&ctrl->q_full[t % NS], (t / NS) & 1, &zero);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score MMAs
     if (lane == 0) {
       bool ok = mbar_wait(&ctrl->k_full, 0, abort);
       tc_fence_after();
@@ -663,16 +670,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         return true;
       };
 
-      if (ok && n_t > 0) ok = issue_scores(0);
+      // Tile t's scores go into buffer t & 1 once its stage has landed and the
+      // accumulate MMAs of tile t - 2 (the buffer's previous reader) are done.
       for (int t = 0; ok && t < n_t; ++t) {
-        // Tile t + 1's scores go first only if its stage has already landed;
-        // otherwise tile t's accumulate MMAs (which free a stage) go first.
-        const bool early = t + 1 < n_t &&
-                           mbar_test(&ctrl->q_full[(t + 1) % NS], ((t + 1) / NS) & 1);
-        if (early && !issue_scores(t + 1)) {
+        if (t >= 2 && !mbar_wait(&ctrl->acc_done[t & 1], ((t - 2) >> 1) & 1, abort)) {
           ok = false;
           break;
         }
+        if (!issue_scores(t)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) record_timeout(status, abort);
+      mma_commit(&ctrl->drain);
+      const int zero = 0;
+      mbar_wait(&ctrl->drain, 0, &zero);
+    }
+  } else if (warp == kBwdAccWarp) {
+    // ------------------------------------------------------------ accumulate MMAs
+    if (lane == 0) {
+      bool ok = true;
+      for (int t = 0; ok && t < n_t; ++t) {
         if (!mbar_wait(&ctrl->p_full[t & 1], (t >> 1) & 1, abort)) {
           ok = false;
           break;
@@ -726,18 +745,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    1u);
         }
         mma_commit(&ctrl->q_empty[s]);
-        if (t + 1 < n_t && !early && !issue_scores(t + 1)) {
-          ok = false;
-          break;
-        }
+        mma_commit(&ctrl->acc_done[t & 1]);
       }
       if (ok && n_t > 0) mma_commit(&ctrl->o_full);
       if (!ok) record_timeout(status, abort);
-      mma_commit(&ctrl->drain);
+      mma_commit(&ctrl->drain_acc);
       const int zero = 0;
-      mbar_wait(&ctrl->drain, 0, &zero);
+      mbar_wait(&ctrl->drain_acc, 0, &zero);
     }
-  } else {
+  } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ elementwise
     // Thread = key (TMEM lane); warpgroup wg owns query rows [wg*QW, wg*QW + QW)
     // of every tile, taken 16 at a time.
@@ -916,7 +932,7 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
     const int BHk = p.B * (p.H / p.kv_group);
     const int G = max(1, min(BHk, num_sms / max(1, nk)));
     static_assert(L::BQ == 32 || L::BQ == 64, "query-side box heights of kmaps");
-    kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk), kBwdThreads, L::SMEM_BYTES,
+    kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk), kBwdThreadsK, L::SMEM_BYTES,
            stream>>>(kmaps, p, G, status);
     return cudaGetLastError();
   };
