@@ -58,14 +58,19 @@ struct BqLayout {
   static constexpr int BM = 128;  // query rows per CTA
   static constexpr int BN = 64;   // keys per tile
   static constexpr int KCH = D / 64;
-  static constexpr int NS = (D == 64) ? 3 : 1;
+  // [K ; dK] stays until the accumulate MMAs, [V ; dV] is freed after the
+  // score MMAs: at D = 128 two K stages and one V stage fit next to the 128 KB
+  // of resident query-side tiles, so the next K tile loads during the current
+  // tile's elementwise stage and accumulate MMAs.
+  static constexpr int NSK = (D == 64) ? 3 : 2;
+  static constexpr int NSV = (D == 64) ? 3 : 1;
   static constexpr int QT_BYTES = KCH * BM * 128;  // one [128 x D] query-side tile
   static constexpr int KCHUNK = 2 * BN * 128;      // [K rows | dK rows] of one 64-column chunk
   static constexpr int KBLK = KCH * KCHUNK;        // [K ; dK] block of one stage
   static constexpr int OFF_Q = 0, OFF_DQ = QT_BYTES, OFF_GO = 2 * QT_BYTES, OFF_GTO = 3 * QT_BYTES;
   static constexpr int OFF_K = 4 * QT_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * KBLK;
-  static constexpr int OFF_CTRL = OFF_V + NS * KBLK;
+  static constexpr int OFF_V = OFF_K + NSK * KBLK;
+  static constexpr int OFF_CTRL = OFF_V + NSV * KBLK;
   static constexpr int CTRL_BYTES = 512;
   static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
   // TMEM columns
@@ -73,10 +78,10 @@ struct BqLayout {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-template <int NS>
+template <int NSK, int NSV>
 struct BwdCtrl {
   uint64_t q_full;
-  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
   uint64_t s_full, p_full, o_full, drain;
   uint32_t tmem_base;
   int abort;
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_q_tc_kernel(const __grid_constant__ BwdTcMaps maps, const BwdParams p, int group_heads,
                     unsigned int* status) {
   using L = BqLayout<D>;
-  constexpr int NS = L::NS, BN = L::BN, BM = L::BM;
+  constexpr int NSK = L::NSK, NSV = L::NSV, BN = L::BN, BM = L::BM;
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSD = D / 16;   // K-steps over the head dimension
   constexpr int KSN = BN / 16;  // K-steps over a key tile
@@ -119,8 +124,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  static_assert(sizeof(BwdCtrl<NS>) <= L::CTRL_BYTES, "control block budget");
-  BwdCtrl<NS>* ctrl = reinterpret_cast<BwdCtrl<NS>*>(smem + L::OFF_CTRL);
+  static_assert(sizeof(BwdCtrl<NSK, NSV>) <= L::CTRL_BYTES, "control block budget");
+  BwdCtrl<NSK, NSV>* ctrl = reinterpret_cast<BwdCtrl<NSK, NSV>*>(smem + L::OFF_CTRL);
   volatile int* abort = &ctrl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -144,9 +149,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(&ctrl->k_full[s], 1);
       mbar_init(&ctrl->k_empty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(&ctrl->v_full[s], 1);
       mbar_init(&ctrl->v_empty[s], 1);
     }
@@ -179,39 +186,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       int kf = 0, vf = 0;
       for (int t = 0; t < n_kv; ++t) {
-        const int s = t % NS;
-        const uint32_t ph = (t / NS) & 1;
+        const int sk = t % NSK, sv = t % NSV;
         const int j0 = t * BN;
-        if (!mbar_wait(&ctrl->k_empty[s], ph ^ 1, abort)) {
+        if (!mbar_wait(&ctrl->k_empty[sk], ((t / NSK) & 1) ^ 1, abort)) {
           record_timeout(status, abort);
           break;
         }
-        uint8_t* kb = smem + L::OFF_K + s * L::KBLK;
-        mbar_arrive_expect_tx(&ctrl->k_full[s], L::KBLK);
+        uint8_t* kb = smem + L::OFF_K + sk * L::KBLK;
+        mbar_arrive_expect_tx(&ctrl->k_full[sk], L::KBLK);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(kb + c * L::KCHUNK, &maps.k, &ctrl->k_full[s], c * 64, j0, hk, b);
-          tma_load_4d(kb + c * L::KCHUNK + BN * 128, &maps.dk, &ctrl->k_full[s], c * 64, j0, hk, b);
+          tma_load_4d(kb + c * L::KCHUNK, &maps.k, &ctrl->k_full[sk], c * 64, j0, hk, b);
+          tma_load_4d(kb + c * L::KCHUNK + BN * 128, &maps.dk, &ctrl->k_full[sk], c * 64, j0, hk,
+                      b);
         }
         ++kf;
-        if (!mbar_wait(&ctrl->v_empty[s], ph ^ 1, abort)) {
+        if (!mbar_wait(&ctrl->v_empty[sv], ((t / NSV) & 1) ^ 1, abort)) {
           record_timeout(status, abort);
           break;
         }
-        uint8_t* vb = smem + L::OFF_V + s * L::KBLK;
-        mbar_arrive_expect_tx(&ctrl->v_full[s], L::KBLK);
+        uint8_t* vb = smem + L::OFF_V + sv * L::KBLK;
+        mbar_arrive_expect_tx(&ctrl->v_full[sv], L::KBLK);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(vb + c * L::KCHUNK, &maps.v, &ctrl->v_full[s], c * 64, j0, hk, b);
-          tma_load_4d(vb + c * L::KCHUNK + BN * 128, &maps.dv, &ctrl->v_full[s], c * 64, j0, hk, b);
+          tma_load_4d(vb + c * L::KCHUNK, &maps.v, &ctrl->v_full[sv], c * 64, j0, hk, b);
+          tma_load_4d(vb + c * L::KCHUNK + BN * 128, &maps.dv, &ctrl->v_full[sv], c * 64, j0, hk,
+                      b);
         }
         ++vf;
       }
       if (*abort) {
         const int zero = 0;
         mbar_wait(&ctrl->q_full, 0, &zero);
-        for (int t = max(0, kf - NS); t < kf; ++t)
-          mbar_wait(&ctrl->k_full[t % NS], (t / NS) & 1, &zero);
-        for (int t = max(0, vf - NS); t < vf; ++t)
-          mbar_wait(&ctrl->v_full[t % NS], (t / NS) & 1, &zero);
+        for (int t = max(0, kf - NSK); t < kf; ++t)
+          mbar_wait(&ctrl->k_full[t % NSK], (t / NSK) & 1, &zero);
+        for (int t = max(0, vf - NSV); t < vf; ++t)
+          mbar_wait(&ctrl->v_full[t % NSV], (t / NSV) & 1, &zero);
       }
     }
   } else if (warp == 1) {
@@ -222,15 +230,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t aQ = smem_u32(smem + L::OFF_Q), adQ = smem_u32(smem + L::OFF_DQ);
       const uint32_t aGO = smem_u32(smem + L::OFF_GO), aGTO = smem_u32(smem + L::OFF_GTO);
       for (int t = 0; ok && t < n_kv; ++t) {
-        const int s = t % NS;
-        const uint32_t ph = (t / NS) & 1;
-        if (!mbar_wait(&ctrl->k_full[s], ph, abort) || !mbar_wait(&ctrl->v_full[s], ph, abort)) {
+        const int sk = t % NSK, sv = t % NSV;
+        if (!mbar_wait(&ctrl->k_full[sk], (t / NSK) & 1, abort) ||
+            !mbar_wait(&ctrl->v_full[sv], (t / NSV) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + L::OFF_K + s * L::KBLK);
-        const uint32_t vb = smem_u32(smem + L::OFF_V + s * L::KBLK);
+        const uint32_t kb = smem_u32(smem + L::OFF_K + sk * L::KBLK);
+        const uint32_t vb = smem_u32(smem + L::OFF_V + sv * L::KBLK);
 #pragma unroll
         for (int kk = 0; kk < KSD; ++kk) {  // [S | Q dK^T] = Q [K ; dK]^T
           const uint32_t off = (kk & 3) * 32;
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss(tmem + L::TM_GP, sdesc_sw128(aGO + (kk >> 2) * BM * 128 + off, 16, 1024),
                  sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
         }
-        mma_commit(&ctrl->v_empty[s]);
+        mma_commit(&ctrl->v_empty[sv]);
         mma_commit(&ctrl->s_full);
         if (!mbar_wait(&ctrl->p_full, t & 1, abort)) {
           ok = false;
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  sdesc_sw128(kb + kk * 16 * 128, D == 64 ? BN * 128 : L::KCHUNK, 1024), I_ACC1,
                  1u);
         }
-        mma_commit(&ctrl->k_empty[s]);
+        mma_commit(&ctrl->k_empty[sk]);
       }
       if (ok) mma_commit(&ctrl->o_full);
       if (!ok) record_timeout(status, abort);
