@@ -107,3 +107,10 @@ def test_bwd_specified_workload_d128_whole_heads(name, heads):
     # checks every gradient entry of the selected heads.
     w = synth.WORKLOADS[name]
     check(w, run(w, heads=heads))
+
+
+@pytest.mark.parametrize("dtype,D,mask,N", [("bf16", 128, "causal", 4096), ("f16", 64, "none", 8192)])
+def test_bwd_long_sequences_one_head(dtype, D, mask, N):
+    # One (b, h) problem with many key and query tiles per CTA.
+    w = synth.small(dtype, 1, 1, N, D, mask, seed=N + D)
+    check(w, run(w))

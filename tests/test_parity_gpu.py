@@ -420,3 +420,20 @@ def test_split_kv_repeated_calls_are_bit_identical():
     for r in runs[1:]:
         for a, b in zip(runs[0], r):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dtype,D,mask,B,H,Nq,Nk", [
+    ("bf16", 128, "causal", 1, 2, 16384, 16384),   # long causal rows
+    ("f16", 64, "none", 1, 1, 256, 65536),          # long key range: 16-way split-KV
+    ("bf16", 64, "bool", 1, 2, 8192, 8192),
+])
+def test_long_sequences_on_sampled_rows(dtype, D, mask, B, H, Nq, Nk):
+    w = synth.small(dtype, B, H, Nq, D, mask, seed=Nq // 64 + D, Nk=Nk)
+    inp = synth.make_inputs(w)
+    o, t_o, lse, mu, path = run_gpu(w, inp)
+    assert path in (1, 3)
+    eo, et, el = sampled_rows(w, inp, o, t_o, lse, 64)
+    log_error(w.name + "[long]", o=eo, t_o=et, lse=el)
+    assert eo <= TOL[dtype] and et <= TOL[dtype], (w.name, eo, et)
+    assert el <= LSE_TOL[dtype]
+    assert torch.isfinite(o).all() and torch.isfinite(t_o).all()
