@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
-      mbar_init(&ctrl->p_full[s], kSoftmaxThreads);
-      mbar_init(&ctrl->max_ready[s], kSoftmaxThreads);
+      mbar_init(&ctrl->p_full[s], kSoftmaxThreads / 32);     // one arrival per warp
+      mbar_init(&ctrl->max_ready[s], kSoftmaxThreads / 32);
     }
     mbar_init(&ctrl->at_done, 1);
     mbar_init(&ctrl->pv_done[0], 1);
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sa[32], da[32];
+      uint32_t sa[32], da[32];  // S and dS (raw, unscaled) of this half tile
       if (TANGENT) {
         tmem_ld32x2(lane_base + buf * 128 + cofs, lane_base + buf * 128 + BN + cofs, sa, da);
       } else {
@@ -547,13 +547,64 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj > i) x[jj] = -INFINITY;
       }
+      // p~ = 2^(x - m_use), P~ and P~ * s * dS packed to 16 bits, and the sums
+      // of the packed values (l, mu~) and of the fp32 p~; x is left as it is.
+      uint32_t pk[HN / 2], pdk[HN / 2];
+      float l_part = 0.f, lx_part = 0.f, mu_part = 0.f;
+      auto weights = [&](float m_use) {
+        float e[HN];
+        if (MASK == kMaskAdditive) {
+#pragma unroll
+          for (int jj = 0; jj < HN; ++jj) e[jj] = ex2_approx(x[jj] - m_use);
+        } else {
+          const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
+#pragma unroll
+          for (int jj = 0; jj < HN; jj += 2) {
+            const float2 arg = fma2(make_float2(x[jj], x[jj + 1]), c2, nm2);
+            e[jj] = ex2_approx(arg.x);
+            e[jj + 1] = ex2_approx(arg.y);
+          }
+        }
+        float2 lsum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        float2 xsum[2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+        for (int jj = 0; jj < HN; jj += 2) {
+          pk[jj >> 1] = ElemTraits<T>::pack(e[jj], e[jj + 1]);
+          lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], ElemTraits<T>::unpack(pk[jj >> 1]));
+          xsum[(jj >> 1) & 1] = add2(xsum[(jj >> 1) & 1], make_float2(e[jj], e[jj + 1]));
+        }
+        l_part = (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
+                 (lsum[3].x + lsum[3].y);
+        lx_part = (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
+        if (TANGENT) {
+          float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+          const float2 s2 = make_float2(s_scale, s_scale);
+#pragma unroll
+          for (int jj = 0; jj < HN; jj += 2) {
+            const float2 ds = make_float2(__uint_as_float(da[jj]), __uint_as_float(da[jj + 1]));
+            const float2 pd = mul2(make_float2(e[jj], e[jj + 1]), mul2(ds, s2));
+            pdk[jj >> 1] = ElemTraits<T>::pack(pd.x, pd.y);
+            msum[(jj >> 1) & 3] = add2(msum[(jj >> 1) & 3], ElemTraits<T>::unpack(pdk[jj >> 1]));
+          }
+          mu_part = (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
+                    (msum[3].x + msum[3].y);
+        }
+      };
       const float mx = tree_max(x);
       const float m_half = (MASK == kMaskAdditive) ? mx : mx * c;
       float m_tile = m_half;
+      bool spec = false;  // weights already computed with the unchanged row maximum
       if constexpr (!L::kHalfAcc) {
-        // Exchange the half-row maxima between the two warpgroups.
+        // Exchange the half-row maxima between the two warpgroups.  Until the
+        // other half's maximum is in, assume the row maximum stays (the usual
+        // case after the first tile) and compute the weights with it; the
+        // decision below is the same either way, so is every value stored.
         ctrl->xmax[buf][wg][r] = m_half;
-        mbar_arrive(&ctrl->max_ready[buf]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->max_ready[buf]);
+        spec = __all_sync(0xffffffffu,
+                          m_run != -INFINITY && !(m_half > m_run + kRescaleThreshold));
+        if (spec) weights(m_run);
         if (!warp_wait(&ctrl->max_ready[buf], (t >> 1) & 1, p.status, abort)) {
           ok = false;
           break;
@@ -561,61 +612,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m_tile = fmaxf(m_half, ctrl->xmax[buf][wg ^ 1][r]);
       }
       const bool need = m_tile > m_run + kRescaleThreshold;
-      const float m_new = need ? m_tile : m_run;
-      const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-      l_run *= alpha;
-      lx_run *= alpha;
-      mu_run *= alpha;
-      if (t > 0 && __any_sync(0xffffffffu, need)) {
-        // A and T hold tile t-1's contributions once its MMAs are done; each
-        // warpgroup rescales half of the [A | T] columns of its rows.
-        if (!warp_wait(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // Shared accumulator: each warpgroup rescales half of its columns;
-        // per-warpgroup accumulators: each rescales its own.
-        const int c_lo = L::kHalfAcc ? 0 : wg * (ACC_COLS / 2);
-        const int c_hi = L::kHalfAcc ? ACC_COLS : (wg + 1) * (ACC_COLS / 2);
-        const uint32_t a_base = lane_base + L::TM_A + wg * L::ACC_STRIDE;
+      if (!spec || __any_sync(0xffffffffu, need)) {
+        const float m_new = need ? m_tile : m_run;
+        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+        l_run *= alpha;
+        lx_run *= alpha;
+        mu_run *= alpha;
+        if (t > 0 && __any_sync(0xffffffffu, need)) {
+          // A and T hold tile t-1's contributions once its MMAs are done; each
+          // warpgroup rescales half of the [A | T] columns of its rows.
+          if (!warp_wait(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // Shared accumulator: each warpgroup rescales half of its columns;
+          // per-warpgroup accumulators: each rescales its own.
+          const int c_lo = L::kHalfAcc ? 0 : wg * (ACC_COLS / 2);
+          const int c_hi = L::kHalfAcc ? ACC_COLS : (wg + 1) * (ACC_COLS / 2);
+          const uint32_t a_base = lane_base + L::TM_A + wg * L::ACC_STRIDE;
 #pragma unroll 1
-        for (int col = c_lo; col < c_hi; col += 32) {
-          uint32_t acc[32];
-          tmem_ld32(a_base + col, acc);
+          for (int col = c_lo; col < c_hi; col += 32) {
+            uint32_t acc[32];
+            tmem_ld32(a_base + col, acc);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc[e] = __float_as_uint(__uint_as_float(acc[e]) * alpha);
-          tmem_st32(a_base + col, acc);
+            for (int e = 0; e < 32; ++e) acc[e] = __float_as_uint(__uint_as_float(acc[e]) * alpha);
+            tmem_st32(a_base + col, acc);
+          }
+          tmem_st_wait();
         }
-        tmem_st_wait();
+        m_run = m_new;
+        weights((m_run == -INFINITY) ? 0.0f : m_run);
       }
-      m_run = m_new;
-      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-
-      if (MASK == kMaskAdditive) {
-#pragma unroll
-        for (int jj = 0; jj < HN; ++jj) x[jj] = ex2_approx(x[jj] - m_use);
-      } else {
-        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
-#pragma unroll
-        for (int jj = 0; jj < HN; jj += 2) {
-          const float2 arg = fma2(make_float2(x[jj], x[jj + 1]), c2, nm2);
-          x[jj] = ex2_approx(arg.x);
-          x[jj + 1] = ex2_approx(arg.y);
-        }
-      }
-      uint32_t pk[HN / 2];
-      float2 lsum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-      float2 xsum[2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-      for (int jj = 0; jj < HN; jj += 2) {
-        pk[jj >> 1] = ElemTraits<T>::pack(x[jj], x[jj + 1]);
-        lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], ElemTraits<T>::unpack(pk[jj >> 1]));
-        xsum[(jj >> 1) & 1] = add2(xsum[(jj >> 1) & 1], make_float2(x[jj], x[jj + 1]));
-      }
-      l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
-               (lsum[3].x + lsum[3].y);
-      lx_run += (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
+      l_run += l_part;
+      lx_run += lx_part;
+      mu_run += mu_part;
       // Where P~ goes: with per-warpgroup accumulators (no per-tile exchange)
       // into this warpgroup's own S columns, already read, since the other
       // warpgroup may still be reading its scores; otherwise the exchange has
@@ -623,24 +654,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // side by side.
       const uint32_t pofs = L::kHalfAcc ? cofs : wg * (HN / 2);
       tmem_st16(lane_base + buf * 128 + pofs, pk);
-      if (TANGENT) {
-        float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-        const float2 s2 = make_float2(s_scale, s_scale);
-        uint32_t pdk[HN / 2];
-#pragma unroll
-        for (int jj = 0; jj < HN; jj += 2) {
-          const float2 ds = make_float2(__uint_as_float(da[jj]), __uint_as_float(da[jj + 1]));
-          const float2 pd = mul2(make_float2(x[jj], x[jj + 1]), mul2(ds, s2));
-          pdk[jj >> 1] = ElemTraits<T>::pack(pd.x, pd.y);
-          msum[(jj >> 1) & 3] = add2(msum[(jj >> 1) & 3], ElemTraits<T>::unpack(pdk[jj >> 1]));
-        }
-        mu_run += (msum[0].x + msum[0].y) + (msum[1].x + msum[1].y) + (msum[2].x + msum[2].y) +
-                  (msum[3].x + msum[3].y);
-        tmem_st16(lane_base + buf * 128 + BN + pofs, pdk);
-      }
+      if (TANGENT) tmem_st16(lane_base + buf * 128 + BN + pofs, pdk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ctrl->p_full[buf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctrl->p_full[buf]);  // one arrival per softmax warp
     }
 
     // ------------------------------------------------------------ epilogue
