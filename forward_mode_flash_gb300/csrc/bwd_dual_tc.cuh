@@ -45,11 +45,16 @@
 
 namespace jvp {
 
-constexpr int kBwdThreads = 64 + 256;
+// Query-major kernel: warp 0 TMA, warp 1 the [S | dS] score products and the
+// accumulate MMAs, warps 2..9 elementwise, warp 10 the [G | gP] score products.
+constexpr int kBwdThreads = 96 + 256;
+constexpr int kBwdScoreWarpQ = 10;
 // The key-major kernel adds a warp (10) that issues the accumulate MMAs while
-// warp 1 issues the score products.
-constexpr int kBwdThreadsK = 96 + 256;
+// warp 1 issues the score products, and (key part) a warp (11) that issues
+// the second, independent group of score products.
+constexpr int kBwdThreadsK = 128 + 256;
 constexpr int kBwdAccWarp = 10;
+constexpr int kBwdScoreWarpB = 11;
 
 // ----------------------------------------------------------------------------
 // Query-major kernel.
@@ -82,7 +87,7 @@ template <int NSK, int NSV>
 struct BwdCtrl {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
-  uint64_t s_full, p_full, o_full, drain;
+  uint64_t s_full, p_full, o_full, drain, drain_b;
   uint32_t tmem_base;
   int abort;
 };
@@ -157,10 +162,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&ctrl->v_full[s], 1);
       mbar_init(&ctrl->v_empty[s], 1);
     }
-    mbar_init(&ctrl->s_full, 1);
+    mbar_init(&ctrl->s_full, 2);  // one commit from each score-issuing thread
     mbar_init(&ctrl->p_full, 256);
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
+    mbar_init(&ctrl->drain_b, 1);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -228,17 +234,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = mbar_wait(&ctrl->q_full, 0, abort);
       tc_fence_after();
       const uint32_t aQ = smem_u32(smem + L::OFF_Q), adQ = smem_u32(smem + L::OFF_DQ);
-      const uint32_t aGO = smem_u32(smem + L::OFF_GO), aGTO = smem_u32(smem + L::OFF_GTO);
+      // [S | dS] of tile t goes into columns [0, 128) after this thread's
+      // accumulate MMAs of tile t - 1 (which read gS, g_dS there), in issue
+      // order; warp 10 fills [G | gP] in columns [128, 256) meanwhile.
       for (int t = 0; ok && t < n_kv; ++t) {
-        const int sk = t % NSK, sv = t % NSV;
-        if (!mbar_wait(&ctrl->k_full[sk], (t / NSK) & 1, abort) ||
-            !mbar_wait(&ctrl->v_full[sv], (t / NSV) & 1, abort)) {
+        const int sk = t % NSK;
+        if (!mbar_wait(&ctrl->k_full[sk], (t / NSK) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t kb = smem_u32(smem + L::OFF_K + sk * L::KBLK);
-        const uint32_t vb = smem_u32(smem + L::OFF_V + sv * L::KBLK);
 #pragma unroll
         for (int kk = 0; kk < KSD; ++kk) {  // [S | Q dK^T] = Q [K ; dK]^T
           const uint32_t off = (kk & 3) * 32;
@@ -251,19 +257,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss(tmem + L::TM_DS, sdesc_sw128(adQ + (kk >> 2) * BM * 128 + off, 16, 1024),
                  sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
         }
-#pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // [G | gtO dV^T] = gtO [V ; dV]^T
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_G, sdesc_sw128(aGTO + (kk >> 2) * BM * 128 + off, 16, 1024),
-                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N128, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // gtO dV^T += gO V^T
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_GP, sdesc_sw128(aGO + (kk >> 2) * BM * 128 + off, 16, 1024),
-                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
-        }
-        mma_commit(&ctrl->v_empty[sv]);
         mma_commit(&ctrl->s_full);
         if (!mbar_wait(&ctrl->p_full, t & 1, abort)) {
           ok = false;
@@ -303,7 +296,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int zero = 0;
       mbar_wait(&ctrl->drain, 0, &zero);
     }
-  } else {
+  } else if (warp == kBwdScoreWarpQ) {
+    // ------------------------------------------------------------ [G | gP] score MMAs
+    // Columns [128, 256) are free for tile t once the elementwise warps are
+    // done with tile t - 1 (the accumulate MMAs read only columns [0, 128)).
+    if (lane == 0) {
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort);
+      tc_fence_after();
+      const uint32_t aGO = smem_u32(smem + L::OFF_GO), aGTO = smem_u32(smem + L::OFF_GTO);
+      for (int t = 0; ok && t < n_kv; ++t) {
+        const int sv = t % NSV;
+        if ((t > 0 && !mbar_wait(&ctrl->p_full, (t - 1) & 1, abort)) ||
+            !mbar_wait(&ctrl->v_full[sv], (t / NSV) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + L::OFF_V + sv * L::KBLK);
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // [G | gtO dV^T] = gtO [V ; dV]^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_G, sdesc_sw128(aGTO + (kk >> 2) * BM * 128 + off, 16, 1024),
+                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N128, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // gtO dV^T += gO V^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(tmem + L::TM_GP, sdesc_sw128(aGO + (kk >> 2) * BM * 128 + off, 16, 1024),
+                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
+        }
+        mma_commit(&ctrl->v_empty[sv]);
+        mma_commit(&ctrl->s_full);
+      }
+      if (!ok) record_timeout(status, abort);
+      mma_commit(&ctrl->drain_b);
+      const int zero = 0;
+      mbar_wait(&ctrl->drain_b, 0, &zero);
+    }
+  } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ elementwise
     const int wg = (warp - 2) >> 2;
     const int sub = warp & 3;
@@ -474,6 +504,7 @@ struct BwdKCtrl {
   uint64_t q_full[NS], q_empty[NS];
   uint64_t s_full[2], p_full[2], o_full, drain;
   uint64_t acc_done[2], drain_acc;  // accumulate MMAs of the tile in each buffer are complete
+  uint64_t drain_b;
   uint32_t tmem_base;
   int abort;
 };
@@ -531,13 +562,15 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       mbar_init(&ctrl->q_empty[s], 1);
     }
     for (int u = 0; u < 2; ++u) {
-      mbar_init(&ctrl->s_full[u], 1);
+      // key part: one commit from each of the two score-issuing threads
+      mbar_init(&ctrl->s_full[u], L::kK ? 2 : 1);
       mbar_init(&ctrl->p_full[u], 256);
       mbar_init(&ctrl->acc_done[u], 1);
     }
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
     mbar_init(&ctrl->drain_acc, 1);
+    mbar_init(&ctrl->drain_b, 1);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -638,15 +671,14 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       bool ok = mbar_wait(&ctrl->k_full, 0, abort);
       tc_fence_after();
       const uint32_t aK = smem_u32(smem + L::OFF_K), adK = smem_u32(smem + L::OFF_DK);
-      const uint32_t aV = smem_u32(smem + L::OFF_V), adV = smem_u32(smem + L::OFF_DV);
 
-      // Score products of tile t into buffer t & 1.
+      // Score products of tile t into buffer t & 1 (the key part's second
+      // group, [G^T | V gO^T] and its dV gtO^T term, is issued by warp 11).
       auto issue_scores = [&](int t) -> bool {
         const int s = t % NS;
         if (!mbar_wait(&ctrl->q_full[s], (t / NS) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t qb = smem_u32(smem + L::OFF_ST + s * L::STAGE);  // [Q ; dQ]
-        const uint32_t ob = qb + L::QBLK;                               // [gtO ; gO]
         const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
 #pragma unroll
         for (int kk = 0; kk < KSD; ++kk) {  // [S^T | K dQ^T] = K [Q ; dQ]^T
@@ -659,20 +691,6 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
           const uint32_t off = (kk & 3) * 32;
           mma_ss(buf + L::DS_OFF, sdesc_sw128(adK + (kk >> 2) * BK * 128 + off, 16, 1024),
                  sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
-        }
-        if (L::kK) {
-#pragma unroll
-          for (int kk = 0; kk < KSD; ++kk) {  // [G^T | V gO^T] = V [gtO ; gO]^T
-            const uint32_t off = (kk & 3) * 32;
-            mma_ss(buf + L::G_OFF, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
-                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N2Q, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < KSD; ++kk) {  // V gO^T += dV gtO^T  (= gP1^T)
-            const uint32_t off = (kk & 3) * 32;
-            mma_ss(buf + L::GP_OFF, sdesc_sw128(adV + (kk >> 2) * BK * 128 + off, 16, 1024),
-                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
-          }
         }
         mma_commit(&ctrl->s_full[t & 1]);
         return true;
@@ -760,6 +778,45 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       mma_commit(&ctrl->drain_acc);
       const int zero = 0;
       mbar_wait(&ctrl->drain_acc, 0, &zero);
+    }
+  } else if (warp == kBwdScoreWarpB) {
+    // ------------------------------------------------------------ score MMAs, group B
+    // Key part: [G^T | V gO^T] = V [gtO ; gO]^T and V gO^T += dV gtO^T write
+    // columns [G_OFF, G_OFF + 2 BQ) of the buffer, disjoint from warp 1's
+    // products, so the two groups are issued side by side.  Same buffer rule:
+    // tile t waits for its stage and for the accumulate MMAs of tile t - 2.
+    if (L::kK && lane == 0) {
+      bool ok = mbar_wait(&ctrl->k_full, 0, abort);
+      tc_fence_after();
+      const uint32_t aV = smem_u32(smem + L::OFF_V), adV = smem_u32(smem + L::OFF_DV);
+      for (int t = 0; ok && t < n_t; ++t) {
+        const int s = t % NS;
+        if ((t >= 2 && !mbar_wait(&ctrl->acc_done[t & 1], ((t - 2) >> 1) & 1, abort)) ||
+            !mbar_wait(&ctrl->q_full[s], (t / NS) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ob = smem_u32(smem + L::OFF_ST + s * L::STAGE) + L::QBLK;  // [gtO ; gO]
+        const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // [G^T | V gO^T] = V [gtO ; gO]^T
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(buf + L::G_OFF, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                 sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N2Q, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSD; ++kk) {  // V gO^T += dV gtO^T  (= gP1^T)
+          const uint32_t off = (kk & 3) * 32;
+          mma_ss(buf + L::GP_OFF, sdesc_sw128(adV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                 sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
+        }
+        mma_commit(&ctrl->s_full[t & 1]);
+      }
+      if (!ok) record_timeout(status, abort);
+      mma_commit(&ctrl->drain_b);
+      const int zero = 0;
+      mbar_wait(&ctrl->drain_b, 0, &zero);
     }
   } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ elementwise
