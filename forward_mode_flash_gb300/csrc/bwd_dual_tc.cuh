@@ -496,12 +496,18 @@ struct BkLayout {
   static_assert(NS >= 2, "two stages at least");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(D == 64 || PART != 3, "the four accumulators fit TMEM only at D = 64");
+  // Value part alone: the score products read only a stage's [Q ; dQ] half
+  // and the accumulate products only its [gtO ; gO] half, so the two halves
+  // have their own barriers and [Q ; dQ] is released (and refilled, one tile
+  // ahead) as soon as the score products are done.
+  static constexpr bool kSplitStage = kV && !kK;
 };
 
 template <int NS>
 struct BwdKCtrl {
   uint64_t k_full;
   uint64_t q_full[NS], q_empty[NS];
+  uint64_t qq_full[NS], qq_empty[NS];  // the [Q ; dQ] half of a stage, when it has its own
   uint64_t s_full[2], p_full[2], o_full, drain;
   uint64_t acc_done[2], drain_acc;  // accumulate MMAs of the tile in each buffer are complete
   uint64_t drain_b;
@@ -560,6 +566,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&ctrl->q_full[s], 2);  // TMA bytes + the row scalars written by warp 0
       mbar_init(&ctrl->q_empty[s], 1);
+      mbar_init(&ctrl->qq_full[s], 1);
+      mbar_init(&ctrl->qq_empty[s], 1);
     }
     for (int u = 0; u < 2; ++u) {
       // key part: one commit from each of the two score-issuing threads
@@ -628,24 +636,52 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       }
     };
     if (n_t > 0) load_scalars(0);
-    int fills = 0;
-    for (int t = 0; t < n_t; ++t) {
+    int fills = 0, qfills = 0;
+    // The [Q ; dQ] half of tile tq's stage on its own barriers (lane 0).
+    auto load_q = [&](int tq) -> bool {
+      const int sq = tq % NS;
+      if (!mbar_wait(&ctrl->qq_empty[sq], ((tq / NS) & 1) ^ 1, abort)) return false;
+      const int hq = hk * p.kv_group + tq / n_th;
+      const int iq = (t_begin + tq % n_th) * BQ;
+      uint8_t* stq = smem + L::OFF_ST + sq * L::STAGE;
+      mbar_arrive_expect_tx(&ctrl->qq_full[sq], L::QBLK);
+      for (int c = 0; c < L::KCH; ++c) {
+        tma_load_4d(stq + c * L::QCHUNK, mq, &ctrl->qq_full[sq], c * 64, iq, hq, b);
+        tma_load_4d(stq + c * L::QCHUNK + BQ * 128, mdq, &ctrl->qq_full[sq], c * 64, iq, hq, b);
+      }
+      ++qfills;
+      return true;
+    };
+    bool q_ok = true;
+    if (L::kSplitStage && n_t > 0 && lane == 0) q_ok = load_q(0);
+    q_ok = __shfl_sync(0xffffffffu, q_ok, 0);  // warp-uniform loop condition
+    if (!q_ok && lane == 0) record_timeout(status, abort);
+    for (int t = 0; q_ok && t < n_t; ++t) {
       const int s = t % NS;
       const uint32_t ph = (t / NS) & 1;
       const int h = hk * p.kv_group + t / n_th;  // query head of this tile
       const int i0 = (t_begin + t % n_th) * BQ;
       bool got = true;
-      if (lane == 0) got = mbar_wait(&ctrl->q_empty[s], ph ^ 1, abort);
+      if (lane == 0) {
+        if (L::kSplitStage && t + 1 < n_t) got = load_q(t + 1);
+        if (got) got = mbar_wait(&ctrl->q_empty[s], ph ^ 1, abort);
+      }
       if (!__shfl_sync(0xffffffffu, got, 0)) {
         if (lane == 0) record_timeout(status, abort);
         break;
       }
       uint8_t* st = smem + L::OFF_ST + s * L::STAGE;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&ctrl->q_full[s], 2 * L::QBLK);
+        if constexpr (L::kSplitStage) {
+          mbar_arrive_expect_tx(&ctrl->q_full[s], L::QBLK);
+        } else {
+          mbar_arrive_expect_tx(&ctrl->q_full[s], 2 * L::QBLK);
+        }
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(st + c * L::QCHUNK, mq, &ctrl->q_full[s], c * 64, i0, h, b);
-          tma_load_4d(st + c * L::QCHUNK + BQ * 128, mdq, &ctrl->q_full[s], c * 64, i0, h, b);
+          if (!L::kSplitStage) {
+            tma_load_4d(st + c * L::QCHUNK, mq, &ctrl->q_full[s], c * 64, i0, h, b);
+            tma_load_4d(st + c * L::QCHUNK + BQ * 128, mdq, &ctrl->q_full[s], c * 64, i0, h, b);
+          }
           tma_load_4d(st + L::QBLK + c * L::QCHUNK, mgto, &ctrl->q_full[s], c * 64, i0, h, b);
           tma_load_4d(st + L::QBLK + c * L::QCHUNK + BQ * 128, mgo, &ctrl->q_full[s], c * 64, i0,
                       h, b);
@@ -664,6 +700,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       mbar_wait(&ctrl->k_full, 0, &zero);
       for (int t = max(0, fills - NS); t < fills; ++t)
         mbar_wait(&ctrl->q_full[t % NS], (t / NS) & 1, &zero);
+      for (int t = max(0, qfills - NS); t < qfills; ++t)
+        mbar_wait(&ctrl->qq_full[t % NS], (t / NS) & 1, &zero);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ score MMAs
@@ -676,7 +714,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       // group, [G^T | V gO^T] and its dV gtO^T term, is issued by warp 11).
       auto issue_scores = [&](int t) -> bool {
         const int s = t % NS;
-        if (!mbar_wait(&ctrl->q_full[s], (t / NS) & 1, abort)) return false;
+        if (!mbar_wait(L::kSplitStage ? &ctrl->qq_full[s] : &ctrl->q_full[s], (t / NS) & 1, abort))
+          return false;
         tc_fence_after();
         const uint32_t qb = smem_u32(smem + L::OFF_ST + s * L::STAGE);  // [Q ; dQ]
         const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
@@ -692,6 +731,7 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
           mma_ss(buf + L::DS_OFF, sdesc_sw128(adK + (kk >> 2) * BK * 128 + off, 16, 1024),
                  sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
         }
+        if (L::kSplitStage) mma_commit(&ctrl->qq_empty[s]);
         mma_commit(&ctrl->s_full[t & 1]);
         return true;
       };
