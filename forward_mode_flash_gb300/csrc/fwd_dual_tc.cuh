@@ -121,6 +121,7 @@ struct TcCtrl {
   uint64_t kdk_full[NS], kdk_empty[NS];
   uint64_t vdv_full[NS], vdv_empty[NS];
   uint64_t s_full[2], p_full[2], max_ready[2];
+  uint64_t s_ready[2];  // S of a score buffer is final (its dS may still be accumulating)
   uint64_t at_done, o_full, drain, drain_pv, sums_ready;
   uint64_t pv_done[2];  // P~V MMAs of the tile in each score buffer are complete
   uint32_t tmem_base;
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
+      mbar_init(&ctrl->s_ready[s], 1);
       mbar_init(&ctrl->p_full[s], kSoftmaxThreads / 32);     // one arrival per warp
       mbar_init(&ctrl->max_ready[s], kSoftmaxThreads / 32);
     }
@@ -406,6 +408,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
           mma_ss(d_s, a, bd, IDESC_S, kk > 0 ? 1u : 0u);
         }
+        // S is complete: the softmax starts on it while dQ K^T accumulates into dS.
+        if (TANGENT) mma_commit(&ctrl->s_ready[t & 1]);
         if (TANGENT) {
 #pragma unroll
           for (int kk = 0; kk < KSTEPS_D; ++kk) {
@@ -441,15 +445,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + L::OFF_VDV + s * L::VDV_BYTES);
-        // P~ (16-bit pairs) of keys [16 kk, 16 kk + 16), P~ * dS BN columns
-        // further: with per-warpgroup accumulators warpgroup kk / 2 stored them
-        // at the start of its own S columns, otherwise they are packed.
+        // P~ (16-bit pairs) of keys [16 kk, 16 kk + 16): with per-warpgroup
+        // accumulators warpgroup kk / 2 stored them at the start of its own S
+        // columns, otherwise they are packed; P~ * dS, BN columns further, is
+        // always at the start of the warpgroup's own dS columns.
         const uint32_t p_tm = tmem + buf * 128;
         const uint32_t pd_tm = tmem + buf * 128 + BN;
         auto pcol = [](int kk) -> uint32_t {
           return L::kHalfAcc
                      ? static_cast<uint32_t>((kk / (HN / 16)) * HN + (kk % (HN / 16)) * 8)
                      : static_cast<uint32_t>(kk * 8);
+        };
+        // P~ * dS always sits at the start of its warpgroup's own dS columns.
+        auto pdcol = [](int kk) -> uint32_t {
+          return static_cast<uint32_t>((kk / (HN / 16)) * HN + (kk % (HN / 16)) * 8);
         };
         // With per-warpgroup accumulators, K-steps [w * KH, w * KH + KH) (the
         // keys of warpgroup w) go to warpgroup w's [A | T].
@@ -464,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < KSTEPS_N; ++kk) {
             const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
-            mma_ts(tmem + L::TM_T + (kk / KH) * L::ACC_STRIDE, pd_tm + pcol(kk), bd, IDESC_T, 1u);
+            mma_ts(tmem + L::TM_T + (kk / KH) * L::ACC_STRIDE, pd_tm + pdcol(kk), bd, IDESC_T, 1u);
           }
         }
         mma_commit(&ctrl->vdv_empty[s]);
@@ -514,17 +523,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int j0 = (kv0 + t) * BN + cofs;  // first key of this half tile
       MaskRegs<MASK, HN> mreg;
       if (row_ok) mreg.load(p, mrow, j0);
-      if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
+      // With tangents, S is read as soon as it is final and dS (whose
+      // dQ K^T part is still accumulating) only when the tangent terms need it.
+      if (!warp_wait(TANGENT ? &ctrl->s_ready[buf] : &ctrl->s_full[buf], (t >> 1) & 1, p.status,
+                     abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sa[32], da[32];  // S and dS (raw, unscaled) of this half tile
-      if (TANGENT) {
-        tmem_ld32x2(lane_base + buf * 128 + cofs, lane_base + buf * 128 + BN + cofs, sa, da);
-      } else {
-        tmem_ld32(lane_base + buf * 128 + cofs, sa);
-      }
+      tmem_ld32(lane_base + buf * 128 + cofs, sa);
       float x[HN];
 #pragma unroll
       for (int jj = 0; jj < HN; ++jj) x[jj] = __uint_as_float(sa[jj]);
@@ -547,12 +555,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int jj = 0; jj < HN; ++jj)
           if (j0 + jj > i) x[jj] = -INFINITY;
       }
-      // p~ = 2^(x - m_use), P~ and P~ * s * dS packed to 16 bits, and the sums
-      // of the packed values (l, mu~) and of the fp32 p~; x is left as it is.
+      // p~ = 2^(x - m_use) (kept in e), P~ packed to 16 bits, and the sums of
+      // the packed values (l) and of the fp32 p~ (lx); x is left as it is.
       uint32_t pk[HN / 2], pdk[HN / 2];
+      float e[HN];
       float l_part = 0.f, lx_part = 0.f, mu_part = 0.f;
       auto weights = [&](float m_use) {
-        float e[HN];
         if (MASK == kMaskAdditive) {
 #pragma unroll
           for (int jj = 0; jj < HN; ++jj) e[jj] = ex2_approx(x[jj] - m_use);
@@ -576,7 +584,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l_part = (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y) + (lsum[2].x + lsum[2].y) +
                  (lsum[3].x + lsum[3].y);
         lx_part = (xsum[0].x + xsum[0].y) + (xsum[1].x + xsum[1].y);
-        if (TANGENT) {
+      };
+      // P~ * s * dS packed to 16 bits and the sum of the packed values (mu~).
+      auto tangent_terms = [&]() {
+        {
           float2 msum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
           const float2 s2 = make_float2(s_scale, s_scale);
 #pragma unroll
@@ -646,7 +657,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       l_run += l_part;
       lx_run += lx_part;
-      mu_run += mu_part;
       // Where P~ goes: with per-warpgroup accumulators (no per-tile exchange)
       // into this warpgroup's own S columns, already read, since the other
       // warpgroup may still be reading its scores; otherwise the exchange has
@@ -654,7 +664,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // side by side.
       const uint32_t pofs = L::kHalfAcc ? cofs : wg * (HN / 2);
       tmem_st16(lane_base + buf * 128 + pofs, pk);
-      if (TANGENT) tmem_st16(lane_base + buf * 128 + BN + pofs, pdk);
+      if (TANGENT) {
+        // dS is complete once the buffer's dQ K^T products are; P~ * dS goes
+        // into this warpgroup's own dS columns (the other warpgroup may not
+        // have read its dS yet).
+        if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_ld32(lane_base + buf * 128 + BN + cofs, da);
+        tangent_terms();
+        mu_run += mu_part;
+        tmem_st16(lane_base + buf * 128 + BN + cofs, pdk);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
