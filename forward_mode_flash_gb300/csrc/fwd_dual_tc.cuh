@@ -122,6 +122,7 @@ struct TcCtrl {
   uint64_t vdv_full[NS], vdv_empty[NS];
   uint64_t s_full[2], p_full[2], max_ready[2];
   uint64_t s_ready[2];  // S of a score buffer is final (its dS may still be accumulating)
+  uint64_t p_ready[2];  // P~ of a score buffer is stored (P~ * dS may not be yet)
   uint64_t at_done, o_full, drain, drain_pv, sums_ready;
   uint64_t pv_done[2];  // P~V MMAs of the tile in each score buffer are complete
   uint32_t tmem_base;
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
       mbar_init(&ctrl->s_ready[s], 1);
+      mbar_init(&ctrl->p_ready[s], kSoftmaxThreads / 32);
       mbar_init(&ctrl->p_full[s], kSoftmaxThreads / 32);     // one arrival per warp
       mbar_init(&ctrl->max_ready[s], kSoftmaxThreads / 32);
     }
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < n_kv; ++t) {
         const int buf = t & 1;
-        if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+        if (!mbar_wait(TANGENT ? &ctrl->p_ready[buf] : &ctrl->p_full[buf], (t >> 1) & 1, abort)) {
           ok = false;
           break;
         }
@@ -470,6 +472,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_ts(acc_base, p_tm + pcol(kk), bd, IDESC_AT, (t > 0 || kk % KH > 0) ? 1u : 0u);
         }
         if (TANGENT) {
+          if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < KSTEPS_N; ++kk) {
             const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
@@ -665,6 +672,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t pofs = L::kHalfAcc ? cofs : wg * (HN / 2);
       tmem_st16(lane_base + buf * 128 + pofs, pk);
       if (TANGENT) {
+        // Publish P~ first: the P~ [V | dV] products run while the tangent
+        // terms wait for dS.
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->p_ready[buf]);
         // dS is complete once the buffer's dQ K^T products are; P~ * dS goes
         // into this warpgroup's own dS columns (the other warpgroup may not
         // have read its dS yet).
