@@ -525,11 +525,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  : static_cast<const void*>(static_cast<const float*>(p.mask) + off);
     }
 
+    // Mask entries are loaded one tile ahead, so their global-memory latency
+    // overlaps a whole tile of work (not the additive mask at D = 128, whose
+    // two tiles of 32 floats would not fit the register budget).
+    constexpr bool kMaskAhead = !(MASK == kMaskAdditive && D == 128);
+    MaskRegs<MASK, HN> mnext;
+    if (kMaskAhead && row_ok && n_kv > 0) mnext.load(p, mrow, kv0 * BN + cofs);
     for (int t = 0; t < n_kv; ++t) {
       const int buf = t & 1;
       const int j0 = (kv0 + t) * BN + cofs;  // first key of this half tile
       MaskRegs<MASK, HN> mreg;
-      if (row_ok) mreg.load(p, mrow, j0);
+      if constexpr (kMaskAhead) {
+        mreg = mnext;
+        if (row_ok && t + 1 < n_kv) mnext.load(p, mrow, j0 + BN);
+      } else {
+        if (row_ok) mreg.load(p, mrow, j0);
+      }
       // With tangents, S is read as soon as it is final and dS (whose
       // dQ K^T part is still accumulating) only when the tangent terms need it.
       if (!warp_wait(TANGENT ? &ctrl->s_ready[buf] : &ctrl->s_full[buf], (t >> 1) & 1, p.status,
