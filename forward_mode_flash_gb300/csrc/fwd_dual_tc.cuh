@@ -124,6 +124,7 @@ struct TcCtrl {
   uint64_t s_ready[2];  // S of a score buffer is final (its dS may still be accumulating)
   uint64_t p_ready[2];  // P~ of a score buffer is stored (P~ * dS may not be yet)
   uint64_t at_done, o_full, drain, drain_pv, sums_ready;
+  uint64_t o_staged;  // every softmax warp has staged its O / tO rows in shared memory
   uint64_t pv_done[2];  // P~V MMAs of the tile in each score buffer are complete
   uint32_t tmem_base;
   int abort;
@@ -207,6 +208,22 @@ struct MaskRegs<kMaskAdditive, KN> {
     }
   }
 };
+
+// Writes NP 16-byte pieces (8 16-bit values each) of row r, from column col
+// on, into a [128 x D] tile in shared memory laid out as the TMA box of the
+// output tensor map: 64-column chunks of 128 rows x 128 bytes, the 16-byte
+// piece k of a row at position k ^ (row % 8) (128-byte swizzle).
+template <int NP>
+__device__ __forceinline__ void stage_row(uint32_t tile, int r, int col,
+                                          const uint32_t (&v)[NP * 4]) {
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const int cc = col + 8 * q;
+    const uint32_t addr = tile + static_cast<uint32_t>((cc >> 6) * (kTcBlockM * 128) + r * 128 +
+                                                       ((((cc & 63) >> 3) ^ (r & 7)) << 4));
+    st_shared_v4(addr, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
 
 // Maximum of n values by a pairwise tree (log2 n dependent steps).
 template <int N>
@@ -307,6 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
     mbar_init(&ctrl->sums_ready, kSoftmaxThreads);
+    mbar_init(&ctrl->o_staged, kSoftmaxThreads / 32);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -719,6 +737,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
     }
     if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
+    // O and tO rows are staged in the (now idle) [K;dK] ring, laid out as the
+    // output tensor maps' 128-row boxes, and written by TMA stores: a warp
+    // storing its own 32 rows directly would touch 32 lines per instruction.
+    const uint32_t o_tile = smem_u32(smem + L::OFF_KDK);
+    const uint32_t t_tile = o_tile + L::KCH * L::BM * 128;
+    static_assert((TANGENT ? 2 : 1) * L::KCH * L::BM * 128 <= L::OFF_CTRL - L::OFF_KDK,
+                  "output staging fits the key/value rings");
     if (L::kHalfAcc && ok) {
       // Merge of the two warpgroups' states (each relative to its own max):
       // with M = max(m_0, m_1) and a_w = 2^(m_w - M), l = sum a_w l_w (so for
@@ -743,12 +768,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          : nullptr;
       if (SPLIT && row_ok && wg == 0)
         reinterpret_cast<float4*>(p.split_ws)[R] = make_float4(m_all, l_all, lx_all, mu_all);
-      T* orow = static_cast<T*>(p.o) + static_cast<long long>(b) * p.so.b +
-                static_cast<long long>(h) * p.so.h + static_cast<long long>(row_ok ? i : 0) * p.so.n;
-      T* trow = TANGENT ? static_cast<T*>(p.t_o) + static_cast<long long>(b) * p.sto.b +
-                              static_cast<long long>(h) * p.sto.h +
-                              static_cast<long long>(row_ok ? i : 0) * p.sto.n
-                        : nullptr;
 #pragma unroll 1
       for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 16) {
         float fa[16], ft[16];
@@ -790,14 +809,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               pt[e >> 1] = ElemTraits<T>::pack(ft[e] * inv_l - mu_row * o0,
                                                ft[e + 1] * inv_l - mu_row * o1);
           }
-          if (row_ok) {
-            uint4* od = reinterpret_cast<uint4*>(orow + col);
-            od[0] = make_uint4(po[0], po[1], po[2], po[3]);
-            od[1] = make_uint4(po[4], po[5], po[6], po[7]);
+          {
+            stage_row<2>(o_tile, r, col, po);
             if (TANGENT) {
-              uint4* td = reinterpret_cast<uint4*>(trow + col);
-              td[0] = make_uint4(pt[0], pt[1], pt[2], pt[3]);
-              td[1] = make_uint4(pt[4], pt[5], pt[6], pt[7]);
+              stage_row<2>(t_tile, r, col, pt);
             }
           }
         }
@@ -853,12 +868,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float mu_all = mu_run + ctrl->xsum[wg ^ 1][2][r];
       const float inv_l = (l_all > 0.0f) ? 1.0f / l_all : 0.0f;
       const float mu_row = mu_all * inv_l;
-      T* orow = static_cast<T*>(p.o) + static_cast<long long>(b) * p.so.b +
-                static_cast<long long>(h) * p.so.h + static_cast<long long>(row_ok ? i : 0) * p.so.n;
-      T* trow = TANGENT ? static_cast<T*>(p.t_o) + static_cast<long long>(b) * p.sto.b +
-                              static_cast<long long>(h) * p.sto.h +
-                              static_cast<long long>(row_ok ? i : 0) * p.sto.n
-                        : nullptr;
 #pragma unroll 1
       for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 32) {
         uint32_t a[32], tt[32];
@@ -883,24 +892,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             pt[e >> 1] = ElemTraits<T>::pack(t0, t1);
           }
         }
-        if (row_ok) {
-          uint4* od = reinterpret_cast<uint4*>(orow + col);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
-          if (TANGENT) {
-            uint4* td = reinterpret_cast<uint4*>(trow + col);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              td[v4] = make_uint4(pt[4 * v4], pt[4 * v4 + 1], pt[4 * v4 + 2], pt[4 * v4 + 3]);
-          }
-        }
+        stage_row<4>(o_tile, r, col, po);
+        if (TANGENT) stage_row<4>(t_tile, r, col, pt);
       }
       if (row_ok && wg == 0) {
         const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
         if (p.lse)
           p.lse[ridx] = (lx_all > 0.0f) ? (m_run + log2f(lx_all)) * kLn2 : -INFINITY;
         if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+      }
+    }
+    if (!SPLIT && ok) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctrl->o_staged);
+      if (warp == 2 && lane == 0) {
+        if (mbar_wait(&ctrl->o_staged, 0, abort)) {
+          for (int c = 0; c < L::KCH; ++c) {
+            tma_store_4d(&maps.o, smem + L::OFF_KDK + c * L::BM * 128, c * 64, q0, h, b);
+            if (TANGENT)
+              tma_store_4d(&maps.t_o, smem + L::OFF_KDK + (L::KCH + c) * L::BM * 128, c * 64, q0,
+                           h, b);
+          }
+          tma_store_commit();
+          tma_store_wait_read();  // the CTA's shared memory stays valid until then
+        } else {
+          record_timeout(p.status, abort);
+        }
       }
     }
     tc_fence_before();

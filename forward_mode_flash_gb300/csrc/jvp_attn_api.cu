@@ -297,6 +297,10 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     if (tc && !tangent) {
       maps.dq = maps.q, maps.dk = maps.k, maps.dv = maps.v;
     }
+    if (tc) tc = encode_map(&maps.o, dtype, out[0], B, H, Nq, D, out_strides[0], kTcBlockM);
+    if (tc && tangent)
+      tc = encode_map(&maps.t_o, dtype, out[1], B, H, Nq, D, out_strides[1], kTcBlockM);
+    if (tc && !tangent) maps.t_o = maps.o;
   }
   cudaError_t err;
   if (tc) {

@@ -64,6 +64,7 @@ cudaError_t launch_fwd_combine(DType dt, bool tangent, const FwdParams& p, cudaS
 // are unused by the primal-only variant).
 struct TcMaps {
   CUtensorMap q, k, v, dq, dk, dv;
+  CUtensorMap o, t_o;  // outputs, 128-row boxes (the epilogue's TMA stores)
 };
 
 // Tensor-core kernels (fp16/bf16, D in {64, 128}).  Return a cudaError_t.
