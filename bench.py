@@ -66,11 +66,41 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines, each line stripped.
+
+    A comment-only edit does not change the compiled kernel, so it should not
+    invalidate counters recorded for it.  (Scans for // and /* */ outside
+    string and character literals.)
+    """
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.strip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_hash() -> str:
+    """Hash of the tensor-core kernel's code (comments and layout excluded)."""
     h = hashlib.sha256()
     for rel in TC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,23 +12,28 @@
 //   A = sum p~ V          T = sum p~ (dS V + dV)
 // (p~ = exp(S - m)), then O = A / l, mu = mu~ / l, tO = T / l - mu O.
 //
-// Work decomposition: one CTA per (128-row query tile, batch*head), ten warps.
+// Work decomposition: one CTA per (128-row query tile, batch*head), eleven
+// warps, one CTA per SM (it owns all 512 TMEM columns).
 //   warp 0      TMA producer: Q, dQ once; then per 64-key tile the [K;dK]
 //               block and the [V|dV] block, through an NS-deep ring.
-//   warp 1      TMEM allocator and single-thread MMA issuer.
+//   warp 1      TMEM allocator; one thread issues the score MMAs.
 //   warps 2..9  softmax, two warpgroups: a thread owns one query row (its TMEM
 //               lane) and one half (32 keys) of every key tile; the two halves
 //               exchange their maxima through shared memory each tile.  The
 //               epilogue splits the output columns the same way.
+//   warp 10     one thread issues the P~V MMAs.
 // Per key tile t (buffer b = t % 2 of the double-buffered score region):
 //   M1  [S | Q dK^T] = Q [K ; dK]^T          (N = 128, SMEM x SMEM)
+//       -> S is final: the softmax starts (max, exchange, exponentials)
 //   M2  Q dK^T      += dQ K^T                 (N = 64)
-//   softmax: p~ and p~ * s * dS_raw, written back to TMEM as 16-bit values
-//            over the S / dS columns they came from
+//   softmax: P~ written back to TMEM (16-bit) over the S columns, published;
 //   M3  [A | T]     += P~ [V | dV]            (N = 2D, A operand from TMEM)
+//   softmax, once M2 is done: P~ * s * dS_raw into its own dS columns
 //   M4  T           += (P~ * dS) V            (N = D)
-// The MMA warp issues M1/M2 of tile t+1 before M3/M4 of tile t, so the
-// tensor core computes the next scores while the softmax warps work.
+// M1/M2 of tile t+2 reuse buffer b once M3/M4 of tile t are done, so the
+// tensor core computes the next scores while the softmax warps work.  The
+// epilogue stages O and tO in the idle [K;dK] ring and writes them with TMA
+// stores.
 //
 // Rescaling is conditional: the row maximum used in the exponent is only
 // moved when a tile's maximum exceeds it by more than 2^8, so A, T, l and mu~
