@@ -23,7 +23,9 @@
 // with the same shared-memory K/dK tile read as an MN-major operand.
 //
 // Key-major kernel (gK, g_dK, gV, g_dV): one CTA per 128-key tile, looping over
-// 64-row query tiles, with the transposed scores (TMEM lanes = keys):
+// query tiles (64 rows for the value part, 32 when the four score matrices
+// of the key part share a TMEM buffer), with the transposed scores (TMEM
+// lanes = keys):
 //   [S^T | K dQ^T]    = K [Q ; dQ]^T        then  K dQ^T += dK Q^T
 //   [G^T | V gO^T]    = V [gtO ; gO]^T      then  V gO^T += dV gtO^T   (= gP1^T)
 //   [g_dV | gV] += P^T [gtO | gO],  gV += dP^T gtO
@@ -31,9 +33,14 @@
 // At D = 128 the four key-side accumulators do not fit TMEM next to the
 // scores, so the key-major kernel runs twice (value part, key part).
 //
-// Each kernel: warp 0 TMA producer, warp 1 TMEM allocator + single-thread MMA
-// issuer, warps 2..9 two elementwise warpgroups (each owns half of the 64
-// columns of a tile, a thread owns a TMEM lane).  Every wait is bounded.
+// Each kernel: warp 0 TMA producer, warp 1 TMEM allocator and issuer of the
+// first group of score products, warps 2..9 two elementwise warpgroups (each
+// owns half of the columns of a tile, a thread owns a TMEM lane).  The second
+// group of score products ([G | gP], disjoint TMEM columns) has its own
+// issuing warp (query-major: warp 10; key-major key part: warp 11), and the
+// key-major kernel's accumulate products another (warp 10); the query-major
+// kernel's accumulate products follow warp 1's score products in its issue
+// order.  Every wait is bounded.
 #pragma once
 
 #include <cuda_bf16.h>
