@@ -1005,13 +1005,13 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
 // each kernel gets its own per-device record of the attribute being set.
 template <auto kern>
 cudaError_t set_smem(int bytes) {
-  static unsigned long long done = 0;
+  static std::atomic<unsigned long long> done{0};  // per device; shared by host threads
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && (done & (1ull << dev))) return cudaSuccess;
+  if (dev < 64 && (done.load(std::memory_order_relaxed) & (1ull << dev))) return cudaSuccess;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev < 64) done |= 1ull << dev;
+  if (e == cudaSuccess && dev < 64) done.fetch_or(1ull << dev, std::memory_order_relaxed);
   return e;
 }
 

@@ -50,6 +50,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "jvp_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -940,15 +942,16 @@ template <typename T, int D, int MASK, bool TANGENT, bool SPLIT>
 cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream_t stream) {
   using L = TcLayout<D, TANGENT>;
   auto kern = fwd_dual_tc_kernel<T, D, MASK, TANGENT, SPLIT>;
-  // The attribute is per device; setting it is idempotent, the mask only saves calls.
-  static unsigned long long attr_done = 0;
+  // The attribute is per device; setting it is idempotent, the mask (shared
+  // by host threads) only saves calls.
+  static std::atomic<unsigned long long> attr_done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(attr_done & (1ull << dev))) {
+  if (dev >= 64 || !(attr_done.load(std::memory_order_relaxed) & (1ull << dev))) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done |= 1ull << dev;
+    if (dev < 64) attr_done.fetch_or(1ull << dev, std::memory_order_relaxed);
   }
   const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H * (SPLIT ? p.splits : 1);
   kern<<<static_cast<unsigned>(grid), kTcThreads, L::SMEM_BYTES, stream>>>(maps, p);
