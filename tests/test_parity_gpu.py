@@ -238,6 +238,36 @@ def test_strided_inputs_from_a_bnhd_layout():
     assert np.abs(np64(o) - ro).max() <= 2e-2 and np.abs(np64(t_o) - rt).max() <= 2e-2
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_strided_and_offset_outputs(D, causal):
+    # O and tO written through views: a [B, N, H, D] buffer seen as [B, H, N, D],
+    # and the first D columns of a [B, H, N, 2D] buffer (rows 2D apart).  The
+    # results must be bit-identical to contiguous outputs, and the memory
+    # around the views untouched.  140 rows: the last query tile is ragged.
+    w = synth.small("bf16", 2, 4, 140, D, "none", seed=27 + D)
+    inp = synth.make_inputs(w)
+    dev = "cuda"
+    g = [x.to(dev) for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    ref_o, ref_t = A.fwd_dual(*g, is_causal=causal, split_kv=False)
+    B, H, N = 2, 4, 140
+    bnhd = [torch.full((B, N, H, D), 7.0, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    wide = [torch.full((B, H, N, 2 * D), 7.0, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    for bufs, view in ((bnhd, lambda t: t.transpose(1, 2)), (wide, lambda t: t[..., :D])):
+        o, t_o = view(bufs[0]), view(bufs[1])
+        A.fwd_dual(*g, is_causal=causal, out=(o, t_o), split_kv=False)
+        torch.cuda.synchronize()
+        assert A.last_path() == 1
+        assert torch.equal(o, ref_o) and torch.equal(t_o, ref_t)
+        if bufs is wide:
+            for t in bufs:
+                assert torch.all(t[..., D:] == 7.0)
+    kind = "causal" if causal else "none"
+    ro, rt, _, _ = oracle.fwd_dual(*(np64(x) for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk,
+                                                        inp.dv)), kind, None)
+    assert np.abs(np64(ref_o) - ro).max() <= 2e-2 and np.abs(np64(ref_t) - rt).max() <= 2e-2
+
+
 # ------------------------------------------------------------------ specified workloads
 def test_workload_f32_b1h2n32d16_full():
     compare_full(synth.WORKLOADS["f32_b1h2n32d16"], expect_path=2)
