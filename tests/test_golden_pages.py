@@ -46,3 +46,28 @@ def test_algorithmic_bytes():
     assert b == 8 * 4 * 16 * 2048 * 128 * 2 + 8 * 4 * 16 * 2048
     assert metrics.bytes_fwd_dual(2, 8, 1024, 1024, 64, 2, "bool", 2) - \
         metrics.bytes_fwd_dual(2, 8, 1024, 1024, 64, 2) == 2 * 1024 * 1024
+
+
+def test_algorithmic_bytes_equal_the_buffers_a_call_reads_and_writes():
+    # Independent of the formula: build each workload's actual buffers (the
+    # six inputs and the mask from the seeded generator, outputs O and tO of
+    # q's shape and dtype, lse and mu as float32 [B, H, Nq]) and add up their
+    # sizes; every byte is read or written exactly once by one call.
+    import torch
+
+    from forward_mode_flash_gb300 import synth
+
+    for name in ("f16_b2h8n512d64", "bf16_b2h8n1024d64_bool", "bf16_b2h8n1024d64_additive",
+                 "bf16_b4h16n2048d128"):
+        w = synth.WORKLOADS[name]
+        inp = synth.make_inputs(w)
+        ins = (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)
+        total = sum(t.numel() * t.element_size() for t in ins)
+        total += 2 * inp.q.numel() * inp.q.element_size()           # O, tO
+        total += 2 * inp.q.shape[0] * inp.q.shape[1] * inp.q.shape[2] * 4  # lse, mu
+        if inp.mask is not None:
+            m = inp.mask
+            total += m.numel() * (1 if m.dtype == torch.bool else m.element_size())
+        mb = 1 if inp.mask is None else inp.mask.shape[0]
+        assert metrics.bytes_fwd_dual(w.B, w.H, w.N, w.n_keys, w.D, inp.q.element_size(),
+                                      w.mask, mask_batch=mb) == total, name
