@@ -299,3 +299,118 @@ def test_backward_identities_and_torch_double_backward():
     ref = torch.autograd.grad(L, ts)
     for g, r in zip(grads, ref):
         assert np.abs(g - r.numpy()).max() <= 1e-11
+
+
+# ------------------------------------------------- query and key lengths differ
+# The GPU tests with Nq != Nk (cross-length parity, split-KV over long key
+# ranges, the backward at Nq != Nk) rest on the oracle's key-row indexing, its
+# top-left causal rule (key j kept for query i iff j <= i, whatever Nk) and the
+# reverse mode's key-side offsets at unequal lengths.  These pins fix those
+# paths against finite differences, a torch.func evaluation of the plain
+# expression, brute force and the exact dV identity, at shapes where a slip
+# between Nq and Nk (or a causal rule aligned bottom-right) changes the result.
+CROSS = [(5, 13), (13, 5), (1, 9)]
+
+
+@pytest.mark.parametrize("mask", MASKS)
+@pytest.mark.parametrize("Nq,Nk", CROSS)
+def test_cross_length_tangent_matches_central_finite_differences(mask, Nq, Nk):
+    q, k, v, dq, dk, dv, m = make(B=1, H=2, N=Nq, D=5, mask=mask, seed=100 + Nq, Nk=Nk)
+    o, t_o, lse, mu = oracle.fwd_dual(q, k, v, dq, dk, dv, mask, m)
+    assert o.shape == (1, 2, Nq, 5) and lse.shape == (1, 2, Nq)
+    h = 1e-5
+    op, _, lp, _ = primal(q + h * dq, k + h * dk, v + h * dv, mask, m)
+    om, _, lm, _ = primal(q - h * dq, k - h * dk, v - h * dv, mask, m)
+    fd = (op - om) / (2 * h)
+    assert np.abs(fd - t_o).max() / np.abs(t_o).max() <= 1e-6
+    fd_l = (lp - lm) / (2 * h)
+    assert np.abs(fd_l - mu).max() / max(np.abs(mu).max(), 1e-300) <= 1e-6
+
+
+@pytest.mark.parametrize("mask", MASKS)
+@pytest.mark.parametrize("Nq,Nk", CROSS)
+def test_cross_length_agrees_with_torch_func_jvp(mask, Nq, Nk):
+    q, k, v, dq, dk, dv, m = make(B=2, H=2, N=Nq, D=8, mask=mask, seed=110 + Nk, Nk=Nk)
+    s = 1 / math.sqrt(8)
+    o, t_o, lse, mu = oracle.fwd_dual(q, k, v, dq, dk, dv, mask, m)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    mt = None if m is None else T(m)
+    f = lambda q_, k_, v_: torch_attention(q_, k_, v_, mask, mt, s)
+    o_ref, t_ref = torch.func.jvp(f, (T(q), T(k), T(v)), (T(dq), T(dk), T(dv)))
+    assert np.abs(o - o_ref.numpy()).max() <= 1e-12
+    assert np.abs(t_o - t_ref.numpy()).max() <= 1e-12
+    # lse by brute force over the kept keys of every row
+    P, keep = plain_softmax_weights(q, k, mask, m, s)
+    S = s * np.einsum("bhid,bhjd->bhij", q, k) + (m if mask == "additive" else 0.0)
+    for b in range(2):
+        for hh in range(2):
+            for i in range(Nq):
+                terms = [math.exp(S[b, hh, i, j]) for j in range(Nk) if keep[b, hh, i, j]]
+                assert abs(lse[b, hh, i] - math.log(math.fsum(terms))) <= 1e-12
+
+
+@pytest.mark.parametrize("Nq,Nk", CROSS)
+def test_cross_length_causal_is_top_left_aligned(Nq, Nk):
+    # Query i sees keys 0..i: with dV only on the keys j > i of every row, the
+    # tangent of row i is zero; keys beyond Nq - 1 are never seen at all.
+    q, k, v, _, _, _, _ = make(B=1, H=1, N=Nq, D=4, seed=120 + Nq, Nk=Nk)
+    z = np.zeros_like(q)
+    if Nk > Nq:
+        dv = np.zeros_like(v)
+        dv[:, :, Nq:] = 1.0  # only keys no query may see
+        _, t_o, _, _ = oracle.fwd_dual(q, k, v, z, np.zeros_like(k), dv, "causal")
+        assert np.all(t_o == 0.0)
+    # row 0 keeps only key 0: O = V_0, lse = s q_0 . k_0
+    o, _, lse, _ = oracle.fwd_dual(q, k, v, mask_kind="causal", scale=0.3)
+    assert np.array_equal(o[0, 0, 0], v[0, 0, 0])
+    assert abs(lse[0, 0, 0] - 0.3 * float(q[0, 0, 0] @ k[0, 0, 0])) <= 1e-14
+    # the last row keeps min(Nq, Nk) keys: with q = 0 it averages them
+    o, _, _, _ = oracle.fwd_dual(np.zeros_like(q), k, v, mask_kind="causal")
+    n = min(Nq, Nk)
+    assert np.abs(o[0, 0, Nq - 1] - v[0, 0, :n].mean(axis=0)).max() <= 1e-14
+
+
+@pytest.mark.parametrize("mask", MASKS)
+@pytest.mark.parametrize("Nq,Nk", CROSS)
+def test_cross_length_backward_matches_finite_differences(mask, Nq, Nk):
+    q, k, v, dq, dk, dv, m = make(B=1, H=2, N=Nq, D=4, mask=mask, seed=130 + Nq + Nk, Nk=Nk)
+    rng = np.random.default_rng(131)
+    g_o, g_to = rng.standard_normal((2,) + q.shape)
+    grads = oracle.bwd_dual(q, k, v, dq, dk, dv, g_o, g_to, mask, m)
+    xs = [q, k, v, dq, dk, dv]
+    for g, x in zip(grads, xs):
+        assert g.shape == x.shape
+
+    def loss(vals):
+        o, t_o, _, _ = oracle.fwd_dual(*vals, mask, m)
+        return float((g_o * o).sum() + (g_to * t_o).sum())
+
+    h = 1e-5
+    for idx in range(6):
+        u = rng.standard_normal(xs[idx].shape)
+        plus = [x + h * u if n == idx else x for n, x in enumerate(xs)]
+        minus = [x - h * u if n == idx else x for n, x in enumerate(xs)]
+        fd = (loss(plus) - loss(minus)) / (2 * h)
+        an = float((grads[idx] * u).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (idx, fd, an)
+
+
+@pytest.mark.parametrize("mask", MASKS)
+@pytest.mark.parametrize("Nq,Nk", CROSS)
+def test_cross_length_backward_identity_and_torch_double_backward(mask, Nq, Nk):
+    q, k, v, dq, dk, dv, m = make(B=1, H=2, N=Nq, D=6, mask=mask, seed=140 + Nk, Nk=Nk)
+    rng = np.random.default_rng(141)
+    g_o, g_to = rng.standard_normal((2,) + q.shape)
+    s = 1 / math.sqrt(6)
+    grads = oracle.bwd_dual(q, k, v, dq, dk, dv, g_o, g_to, mask, m)
+    P, _ = plain_softmax_weights(q, k, mask, m, s)
+    assert np.abs(grads[5] - np.swapaxes(P, -1, -2) @ g_to).max() <= 1e-12
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).requires_grad_(True)
+    ts = [T(x) for x in (q, k, v, dq, dk, dv)]
+    mt = None if m is None else torch.from_numpy(np.ascontiguousarray(m))
+    f = lambda q_, k_, v_: torch_attention(q_, k_, v_, mask, mt, s)
+    o, t_o = torch.func.jvp(f, tuple(ts[:3]), tuple(ts[3:]))
+    L = (torch.from_numpy(g_o) * o).sum() + (torch.from_numpy(g_to) * t_o).sum()
+    ref = torch.autograd.grad(L, ts)
+    for g, r in zip(grads, ref):
+        assert np.abs(g - r.numpy()).max() <= 1e-11
