@@ -2,10 +2,22 @@
 against the float64 oracle's reverse mode on the same inputs.
 
 Tolerance: max-abs error <= tol * max(1, max |reference|) per gradient, with
-tol = 1e-4 for float32 inputs and 2e-2 for fp16/bf16.  The GPU computes in
-fp32 from its own 16-bit O and tO (which enter delta and nu) and rounds the
-gradients to 16 bits, so relative errors of a few 2^-9 are expected there.
+tol = 1e-4 for float32 inputs and 2e-2 for fp16/bf16.  The method's stated
+bound (2e-2 max-abs for 16-bit inputs) is for outputs of unit-variance scale;
+a gradient has the scale of its cotangents times the attention weights and
+dual logits, often well above 1, and both its 16-bit rounding (relative,
+2^-9 for bf16) and the fp32 sums of 16-bit products that form it err in
+proportion to that scale.  So the bound is applied relative to each
+gradient's own scale, and is never looser than the absolute bound when that
+scale is at most 1.  The GPU computes in fp32 from its own 16-bit O and tO
+(which enter delta and nu) and rounds the gradients to 16 bits.
+
+Every comparison appends its absolute error, the reference scale and their
+ratio to $JVP_PARITY_LOG (JSON lines) when that variable is set.
 """
+
+import json
+import os
 
 import numpy as np
 import pytest
@@ -58,8 +70,19 @@ def run(w, heads=None):
     return errs
 
 
-def check(w, errs):
+def log_errors(name, errs):
+    path = os.environ.get("JVP_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            for g, (e, scale) in errs.items():
+                f.write(json.dumps({"case": name, "grad": g, "abs_err": float(e),
+                                    "max_abs_ref": float(scale),
+                                    "err_over_scale": float(e / max(1.0, scale))}) + "\n")
+
+
+def check(w, errs, tag="[bwd]"):
     tol = TOL[w.dtype]
+    log_errors(w.name + tag, errs)
     for name, (e, scale) in errs.items():
         assert e <= tol * max(1.0, scale), (w.name, name, e, scale)
 
@@ -85,11 +108,11 @@ def test_bwd_workspace_is_required_and_sized():
     assert ei.value.status == A._abi.JVP_ERR_WORKSPACE
 
 
-def test_bwd_specified_workload_f16_b2h8n2048d64_causal_two_heads():
-    # Full-size launch; the oracle checks two whole heads (every gradient entry).
+def test_bwd_specified_workload_f16_b2h8n2048d64_causal_every_element():
+    # Full-size launch; the oracle's reverse mode checks every entry of all six
+    # gradients of all 16 (batch, head) problems.
     w = synth.WORKLOADS["f16_b2h8n2048d64_causal"]
-    errs = run(w, heads=(slice(0, 2), slice(3, 4)))
-    check(w, errs)
+    check(w, run(w), "[bwd, every element]")
 
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("f32", 40)])
@@ -106,7 +129,7 @@ def test_bwd_specified_workload_d128_whole_heads(name, heads):
     # Full-size launch (value and key parts of the key-major kernel); the oracle
     # checks every gradient entry of the selected heads.
     w = synth.WORKLOADS[name]
-    check(w, run(w, heads=heads))
+    check(w, run(w, heads=heads), "[bwd, whole heads]")
 
 
 @pytest.mark.parametrize("dtype,D,mask,N", [("bf16", 128, "causal", 4096), ("f16", 64, "none", 8192)])
