@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libjvp_attn.so")
 
 JVP_OK, JVP_ERR_INVALID_ARG, JVP_ERR_UNSUPPORTED, JVP_ERR_ALIGNMENT = 0, 1, 2, 3
 JVP_ERR_CUDA, JVP_ERR_DEVICE_TIMEOUT, JVP_ERR_WORKSPACE = 4, 5, 6
+# fixed device scratch of jvp_attn_bwd_dual_noalloc (JVP_BWD_NOALLOC_SCRATCH_BYTES)
+JVP_BWD_NOALLOC_SCRATCH_BYTES = 4 << 20
 JVP_F32, JVP_F16, JVP_BF16 = 0, 1, 2
 JVP_MASK_NONE, JVP_MASK_BOOL, JVP_MASK_ADDITIVE, JVP_MASK_CAUSAL = 0, 1, 2, 3
 JVP_MASK_BOOL_CAUSAL, JVP_MASK_ADDITIVE_CAUSAL = 4, 5

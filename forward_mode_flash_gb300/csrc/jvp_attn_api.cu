@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 
@@ -38,6 +39,25 @@ jvp_status_t ok() {
 }
 
 size_t elem_size(int dt) { return dt == JVP_F32 ? 4 : 2; }
+
+// The kernels index sizes and grid dimensions with 32-bit ints.
+constexpr int64_t kMaxDim = (1ll << 31) - 1;
+
+// Product of non-negative sizes into *out; false if it overflows int64.
+bool checked_product(std::initializer_list<int64_t> xs, int64_t* out) {
+  int64_t p = 1;
+  for (int64_t x : xs)
+    if (__builtin_mul_overflow(p, x, &p)) return false;
+  *out = p;
+  return true;
+}
+
+// Every size of the shape record is at most kMaxDim (checked before any
+// product of them is formed).
+bool dims_in_range(const jvp_shape_t* s) {
+  return s->B <= kMaxDim && s->H <= kMaxDim && s->Nq <= kMaxDim && s->Nk <= kMaxDim &&
+         s->D <= kMaxDim && s->Hkv <= kMaxDim;
+}
 
 struct DeviceInfo {
   bool queried = false;
@@ -180,9 +200,11 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     return fail(JVP_ERR_INVALID_ARG, "unknown dtype");
   if (!in_strides || !out_strides) return fail(JVP_ERR_INVALID_ARG, "strides are NULL");
   if (!std::isfinite(scale)) return fail(JVP_ERR_INVALID_ARG, "scale is not finite");
-  const int64_t lim = (1ll << 31) - 1;
-  if (Nq > lim || Nk > lim || B * H > lim || ((Nq + 127) / 128) * B * H > lim ||
-      ((Nq + 7) / 8) * B * H > lim)
+  if (!dims_in_range(shape)) return fail(JVP_ERR_UNSUPPORTED, "a size exceeds 2^31 - 1");
+  int64_t bh = 0, q_tiles = 0, q_groups = 0;
+  if (!checked_product({B, H}, &bh) || bh > kMaxDim ||
+      !checked_product({(Nq + 127) / 128, bh}, &q_tiles) || q_tiles > kMaxDim ||
+      !checked_product({(Nq + 7) / 8, bh}, &q_groups) || q_groups > kMaxDim)
     return fail(JVP_ERR_UNSUPPORTED, "problem too large for one launch");
   for (int t = 0; t < n_in; ++t) {
     const jvp_strides_t& s = in_strides[t];
@@ -211,14 +233,15 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
                   "JVP_MASK_ADDITIVE_CAUSAL)");
     if (kind == JVP_MASK_NONE && mptr)
       return fail(JVP_ERR_INVALID_ARG, "mask kind NONE with a mask tensor");
-    if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && B * H * Nq * Nk > 0)
+    if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && bh > 0 && Nq > 0 &&
+        Nk > 0)
       return fail(JVP_ERR_INVALID_ARG, "mask tensor is NULL");
     if (msb < 0 || msh < 0 || msq < 0 || msk < 0) return fail(JVP_ERR_INVALID_ARG, "negative mask stride");
     if (kind == JVP_MASK_ADDITIVE && !aligned(mptr, 4))
       return fail(JVP_ERR_ALIGNMENT, "additive mask is not 4-byte aligned");
   }
   const size_t e = elem_size(dtype);
-  const bool rows_exist = B * H * Nq > 0;
+  const bool rows_exist = bh > 0 && Nq > 0;
   if (!rows_exist) {
     t_last_path = 0;
     return ok();  // nothing to compute
@@ -345,8 +368,10 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
     return fail(JVP_ERR_INVALID_ARG, "unknown dtype");
   if (!in_strides || !out_strides) return fail(JVP_ERR_INVALID_ARG, "strides are NULL");
   if (!std::isfinite(scale)) return fail(JVP_ERR_INVALID_ARG, "scale is not finite");
-  const int64_t lim = (1ll << 31) - 1;
-  if (Nq > lim || Nk > lim || B * H * Nq > lim / 32 || B * H * Nk > lim)
+  if (!dims_in_range(shape)) return fail(JVP_ERR_UNSUPPORTED, "a size exceeds 2^31 - 1");
+  int64_t bh = 0, q_rows = 0, k_rows = 0;
+  if (!checked_product({B, H}, &bh) || !checked_product({bh, Nq}, &q_rows) ||
+      q_rows > kMaxDim / 32 || !checked_product({bh, Nk}, &k_rows) || k_rows > kMaxDim)
     return fail(JVP_ERR_UNSUPPORTED, "problem too large for one launch");
   for (int t = 0; t < 10; ++t) {
     const jvp_strides_t& s = in_strides[t];
@@ -371,13 +396,13 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
     split_mask_kind(mask->kind, &kind, &causal_flag);
     if ((kind == JVP_MASK_CAUSAL || kind == JVP_MASK_NONE) && mptr)
       return fail(JVP_ERR_INVALID_ARG, "this mask kind takes no mask tensor");
-    if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && B * H * Nq * Nk > 0)
+    if ((kind == JVP_MASK_BOOL || kind == JVP_MASK_ADDITIVE) && !mptr && q_rows > 0 && Nk > 0)
       return fail(JVP_ERR_INVALID_ARG, "mask tensor is NULL");
     if (msb < 0 || msh < 0 || msq < 0 || msk < 0) return fail(JVP_ERR_INVALID_ARG, "negative mask stride");
     if (kind == JVP_MASK_ADDITIVE && !aligned(mptr, 4))
       return fail(JVP_ERR_ALIGNMENT, "additive mask is not 4-byte aligned");
   }
-  if (B * H * (Nq + Nk) == 0) return ok();  // nothing to compute
+  if (q_rows == 0 && k_rows == 0) return ok();  // nothing to compute
   const size_t e = elem_size(dtype);
   for (int t = 0; t < 10; ++t) {
     const bool on_keys = (t == 1 || t == 2 || t == 4 || t == 5);
@@ -393,7 +418,7 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   }
   if (Nq > 0 && (!lse || !mu)) return fail(JVP_ERR_INVALID_ARG, "lse and mu are required");
   if (!aligned(lse, 4) || !aligned(mu, 4)) return fail(JVP_ERR_ALIGNMENT, "lse/mu not 4-byte aligned");
-  const size_t need = bwd_workspace_bytes(B * H * Nq);
+  const size_t need = bwd_workspace_bytes(q_rows);
   if (need > 0 && (!workspace || ws_bytes < need))
     return fail(JVP_ERR_WORKSPACE, "workspace is NULL or smaller than jvp_attn_bwd_dual_workspace_size()");
   if (!aligned(workspace, 4)) return fail(JVP_ERR_ALIGNMENT, "workspace is not 4-byte aligned");
@@ -422,7 +447,7 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   Strides* sout[6] = {&p.sgq, &p.sgk, &p.sgv, &p.sgdq, &p.sgdk, &p.sgdv};
   for (int t = 0; t < 6; ++t) *sout[t] = to_strides(out_strides[t]);
   p.nu = static_cast<float*>(workspace);
-  p.delta = p.nu + B * H * Nq;
+  p.delta = p.nu + q_rows;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   // Tensor-core path: fp16/bf16, D in {64, 128}, at least one row and one key,
@@ -533,6 +558,10 @@ jvp_status_t jvp_attn_fwd_dual_ws(const jvp_shape_t* shape, jvp_dtype_t dtype, c
 
 size_t jvp_attn_fwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype) {
   if (!shape || shape->B <= 0 || shape->H <= 0 || shape->Nq <= 0 || shape->Nk <= 0) return 0;
+  int64_t rows = 0;
+  if (!jvp::dims_in_range(shape) || !jvp::checked_product({shape->B, shape->H, shape->Nq}, &rows) ||
+      rows > jvp::kMaxDim * 128)
+    return 0;  // the call itself rejects this shape
   if ((dtype != JVP_F16 && dtype != JVP_BF16) || (shape->D != 64 && shape->D != 128)) return 0;
   jvp::DeviceInfo* dev = nullptr;
   if (jvp::current_device(&dev) != JVP_OK || !dev->sm103) {
@@ -571,7 +600,11 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
 
 size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t) {
   if (!shape || shape->B < 0 || shape->H < 0 || shape->Nq < 0) return 0;
-  return jvp::bwd_workspace_bytes(shape->B * shape->H * shape->Nq);
+  int64_t rows = 0;
+  if (!jvp::dims_in_range(shape) || !jvp::checked_product({shape->B, shape->H, shape->Nq}, &rows) ||
+      rows > jvp::kMaxDim)
+    return SIZE_MAX;  // beyond any launch (jvp_attn_bwd_dual rejects the shape)
+  return jvp::bwd_workspace_bytes(rows);
 }
 
 jvp_status_t jvp_attn_get_device_status(void* stream) {
@@ -695,7 +728,11 @@ extern "C" size_t jvp_attn_fwd_dual_host_workspace_size(const jvp_shape_t* shape
   if (!shape || shape->B <= 0 || shape->H <= 0 || shape->Nq <= 0 || shape->D <= 0 ||
       shape->Nk < 0 || chunks < 1)
     return 0;
-  const int64_t n = jvp::chunk_pairs(shape->B * shape->H, chunks);
+  int64_t bh = 0, rows = 0;
+  if (!jvp::dims_in_range(shape) || !jvp::checked_product({shape->B, shape->H}, &bh) ||
+      !jvp::checked_product({bh, shape->Nq + shape->Nk, shape->D}, &rows) || rows > (1ll << 56))
+    return 0;  // the call itself rejects this shape
+  const int64_t n = jvp::chunk_pairs(bh, chunks);
   return 2 * jvp::SlotLayout(n, shape->Nq, shape->Nk, shape->D, jvp::elem_size(dtype)).bytes;
 }
 
@@ -710,6 +747,10 @@ extern "C" jvp_status_t jvp_attn_fwd_dual_host(
   const int64_t B = shape->B, H = shape->H, Nq = shape->Nq, Nk = shape->Nk, D = shape->D;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return fail(JVP_ERR_INVALID_ARG, "bad sizes");
   if (D > 128) return fail(JVP_ERR_UNSUPPORTED, "D > 128 is not supported");
+  int64_t bh_all = 0, q_tiles = 0;
+  if (!dims_in_range(shape) || !checked_product({B, H}, &bh_all) || bh_all > kMaxDim ||
+      !checked_product({(Nq + 127) / 128, bh_all}, &q_tiles) || q_tiles > kMaxDim)
+    return fail(JVP_ERR_UNSUPPORTED, "problem too large for one launch");
   if (dtype != JVP_F32 && dtype != JVP_F16 && dtype != JVP_BF16)
     return fail(JVP_ERR_INVALID_ARG, "unknown dtype");
   if (!std::isfinite(scale)) return fail(JVP_ERR_INVALID_ARG, "scale is not finite");
@@ -853,6 +894,8 @@ extern "C" jvp_status_t jvp_attn_bwd_dual_noalloc(
     void* g_v, void* g_dq, void* g_dk, void* g_dv, const jvp_strides_t* out_strides,
     void* stream) {
   if (!shape) return jvp::fail(JVP_ERR_INVALID_ARG, "shape is NULL");
+  // (jvp_attn_bwd_dual_workspace_size returns SIZE_MAX for shapes whose
+  // product of sizes overflows, so those are rejected here too)
   if (shape->B > 0 && shape->H > 0 && shape->Nq > 0 &&
       jvp_attn_bwd_dual_workspace_size(shape, dtype) > JVP_BWD_NOALLOC_SCRATCH_BYTES)
     return jvp::fail(JVP_ERR_WORKSPACE,

@@ -31,6 +31,14 @@
  *   - A device-side wait that exceeds its time limit (about two seconds) makes
  *     the kernel return early and records JVP_ERR_DEVICE_TIMEOUT, which
  *     jvp_attn_get_device_status() reports.
+ *   - Every size (B, H, Hkv, Nq, Nk, D) must be at most 2^31 - 1, and the
+ *     products the launches form from them must fit too; larger problems are
+ *     rejected with JVP_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The library caches, per device, device addresses of its own globals
+ *     (the status word, the scratch of jvp_attn_bwd_dual_noalloc) the first
+ *     time a device is used.  cudaDeviceReset() (or anything else that
+ *     destroys the device's primary context) invalidates them: do not call the
+ *     library on that device again in the same process after a reset.
  */
 #ifndef JVP_ATTN_H_
 #define JVP_ATTN_H_
@@ -241,7 +249,9 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
                                void* g_dk, void* g_dv, const jvp_strides_t* out_strides,
                                void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes jvp_attn_bwd_dual needs for `shape` (8 * B * H * Nq). */
+/* Workspace bytes jvp_attn_bwd_dual needs for `shape` (8 * B * H * Nq); 0 for
+ * a NULL shape or a negative size, SIZE_MAX for a shape too large for any
+ * launch (a size above 2^31 - 1, or B * H * Nq above it). */
 size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
 
 /*

@@ -146,3 +146,39 @@ def test_host_buffer_entry_point_validates_before_touching_a_device(lib):
     assert call(mask=per_head) == _abi.JVP_ERR_INVALID_ARG
     assert b"shared by every" in lib.jvp_attn_last_error()
 
+
+
+def _bwd_args(n):
+    return [ctypes.c_void_p(0x10000)] * n
+
+
+def test_sizes_that_would_overflow_are_rejected_without_a_device(lib):
+    # Sizes above 2^31 - 1, and products of sizes that would wrap int64 (or
+    # wrap to zero: B = H = 2^32), are rejected before anything else happens.
+    big, wrap = (1 << 31) - 1, 1 << 32
+    for B, H, N in ((wrap, wrap, 64), (big, big, big), (1 << 31, 1, 64), (big, big, 64)):
+        assert call_fwd_dual(lib, shape=(B, H, N, 64)) == _abi.JVP_ERR_UNSUPPORTED, (B, H, N)
+        sh = _abi.Shape(B, H, N, N, 64, 0)
+        ins = _strides(10, (1, 1, 64, 64))
+        outs = _strides(6, (1, 1, 64, 64))
+        none = _abi.Mask(_abi.JVP_MASK_NONE, None, 0, 0, 0, 0)
+        st = lib.jvp_attn_bwd_dual(ctypes.byref(sh), _abi.JVP_BF16, *_bwd_args(10), *_bwd_args(2),
+                                   ins, ctypes.byref(none), 0.125, *_bwd_args(6), outs,
+                                   ctypes.c_void_p(0x100000), 1 << 40, None)
+        assert st == _abi.JVP_ERR_UNSUPPORTED, (B, H, N, st)
+        # the no-allocation backward: such a problem never fits its fixed scratch
+        st = lib.jvp_attn_bwd_dual_noalloc(ctypes.byref(sh), _abi.JVP_BF16, *_bwd_args(10),
+                                           *_bwd_args(2), ins, ctypes.byref(none), 0.125,
+                                           *_bwd_args(6), outs, None)
+        assert st == _abi.JVP_ERR_WORKSPACE, (B, H, N, st)
+        assert lib.jvp_attn_bwd_dual_workspace_size(ctypes.byref(sh), _abi.JVP_BF16) == \
+            ctypes.c_size_t(-1).value
+        assert lib.jvp_attn_fwd_dual_workspace_size(ctypes.byref(sh), _abi.JVP_BF16) == 0
+        assert lib.jvp_attn_fwd_dual_host_workspace_size(ctypes.byref(sh), _abi.JVP_BF16, 4) == 0
+    # the forward-only entry point shares the checks
+    sh = _abi.Shape(wrap, wrap, 64, 64, 64, 0)
+    p = ctypes.c_void_p(0x10000)
+    st = lib.jvp_attn_fwd(ctypes.byref(sh), _abi.JVP_BF16, p, p, p, _strides(3, (1, 1, 64, 64)),
+                          None, 0.125, p, _strides(1, (1, 1, 64, 64)), None, None)
+    assert st == _abi.JVP_ERR_UNSUPPORTED
+    assert b"2^31" in lib.jvp_attn_last_error() or b"too large" in lib.jvp_attn_last_error()
