@@ -1,10 +1,11 @@
 """jvp_attn_bwd_dual_noalloc: the backward for callers that cannot allocate
 device memory (it keeps its scratch in a fixed device array of the library).
 
-The GPU test calls the entry point through the C ABI, twice in a row on two
-different problems, and checks each result against the ordinary
-jvp_attn_bwd_dual (with a caller workspace) within the backward tests'
-tolerance.  This file is collected last on purpose.
+The GPU test calls the entry point through the C ABI several times in a row on
+different problems (one of them needs exactly the whole fixed scratch), and
+checks that each result is bit-identical to the ordinary jvp_attn_bwd_dual
+with a caller workspace: both run the same kernels.  This file is collected
+last on purpose.
 """
 
 import ctypes
@@ -13,8 +14,6 @@ import pytest
 import torch
 
 from forward_mode_flash_gb300 import _abi, api, build, synth
-
-TOL = {"f32": 1e-4, "f16": 2e-2, "bf16": 2e-2}
 
 
 def call_noalloc(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to, causal):
@@ -47,21 +46,34 @@ def test_rejects_problems_beyond_the_fixed_scratch():
     assert b"4 MiB" in lib.jvp_attn_last_error()
 
 
+def _case(w):
+    inp = synth.make_inputs(w, with_cotangents=True)
+    g = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    causal = w.mask == "causal"
+    o, t_o, lse, mu = api.fwd_dual(*g, is_causal=causal, return_stats=True)
+    return g, o, t_o, lse, mu, inp.g_o.cuda(), inp.g_to.cuda(), causal
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
     build.build()
-    cases = [synth.small("bf16", 2, 4, 300, 64, "causal", seed=31),
-             synth.small("f32", 1, 3, 77, 40, "none", seed=32)]
-    for w in cases:  # two calls in a row; the second reuses the scratch the first left
-        inp = synth.make_inputs(w, with_cotangents=True)
-        g = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
-        causal = w.mask == "causal"
-        o, t_o, lse, mu = api.fwd_dual(*g, is_causal=causal, return_stats=True)
-        go, gto = inp.g_o.cuda(), inp.g_to.cuda()
-        ref = api.bwd_dual(*g, o, t_o, lse, mu, go, gto, is_causal=causal)
+    # Both entry points run the same kernels in the same order, so the results
+    # must be bit-identical; the workspace of the reference call is filled with
+    # NaN first, so neither side can lean on scratch contents left behind.
+    B, H, Nq = 8, 16, 4096  # 8 * B * H * Nq == 4 MiB: exactly the fixed scratch
+    assert 8 * B * H * Nq == _abi.JVP_BWD_NOALLOC_SCRATCH_BYTES
+    cases = [(synth.small("bf16", 2, 4, 300, 64, "causal", seed=31), 1),
+             (synth.small("f32", 1, 3, 77, 40, "none", seed=32), 2),
+             (synth.small("f16", B, H, Nq, 64, "none", seed=33, Nk=128), 1),
+             (synth.small("bf16", 1, 2, 130, 128, "causal", seed=34), 1)]
+    for w, path in cases:  # calls in a row; each reuses the scratch the previous one left
+        g, o, t_o, lse, mu, go, gto, causal = _case(w)
+        ws = torch.full((api.bwd_dual_workspace_size(w.B, w.H, w.N, w.n_keys, w.D) // 4,),
+                        float("nan"), dtype=torch.float32, device="cuda")
+        ref = api.bwd_dual(*g, o, t_o, lse, mu, go, gto, is_causal=causal, workspace=ws)
         got = call_noalloc(*g, o, t_o, lse, mu, go, gto, causal)
+        assert api.last_path() == path, (w.name, api.last_path())
         torch.cuda.synchronize()
         for r, x in zip(ref, got):
-            scale = max(1.0, r.float().abs().max().item())
-            assert (r.float() - x.float()).abs().max().item() <= TOL[w.dtype] * scale
+            assert torch.equal(r, x), w.name
     assert api.device_status() == 0
