@@ -414,3 +414,31 @@ def test_cross_length_backward_identity_and_torch_double_backward(mask, Nq, Nk):
     ref = torch.autograd.grad(L, ts)
     for g, r in zip(grads, ref):
         assert np.abs(g - r.numpy()).max() <= 1e-11
+
+
+# ------------------------------------------- Hessian-vector products (reverse over forward)
+@pytest.mark.parametrize("mask", MASKS)
+def test_reverse_mode_of_the_tangent_is_a_hessian_vector_product(mask):
+    # For f(q, k, v) = <w, O>, the tangent along u = (dq, dk, dv) is <w, tO> =
+    # grad f . u.  Its gradient with respect to (q, k, v) is the Hessian-vector
+    # product H u (the use named in the project page's Description); with
+    # respect to u it is grad f itself.  The oracle's reverse mode with
+    # cotangents (gO, gtO) = (0, w) must give both: H u against a central
+    # difference of grad f (itself the reverse mode with (w, 0)), grad f exactly.
+    q, k, v, dq, dk, dv, m = make(B=1, H=2, N=7, D=4, mask=mask, seed=150, Nk=9)
+    w = np.random.default_rng(151).standard_normal(q.shape)
+    z = np.zeros_like(q)
+    hvp = oracle.bwd_dual(q, k, v, dq, dk, dv, z, w, mask, m)
+
+    def grad_f(qq, kk, vv):
+        return oracle.bwd_dual(qq, kk, vv, dq, dk, dv, w, z, mask, m)[:3]
+
+    h = 1e-5
+    gp = grad_f(q + h * dq, k + h * dk, v + h * dv)
+    gm = grad_f(q - h * dq, k - h * dk, v - h * dv)
+    for a, b, c in zip(hvp[:3], gp, gm):
+        fd = (b - c) / (2 * h)
+        assert np.abs(a - fd).max() <= 1e-6 * max(1.0, np.abs(fd).max())
+    g0 = grad_f(q, k, v)
+    for a, b in zip(hvp[3:], g0):
+        assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(b).max())
