@@ -46,6 +46,8 @@ def parse():
                     help="target length of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-causal", action="store_true",
+                    help="skip the causal companion timing of the default workload")
     ap.add_argument("--mode", default="fwd_dual",
                     choices=["fwd_dual", "bwd_dual", "sweep", "memory"],
                     help="fwd_dual (the headline), the backward of the dual computation, the "
@@ -124,7 +126,12 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+    """Samples nvidia-smi clocks and throttle reasons during the timed region.
+
+    A reader thread collects nvidia-smi's lines (one per 100 ms).  Entering
+    waits for the first sample, and leaving waits for one more sample taken
+    after the region ends, so even a region shorter than the sampling period
+    is bracketed by samples taken under the same load conditions."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -133,8 +140,21 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.out = ""
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+
+    def _wait_for(self, n, timeout):
+        t_end = time.time() + timeout
+        while len(self.lines) < n and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.005)
 
     def __enter__(self):
+        import threading
+
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
@@ -142,17 +162,23 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        self._wait_for(1, 3.0)
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                self.out = ""
+        if self.proc is None:
+            return
+        self._wait_for(len(self.lines) + 1, 1.0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        self.out = "".join(self.lines)
 
     def summary(self):
         rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
@@ -205,6 +231,64 @@ def cpu_baseline(workload, target_s: float):
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} random query rows of {workload} (every key of each row), float64 "
                       f"dual-number oracle, {dt:.1f} s wall"}, dt
+
+
+def timed_steps(step, steps, flush, stream, local):
+    """Times `steps` calls of step() with CUDA events on `stream`, writing the
+    L2-flush buffer before each call (outside the events); returns the
+    per-call milliseconds and the clocks sampled meanwhile."""
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for s in range(steps):
+            flush.fill_(float(s))  # evict L2 between timed steps (outside the events)
+            starts[s].record(stream)
+            step()
+            ends[s].record(stream)
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], clocks
+
+
+CAUSAL_WORKLOAD = "bf16_b4h16n2048d128_causal"
+
+
+def causal_companion(args, dev, world, flush, stream, local, peak, pk_src):
+    """The headline shape with the causal mask, timed like the headline: the
+    same number of steps, after its own warm-up, with its own clock record."""
+    import torch
+
+    from forward_mode_flash_gb300 import api, metrics, replicas, synth
+
+    w = synth.WORKLOADS[CAUSAL_WORKLOAD]
+    inp = synth.make_inputs(w, device=str(dev))
+    g = [inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv]
+    out = (torch.empty_like(g[0]), torch.empty_like(g[0]))
+
+    def step():
+        return api.fwd_dual(*g, is_causal=True, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    per_ms, clocks = timed_steps(step, args.steps, flush, stream, local)
+    if api.last_path() != 1:
+        raise SystemExit("the tensor-core path did not run for the causal workload")
+    total_ms = replicas.max_over_ranks(sum(per_ms), device=dev)
+    ms_step = total_ms / args.steps
+    flops = metrics.flops_fwd_dual(w.B, w.H, w.N, w.N, w.D, True)
+    value = replicas.aggregate_throughput(world, flops, args.steps, total_ms * 1e-3) / 1e12
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    return {"workload": CAUSAL_WORKLOAD, "ms_per_step": ms_step, "value": value,
+            "unit": "TFLOP/s", "steps": args.steps, "flops_per_step": flops,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{pk_src} bf16_tflops (burst; kernel timed alone)",
+                         "kernel": "fwd_dual_tc_kernel"},
+            "clocks": clocks.summary(), "gpu_launches": args.steps,
+            "per_step_ms": {"min": min(per_ms), "median": statistics.median(per_ms),
+                            "max": max(per_ms)}}
 
 
 def run_reference(args, rank, world):
@@ -294,12 +378,16 @@ def run_bwd(args, rank, world, local):
     pk, pk_src = peaks()
     clk = pk.get("sm_max_mhz", 2070.0) * 1e6
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    achieved = exec_flops / (ms_step * 1e-3) / 1e12
+    achieved = alg_flops / (ms_step * 1e-3) / 1e12
+    achieved_exec = exec_flops / (ms_step * 1e-3) / 1e12
     if tensor_core:
         tc_peak = float(pk.get("bf16_tflops", 1900.0))  # fp16 and bf16 share the dense rate
         launches = 3 if w.D == 64 else 4
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": achieved / tc_peak, "traffic": None,
+                    "flops": "algorithmic: 30 B H Nq Nk D (half for causal), the 15 N x N x D "
+                             "products of the reverse mode",
+                    "achieved_executed": achieved_exec, "frac_executed": achieved_exec / tc_peak,
                     "peak_source": f"{pk_src} bf16 dense (cuBLAS burst)",
                     "kernel": "whole step: bwd_rows_kernel + bwd_q_tc_kernel + bwd_k_tc_kernel"
                               + (" x2 (value, key parts)" if w.D == 128 else "")}
@@ -308,6 +396,7 @@ def run_bwd(args, rank, world, local):
         launches = 3
         roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
                     "frac": achieved / alu_peak, "traffic": None,
+                    "achieved_executed": achieved_exec, "frac_executed": achieved_exec / alu_peak,
                     "peak_source": f"{n_sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 x "
                                    f"{clk / 1e6:.0f} MHz (CUDA-core fp32)",
                     "kernel": "bwd_keys_kernel + bwd_queries_kernel + bwd_rows_kernel"}
@@ -412,19 +501,9 @@ def main():
     if world > 1:
         dist.barrier()
     stream = torch.cuda.current_stream()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        for s in range(args.steps):
-            flush.fill_(float(s))  # evict L2 between timed steps (outside the events)
-            starts[s].record(stream)
-            step()
-            ends[s].record(stream)
-        torch.cuda.synchronize()
+    per_ms, clocks = timed_steps(step, args.steps, flush, stream, local)
     if world > 1:
         dist.barrier()
-    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = replicas.max_over_ranks(sum(per_ms), device=dev)
     ms_step = total_ms / args.steps
     value = replicas.aggregate_throughput(world, flops, args.steps, total_ms * 1e-3) / 1e12
@@ -512,6 +591,8 @@ def main():
         "per_step_ms": {"min": min(per_ms), "median": statistics.median(per_ms),
                         "max": max(per_ms)},
     }
+    if args.workload == DEFAULT_WORKLOAD and not args.no_causal:
+        line["causal"] = causal_companion(args, dev, world, flush, stream, local, peak, pk_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"], _ = cpu_baseline(args.workload, args.cpu_seconds)
     if rank == 0:
