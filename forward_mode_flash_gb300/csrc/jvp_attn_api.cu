@@ -113,8 +113,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 4-D tiled map over a [B, H, N, D] tensor with a {64, rows} box and the
-// 128-byte swizzle the MMA descriptors expect.  Returns false if the layout
-// cannot be described (the caller then takes the CUDA-core path).
+// 128-byte swizzle the MMA descriptors expect (for D < 64 the box reaches past
+// the row: loads fill those columns with zeros, stores skip them).  Returns
+// false if the layout cannot be described (the caller then takes the
+// CUDA-core path).
 bool encode_map(CUtensorMap* map, int dt, const void* ptr, int64_t B, int64_t H, int64_t N,
                 int64_t D, const jvp_strides_t& st, int rows) {
   auto enc = tensor_map_encoder();
@@ -300,10 +302,15 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   p.status = dev->status;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-  // Tensor-core path: fp16/bf16, D in {64, 128}, positive scale, at least one
-  // key, and every tensor 16-byte aligned with 16-byte-multiple strides.
-  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) && (D == 64 || D == 128) && scale > 0.f &&
-            Nk > 0;
+  // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, positive scale, at
+  // least one key, and every tensor 16-byte aligned with 16-byte-multiple
+  // strides.  D = 16 and 32 run the D = 64 kernel: the tensor maps' 64-column
+  // boxes reach past the D columns of each row, TMA fills those with zeros
+  // (they add nothing to Q K^T, dQ K^T or Q dK^T and give zero columns of
+  // A and T), and the output maps' stores drop them.
+  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) &&
+            (D == 16 || D == 32 || D == 64 || D == 128) && scale > 0.f && Nk > 0;
+  const int kernel_d = D <= 64 ? 64 : 128;
   for (int t = 0; tc && t < n_in; ++t)
     tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
   for (int t = 0; tc && t < n_out; ++t)
@@ -330,15 +337,15 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     p.num_q_tiles = static_cast<int>((Nq + kTcBlockM - 1) / kTcBlockM);
     // About one wave of CTAs per group of heads (one CTA per SM).
     p.group_heads = std::max(1, std::min(static_cast<int>(B * H), dev->num_sms / p.num_q_tiles));
-    // Split-KV when the caller gave a large enough workspace and it pays.
-    const int splits = choose_splits(B, H, Nq, Nk, dev->num_sms);
+    // Split-KV when the caller gave a large enough workspace and it pays (its
+    // partial states are laid out for the kernel's D, so D < 64 does not split).
+    const int splits = (D == kernel_d) ? choose_splits(B, H, Nq, Nk, dev->num_sms) : 1;
     if (tangent && workspace && splits > 1 &&
         ws_bytes >= SplitLayout::bytes(B * H * Nq, static_cast<int>(D), splits)) {
       p.splits = splits;
       p.split_ws = static_cast<float*>(workspace);
     }
-    err = launch_fwd_tc(static_cast<DType>(dtype), static_cast<int>(D), kind, tangent, maps, p,
-                        stream);
+    err = launch_fwd_tc(static_cast<DType>(dtype), kernel_d, kind, tangent, maps, p, stream);
     if (err == cudaSuccess && p.splits > 1)
       err = launch_fwd_combine(static_cast<DType>(dtype), tangent, p, stream);
     t_last_path = p.splits > 1 ? 3 : 1;

@@ -118,8 +118,9 @@ typedef struct {
  *   lse, mu        NULL or [B,H,Nq] contiguous float32 outputs (device).
  *   stream         cudaStream_t as void*.
  *
- * fp16/bf16 inputs with D in {64, 128}, 16-byte aligned base pointers and
- * strides take the tensor-core path (TMA + tcgen05 + TMEM, fp32 accumulation);
+ * fp16/bf16 inputs with D in {16, 32, 64, 128}, 16-byte aligned base pointers
+ * and strides take the tensor-core path (TMA + tcgen05 + TMEM, fp32
+ * accumulation; D = 16 and 32 run the D = 64 kernel on zero-filled columns);
  * every other valid case (float32, other D) takes the CUDA-core path, which
  * computes in fp32 FFMA.
  */

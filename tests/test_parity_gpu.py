@@ -127,9 +127,39 @@ def test_cuda_core_path_f32(D, mask):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("D", [16, 32, 80])
-def test_cuda_core_path_half_other_head_dims(dtype, D):
+def test_half_precision_other_head_dims(dtype, D):
+    # D = 16 and 32 take the tensor-core kernel (zero-filled columns up to 64);
+    # other head dimensions the CUDA-core kernel.
     w = synth.small(dtype, 1, 2, 70, D, "causal", seed=D)
-    compare_full(w, expect_path=2)
+    compare_full(w, expect_path=1 if D in (16, 32) else 2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [16, 32])
+@pytest.mark.parametrize("N", [1, 17, 64, 129, 333])
+@pytest.mark.parametrize("mask", ["none", "causal", "bool", "additive"])
+def test_tensor_core_path_small_head_dims(dtype, D, N, mask):
+    w = synth.small(dtype, 2, 3, N, D, mask, seed=N + D + len(mask))
+    compare_full(w, expect_path=1)
+
+
+@pytest.mark.parametrize("D", [16, 32])
+@pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 77)])
+def test_tensor_core_path_small_head_dims_cross_lengths_and_outputs(D, Nq, Nk):
+    # unequal lengths, and outputs written through a wider buffer: columns
+    # beyond D must stay untouched (the kernel computes 64 columns and its
+    # stores drop the rest)
+    w = synth.small("bf16", 2, 2, Nq, D, "causal", seed=Nq + Nk + D, Nk=Nk)
+    compare_full(w, expect_path=1)
+    inp = synth.make_inputs(w)
+    g = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    ref_o, ref_t = A.fwd_dual(*g, is_causal=True)
+    wide = [torch.full((2, 2, Nq, 64), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    A.fwd_dual(*g, is_causal=True, out=(wide[0][..., :D], wide[1][..., :D]))
+    torch.cuda.synchronize()
+    assert A.last_path() == 1
+    assert torch.equal(wide[0][..., :D], ref_o) and torch.equal(wide[1][..., :D], ref_t)
+    assert torch.all(wide[0][..., D:] == 7.0) and torch.all(wide[1][..., D:] == 7.0)
 
 
 def test_nondefault_scale():
