@@ -444,10 +444,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < 32; e += 2)
           po[e >> 1] = ElemTraits<T>::pack(__uint_as_float(a[e]) * s, __uint_as_float(a[e + 1]) * s);
         if (row_ok) {
+          // 8 columns per 16-byte piece; pieces at or past the tensor's own
+          // head dimension (D < 64 runs this kernel on zero-filled columns)
+          // are not written.
           uint4* od = reinterpret_cast<uint4*>(row + col);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
+            if (col + 8 * v4 < p.D)
+              od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
         }
       }
     }
@@ -985,7 +989,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
             uint4* od = reinterpret_cast<uint4*>(row + col);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
-              od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
+              if (col + 8 * v4 < p.D)  // (see the query-major kernel's store)
+                od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
           }
         }
       }

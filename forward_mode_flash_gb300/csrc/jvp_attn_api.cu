@@ -457,9 +457,12 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   p.delta = p.nu + q_rows;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-  // Tensor-core path: fp16/bf16, D in {64, 128}, at least one row and one key,
-  // every tensor 16-byte aligned with 16-byte-multiple strides.
-  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) && (D == 64 || D == 128) && Nq > 0 && Nk > 0;
+  // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, at least one row and
+  // one key, every tensor 16-byte aligned with 16-byte-multiple strides.  As in
+  // the forward, D = 16 and 32 run the D = 64 kernels on zero-filled columns
+  // (their gradient stores stop at D).
+  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) &&
+            (D == 16 || D == 32 || D == 64 || D == 128) && Nq > 0 && Nk > 0;
   for (int t = 0; tc && t < 10; ++t) tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
   for (int t = 0; tc && t < 6; ++t) tc = aligned(out[t], 16) && strides_aligned16(out_strides[t], e);
   // Tensor maps: qm for the query-major kernel (query side 128 rows, key side
@@ -488,7 +491,7 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   if (tc) {
     err = launch_bwd_rows(static_cast<DType>(dtype), p, stream);
     if (err == cudaSuccess)
-      err = launch_bwd_tc(static_cast<DType>(dtype), static_cast<int>(D), kind, qm, km, p,
+      err = launch_bwd_tc(static_cast<DType>(dtype), D <= 64 ? 64 : 128, kind, qm, km, p,
                           dev->num_sms, dev->status, stream);
     t_last_path = 1;
   } else {

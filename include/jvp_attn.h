@@ -235,10 +235,11 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
  *                         do not matter and are overwritten.
  *
  * Every tensor has the same dtype; mask and scale as in the forward call.
- * fp16/bf16 with D in {64, 128} and 16-byte aligned tensors run a row pass
- * and tcgen05 kernels (query-major for g_q, g_dq; key-major for g_k, g_dk,
- * g_v, g_dv), fp32 accumulation; every other case runs three CUDA-core
- * kernels in fp32.  All are enqueued on `stream`.  Returns JVP_ERR_WORKSPACE
+ * fp16/bf16 with D in {16, 32, 64, 128} and 16-byte aligned tensors run a
+ * row pass and tcgen05 kernels (query-major for g_q, g_dq; key-major for g_k,
+ * g_dk, g_v, g_dv), fp32 accumulation (D = 16 and 32 on the D = 64 kernels,
+ * with zero-filled columns); every other case runs three CUDA-core kernels in
+ * fp32.  All are enqueued on `stream`.  Returns JVP_ERR_WORKSPACE
  * if the workspace is NULL or too small.
  */
 jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,

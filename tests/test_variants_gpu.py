@@ -101,7 +101,7 @@ def check_bwd(w, inp, causal):
     path = A.last_path()
     torch.cuda.synchronize()
     assert A.device_status() == 0
-    assert path == (2 if w.dtype == "f32" or w.D not in (64, 128) else 1)
+    assert path == (2 if w.dtype == "f32" or w.D not in (16, 32, 64, 128) else 1)
     H, Hkv = inp.q.shape[1], inp.k.shape[1]
     group = H // Hkv
     kind, mm = oracle_mask(w, inp, causal)
