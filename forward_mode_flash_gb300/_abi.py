@@ -39,6 +39,7 @@ EXPORTS = (
     "jvp_attn_version",
     "jvp_attn_selftest_wait_timeout",
     "jvp_attn_debug_last_path",
+    "jvp_attn_debug_set_cluster_split",
 )
 
 
@@ -118,6 +119,8 @@ def load(path: str | None = None):
         lib.jvp_attn_selftest_wait_timeout.restype = i32
         lib.jvp_attn_debug_last_path.argtypes = []
         lib.jvp_attn_debug_last_path.restype = i32
+        lib.jvp_attn_debug_set_cluster_split.argtypes = [i32]
+        lib.jvp_attn_debug_set_cluster_split.restype = i32
         _lib = lib
         return lib
 

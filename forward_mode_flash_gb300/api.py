@@ -425,5 +425,15 @@ def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
 
 
 def last_path() -> int:
-    """1 if the last forward call on this thread took the tensor-core path, 2 if CUDA-core."""
+    """Kernel family of the last call on this thread: 1 tensor-core, 2 CUDA-core,
+    3 tensor-core with split-KV and the merge kernel, 4 tensor-core with each
+    query tile's key range split between the two CTAs of a cluster."""
     return int(_abi.load().jvp_attn_debug_last_path())
+
+
+TENSOR_CORE_PATHS = (1, 3, 4)
+
+
+def set_cluster_split(enable: bool) -> None:
+    """Diagnostic: allow (default) or forbid the cluster key split (process-wide)."""
+    _abi.check(_abi.load().jvp_attn_debug_set_cluster_split(1 if enable else 0))

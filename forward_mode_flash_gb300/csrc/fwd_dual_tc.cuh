@@ -133,6 +133,7 @@ struct TcCtrl {
   uint64_t at_done, o_full, drain, drain_pv, sums_ready;
   uint64_t o_staged;  // every softmax warp has staged its O / tO rows in shared memory
   uint64_t pv_done[2];  // P~V MMAs of the tile in each score buffer are complete
+  uint64_t ring_free, peer_ready;  // cluster split (arrived on by the other CTA)
   uint32_t tmem_base;
   int abort;
   float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
@@ -154,6 +155,14 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, volatile in
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
                                           volatile int* abort) {
   const bool got = mbar_wait(bar, parity, abort);
+  if (!got) record_timeout(status, abort);
+  return __all_sync(0xffffffffu, got);
+}
+
+// warp_wait for a barrier that another CTA of the cluster arrives on.
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  unsigned int* status, volatile int* abort) {
+  const bool got = mbar_wait_cluster(bar, parity, abort);
   if (!got) record_timeout(status, abort);
   return __all_sync(0xffffffffu, got);
 }
@@ -246,12 +255,35 @@ __device__ __forceinline__ float tree_max(const float (&x)[N]) {
   return y[0];
 }
 
-// SPLIT: split-KV variant (p.splits CTAs per query tile, partial states to
-// p.split_ws); the single-pass variant compiles without any of it.
-template <typename T, int D, int MASK, bool TANGENT, bool SPLIT>
+// SPLIT: 0 single pass; kSplitWorkspace: split-KV over p.splits CTAs per
+// query tile, partial states to p.split_ws for fwd_combine_kernel;
+// kSplitCluster (D = 64): the key range of a query tile split between the two
+// CTAs of a cluster, rank 1 handing its partial state to rank 0 through
+// distributed shared memory.  The single-pass variant compiles without either.
+constexpr int kSplitWorkspace = 1, kSplitCluster = 2;
+
+// Receive area of the cluster split in rank 0 (inside its idle key/value
+// rings, after the 2 x 16 KB where O and tO are staged): a float4
+// {m, l, lx, mu~} per row, then one block per softmax warpgroup w holding,
+// for each row, the fp32 A and T columns [32 w, 32 w + 32) of the peer (rows
+// 16 bytes apart beyond their 64 floats, to spread shared-memory banks).  A
+// softmax warp's 32 rows of a block are contiguous, so each warp sends its
+// own part as soon as it has staged it.
+constexpr int kPairRecvOffset = 32768;
+constexpr int kPairRecvStats = 128 * 16;
+constexpr int kPairRecvRowBytes = 2 * 32 * 4 + 16;
+constexpr int kPairRecvBlock = 128 * kPairRecvRowBytes;
+constexpr int kPairRecvBytes = kPairRecvStats + 2 * kPairRecvBlock;
+
+template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
   using L = TcLayout<D, TANGENT>;
+  constexpr bool kWsSplit = SPLIT == kSplitWorkspace;
+  constexpr bool kPair = SPLIT == kSplitCluster;
+  static_assert(!kPair || (D == 64 && TANGENT), "the cluster split is built for D = 64 with tangents");
+  static_assert(!kPair || kPairRecvOffset + kPairRecvBytes <= L::OFF_CTRL - L::OFF_KDK,
+                "cluster receive area fits the rings");
   constexpr int NS = L::NS;
   constexpr int BN = L::BN;
   constexpr int HN = BN / 2;  // key columns per softmax warpgroup
@@ -332,6 +364,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&ctrl->drain, 1);
     mbar_init(&ctrl->sums_ready, kSoftmaxThreads);
     mbar_init(&ctrl->o_staged, kSoftmaxThreads / 32);
+    mbar_init(&ctrl->ring_free, 1);    // cluster split: rank 0's rings are idle
+    mbar_init(&ctrl->peer_ready, 1);   // cluster split: rank 1's state has landed (with bytes)
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -341,6 +375,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // Cluster split: every thread arrives once its CTA's barriers are
+  // initialised; a thread that touches the other CTA waits for the cluster
+  // first (the rest wait before exiting).
+  if constexpr (kPair) cluster_arrive();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
 
@@ -751,11 +789,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t t_tile = o_tile + L::KCH * L::BM * 128;
     static_assert((TANGENT ? 2 : 1) * L::KCH * L::BM * 128 <= L::OFF_CTRL - L::OFF_KDK,
                   "output staging fits the key/value rings");
+    if constexpr (kPair) {
+      if (warp == 2) cluster_wait();  // both CTAs' barriers are initialised
+      if (split == 0 && warp == 2 && lane == 0) {
+        // the peer's state arrives as one bulk copy into the idle rings
+        mbar_arrive_expect_tx(&ctrl->peer_ready, kPairRecvBytes);
+        // Rank 0's rings are idle once its MMAs are done: rank 1 may fill them.
+        if (ok) mbar_arrive_cluster(cluster_map(smem_u32(&ctrl->ring_free), 1));
+      }
+    }
     if (L::kHalfAcc && ok) {
       // Merge of the two warpgroups' states (each relative to its own max):
       // with M = max(m_0, m_1) and a_w = 2^(m_w - M), l = sum a_w l_w (so for
       // lx, mu~) and A = sum a_w A_w, T = sum a_w T_w, then the usual epilogue
-      // (or, split-KV, the merged partial state).
+      // (or, split-KV, the merged partial state; or, cluster split, the same
+      // merge once more with the peer CTA's state).
       tc_fence_after();
       const float m_oth = ctrl->xsum[wg ^ 1][3][r];
       const float m_all = fmaxf(m_run, m_oth);
@@ -764,16 +812,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float l_all = a_own * l_run + a_oth * ctrl->xsum[wg ^ 1][0][r];
       const float lx_all = a_own * lx_run + a_oth * ctrl->xsum[wg ^ 1][1][r];
       const float mu_all = a_own * mu_run + a_oth * ctrl->xsum[wg ^ 1][2][r];
-      const float inv_l = (l_all > 0.0f) ? 1.0f / l_all : 0.0f;
-      const float mu_row = mu_all * inv_l;
+      // Cluster split: the final state merges this CTA's (a_self) and the peer's (a_peer).
+      float m_fin = m_all, l_fin = l_all, lx_fin = lx_all, mu_fin = mu_all;
+      float a_self = 1.0f, a_peer = 0.0f;
+      const uint32_t recv = smem_u32(smem + L::OFF_KDK + kPairRecvOffset);
+      const uint32_t recv_row = recv + kPairRecvStats + wg * kPairRecvBlock + r * kPairRecvRowBytes;
+      if constexpr (kPair) {
+        if (split == 1) {
+          // This CTA's state is staged in its own rings (same layout as the
+          // peer's receive area) and sent as one bulk copy below.
+          if (wg == 0) st_shared_v4(recv + r * 16, __float_as_uint(m_all), __float_as_uint(l_all),
+                                    __float_as_uint(lx_all), __float_as_uint(mu_all));
+        } else {
+          ok = warp_wait(&ctrl->peer_ready, 0, p.status, abort);
+          if (ok) {
+            float4 st;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(st.x), "=f"(st.y), "=f"(st.z), "=f"(st.w)
+                         : "r"(recv + r * 16));
+            m_fin = fmaxf(m_all, st.x);
+            a_self = (m_all == -INFINITY) ? 0.0f : exp2f(m_all - m_fin);
+            a_peer = (st.x == -INFINITY) ? 0.0f : exp2f(st.x - m_fin);
+            l_fin = a_self * l_all + a_peer * st.y;
+            lx_fin = a_self * lx_all + a_peer * st.z;
+            mu_fin = a_self * mu_all + a_peer * st.w;
+          }
+        }
+      }
+      const float inv_l = (l_fin > 0.0f) ? 1.0f / l_fin : 0.0f;
+      const float mu_row = mu_fin * inv_l;
       const uint32_t own = lane_base + L::TM_A + wg * L::ACC_STRIDE;
       const uint32_t oth = lane_base + L::TM_A + (wg ^ 1) * L::ACC_STRIDE;
       const long long rows = static_cast<long long>(BH) * p.Nq;
       const long long R = static_cast<long long>(split) * rows +
                           (static_cast<long long>(b) * p.H + h) * p.Nq + (row_ok ? i : 0);
-      float* acc = SPLIT ? p.split_ws + static_cast<long long>(p.splits) * rows * 4 + R * (2 * D)
-                         : nullptr;
-      if (SPLIT && row_ok && wg == 0)
+      float* acc = kWsSplit
+                       ? p.split_ws + static_cast<long long>(p.splits) * rows * 4 + R * (2 * D)
+                       : nullptr;
+      if (kWsSplit && row_ok && wg == 0)
         reinterpret_cast<float4*>(p.split_ws)[R] = make_float4(m_all, l_all, lx_all, mu_all);
 #pragma unroll 1
       for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 16) {
@@ -795,7 +871,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) fa[e] = ft[e] = 0.f;
         }
-        if (SPLIT) {
+        if (kPair && split == 1) {
+          // this CTA's A and T rows (its warpgroup's columns), staged locally
+          const int lc = col - wg * (D / 2);  // column within the warpgroup's block
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            st_shared_v4(recv_row + (lc + 4 * v4) * 4, __float_as_uint(fa[4 * v4]),
+                         __float_as_uint(fa[4 * v4 + 1]), __float_as_uint(fa[4 * v4 + 2]),
+                         __float_as_uint(fa[4 * v4 + 3]));
+            st_shared_v4(recv_row + (D / 2 + lc + 4 * v4) * 4, __float_as_uint(ft[4 * v4]),
+                         __float_as_uint(ft[4 * v4 + 1]), __float_as_uint(ft[4 * v4 + 2]),
+                         __float_as_uint(ft[4 * v4 + 3]));
+          }
+        } else if (kWsSplit) {
           if (row_ok) {
             float4* ad = reinterpret_cast<float4*>(acc + col);
             float4* td = reinterpret_cast<float4*>(acc + D + col);
@@ -807,6 +895,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         } else {
+          if (kPair && ok) {
+            // merge the peer's A and T (received into this CTA's rings)
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              float4 pa, pt4;
+              const int lc = col - wg * (D / 2);
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(pa.x), "=f"(pa.y), "=f"(pa.z), "=f"(pa.w)
+                           : "r"(recv_row + (lc + 4 * v4) * 4));
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(pt4.x), "=f"(pt4.y), "=f"(pt4.z), "=f"(pt4.w)
+                           : "r"(recv_row + (D / 2 + lc + 4 * v4) * 4));
+              fa[4 * v4] = a_self * fa[4 * v4] + a_peer * pa.x;
+              fa[4 * v4 + 1] = a_self * fa[4 * v4 + 1] + a_peer * pa.y;
+              fa[4 * v4 + 2] = a_self * fa[4 * v4 + 2] + a_peer * pa.z;
+              fa[4 * v4 + 3] = a_self * fa[4 * v4 + 3] + a_peer * pa.w;
+              ft[4 * v4] = a_self * ft[4 * v4] + a_peer * pt4.x;
+              ft[4 * v4 + 1] = a_self * ft[4 * v4 + 1] + a_peer * pt4.y;
+              ft[4 * v4 + 2] = a_self * ft[4 * v4 + 2] + a_peer * pt4.z;
+              ft[4 * v4 + 3] = a_self * ft[4 * v4 + 3] + a_peer * pt4.w;
+            }
+          }
           uint32_t po[8], pt[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
@@ -824,12 +934,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      if (!SPLIT && row_ok && wg == 0) {
+      if constexpr (kPair) {
+        if (split == 1) {
+          // Each warp sends its staged rows to rank 0 (once rank 0's rings
+          // are free) as bulk copies that complete on rank 0's barrier; this
+          // CTA's shared memory stays valid until then because rank 0 passes
+          // the final cluster barrier only after that completion.
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (mbar_wait_cluster(&ctrl->ring_free, 0, abort)) {
+              const uint32_t bar = cluster_map(smem_u32(&ctrl->peer_ready), 0);
+              const uint32_t rows = recv + kPairRecvStats + wg * kPairRecvBlock +
+                                    sub * 32 * kPairRecvRowBytes;
+              bulk_copy_to_cluster(cluster_map(rows, 0), rows, 32 * kPairRecvRowBytes, bar);
+              if (wg == 0) {
+                const uint32_t stats = recv + sub * 32 * 16;
+                bulk_copy_to_cluster(cluster_map(stats, 0), stats, 32 * 16, bar);
+              }
+            } else {
+              record_timeout(p.status, abort);
+            }
+          }
+        }
+      }
+      if (!kWsSplit && !(kPair && split == 1) && row_ok && wg == 0) {
         const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
-        if (p.lse) p.lse[ridx] = (lx_all > 0.0f) ? (m_all + log2f(lx_all)) * kLn2 : -INFINITY;
+        if (p.lse) p.lse[ridx] = (lx_fin > 0.0f) ? (m_fin + log2f(lx_fin)) * kLn2 : -INFINITY;
         if (TANGENT && p.mu) p.mu[ridx] = mu_row;
       }
-    } else if (SPLIT && ok) {
+    } else if (kWsSplit && ok) {
       // Split-KV: store this key range's unnormalised state (m, l, lx, mu~,
       // A, T) for the combine kernel.
       tc_fence_after();
@@ -909,7 +1043,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (TANGENT && p.mu) p.mu[ridx] = mu_row;
       }
     }
-    if (!SPLIT && ok) {
+    if (!kWsSplit && !(kPair && split == 1) && ok) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->o_staged);
@@ -936,9 +1070,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, L::TM_COLS);
   }
+  // Cluster split: neither CTA exits while the other may still reach its
+  // shared memory.
+  if constexpr (kPair) {
+    if (warp != 2) cluster_wait();
+    cluster_sync();
+  }
 }
 
-template <typename T, int D, int MASK, bool TANGENT, bool SPLIT>
+template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream_t stream) {
   using L = TcLayout<D, TANGENT>;
   auto kern = fwd_dual_tc_kernel<T, D, MASK, TANGENT, SPLIT>;
@@ -954,6 +1094,22 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     if (dev < 64) attr_done.fetch_or(1ull << dev, std::memory_order_relaxed);
   }
   const long long grid = static_cast<long long>(p.num_q_tiles) * p.B * p.H * (SPLIT ? p.splits : 1);
+  if constexpr (SPLIT == kSplitCluster) {
+    // the two CTAs of a query tile (consecutive blocks) form a cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, maps, p);
+  }
   kern<<<static_cast<unsigned>(grid), kTcThreads, L::SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }
@@ -963,9 +1119,14 @@ cudaError_t launch_tc_dispatch(int mask_kind, bool tangent, const TcMaps& maps,
                                const FwdParams& p, cudaStream_t stream) {
 #define JVP_TC_CASE(MK)                                                                  \
   case MK:                                                                               \
-    if (!tangent) return launch_tc_variant<T, D, MK, false, false>(maps, p, stream);     \
-    return p.splits > 1 ? launch_tc_variant<T, D, MK, true, true>(maps, p, stream)       \
-                        : launch_tc_variant<T, D, MK, true, false>(maps, p, stream);
+    if (!tangent) return launch_tc_variant<T, D, MK, false, 0>(maps, p, stream);         \
+    if (p.splits > 1 && p.split_ws)                                                      \
+      return launch_tc_variant<T, D, MK, true, kSplitWorkspace>(maps, p, stream);        \
+    if (p.splits > 1) {                                                                  \
+      if constexpr (D == 64) return launch_tc_variant<T, D, MK, true, kSplitCluster>(maps, p, stream); \
+      return cudaErrorInvalidValue;                                                      \
+    }                                                                                    \
+    return launch_tc_variant<T, D, MK, true, 0>(maps, p, stream);
   switch (mask_kind) {
     JVP_TC_CASE(kMaskNone)
     JVP_TC_CASE(kMaskBool)

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -26,7 +27,10 @@ __device__ unsigned int g_device_status = 0;
 namespace {
 
 thread_local std::string t_last_error;
-thread_local int t_last_path = 0;  // 0 none, 1 tensor-core, 2 CUDA-core, 3 tensor-core split-KV
+// 0 none, 1 tensor-core, 2 CUDA-core, 3 tensor-core split-KV (workspace and
+// merge kernel), 4 tensor-core split between the two CTAs of a cluster
+thread_local int t_last_path = 0;
+std::atomic<int> g_cluster_split{1};  // diagnostic switch: 0 never splits across a cluster
 
 jvp_status_t fail(jvp_status_t s, const std::string& msg) {
   t_last_error = msg;
@@ -183,6 +187,21 @@ int choose_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_sms) {
   const int64_t by_sms = (num_sms + base - 1) / base;
   const int64_t by_keys = ((Nk + kTcBlockN - 1) / kTcBlockN) / 16;
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({by_sms, by_keys, 16})));
+}
+
+// Key-range split between the two CTAs of a cluster (D <= 64, fused forward +
+// JVP): for problems whose query tiles fill at most half of the SMs, each
+// tile's key loop is shared by two CTAs and rank 1's partial state is merged
+// into rank 0's epilogue through distributed shared memory (no workspace, no
+// second launch).  The hand-over of rank 1's 70 KB state takes ~4400 cycles
+// and the doubled grid slows every CTA's first loads, which halving the loop
+// repays from 16 key tiles on (measured: B=1 H=8 N=1024 22.5 -> 20.5 us,
+// B=1 H=4 N=2048 causal 34.8 -> 26.6 us; at 8 key tiles, B=2 H=8 N=512,
+// 16.4 us single pass against 18.4 us split).
+bool choose_cluster_split(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_sms) {
+  const int64_t ctas = ((Nq + kTcBlockM - 1) / kTcBlockM) * B * H;
+  const int64_t key_tiles = (Nk + kTcBlockN - 1) / kTcBlockN;
+  return ctas > 0 && 2 * ctas <= num_sms && key_tiles >= 16;
 }
 
 // Shared body of jvp_attn_fwd_dual(_ws) and jvp_attn_fwd.
@@ -344,11 +363,14 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
         ws_bytes >= SplitLayout::bytes(B * H * Nq, static_cast<int>(D), splits)) {
       p.splits = splits;
       p.split_ws = static_cast<float*>(workspace);
+    } else if (tangent && kernel_d == 64 && g_cluster_split.load(std::memory_order_relaxed) &&
+               choose_cluster_split(B, H, Nq, Nk, dev->num_sms)) {
+      p.splits = 2;  // with split_ws == nullptr: the cluster split
     }
     err = launch_fwd_tc(static_cast<DType>(dtype), kernel_d, kind, tangent, maps, p, stream);
-    if (err == cudaSuccess && p.splits > 1)
+    if (err == cudaSuccess && p.splits > 1 && p.split_ws)
       err = launch_fwd_combine(static_cast<DType>(dtype), tangent, p, stream);
-    t_last_path = p.splits > 1 ? 3 : 1;
+    t_last_path = p.splits > 1 ? (p.split_ws ? 3 : 4) : 1;
   } else {
     p.num_q_tiles = static_cast<int>((Nq + 7) / 8);
     err = launch_fwd_simt(static_cast<DType>(dtype), kind, tangent, p, stream);
@@ -653,6 +675,12 @@ const char* jvp_attn_last_error(void) { return jvp::t_last_error.c_str(); }
 int jvp_attn_version(void) { return 200; }
 
 int jvp_attn_debug_last_path(void) { return jvp::t_last_path; }
+
+jvp_status_t jvp_attn_debug_set_cluster_split(int enable) {
+  if (enable != 0 && enable != 1) return jvp::fail(JVP_ERR_INVALID_ARG, "enable must be 0 or 1");
+  jvp::g_cluster_split.store(enable, std::memory_order_relaxed);
+  return jvp::ok();
+}
 
 jvp_status_t jvp_attn_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
   if (limit_cycles < 1 || limit_cycles >= (1ll << 31))

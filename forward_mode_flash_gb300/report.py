@@ -106,8 +106,8 @@ def sweep(dtypes=("bf16", "f16"), Ns=SWEEP_N, masks=SWEEP_MASKS, B: int = 2, H: 
                                             mask_batch=B)
                 best = min(t for t in (hot, graph) if t is not None)
                 yield {"dtype": dtype, "N": N, "mask": mask, "B": B, "H": H, "D": D,
-                       "path": {1: "tensor-core", 3: "tensor-core split-KV"}.get(
-                           api.last_path(), "cuda-core"),
+                       "path": {1: "tensor-core", 3: "tensor-core split-KV",
+                                4: "tensor-core cluster split"}.get(api.last_path(), "cuda-core"),
                        "ms_hot": hot, "ms_cold_l2": cold, "ms_graph_batch100": graph,
                        "tflops_hot": fl / hot / 1e9, "tflops_cold_l2": fl / cold / 1e9,
                        "tflops_graph": None if graph is None else fl / graph / 1e9,

@@ -316,10 +316,22 @@ jvp_status_t jvp_attn_selftest_wait_timeout(int64_t limit_cycles, void* stream);
 /*
  * Diagnostic: which kernel family the last successful call on the calling
  * thread enqueued: 1 = tensor-core path, 2 = CUDA-core path, 3 = tensor-core
- * path with split-KV and the merge kernel, 0 = nothing was enqueued (empty
+ * path with split-KV and the merge kernel, 4 = tensor-core path with each
+ * query tile's key range split between the two CTAs of a cluster (small
+ * problems at D <= 64; no workspace), 0 = nothing was enqueued (empty
  * problem or an error).
  */
 int jvp_attn_debug_last_path(void);
+
+/*
+ * Diagnostic: enable = 1 (the default) lets jvp_attn_fwd_dual split the key
+ * range of small problems between the two CTAs of a cluster (path 4 above);
+ * enable = 0 keeps later calls (process-wide) on the single pass.  Both give
+ * the same function up to floating-point rounding order; this exists so that
+ * tests and benchmarks can compare them.  Returns JVP_ERR_INVALID_ARG for
+ * other values.
+ */
+jvp_status_t jvp_attn_debug_set_cluster_split(int enable);
 
 #ifdef __cplusplus
 }
