@@ -243,12 +243,14 @@ def timed_steps(step, steps, flush, stream, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        for s in range(steps):
-            flush.fill_(float(s))  # evict L2 between timed steps (outside the events)
-            starts[s].record(stream)
-            step()
-            ends[s].record(stream)
-        torch.cuda.synchronize()
+        with torch.cuda.nvtx.range(f"timed region: {steps} steps"):
+            for s in range(steps):
+                flush.fill_(float(s))  # evict L2 between timed steps (outside the events)
+                starts[s].record(stream)
+                with torch.cuda.nvtx.range("step"):
+                    step()
+                ends[s].record(stream)
+            torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in zip(starts, ends)], clocks
 
 
@@ -358,12 +360,14 @@ def run_bwd(args, rank, world, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
-        for s in range(args.steps):
-            flush.fill_(float(s))
-            starts[s].record(stream)
-            step()
-            ends[s].record(stream)
-        torch.cuda.synchronize()
+        with torch.cuda.nvtx.range(f"bwd_dual timed region: {args.steps} steps"):
+            for s in range(args.steps):
+                flush.fill_(float(s))
+                starts[s].record(stream)
+                with torch.cuda.nvtx.range("step"):
+                    step()
+                ends[s].record(stream)
+            torch.cuda.synchronize()
     per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = replicas.max_over_ranks(sum(per_ms), device=dev)
     ms_step = total_ms / args.steps
@@ -554,8 +558,9 @@ def main():
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(k_e2e):
-            e2e_step()
+        with torch.cuda.nvtx.range(f"e2e timed region: {k_e2e} steps"):
+            for _ in range(k_e2e):
+                e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = replicas.max_over_ranks(a.elapsed_time(b) / k_e2e, device=dev)

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libjvp_attn.so")
 
 JVP_OK, JVP_ERR_INVALID_ARG, JVP_ERR_UNSUPPORTED, JVP_ERR_ALIGNMENT = 0, 1, 2, 3
-JVP_ERR_CUDA, JVP_ERR_DEVICE_TIMEOUT, JVP_ERR_WORKSPACE = 4, 5, 6
+JVP_ERR_CUDA, JVP_ERR_DEVICE_TIMEOUT, JVP_ERR_WORKSPACE, JVP_ERR_BOUNDS = 4, 5, 6, 7
 # fixed device scratch of jvp_attn_bwd_dual_noalloc (JVP_BWD_NOALLOC_SCRATCH_BYTES)
 JVP_BWD_NOALLOC_SCRATCH_BYTES = 4 << 20
 JVP_F32, JVP_F16, JVP_BF16 = 0, 1, 2
@@ -61,7 +61,8 @@ class Mask(ctypes.Structure):
 
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}           # path -> loaded library
+_debug_path = None   # when set, load() returns this debug build instead
 
 
 class JvpAttnError(RuntimeError):
@@ -70,13 +71,20 @@ class JvpAttnError(RuntimeError):
         self.status = status
 
 
+def use_debug_build(path: str | None) -> None:
+    """Route load() to a debug build of the library (device-side bounds checks;
+    forward_mode_flash_gb300.build.build(debug=True) makes it), or back to the
+    ordinary build with None."""
+    global _debug_path
+    _debug_path = path
+
+
 def load(path: str | None = None):
-    """Load (once) and return the library with argument types declared."""
-    global _lib
+    """Load (once per file) and return the library with argument types declared."""
     with _lock:
-        if _lib is not None:
-            return _lib
-        p = path or LIB_PATH
+        p = path or _debug_path or LIB_PATH
+        if p in _libs:
+            return _libs[p]
         if not os.path.exists(p):
             raise ImportError(
                 f"{p} is missing: build it with forward_mode_flash_gb300.build.build() "
@@ -121,7 +129,7 @@ def load(path: str | None = None):
         lib.jvp_attn_debug_last_path.restype = i32
         lib.jvp_attn_debug_set_cluster_split.argtypes = [i32]
         lib.jvp_attn_debug_set_cluster_split.restype = i32
-        _lib = lib
+        _libs[p] = lib
         return lib
 
 

@@ -19,6 +19,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libjvp_attn.so")
+# Debug build: device-side bounds checks (-DJVP_DEBUG_CHECKS), built on request only.
+DEBUG_BUILD = os.path.join(BUILD, "debug")
+DEBUG_LIB = os.path.join(DEBUG_BUILD, "libjvp_attn_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]
@@ -37,28 +40,34 @@ def _sources():
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(
-        os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "jvp_attn.h")]
+        os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "jvp_attn.h"),
+                                      os.path.join(CSRC, "exports.map")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile every translation unit and link the library; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), debug: bool = False) -> str:
+    """Compile every translation unit and link the library; returns its path.
+
+    debug=True builds the separate debug library (DEBUG_LIB) whose
+    tensor-core kernels bounds-check their hand-computed indices."""
+    lib, out_dir = (DEBUG_LIB, DEBUG_BUILD) if debug else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
     objs = []
     cmds = []
+    defs = ["-DJVP_DEBUG_CHECKS"] if debug else []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
         objs.append(obj)
-        cmds.append([cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj])
+        cmds.append([cc, *ARCH, *FLAGS, *defs, *extra, "-c", src, "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -74,13 +83,14 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    tmp = LIB + f".tmp{os.getpid()}"
-    link = [cc, *ARCH, "-shared", "-o", tmp, *objs]
+    tmp = lib + f".tmp{os.getpid()}"
+    link = [cc, *ARCH, "-shared", "-Xlinker", "--version-script=" + os.path.join(CSRC, "exports.map"),
+            "-o", tmp, *objs]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -349,12 +349,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool row_ok = i < p.Nq;
     const uint32_t lb = tmem + (static_cast<uint32_t>(sub * 32) << 16);
     const long long ridx = static_cast<long long>(bh) * p.Nq + (row_ok ? i : 0);
-    const float lse = row_ok ? p.lse[ridx] : -INFINITY;
+    const bool rd = row_ok && JVP_CHECK(ridx < static_cast<long long>(p.B) * p.H * p.Nq, status,
+                                        kChkGlobalRow);
+    const float lse = rd ? p.lse[ridx] : -INFINITY;
     const float lse2 = lse * kLog2e;
-    const bool live = row_ok && lse != -INFINITY;
-    const float mu = row_ok ? p.mu[ridx] : 0.f;
-    const float nu = row_ok ? p.nu[ridx] : 0.f;
-    const float delta = row_ok ? p.delta[ridx] : 0.f;
+    const bool live = rd && lse != -INFINITY;
+    const float mu = rd ? p.mu[ridx] : 0.f;
+    const float nu = rd ? p.nu[ridx] : 0.f;
+    const float delta = rd ? p.delta[ridx] : 0.f;
     const float c = p.scale * kLog2e;
     const float s = p.scale;
     bool ok = true;
@@ -377,8 +379,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the other half's inputs stay intact.
     auto half = [&](int j0h, uint32_t col, const MaskRegs<MASK, 16>& mreg) {
       uint32_t rs[16], rds[16], rg[16], rgp[16];
-      tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_DS + col, rs, rds);
-      tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
+      const bool cols_ok = JVP_CHECK(L::TM_GP + col + 16 <= 512u && L::TM_DS + col + 16 <= 512u,
+                                     status, kChkTmem);
+      if (cols_ok) {
+        tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_DS + col, rs, rds);
+        tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
+      }
       uint32_t pgs[8], pgds[8];
 #pragma unroll
       for (int jj = 0; jj < 16; jj += 2) {
@@ -403,8 +409,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pgs[jj >> 1] = ElemTraits<T>::pack(gs[0], gs[1]);
         pgds[jj >> 1] = ElemTraits<T>::pack(gds[0], gds[1]);
       }
-      tmem_st8(lb + col, pgs);
-      tmem_st8(lb + col + 8, pgds);
+      if (cols_ok) {
+        tmem_st8(lb + col, pgs);
+        tmem_st8(lb + col + 8, pgds);
+      }
     };
     for (int t = 0; t < n_kv; ++t) {
       const int j0 = t * BN + wg * 32;
@@ -433,7 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
         uint32_t a[32];
-        if (n_kv > 0) {
+        if (n_kv > 0 && JVP_CHECK(L::TM_ACC + wg * D + col + 32 <= 512u, status, kChkTmem)) {
           tmem_ld32(lb + L::TM_ACC + wg * D + col, a);
         } else {
 #pragma unroll
@@ -450,7 +458,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint4* od = reinterpret_cast<uint4*>(row + col);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            if (col + 8 * v4 < p.D)
+            if (col + 8 * v4 < p.D &&
+                JVP_CHECK(col + 8 * v4 + 8 <= p.D && i < p.Nq, status, kChkGlobalCol))
               od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
         }
       }
@@ -634,7 +643,7 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       for (int u = 0; u < RPL; ++u) {
         const int i = (t_begin + t % n_th) * BQ + lane + 32 * u;
         float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        if (i < p.Nq) {
+        if (i < p.Nq && JVP_CHECK(h < p.H, status, kChkGlobalRow)) {
           const long long idx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
           v.x = p.lse[idx] * kLog2e;
           v.y = p.mu[idx];
@@ -905,8 +914,14 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         // read (S^T at col, dS^T at DS_OFF + col), so the other halves' inputs stay intact.
         const uint32_t col = bcol + hq * 16;
         uint32_t rs[16], rds[16], rg[16], rgp[16];
-        tmem_ld16x2(lb + col + L::S_OFF, lb + col + L::DS_OFF, rs, rds);
-        if (L::kK) tmem_ld16x2(lb + col + L::G_OFF, lb + col + L::GP_OFF, rg, rgp);
+        const uint32_t top = L::kK ? L::GP_OFF : L::DS_OFF;
+        const bool cols_ok = JVP_CHECK(col + top + 16 <= 512u && col + L::DS_OFF + 16 <= 512u &&
+                                           wg * QW + hq * 16 + 16 <= L::SCAL_BYTES / 16,
+                                       status, kChkTmem);
+        if (cols_ok) {
+          tmem_ld16x2(lb + col + L::S_OFF, lb + col + L::DS_OFF, rs, rds);
+          if (L::kK) tmem_ld16x2(lb + col + L::G_OFF, lb + col + L::GP_OFF, rg, rgp);
+        }
         uint32_t pa[8], pb[8], pc[8], pd[8];  // P^T, dP^T, gS^T, g_dS^T (packed pairs)
 #pragma unroll
         for (int qq = 0; qq < 16; qq += 2) {
@@ -943,11 +958,11 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
           pc[qq >> 1] = ElemTraits<T>::pack(gS2[0], gS2[1]);
           pd[qq >> 1] = ElemTraits<T>::pack(gdS2[0], gdS2[1]);
         }
-        if (L::kV) {
+        if (L::kV && cols_ok) {
           tmem_st8(lb + col + L::S_OFF, pa);
           tmem_st8(lb + col + L::S_OFF + 8, pb);
         }
-        if (L::kK) {
+        if (L::kK && cols_ok) {
           tmem_st8(lb + col + L::DS_OFF, pc);
           tmem_st8(lb + col + L::DS_OFF + 8, pd);
         }
@@ -974,7 +989,7 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
 #pragma unroll 1
         for (int col = 0; col < D; col += 32) {
           uint32_t a[32];
-          if (n_t > 0) {
+          if (n_t > 0 && JVP_CHECK(L::TM_ACC + acol + col + 32 <= 512u, status, kChkTmem)) {
             tmem_ld32(lb + L::TM_ACC + acol + col, a);
           } else {
 #pragma unroll
@@ -989,7 +1004,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
             uint4* od = reinterpret_cast<uint4*>(row + col);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
-              if (col + 8 * v4 < p.D)  // (see the query-major kernel's store)
+              if (col + 8 * v4 < p.D &&  // (see the query-major kernel's store)
+                  JVP_CHECK(col + 8 * v4 + 8 <= p.D && j < p.Nk, status, kChkGlobalCol))
                 od[v4] = make_uint4(po[4 * v4], po[4 * v4 + 1], po[4 * v4 + 2], po[4 * v4 + 3]);
           }
         }

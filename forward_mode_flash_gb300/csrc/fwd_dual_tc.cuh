@@ -52,6 +52,7 @@
 
 #include <atomic>
 
+#include "debug_checks.cuh"
 #include "jvp_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -229,15 +230,18 @@ struct MaskRegs<kMaskAdditive, KN> {
 // on, into a [128 x D] tile in shared memory laid out as the TMA box of the
 // output tensor map: 64-column chunks of 128 rows x 128 bytes, the 16-byte
 // piece k of a row at position k ^ (row % 8) (128-byte swizzle).
+// (tile_bytes and status serve the debug build's bounds check only.)
 template <int NP>
 __device__ __forceinline__ void stage_row(uint32_t tile, int r, int col,
-                                          const uint32_t (&v)[NP * 4]) {
+                                          const uint32_t (&v)[NP * 4], uint32_t tile_bytes,
+                                          unsigned int* status) {
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int cc = col + 8 * q;
-    const uint32_t addr = tile + static_cast<uint32_t>((cc >> 6) * (kTcBlockM * 128) + r * 128 +
-                                                       ((((cc & 63) >> 3) ^ (r & 7)) << 4));
-    st_shared_v4(addr, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    const uint32_t off = static_cast<uint32_t>((cc >> 6) * (kTcBlockM * 128) + r * 128 +
+                                               ((((cc & 63) >> 3) ^ (r & 7)) << 4));
+    if (JVP_CHECK(off + 16 <= tile_bytes && r < kTcBlockM, status, kChkSmem))
+      st_shared_v4(tile + off, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   }
 }
 
@@ -613,7 +617,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_after();
       uint32_t sa[32], da[32];  // S and dS (raw, unscaled) of this half tile
-      tmem_ld32(lane_base + buf * 128 + cofs, sa);
+      if (JVP_CHECK(buf * 128 + cofs + 32 <= L::TM_COLS, p.status, kChkTmem))
+        tmem_ld32(lane_base + buf * 128 + cofs, sa);
       float x[HN];
 #pragma unroll
       for (int jj = 0; jj < HN; ++jj) x[jj] = __uint_as_float(sa[jj]);
@@ -726,6 +731,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
           for (int col = c_lo; col < c_hi; col += 32) {
             uint32_t acc[32];
+            if (!JVP_CHECK(L::TM_A + wg * L::ACC_STRIDE + col + 32 <= L::TM_COLS, p.status,
+                           kChkTmem))
+              continue;
             tmem_ld32(a_base + col, acc);
 #pragma unroll
             for (int e = 0; e < 32; ++e) acc[e] = __float_as_uint(__uint_as_float(acc[e]) * alpha);
@@ -744,7 +752,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ordered both warpgroups' reads first and the two halves are packed
       // side by side.
       const uint32_t pofs = L::kHalfAcc ? cofs : wg * (HN / 2);
-      tmem_st16(lane_base + buf * 128 + pofs, pk);
+      if (JVP_CHECK(buf * 128 + pofs + 16 <= L::TM_COLS, p.status, kChkTmem))
+        tmem_st16(lane_base + buf * 128 + pofs, pk);
       if (TANGENT) {
         // Publish P~ first: the P~ [V | dV] products run while the tangent
         // terms wait for dS.
@@ -760,10 +769,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        tmem_ld32(lane_base + buf * 128 + BN + cofs, da);
+        if (JVP_CHECK(buf * 128 + BN + cofs + 32 <= L::TM_COLS, p.status, kChkTmem))
+          tmem_ld32(lane_base + buf * 128 + BN + cofs, da);
         tangent_terms();
         mu_run += mu_part;
-        tmem_st16(lane_base + buf * 128 + BN + cofs, pdk);
+        if (JVP_CHECK(buf * 128 + BN + cofs + 16 <= L::TM_COLS, p.status, kChkTmem))
+          tmem_st16(lane_base + buf * 128 + BN + cofs, pdk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -821,7 +832,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (split == 1) {
           // This CTA's state is staged in its own rings (same layout as the
           // peer's receive area) and sent as one bulk copy below.
-          if (wg == 0) st_shared_v4(recv + r * 16, __float_as_uint(m_all), __float_as_uint(l_all),
+          if (wg == 0 && JVP_CHECK(kPairRecvOffset + r * 16 + 16 <= L::OFF_CTRL - L::OFF_KDK,
+                                   p.status, kChkSmem))
+            st_shared_v4(recv + r * 16, __float_as_uint(m_all), __float_as_uint(l_all),
                                     __float_as_uint(lx_all), __float_as_uint(mu_all));
         } else {
           ok = warp_wait(&ctrl->peer_ready, 0, p.status, abort);
@@ -849,17 +862,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float* acc = kWsSplit
                        ? p.split_ws + static_cast<long long>(p.splits) * rows * 4 + R * (2 * D)
                        : nullptr;
-      if (kWsSplit && row_ok && wg == 0)
+      if (kWsSplit && row_ok && wg == 0 &&
+          JVP_CHECK(R < static_cast<long long>(p.splits) * rows, p.status, kChkGlobalRow))
         reinterpret_cast<float4*>(p.split_ws)[R] = make_float4(m_all, l_all, lx_all, mu_all);
 #pragma unroll 1
       for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 16) {
         float fa[16], ft[16];
         if (n_kv > 0) {
           uint32_t a0[16], t0[16], a1[16], t1[16];
-          if (TANGENT) {
+          const bool cols_ok = JVP_CHECK(
+              L::TM_A + L::ACC_STRIDE + (TANGENT ? D : 0) + col + 16 <= L::TM_COLS, p.status, kChkTmem);
+          if (cols_ok && TANGENT) {
             tmem_ld16x2(own + col, own + D + col, a0, t0);
             tmem_ld16x2(oth + col, oth + D + col, a1, t1);
-          } else {
+          } else if (cols_ok) {
             tmem_ld16x2(own + col, oth + col, a0, a1);
           }
 #pragma unroll
@@ -874,8 +890,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (kPair && split == 1) {
           // this CTA's A and T rows (its warpgroup's columns), staged locally
           const int lc = col - wg * (D / 2);  // column within the warpgroup's block
+          const bool in_recv = JVP_CHECK(
+              kPairRecvOffset + kPairRecvStats + wg * kPairRecvBlock + (r + 1) * kPairRecvRowBytes <=
+                  L::OFF_CTRL - L::OFF_KDK && (D / 2 + lc + 16) * 4 <= kPairRecvRowBytes,
+              p.status, kChkSmem);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
+            if (!in_recv) break;
             st_shared_v4(recv_row + (lc + 4 * v4) * 4, __float_as_uint(fa[4 * v4]),
                          __float_as_uint(fa[4 * v4 + 1]), __float_as_uint(fa[4 * v4 + 2]),
                          __float_as_uint(fa[4 * v4 + 3]));
@@ -927,9 +948,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                ft[e + 1] * inv_l - mu_row * o1);
           }
           {
-            stage_row<2>(o_tile, r, col, po);
+            stage_row<2>(o_tile, r, col, po, L::KCH * L::BM * 128, p.status);
             if (TANGENT) {
-              stage_row<2>(t_tile, r, col, pt);
+              stage_row<2>(t_tile, r, col, pt, L::KCH * L::BM * 128, p.status);
             }
           }
         }
@@ -960,8 +981,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!kWsSplit && !(kPair && split == 1) && row_ok && wg == 0) {
         const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
-        if (p.lse) p.lse[ridx] = (lx_fin > 0.0f) ? (m_fin + log2f(lx_fin)) * kLn2 : -INFINITY;
-        if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+        if (JVP_CHECK(ridx < static_cast<long long>(BH) * p.Nq, p.status, kChkGlobalRow)) {
+          if (p.lse) p.lse[ridx] = (lx_fin > 0.0f) ? (m_fin + log2f(lx_fin)) * kLn2 : -INFINITY;
+          if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+        }
       }
     } else if (kWsSplit && ok) {
       // Split-KV: store this key range's unnormalised state (m, l, lx, mu~,
@@ -970,7 +993,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const long long rows = static_cast<long long>(BH) * p.Nq;
       const long long R = static_cast<long long>(split) * rows +
                           (static_cast<long long>(b) * p.H + h) * p.Nq + (row_ok ? i : 0);
-      if (row_ok && wg == 0) {
+      if (row_ok && wg == 0 &&
+          JVP_CHECK(R < static_cast<long long>(p.splits) * rows, p.status, kChkGlobalRow)) {
         reinterpret_cast<float4*>(p.split_ws)[R] =
             make_float4(m_run, l_run + ctrl->xsum[1][0][r], lx_run + ctrl->xsum[1][1][r],
                         mu_run + ctrl->xsum[1][2][r]);
@@ -980,9 +1004,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 32) {
         uint32_t a[32], tt[32];
         if (n_kv > 0) {
-          if (TANGENT) {
+          const bool cols_ok =
+              JVP_CHECK(L::TM_T + col + 32 <= L::TM_COLS, p.status, kChkTmem);
+          if (cols_ok && TANGENT) {
             tmem_ld32x2(lane_base + L::TM_A + col, lane_base + L::TM_T + col, a, tt);
-          } else {
+          } else if (cols_ok) {
             tmem_ld32(lane_base + L::TM_A + col, a);
           }
         } else {
@@ -1013,9 +1039,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 32) {
         uint32_t a[32], tt[32];
         if (n_kv > 0) {
-          if (TANGENT) {
+          const bool cols_ok =
+              JVP_CHECK(L::TM_T + col + 32 <= L::TM_COLS, p.status, kChkTmem);
+          if (cols_ok && TANGENT) {
             tmem_ld32x2(lane_base + L::TM_A + col, lane_base + L::TM_T + col, a, tt);
-          } else {
+          } else if (cols_ok) {
             tmem_ld32(lane_base + L::TM_A + col, a);
           }
         } else {
@@ -1033,14 +1061,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             pt[e >> 1] = ElemTraits<T>::pack(t0, t1);
           }
         }
-        stage_row<4>(o_tile, r, col, po);
-        if (TANGENT) stage_row<4>(t_tile, r, col, pt);
+        stage_row<4>(o_tile, r, col, po, L::KCH * L::BM * 128, p.status);
+        if (TANGENT) stage_row<4>(t_tile, r, col, pt, L::KCH * L::BM * 128, p.status);
       }
       if (row_ok && wg == 0) {
         const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
-        if (p.lse)
-          p.lse[ridx] = (lx_all > 0.0f) ? (m_run + log2f(lx_all)) * kLn2 : -INFINITY;
-        if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+        if (JVP_CHECK(ridx < static_cast<long long>(BH) * p.Nq, p.status, kChkGlobalRow)) {
+          if (p.lse)
+            p.lse[ridx] = (lx_all > 0.0f) ? (m_run + log2f(lx_all)) * kLn2 : -INFINITY;
+          if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+        }
       }
     }
     if (!kWsSplit && !(kPair && split == 1) && ok) {

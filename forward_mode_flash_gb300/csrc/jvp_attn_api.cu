@@ -652,6 +652,14 @@ jvp_status_t jvp_attn_get_device_status(void* stream) {
     e = cudaMemcpyToSymbol(jvp::g_device_status, &zero, sizeof(zero));
     if (e != cudaSuccess)
       return jvp::fail(JVP_ERR_CUDA, std::string("clearing the status word: ") + cudaGetErrorString(e));
+    if (word & 2u) {
+      static const char* kinds[4] = {"TMEM column", "shared-memory offset", "global row",
+                                     "global column"};
+      std::string what;
+      for (unsigned k = 0; k < 4; ++k)
+        if (word & (1u << (8 + k))) what += std::string(what.empty() ? "" : ", ") + kinds[k];
+      return jvp::fail(JVP_ERR_BOUNDS, "a device-side bounds check failed (" + what + ")");
+    }
     return jvp::fail(JVP_ERR_DEVICE_TIMEOUT, "a device-side wait ran out of time");
   }
   return jvp::ok();
@@ -666,6 +674,7 @@ const char* jvp_attn_status_string(jvp_status_t status) {
     case JVP_ERR_CUDA: return "CUDA error";
     case JVP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case JVP_ERR_WORKSPACE: return "workspace missing or too small";
+    case JVP_ERR_BOUNDS: return "device-side bounds check failed (debug build)";
   }
   return "unknown status";
 }

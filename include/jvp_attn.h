@@ -57,7 +57,9 @@ typedef enum {
   JVP_ERR_ALIGNMENT = 3,      /* pointer or stride not aligned to the element size */
   JVP_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, attribute, ...) */
   JVP_ERR_DEVICE_TIMEOUT = 5, /* a device-side wait ran out (reported asynchronously) */
-  JVP_ERR_WORKSPACE = 6       /* workspace missing or too small */
+  JVP_ERR_WORKSPACE = 6,      /* workspace missing or too small */
+  JVP_ERR_BOUNDS = 7          /* debug build only: a device-side bounds check failed
+                                 (reported asynchronously, like a timeout) */
 } jvp_status_t;
 
 typedef enum { JVP_F32 = 0, JVP_F16 = 1, JVP_BF16 = 2 } jvp_dtype_t;
@@ -291,8 +293,10 @@ jvp_status_t jvp_attn_bwd_dual_noalloc(const jvp_shape_t* shape, jvp_dtype_t dty
 
 /*
  * Synchronises `stream`, then returns and clears the device-side status word:
- * JVP_ERR_DEVICE_TIMEOUT if any kernel of this library gave up on a wait since
- * the last call, JVP_ERR_CUDA if the stream reports an error, else JVP_OK.
+ * JVP_ERR_BOUNDS if a kernel of a debug build of the library found an index
+ * out of its bounds (and skipped that access), else JVP_ERR_DEVICE_TIMEOUT if
+ * any kernel gave up on a wait since the last call, JVP_ERR_CUDA if the
+ * stream reports an error, else JVP_OK.
  */
 jvp_status_t jvp_attn_get_device_status(void* stream);
 

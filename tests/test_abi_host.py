@@ -182,3 +182,13 @@ def test_sizes_that_would_overflow_are_rejected_without_a_device(lib):
                           None, 0.125, p, _strides(1, (1, 1, 64, 64)), None, None)
     assert st == _abi.JVP_ERR_UNSUPPORTED
     assert b"2^31" in lib.jvp_attn_last_error() or b"too large" in lib.jvp_attn_last_error()
+
+
+def test_debug_build_compiles_and_exports_the_same_functions():
+    # The bounds-checking build (-DJVP_DEBUG_CHECKS) of every translation unit.
+    path = build.build(debug=True)
+    dbg = ctypes.CDLL(path)
+    for n in header_functions():
+        assert hasattr(dbg, n), n
+    dbg.jvp_attn_status_string.restype = ctypes.c_char_p
+    assert dbg.jvp_attn_status_string(_abi.JVP_ERR_BOUNDS).startswith(b"device-side bounds")
