@@ -245,18 +245,23 @@ __device__ __forceinline__ void stage_row(uint32_t tile, int r, int col,
   }
 }
 
-// Maximum of n values by a pairwise tree (log2 n dependent steps).
+// Maximum of n values by a tree of three-input maxima (32 values: 17
+// instructions, 4 dependent steps).
 template <int N>
 __device__ __forceinline__ float tree_max(const float (&x)[N]) {
-  float y[N / 2];
+  if constexpr (N == 1) {
+    return x[0];
+  } else if constexpr (N == 2) {
+    return fmaxf(x[0], x[1]);
+  } else {
+    constexpr int M = (N + 2) / 3;
+    float y[M];
 #pragma unroll
-  for (int k = 0; k < N / 2; ++k) y[k] = fmaxf(x[k], x[k + N / 2]);
-#pragma unroll
-  for (int w = N / 4; w >= 1; w /= 2) {
-#pragma unroll
-    for (int k = 0; k < w; ++k) y[k] = fmaxf(y[k], y[k + w]);
+    for (int k = 0; k < N / 3; ++k) y[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+    if constexpr (N % 3 == 1) y[M - 1] = x[N - 1];
+    if constexpr (N % 3 == 2) y[M - 1] = fmaxf(x[N - 2], x[N - 1]);
+    return tree_max<M>(y);
   }
-  return y[0];
 }
 
 // SPLIT: 0 single pass; kSplitWorkspace: split-KV over p.splits CTAs per
@@ -792,7 +797,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive(&ctrl->sums_ready);
       ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
     }
-    if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
+    // The accumulators are final once the last P~V products are: the cluster
+    // split waits here (rank 0's rings are then idle for the peer's state),
+    // the other variants only before their first TMEM load, so the row
+    // statistics below are formed while those products finish.
+    if (kPair && ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
+    auto wait_acc = [&]() {
+      if (!kPair && ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
+      tc_fence_after();
+    };
     // O and tO rows are staged in the (now idle) [K;dK] ring, laid out as the
     // output tensor maps' 128-row boxes, and written by TMA stores: a warp
     // storing its own 32 rows directly would touch 32 lines per instruction.
@@ -815,7 +828,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // lx, mu~) and A = sum a_w A_w, T = sum a_w T_w, then the usual epilogue
       // (or, split-KV, the merged partial state; or, cluster split, the same
       // merge once more with the peer CTA's state).
-      tc_fence_after();
       const float m_oth = ctrl->xsum[wg ^ 1][3][r];
       const float m_all = fmaxf(m_run, m_oth);
       const float a_own = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_all);
@@ -854,6 +866,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const float inv_l = (l_fin > 0.0f) ? 1.0f / l_fin : 0.0f;
       const float mu_row = mu_fin * inv_l;
+      if (!kWsSplit && !(kPair && split == 1) && row_ok && wg == 0) {
+        const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
+        if (JVP_CHECK(ridx < static_cast<long long>(BH) * p.Nq, p.status, kChkGlobalRow)) {
+          if (p.lse) p.lse[ridx] = (lx_fin > 0.0f) ? (m_fin + log2f(lx_fin)) * kLn2 : -INFINITY;
+          if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+        }
+      }
       const uint32_t own = lane_base + L::TM_A + wg * L::ACC_STRIDE;
       const uint32_t oth = lane_base + L::TM_A + (wg ^ 1) * L::ACC_STRIDE;
       const long long rows = static_cast<long long>(BH) * p.Nq;
@@ -865,16 +884,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (kWsSplit && row_ok && wg == 0 &&
           JVP_CHECK(R < static_cast<long long>(p.splits) * rows, p.status, kChkGlobalRow))
         reinterpret_cast<float4*>(p.split_ws)[R] = make_float4(m_all, l_all, lx_all, mu_all);
+      wait_acc();
 #pragma unroll 1
-      for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 16) {
+      for (int col = wg * (D / 2); ok && col < (wg + 1) * (D / 2); col += 16) {
         float fa[16], ft[16];
         if (n_kv > 0) {
           uint32_t a0[16], t0[16], a1[16], t1[16];
           const bool cols_ok = JVP_CHECK(
               L::TM_A + L::ACC_STRIDE + (TANGENT ? D : 0) + col + 16 <= L::TM_COLS, p.status, kChkTmem);
           if (cols_ok && TANGENT) {
-            tmem_ld16x2(own + col, own + D + col, a0, t0);
-            tmem_ld16x2(oth + col, oth + D + col, a1, t1);
+            tmem_ld16x4(own + col, own + D + col, oth + col, oth + D + col, a0, t0, a1, t1);
           } else if (cols_ok) {
             tmem_ld16x2(own + col, oth + col, a0, a1);
           }
@@ -979,17 +998,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      if (!kWsSplit && !(kPair && split == 1) && row_ok && wg == 0) {
-        const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
-        if (JVP_CHECK(ridx < static_cast<long long>(BH) * p.Nq, p.status, kChkGlobalRow)) {
-          if (p.lse) p.lse[ridx] = (lx_fin > 0.0f) ? (m_fin + log2f(lx_fin)) * kLn2 : -INFINITY;
-          if (TANGENT && p.mu) p.mu[ridx] = mu_row;
-        }
-      }
     } else if (kWsSplit && ok) {
       // Split-KV: store this key range's unnormalised state (m, l, lx, mu~,
       // A, T) for the combine kernel.
-      tc_fence_after();
       const long long rows = static_cast<long long>(BH) * p.Nq;
       const long long R = static_cast<long long>(split) * rows +
                           (static_cast<long long>(b) * p.H + h) * p.Nq + (row_ok ? i : 0);
@@ -1000,8 +1011,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mu_run + ctrl->xsum[1][2][r]);
       }
       float* acc = p.split_ws + static_cast<long long>(p.splits) * rows * 4 + R * (2 * D);
+      wait_acc();
 #pragma unroll 1
-      for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 32) {
+      for (int col = wg * (D / 2); ok && col < (wg + 1) * (D / 2); col += 32) {
         uint32_t a[32], tt[32];
         if (n_kv > 0) {
           const bool cols_ok =
@@ -1029,14 +1041,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     } else if (ok) {
-      tc_fence_after();
       const float l_all = l_run + ctrl->xsum[wg ^ 1][0][r];
       const float lx_all = lx_run + ctrl->xsum[wg ^ 1][1][r];
       const float mu_all = mu_run + ctrl->xsum[wg ^ 1][2][r];
       const float inv_l = (l_all > 0.0f) ? 1.0f / l_all : 0.0f;
       const float mu_row = mu_all * inv_l;
+      if (row_ok && wg == 0) {
+        const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
+        if (JVP_CHECK(ridx < static_cast<long long>(BH) * p.Nq, p.status, kChkGlobalRow)) {
+          if (p.lse)
+            p.lse[ridx] = (lx_all > 0.0f) ? (m_run + log2f(lx_all)) * kLn2 : -INFINITY;
+          if (TANGENT && p.mu) p.mu[ridx] = mu_row;
+        }
+      }
+      wait_acc();
 #pragma unroll 1
-      for (int col = wg * (D / 2); col < (wg + 1) * (D / 2); col += 32) {
+      for (int col = wg * (D / 2); ok && col < (wg + 1) * (D / 2); col += 32) {
         uint32_t a[32], tt[32];
         if (n_kv > 0) {
           const bool cols_ok =
@@ -1063,14 +1083,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         stage_row<4>(o_tile, r, col, po, L::KCH * L::BM * 128, p.status);
         if (TANGENT) stage_row<4>(t_tile, r, col, pt, L::KCH * L::BM * 128, p.status);
-      }
-      if (row_ok && wg == 0) {
-        const long long ridx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
-        if (JVP_CHECK(ridx < static_cast<long long>(BH) * p.Nq, p.status, kChkGlobalRow)) {
-          if (p.lse)
-            p.lse[ridx] = (lx_all > 0.0f) ? (m_run + log2f(lx_all)) * kLn2 : -INFINITY;
-          if (TANGENT && p.mu) p.mu[ridx] = mu_row;
-        }
       }
     }
     if (!kWsSplit && !(kPair && split == 1) && ok) {

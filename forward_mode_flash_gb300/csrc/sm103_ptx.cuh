@@ -325,6 +325,25 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (
       : "r"(ta), "r"(tb)
       : "memory");
 }
+// Four 16-column loads under one wait.
+__device__ __forceinline__ void tmem_ld16x4(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td,
+                                            uint32_t (&a)[16], uint32_t (&b)[16],
+                                            uint32_t (&c)[16], uint32_t (&d)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : JVP_R8(a, 0), JVP_R8(a, 8), JVP_R8(b, 0), JVP_R8(b, 8), JVP_R8(c, 0), JVP_R8(c, 8),
+        JVP_R8(d, 0), JVP_R8(d, 8)
+      : "r"(ta), "r"(tb), "r"(tc), "r"(td)
+      : "memory");
+}
 #undef JVP_R8
 
 #define JVP_W8(a, i) "r"(a[i]), "r"(a[i + 1]), "r"(a[i + 2]), "r"(a[i + 3]), "r"(a[i + 4]), \
@@ -364,6 +383,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Maximum of three values in one instruction (the two-input rule for NaN).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // Packed two-wide fp32 arithmetic (one instruction for two lanes of data).
