@@ -49,8 +49,9 @@ def parse():
     ap.add_argument("--no-causal", action="store_true",
                     help="skip the causal companion timing of the default workload")
     ap.add_argument("--mode", default="fwd_dual",
-                    choices=["fwd_dual", "bwd_dual", "sweep", "memory"],
-                    help="fwd_dual (the headline), the backward of the dual computation, the "
+                    choices=["fwd_dual", "bwd_dual", "bwd", "sweep", "memory"],
+                    help="fwd_dual (the headline), the backward of the dual computation (bwd_dual) "
+                         "or of attention without tangents (bwd), the "
                          "sequence-length sweep (one JSON line per configuration) or the "
                          "memory-scaling report (one JSON line per N)")
     ap.add_argument("--sweep-dtypes", default="bf16,f16")
@@ -329,11 +330,14 @@ FP32_LANES_PER_SM = 128  # CUDA-core fp32 FMA lanes per SM (4 partitions x 32)
 
 
 def run_bwd(args, rank, world, local):
-    """Times jvp_attn_bwd_dual on one workload.
+    """Times jvp_attn_bwd_dual (--mode bwd_dual) or jvp_attn_bwd, the backward
+    of attention without tangents (--mode bwd), on one workload.
 
     fp16/bf16 inputs with D in {64, 128} run the row pre-pass and the tcgen05
-    kernels (query-major, then key-major: one launch at D = 64, value and key
-    parts at D = 128); other shapes run three CUDA-core kernels."""
+    kernels (query-major, then key-major: one launch at D = 64 and for the
+    primal, value and key parts for the dual at D = 128); other shapes run
+    three CUDA-core kernels."""
+    primal = args.mode == "bwd"
     import numpy as np
     import torch
 
@@ -348,14 +352,22 @@ def run_bwd(args, rank, world, local):
     causal = w.mask == "causal"
     inp = synth.make_inputs(w, with_cotangents=True, device=str(dev))
     g = [inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv]
-    o, t_o, lse, mu = api.fwd_dual(*g, attn_mask=inp.mask, is_causal=causal, return_stats=True)
     ws = torch.empty(max(1, api.bwd_dual_workspace_size(w.B, w.H, w.N, w.N, w.D)),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if primal:
+        o, lse = api.attention(*g[:3], attn_mask=inp.mask, is_causal=causal, return_lse=True)
 
-    def step():
-        return api.bwd_dual(*g, o, t_o, lse, mu, inp.g_o, inp.g_to, attn_mask=inp.mask,
-                            is_causal=causal, workspace=ws)
+        def step():
+            return api.bwd(*g[:3], o, lse, inp.g_o, attn_mask=inp.mask, is_causal=causal,
+                           workspace=ws)
+    else:
+        o, t_o, lse, mu = api.fwd_dual(*g, attn_mask=inp.mask, is_causal=causal,
+                                       return_stats=True)
+
+        def step():
+            return api.bwd_dual(*g, o, t_o, lse, mu, inp.g_o, inp.g_to, attn_mask=inp.mask,
+                                is_causal=causal, workspace=ws)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -365,7 +377,9 @@ def run_bwd(args, rank, world, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
-        with torch.cuda.nvtx.range(f"bwd_dual timed region: {args.steps} steps"):
+        for _ in range(4):  # device head start (see timed_steps)
+            flush.fill_(0.0)
+        with torch.cuda.nvtx.range(f"{args.mode} timed region: {args.steps} steps"):
             for s in range(args.steps):
                 flush.fill_(float(s))
                 starts[s].record(stream)
@@ -378,11 +392,15 @@ def run_bwd(args, rank, world, local):
     ms_step = total_ms / args.steps
     half = 0.5 if causal else 1.0
     bhnnd = w.B * w.H * w.N * w.N * w.D * half
-    alg_flops = 30.0 * bhnnd       # the 15 N x N x D products of the reverse mode
-    # Products executed (scores recomputed): 21 per (row, key, d) in the
-    # CUDA-core kernels and in the tensor-core kernels at D = 64; the D = 128
-    # key-major split recomputes the three score products once more (24).
-    exec_flops = (48.0 if (tensor_core and w.D == 128) else 42.0) * bhnnd
+    if primal:
+        alg_flops = 8.0 * bhnnd    # gO V^T, gS K, gS^T Q, P^T gO
+        exec_flops = 14.0 * bhnnd  # S and gO V^T formed in both kernels
+    else:
+        alg_flops = 30.0 * bhnnd   # the 15 N x N x D products of the reverse mode
+        # Products executed (scores recomputed): 21 per (row, key, d) in the
+        # CUDA-core kernels and in the tensor-core kernels at D = 64; the D = 128
+        # key-major split recomputes the three score products once more (24).
+        exec_flops = (48.0 if (tensor_core and w.D == 128) else 42.0) * bhnnd
     value = replicas.aggregate_throughput(world, alg_flops, args.steps, total_ms * 1e-3) / 1e12
     pk, pk_src = peaks()
     clk = pk.get("sm_max_mhz", 2070.0) * 1e6
@@ -391,15 +409,17 @@ def run_bwd(args, rank, world, local):
     achieved_exec = exec_flops / (ms_step * 1e-3) / 1e12
     if tensor_core:
         tc_peak = float(pk.get("bf16_tflops", 1900.0))  # fp16 and bf16 share the dense rate
-        launches = 3 if w.D == 64 else 4
+        launches = 3 if (w.D == 64 or primal) else 4
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": achieved / tc_peak, "traffic": None,
-                    "flops": "algorithmic: 30 B H Nq Nk D (half for causal), the 15 N x N x D "
-                             "products of the reverse mode",
+                    "flops": ("algorithmic: 8 B H Nq Nk D (half for causal), the four N x N x D "
+                              "products of the backward" if primal else
+                              "algorithmic: 30 B H Nq Nk D (half for causal), the 15 N x N x D "
+                              "products of the reverse mode"),
                     "achieved_executed": achieved_exec, "frac_executed": achieved_exec / tc_peak,
                     "peak_source": f"{pk_src} bf16 dense (cuBLAS burst)",
                     "kernel": "whole step: bwd_rows_kernel + bwd_q_tc_kernel + bwd_k_tc_kernel"
-                              + (" x2 (value, key parts)" if w.D == 128 else "")}
+                              + (" x2 (value, key parts)" if (w.D == 128 and not primal) else "")}
     else:
         alu_peak = n_sms * FP32_LANES_PER_SM * 2 * clk / 1e12
         launches = 3
@@ -410,7 +430,8 @@ def run_bwd(args, rank, world, local):
                                    f"{clk / 1e6:.0f} MHz (CUDA-core fp32)",
                     "kernel": "bwd_keys_kernel + bwd_queries_kernel + bwd_rows_kernel"}
     line = {
-        "metric": "bwd_dual (reverse mode of fwd+JVP attention) TFLOP/s", "mode": "bwd_dual",
+        "metric": ("bwd (backward of attention without tangents) TFLOP/s" if primal else
+                   "bwd_dual (reverse mode of fwd+JVP attention) TFLOP/s"), "mode": args.mode,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
@@ -426,10 +447,12 @@ def run_bwd(args, rank, world, local):
         # The float64 oracle's reverse mode on one whole head of the same workload.
         x = [t[:1, :1].double().cpu().numpy() for t in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv,
                                                          inp.g_o, inp.g_to)]
+        if primal:  # zero tangents and tangent cotangent: the primal backward
+            x = x[:3] + [np.zeros_like(a) for a in x[3:6]] + [x[6], np.zeros_like(x[7])]
         t0 = time.perf_counter()
         oracle.bwd_dual(*x, w.mask, None)
         dt = time.perf_counter() - t0
-        line["cpu_baseline"] = {"value": 30.0 * w.N * w.N * w.D * half / dt / 1e12,
+        line["cpu_baseline"] = {"value": alg_flops / (w.B * w.H) / dt / 1e12,
                                 "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                                 "sample": f"one (b, h) head of {name}, float64 reverse mode, "
                                           f"{dt:.1f} s wall (the oracle threads over heads)"}
@@ -481,7 +504,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     if args.mode in ("sweep", "memory"):
         return run_report(args, rank, world, local)
-    if args.mode == "bwd_dual":
+    if args.mode in ("bwd_dual", "bwd"):
         rc = run_bwd(args, rank, world, local)
         if world > 1:
             dist.barrier()

@@ -33,6 +33,8 @@ EXPORTS = (
     "jvp_attn_bwd_dual",
     "jvp_attn_bwd_dual_workspace_size",
     "jvp_attn_bwd_dual_noalloc",
+    "jvp_attn_bwd",
+    "jvp_attn_bwd_workspace_size",
     "jvp_attn_get_device_status",
     "jvp_attn_status_string",
     "jvp_attn_last_error",
@@ -115,6 +117,13 @@ def load(path: str | None = None):
         lib.jvp_attn_bwd_dual_noalloc.restype = i32
         lib.jvp_attn_bwd_dual_workspace_size.argtypes = [SP, i32]
         lib.jvp_attn_bwd_dual_workspace_size.restype = ctypes.c_size_t
+        # shape, dtype, q k v o lse g_o, in_strides, mask, scale, g_q g_k g_v,
+        # out_strides, workspace, bytes, stream
+        lib.jvp_attn_bwd.argtypes = [SP, i32] + [vp] * 6 + [STP, MP, f32] + [vp] * 3 + \
+            [STP, vp, ctypes.c_size_t, vp]
+        lib.jvp_attn_bwd.restype = i32
+        lib.jvp_attn_bwd_workspace_size.argtypes = [SP, i32]
+        lib.jvp_attn_bwd_workspace_size.restype = ctypes.c_size_t
         lib.jvp_attn_get_device_status.argtypes = [vp]
         lib.jvp_attn_get_device_status.restype = i32
         lib.jvp_attn_status_string.argtypes = [i32]

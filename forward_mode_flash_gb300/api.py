@@ -348,6 +348,49 @@ def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
     return tuple(outs)
 
 
+def bwd_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,
+                       dtype: torch.dtype = torch.bfloat16) -> int:
+    """Bytes of device scratch jvp_attn_bwd needs for this shape."""
+    shape = _abi.Shape(B, H, Nq, Nk, D)
+    return int(_abi.load().jvp_attn_bwd_workspace_size(ctypes.byref(shape), _DT[dtype]))
+
+
+def bwd(q, k, v, o, lse, g_o, attn_mask: Optional[torch.Tensor] = None, is_causal: bool = False,
+        scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None):
+    """Gradients of <g_o, O> with respect to (q, k, v): the backward of
+    attention without tangents.
+
+    o, lse are the outputs of ``attention(..., return_lse=True)`` (or of
+    ``fwd_dual``) on the same inputs.  ``workspace`` (uint8, on q's device) is
+    allocated here if not given; its size is ``bwd_workspace_size``.
+    """
+    lib = _abi.load()
+    hkv = _check_inputs([q, k, v, o, g_o], ["q", "k", "v", "o", "g_o"])
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    outs = [torch.empty_like(x) for x in (q, k, v)]
+    need = bwd_workspace_size(B, H, Nq, Nk, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
+    ins = (_abi.Strides * 5)(*[_strides(t) for t in (q, k, v, o, g_o)])
+    ost = (_abi.Strides * 3)(*[_strides(t) for t in outs])
+    shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = lib.jvp_attn_bwd(ctypes.byref(shape), _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v),
+                              _ptr(o), _ptr(lse), _ptr(g_o), ins, ctypes.byref(mask),
+                              float(scale), *[_ptr(x) for x in outs], ost, _ptr(workspace),
+                              workspace.numel() * workspace.element_size(),
+                              ctypes.c_void_p(stream))
+    _abi.check(st)
+    return tuple(outs)
+
+
 def fwd_dual_host(q, k, v, dq, dk, dv, attn_mask: Optional[torch.Tensor] = None,
                   is_causal: bool = False, scale: Optional[float] = None, chunks: int = 4,
                   device=None, out: Optional[Tuple[torch.Tensor, ...]] = None,

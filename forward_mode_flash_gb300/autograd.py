@@ -14,7 +14,8 @@ Mirrors the "JVP Flash Attention" project page (Usage section):
 * ``jvp_attention(q, k, v, attn_mask=None, is_causal=False, scale=None)`` is a
   drop-in for ``scaled_dot_product_attention``.  Under ``torch.func.jvp`` it
   takes the same fused route; elsewhere it is an autograd.Function whose
-  forward-mode rule calls ``fwd_dual`` and whose backward calls ``bwd_dual``.
+  forward-mode rule calls ``fwd_dual`` and whose backward calls the
+  primal-only ``bwd`` (no tangent terms).
 
 All arithmetic runs in the library's kernels; this module only wires them
 into autograd.
@@ -160,12 +161,11 @@ class JVPAttn(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, g_o, _g_lse):
+        # The primal-only backward (no tangent terms); lse is an auxiliary
+        # output whose cotangent is not propagated.
         q, k, v, o, lse = ctx.saved_tensors
-        zq, zk = torch.zeros_like(q), torch.zeros_like(k)
-        zmu = torch.zeros_like(lse)
-        g = api.bwd_dual(q, k, v, zq, zk, torch.zeros_like(v), o, torch.zeros_like(o), lse, zmu,
-                         _dense_cotangent(g_o, o), torch.zeros_like(o), attn_mask=ctx.attn_mask,
-                         is_causal=ctx.is_causal, scale=ctx.scale)
+        g = api.bwd(q, k, v, o, lse, _dense_cotangent(g_o, o), attn_mask=ctx.attn_mask,
+                    is_causal=ctx.is_causal, scale=ctx.scale)
         return g[0], g[1], g[2], None, None, None
 
     @staticmethod

@@ -16,6 +16,10 @@
 // (no gradient reaches the mask).  Each (i, j) term is recomputed from the
 // saved lse and mu, so nothing of size N x N is stored.
 //
+// The same kernels serve the backward of attention without tangents
+// (p.primal: dQ = dK = dV = gtO = 0, so nu = 0, delta = gO . O and only gQ,
+// gK, gV are written).
+//
 // Three kernels on the caller's stream:
 //   1. rows:   nu and delta per query row, into the workspace;
 //   2. keys:   one thread group per key (16 head-dim elements per thread),
@@ -116,14 +120,18 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(BwdParams p) {
   if (warp >= rows) return;
   const int i = warp % p.Nq, bh = warp / p.Nq, b = bh / p.H, h = bh % p.H;
   const T* o = row_ptr<T>(p.o, p.so, b, h, i);
-  const T* to = row_ptr<T>(p.t_o, p.sto, b, h, i);
   const T* go = row_ptr<T>(p.g_o, p.sgo, b, h, i);
-  const T* gto = row_ptr<T>(p.g_to, p.sgto, b, h, i);
   float nu = 0.f, a = 0.f;
-  for (int d = lane; d < p.D; d += 32) {
-    const float od = ld(o + d), gtod = ld(gto + d);
-    nu = fmaf(gtod, od, nu);
-    a = fmaf(ld(go + d), od, fmaf(gtod, ld(to + d), a));
+  if (p.primal) {  // no tangents: nu = 0, delta = gO . O
+    for (int d = lane; d < p.D; d += 32) a = fmaf(ld(go + d), ld(o + d), a);
+  } else {
+    const T* to = row_ptr<T>(p.t_o, p.sto, b, h, i);
+    const T* gto = row_ptr<T>(p.g_to, p.sgto, b, h, i);
+    for (int d = lane; d < p.D; d += 32) {
+      const float od = ld(o + d), gtod = ld(gto + d);
+      nu = fmaf(gtod, od, nu);
+      a = fmaf(ld(go + d), od, fmaf(gtod, ld(to + d), a));
+    }
   }
   for (int off = 16; off > 0; off >>= 1) {
     nu += __shfl_xor_sync(0xffffffffu, nu, off);
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(BwdParams p) {
   }
   if (lane == 0) {
     p.nu[warp] = nu;
-    p.delta[warp] = a - p.mu[warp] * nu;
+    p.delta[warp] = p.primal ? a : a - p.mu[warp] * nu;
   }
 }
 
@@ -184,10 +192,11 @@ __global__ void __launch_bounds__(kThreads) bwd_keys_kernel(BwdParams p, int par
   for (int e = 0; e < kPart; ++e) {
     const int d = part * kPart + e;
     const bool in = key_ok && d < D;
+    const bool tin = in && !p.primal;  // tangent inputs (absent in the primal)
     k_[e] = in ? ld(row_ptr<T>(p.k, p.sk, b, hk, j) + d) : 0.f;
-    dk_[e] = in ? ld(row_ptr<T>(p.dk, p.sdk, b, hk, j) + d) : 0.f;
+    dk_[e] = tin ? ld(row_ptr<T>(p.dk, p.sdk, b, hk, j) + d) : 0.f;
     v_[e] = in ? ld(row_ptr<T>(p.v, p.sv, b, hk, j) + d) : 0.f;
-    dv_[e] = in ? ld(row_ptr<T>(p.dv, p.sdv, b, hk, j) + d) : 0.f;
+    dv_[e] = tin ? ld(row_ptr<T>(p.dv, p.sdv, b, hk, j) + d) : 0.f;
     gk[e] = gdk[e] = gv[e] = gdv[e] = 0.f;
   }
 
@@ -203,9 +212,9 @@ __global__ void __launch_bounds__(kThreads) bwd_keys_kernel(BwdParams p, int par
     for (int x = threadIdx.x; x < ni * D; x += blockDim.x) {
       const int r = x / D, d = x % D, at = r * stride + sm_pos(d, parts);
       sQ[at] = ld(row_ptr<T>(p.q, p.sq, b, h, i0 + r) + d);
-      sdQ[at] = ld(row_ptr<T>(p.dq, p.sdq, b, h, i0 + r) + d);
+      sdQ[at] = p.primal ? 0.f : ld(row_ptr<T>(p.dq, p.sdq, b, h, i0 + r) + d);
       sgO[at] = ld(row_ptr<T>(p.g_o, p.sgo, b, h, i0 + r) + d);
-      sgtO[at] = ld(row_ptr<T>(p.g_to, p.sgto, b, h, i0 + r) + d);
+      sgtO[at] = p.primal ? 0.f : ld(row_ptr<T>(p.g_to, p.sgto, b, h, i0 + r) + d);
     }
     for (int x = threadIdx.x; x < stride * kChunk; x += blockDim.x) {
       // zero the padding of head dims beyond D so partial dots ignore it
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) bwd_keys_kernel(BwdParams p, int par
     }
     for (int r = threadIdx.x; r < ni; r += blockDim.x) {
       sRow[r] = p.lse[rbase + i0 + r];
-      sRow[kChunk + r] = p.mu[rbase + i0 + r];
+      sRow[kChunk + r] = p.primal ? 0.f : p.mu[rbase + i0 + r];
       sRow[2 * kChunk + r] = p.nu[rbase + i0 + r];
       sRow[3 * kChunk + r] = p.delta[rbase + i0 + r];
     }
@@ -271,9 +280,11 @@ __global__ void __launch_bounds__(kThreads) bwd_keys_kernel(BwdParams p, int par
     const int d = part * kPart + e;
     if (d < D) {
       st(static_cast<T*>(p.g_k) + b * p.sgk.b + hk * p.sgk.h + static_cast<long long>(j) * p.sgk.n + d, gk[e]);
-      st(static_cast<T*>(p.g_dk) + b * p.sgdk.b + hk * p.sgdk.h + static_cast<long long>(j) * p.sgdk.n + d, gdk[e]);
       st(static_cast<T*>(p.g_v) + b * p.sgv.b + hk * p.sgv.h + static_cast<long long>(j) * p.sgv.n + d, gv[e]);
-      st(static_cast<T*>(p.g_dv) + b * p.sgdv.b + hk * p.sgdv.h + static_cast<long long>(j) * p.sgdv.n + d, gdv[e]);
+      if (!p.primal) {
+        st(static_cast<T*>(p.g_dk) + b * p.sgdk.b + hk * p.sgdk.h + static_cast<long long>(j) * p.sgdk.n + d, gdk[e]);
+        st(static_cast<T*>(p.g_dv) + b * p.sgdv.b + hk * p.sgdv.h + static_cast<long long>(j) * p.sgdv.n + d, gdv[e]);
+      }
     }
   }
 }
@@ -301,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) bwd_queries_kernel(BwdParams p, int 
   const int D = p.D;
   const long long ridx = static_cast<long long>(bh) * p.Nq + (row_ok ? i : 0);
   const float lse = row_ok ? p.lse[ridx] : -INFINITY;
-  const float mu = row_ok ? p.mu[ridx] : 0.f;
+  const float mu = (row_ok && !p.primal) ? p.mu[ridx] : 0.f;
   const float nu = row_ok ? p.nu[ridx] : 0.f;
   const float delta = row_ok ? p.delta[ridx] : 0.f;
 
@@ -310,10 +321,11 @@ __global__ void __launch_bounds__(kThreads) bwd_queries_kernel(BwdParams p, int 
   for (int e = 0; e < kPart; ++e) {
     const int d = part * kPart + e;
     const bool in = row_ok && d < D;
+    const bool tin = in && !p.primal;  // tangent inputs (absent in the primal)
     q_[e] = in ? ld(row_ptr<T>(p.q, p.sq, b, h, i) + d) : 0.f;
-    dq_[e] = in ? ld(row_ptr<T>(p.dq, p.sdq, b, h, i) + d) : 0.f;
+    dq_[e] = tin ? ld(row_ptr<T>(p.dq, p.sdq, b, h, i) + d) : 0.f;
     go_[e] = in ? ld(row_ptr<T>(p.g_o, p.sgo, b, h, i) + d) : 0.f;
-    gto_[e] = in ? ld(row_ptr<T>(p.g_to, p.sgto, b, h, i) + d) : 0.f;
+    gto_[e] = tin ? ld(row_ptr<T>(p.g_to, p.sgto, b, h, i) + d) : 0.f;
     gq[e] = gdq[e] = 0.f;
   }
 
@@ -325,9 +337,9 @@ __global__ void __launch_bounds__(kThreads) bwd_queries_kernel(BwdParams p, int 
     for (int x = threadIdx.x; x < nj * D; x += blockDim.x) {
       const int r = x / D, d = x % D, at = r * stride + sm_pos(d, parts);
       sK[at] = ld(row_ptr<T>(p.k, p.sk, b, hk, j0 + r) + d);
-      sdK[at] = ld(row_ptr<T>(p.dk, p.sdk, b, hk, j0 + r) + d);
+      sdK[at] = p.primal ? 0.f : ld(row_ptr<T>(p.dk, p.sdk, b, hk, j0 + r) + d);
       sV[at] = ld(row_ptr<T>(p.v, p.sv, b, hk, j0 + r) + d);
-      sdV[at] = ld(row_ptr<T>(p.dv, p.sdv, b, hk, j0 + r) + d);
+      sdV[at] = p.primal ? 0.f : ld(row_ptr<T>(p.dv, p.sdv, b, hk, j0 + r) + d);
     }
     for (int x = threadIdx.x; x < stride * kChunk; x += blockDim.x) {
       const int q = x % stride;
@@ -380,7 +392,8 @@ __global__ void __launch_bounds__(kThreads) bwd_queries_kernel(BwdParams p, int 
     const int d = part * kPart + e;
     if (d < D) {
       st(static_cast<T*>(p.g_q) + b * p.sgq.b + h * p.sgq.h + static_cast<long long>(i) * p.sgq.n + d, gq[e]);
-      st(static_cast<T*>(p.g_dq) + b * p.sgdq.b + h * p.sgdq.h + static_cast<long long>(i) * p.sgdq.n + d, gdq[e]);
+      if (!p.primal)
+        st(static_cast<T*>(p.g_dq) + b * p.sgdq.b + h * p.sgdq.h + static_cast<long long>(i) * p.sgdq.n + d, gdq[e]);
     }
   }
 }

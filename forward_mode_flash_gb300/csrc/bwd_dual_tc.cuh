@@ -119,7 +119,11 @@ __device__ __forceinline__ BwdTerms bwd_terms(bool keep, float xm, float ds_raw,
   return r;
 }
 
-template <typename T, int D, int MASK>
+// PRIMAL: the backward of attention without tangents (dQ = dK = dV = 0 and
+// gtO = 0, so dS, G, g_dS and the tangent gradients vanish): only S = Q K^T
+// and gP1 = gO V^T are formed, gS = P (gP1 - delta), and gQ += gS K.  The
+// tangent operands are neither loaded nor multiplied.
+template <typename T, int D, int MASK, bool PRIMAL = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_q_tc_kernel(const __grid_constant__ BwdTcMaps maps, const BwdParams p, int group_heads,
                     unsigned int* status) {
@@ -189,13 +193,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&ctrl->q_full, 4 * L::QT_BYTES);
+      mbar_arrive_expect_tx(&ctrl->q_full, (PRIMAL ? 2 : 4) * L::QT_BYTES);
       for (int c = 0; c < L::KCH; ++c) {
         const int o = c * BM * 128;
         tma_load_4d(smem + L::OFF_Q + o, &maps.q, &ctrl->q_full, c * 64, q0, h, b);
-        tma_load_4d(smem + L::OFF_DQ + o, &maps.dq, &ctrl->q_full, c * 64, q0, h, b);
         tma_load_4d(smem + L::OFF_GO + o, &maps.go, &ctrl->q_full, c * 64, q0, h, b);
-        tma_load_4d(smem + L::OFF_GTO + o, &maps.gto, &ctrl->q_full, c * 64, q0, h, b);
+        if (!PRIMAL) {
+          tma_load_4d(smem + L::OFF_DQ + o, &maps.dq, &ctrl->q_full, c * 64, q0, h, b);
+          tma_load_4d(smem + L::OFF_GTO + o, &maps.gto, &ctrl->q_full, c * 64, q0, h, b);
+        }
       }
       int kf = 0, vf = 0;
       for (int t = 0; t < n_kv; ++t) {
@@ -206,11 +212,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         uint8_t* kb = smem + L::OFF_K + sk * L::KBLK;
-        mbar_arrive_expect_tx(&ctrl->k_full[sk], L::KBLK);
+        mbar_arrive_expect_tx(&ctrl->k_full[sk], PRIMAL ? L::KBLK / 2 : L::KBLK);
         for (int c = 0; c < L::KCH; ++c) {
           tma_load_4d(kb + c * L::KCHUNK, &maps.k, &ctrl->k_full[sk], c * 64, j0, hk, b);
-          tma_load_4d(kb + c * L::KCHUNK + BN * 128, &maps.dk, &ctrl->k_full[sk], c * 64, j0, hk,
-                      b);
+          if (!PRIMAL)
+            tma_load_4d(kb + c * L::KCHUNK + BN * 128, &maps.dk, &ctrl->k_full[sk], c * 64, j0, hk,
+                        b);
         }
         ++kf;
         if (!mbar_wait(&ctrl->v_empty[sv], ((t / NSV) & 1) ^ 1, abort)) {
@@ -218,11 +225,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         uint8_t* vb = smem + L::OFF_V + sv * L::KBLK;
-        mbar_arrive_expect_tx(&ctrl->v_full[sv], L::KBLK);
+        mbar_arrive_expect_tx(&ctrl->v_full[sv], PRIMAL ? L::KBLK / 2 : L::KBLK);
         for (int c = 0; c < L::KCH; ++c) {
           tma_load_4d(vb + c * L::KCHUNK, &maps.v, &ctrl->v_full[sv], c * 64, j0, hk, b);
-          tma_load_4d(vb + c * L::KCHUNK + BN * 128, &maps.dv, &ctrl->v_full[sv], c * 64, j0, hk,
-                      b);
+          if (!PRIMAL)
+            tma_load_4d(vb + c * L::KCHUNK + BN * 128, &maps.dv, &ctrl->v_full[sv], c * 64, j0, hk,
+                        b);
         }
         ++vf;
       }
@@ -253,16 +261,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const uint32_t kb = smem_u32(smem + L::OFF_K + sk * L::KBLK);
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // [S | Q dK^T] = Q [K ; dK]^T
+        for (int kk = 0; kk < KSD; ++kk) {  // [S | Q dK^T] = Q [K ; dK]^T  (primal: S = Q K^T)
           const uint32_t off = (kk & 3) * 32;
           mma_ss(tmem + L::TM_S, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + off, 16, 1024),
-                 sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N128, kk > 0);
+                 sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024),
+                 PRIMAL ? I_N64 : I_N128, kk > 0);
         }
+        if (!PRIMAL) {
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // Q dK^T += dQ K^T
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_DS, sdesc_sw128(adQ + (kk >> 2) * BM * 128 + off, 16, 1024),
-                 sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
+          for (int kk = 0; kk < KSD; ++kk) {  // Q dK^T += dQ K^T
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(tmem + L::TM_DS, sdesc_sw128(adQ + (kk >> 2) * BM * 128 + off, 16, 1024),
+                   sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
+          }
         }
         mma_commit(&ctrl->s_full);
         if (!mbar_wait(&ctrl->p_full, t & 1, abort)) {
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // gS and g_dS of keys [16 kk, 16 kk + 16) (warpgroup kk / 2, half
         // kk % 2): gS at columns 16 kk, g_dS at 16 kk + 8.
 #pragma unroll
-        for (int kk = 0; kk < KSN; ++kk) {
+        for (int kk = 0; kk < KSN && !PRIMAL; ++kk) {
           const uint32_t a_gs = tmem + kk * 16;
           const uint32_t a_gds = a_gs + 8;
           const uint32_t kx = kb + kk * 16 * 128;  // MN-major: 16 keys per K-step
@@ -289,11 +300,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
 #pragma unroll
-        for (int kk = 0; kk < KSN; ++kk) {  // gQ += gS K
+        for (int kk = 0; kk < KSN; ++kk) {  // gQ += gS K  (the first products of the primal)
           const uint32_t a_gs = tmem + kk * 16;
           mma_ts(tmem + L::TM_ACC + D, a_gs,
                  sdesc_sw128(kb + kk * 16 * 128, D == 64 ? BN * 128 : L::KCHUNK, 1024), I_ACC1,
-                 1u);
+                 PRIMAL ? ((t > 0 || kk > 0) ? 1u : 0u) : 1u);
         }
         mma_commit(&ctrl->k_empty[sk]);
       }
@@ -320,17 +331,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + L::OFF_V + sv * L::KBLK);
+        if (!PRIMAL) {
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // [G | gtO dV^T] = gtO [V ; dV]^T
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_G, sdesc_sw128(aGTO + (kk >> 2) * BM * 128 + off, 16, 1024),
-                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N128, kk > 0);
+          for (int kk = 0; kk < KSD; ++kk) {  // [G | gtO dV^T] = gtO [V ; dV]^T
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(tmem + L::TM_G, sdesc_sw128(aGTO + (kk >> 2) * BM * 128 + off, 16, 1024),
+                   sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N128, kk > 0);
+          }
         }
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // gtO dV^T += gO V^T
+        for (int kk = 0; kk < KSD; ++kk) {  // gtO dV^T += gO V^T  (primal: gP1 = gO V^T)
           const uint32_t off = (kk & 3) * 32;
           mma_ss(tmem + L::TM_GP, sdesc_sw128(aGO + (kk >> 2) * BM * 128 + off, 16, 1024),
-                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
+                 sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64,
+                 PRIMAL ? (kk > 0 ? 1u : 0u) : 1u);
         }
         mma_commit(&ctrl->v_empty[sv]);
         mma_commit(&ctrl->s_full);
@@ -354,8 +368,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float lse = rd ? p.lse[ridx] : -INFINITY;
     const float lse2 = lse * kLog2e;
     const bool live = rd && lse != -INFINITY;
-    const float mu = rd ? p.mu[ridx] : 0.f;
-    const float nu = rd ? p.nu[ridx] : 0.f;
+    const float mu = (rd && !PRIMAL) ? p.mu[ridx] : 0.f;
+    const float nu = (rd && !PRIMAL) ? p.nu[ridx] : 0.f;
     const float delta = rd ? p.delta[ridx] : 0.f;
     const float c = p.scale * kLog2e;
     const float s = p.scale;
@@ -381,7 +395,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t rs[16], rds[16], rg[16], rgp[16];
       const bool cols_ok = JVP_CHECK(L::TM_GP + col + 16 <= 512u && L::TM_DS + col + 16 <= 512u,
                                      status, kChkTmem);
-      if (cols_ok) {
+      if (PRIMAL) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) rds[e] = rg[e] = 0u;  // dS = G = 0
+        if (cols_ok) tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_GP + col, rs, rgp);
+      } else if (cols_ok) {
         tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_DS + col, rs, rds);
         tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
       }
@@ -411,7 +429,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (cols_ok) {
         tmem_st8(lb + col, pgs);
-        tmem_st8(lb + col + 8, pgds);
+        if (!PRIMAL) tmem_st8(lb + col + 8, pgds);
       }
     };
     for (int t = 0; t < n_kv; ++t) {
@@ -431,9 +449,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(&ctrl->p_full);
     }
     if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, status, abort);
-    if (ok) {
+    if (ok && !(PRIMAL && wg == 0)) {
       tc_fence_after();
-      // Warpgroup 0 writes g_dQ, warpgroup 1 writes gQ (both scaled by s).
+      // Warpgroup 0 writes g_dQ, warpgroup 1 writes gQ (both scaled by s);
+      // the primal has gQ alone.
       void* dst = wg == 0 ? p.g_dq : p.g_q;
       const Strides& ds = wg == 0 ? p.sgdq : p.sgq;
       T* row = static_cast<T*>(dst) + static_cast<long long>(b) * ds.b +
@@ -483,21 +502,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // While the elementwise warps work on tile t, the score MMAs of tile t + 1
 // fill the other buffer.  Shared memory: the resident key-side tiles, NS
 // stages of query-side tiles, the stages' row scalars, the control block.
-template <int D, int PART>
+//
+// PRIMAL (with PART = 3, at either D): the backward of attention without
+// tangents.  A tile's buffer is [S^T | gP1^T] (BQ = 64 query rows, gP1 =
+// gO V^T), the resident key-side tiles are K and V, a stage holds [Q] and
+// [gO], and the accumulators are gV = P^T gO and gK = gS^T Q (2D columns, so
+// one pass fits TMEM at D = 128 too).
+template <int D, int PART, bool PRIMAL = false>
 struct BkLayout {
   static constexpr bool kV = (PART & 1) != 0;
   static constexpr bool kK = (PART & 2) != 0;
-  static constexpr int BK = 128;          // keys per CTA
-  static constexpr int NSC = kK ? 4 : 2;  // score matrices per tile
+  static constexpr int BK = 128;                          // keys per CTA
+  static constexpr int NSC = (kK && !PRIMAL) ? 4 : 2;     // score matrices per tile
   static constexpr int BQ = 128 / NSC;    // query rows per tile (a buffer is 128 columns)
   static constexpr int KCH = D / 64;
   static constexpr int KT_BYTES = KCH * BK * 128;  // one [128 x D] key-side tile
-  static constexpr int QCHUNK = 2 * BQ * 128;      // [X rows | Y rows] of one 64-column chunk
+  // [X rows | Y rows] of one 64-column chunk (primal: X rows alone)
+  static constexpr int QCHUNK = (PRIMAL ? 1 : 2) * BQ * 128;
   static constexpr int QBLK = KCH * QCHUNK;        // a [X ; Y] block of one stage
-  // key-side tiles resident for the whole CTA: K and dK always, V and dV for the key part
+  // key-side tiles resident for the whole CTA: K and dK always, V and dV for
+  // the key part (primal: K and V)
   static constexpr int OFF_K = 0, OFF_DK = KT_BYTES;
-  static constexpr int OFF_V = 2 * KT_BYTES, OFF_DV = 3 * KT_BYTES;
-  static constexpr int KSIDE = (kK ? 4 : 2) * KT_BYTES;
+  static constexpr int OFF_V = (PRIMAL ? 1 : 2) * KT_BYTES, OFF_DV = 3 * KT_BYTES;
+  static constexpr int KSIDE = (PRIMAL ? 2 : kK ? 4 : 2) * KT_BYTES;
   // per stage: [Q ; dQ] and [gtO ; gO]; the row scalars (a float4 per query
   // row) of each stage live in a separate array so stages stay 1 KB aligned
   static constexpr int STAGE = 2 * QBLK;
@@ -515,7 +542,8 @@ struct BkLayout {
   static_assert(NS >= 3 || D == 64 || !kK, "three stages for the key part");
   static_assert(NS >= 2, "two stages at least");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(D == 64 || PART != 3, "the four accumulators fit TMEM only at D = 64");
+  static_assert(D == 64 || PART != 3 || PRIMAL, "the four accumulators fit TMEM only at D = 64");
+  static_assert(!PRIMAL || PART == 3, "the primal computes both key-side gradients in one pass");
   // Value part alone: the score products read only a stage's [Q ; dQ] half
   // and the accumulate products only its [gtO ; gO] half, so the two halves
   // have their own barriers and [Q ; dQ] is released (and refilled, one tile
@@ -535,11 +563,11 @@ struct BwdKCtrl {
   int abort;
 };
 
-template <typename T, int D, int MASK, int PART>
+template <typename T, int D, int MASK, int PART, bool PRIMAL = false>
 __global__ void __launch_bounds__(kBwdThreadsK, 1)
     bwd_k_tc_kernel(const __grid_constant__ BwdTcMaps maps, const BwdParams p, int group_heads,
                     unsigned int* status) {
-  using L = BkLayout<D, PART>;
+  using L = BkLayout<D, PART, PRIMAL>;
   constexpr int NS = L::NS, BK = L::BK, BQ = L::BQ;
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSD = D / 16;
@@ -549,8 +577,9 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
   constexpr uint32_t I_ACC2 = idesc_f16(kBF16, 128, 2 * D, true);
   constexpr uint32_t I_ACC1 = idesc_f16(kBF16, 128, D, true);
   // Accumulator columns (relative to TM_ACC)
-  constexpr uint32_t A_GDV = 0, A_GV = D;                        // value part
-  constexpr uint32_t A_GDK = L::kV ? 2 * D : 0, A_GK = A_GDK + D;  // key part
+  constexpr uint32_t A_GDV = 0, A_GV = PRIMAL ? 0 : D;              // value part
+  constexpr uint32_t A_GDK = L::kV ? 2 * D : 0;                      // key part
+  constexpr uint32_t A_GK = PRIMAL ? D : A_GDK + D;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -617,14 +646,18 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
     // scalars (lse * log2 e, mu, nu, delta per query row; rows past Nq get
     // lse = -inf) and lane 0 adds the second arrival on q_full.
     if (lane == 0) {
-      mbar_arrive_expect_tx(&ctrl->k_full, (L::kK ? 4 : 2) * L::KT_BYTES);
+      mbar_arrive_expect_tx(&ctrl->k_full, L::KSIDE);
       for (int c = 0; c < L::KCH; ++c) {
         const int o = c * BK * 128;
         tma_load_4d(smem + L::OFF_K + o, &maps.k, &ctrl->k_full, c * 64, j0, hk, b);
-        tma_load_4d(smem + L::OFF_DK + o, &maps.dk, &ctrl->k_full, c * 64, j0, hk, b);
-        if (L::kK) {
+        if (PRIMAL) {
           tma_load_4d(smem + L::OFF_V + o, &maps.v, &ctrl->k_full, c * 64, j0, hk, b);
-          tma_load_4d(smem + L::OFF_DV + o, &maps.dv, &ctrl->k_full, c * 64, j0, hk, b);
+        } else {
+          tma_load_4d(smem + L::OFF_DK + o, &maps.dk, &ctrl->k_full, c * 64, j0, hk, b);
+          if (L::kK) {
+            tma_load_4d(smem + L::OFF_V + o, &maps.v, &ctrl->k_full, c * 64, j0, hk, b);
+            tma_load_4d(smem + L::OFF_DV + o, &maps.dv, &ctrl->k_full, c * 64, j0, hk, b);
+          }
         }
       }
     }
@@ -646,9 +679,9 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         if (i < p.Nq && JVP_CHECK(h < p.H, status, kChkGlobalRow)) {
           const long long idx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
           v.x = p.lse[idx] * kLog2e;
-          v.y = p.mu[idx];
+          if (!PRIMAL) v.y = p.mu[idx];
           if (L::kK) {
-            v.z = p.nu[idx];
+            if (!PRIMAL) v.z = p.nu[idx];
             v.w = p.delta[idx];
           }
         }
@@ -698,6 +731,11 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
           mbar_arrive_expect_tx(&ctrl->q_full[s], 2 * L::QBLK);
         }
         for (int c = 0; c < L::KCH; ++c) {
+          if (PRIMAL) {  // [Q] then [gO]
+            tma_load_4d(st + c * L::QCHUNK, mq, &ctrl->q_full[s], c * 64, i0, h, b);
+            tma_load_4d(st + L::QBLK + c * L::QCHUNK, mgo, &ctrl->q_full[s], c * 64, i0, h, b);
+            continue;
+          }
           if (!L::kSplitStage) {
             tma_load_4d(st + c * L::QCHUNK, mq, &ctrl->q_full[s], c * 64, i0, h, b);
             tma_load_4d(st + c * L::QCHUNK + BQ * 128, mdq, &ctrl->q_full[s], c * 64, i0, h, b);
@@ -740,16 +778,19 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         const uint32_t qb = smem_u32(smem + L::OFF_ST + s * L::STAGE);  // [Q ; dQ]
         const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // [S^T | K dQ^T] = K [Q ; dQ]^T
+        for (int kk = 0; kk < KSD; ++kk) {  // [S^T | K dQ^T] = K [Q ; dQ]^T  (primal: S^T = K Q^T)
           const uint32_t off = (kk & 3) * 32;
           mma_ss(buf + L::S_OFF, sdesc_sw128(aK + (kk >> 2) * BK * 128 + off, 16, 1024),
-                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N2Q, kk > 0);
+                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024),
+                 PRIMAL ? I_NQ : I_N2Q, kk > 0);
         }
+        if (!PRIMAL) {
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // K dQ^T += dK Q^T  (= dS_raw^T)
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(buf + L::DS_OFF, sdesc_sw128(adK + (kk >> 2) * BK * 128 + off, 16, 1024),
-                 sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
+          for (int kk = 0; kk < KSD; ++kk) {  // K dQ^T += dK Q^T  (= dS_raw^T)
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(buf + L::DS_OFF, sdesc_sw128(adK + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(qb + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
+          }
         }
         if (L::kSplitStage) mma_commit(&ctrl->qq_empty[s]);
         mma_commit(&ctrl->s_full[t & 1]);
@@ -789,8 +830,20 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
         // A operands of query rows [16 kk, 16 kk + 16) of the tile: P^T at
         // buffer column 16 kk (dP^T at + 8), gS^T at DS_OFF + 16 kk (g_dS^T at + 8).
+        if constexpr (PRIMAL) {
+          // gV += P^T gO ; gK += gS^T Q  (P^T at buffer column 16 kk, gS^T at
+          // DS_OFF + 16 kk; [Q] and [gO] chunks QCHUNK apart)
 #pragma unroll
-        for (int kk = 0; kk < KSQ; ++kk) {
+          for (int kk = 0; kk < KSQ; ++kk) {
+            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tmem + L::TM_ACC + A_GV, buf + kk * 16,
+                   sdesc_sw128(ob + kk * 16 * 128, L::QCHUNK, 1024), I_ACC1, acc);
+            mma_ts(tmem + L::TM_ACC + A_GK, buf + L::DS_OFF + kk * 16,
+                   sdesc_sw128(qb + kk * 16 * 128, L::QCHUNK, 1024), I_ACC1, acc);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < KSQ && !PRIMAL; ++kk) {
           const uint32_t a0 = buf + kk * 16;
           const uint32_t ag = buf + L::DS_OFF + kk * 16;
           const uint32_t xq = qb + kk * 16 * 128;  // MN-major: 16 query rows per K-step
@@ -818,7 +871,7 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
           }
         }
 #pragma unroll
-        for (int kk = 0; kk < KSQ; ++kk) {
+        for (int kk = 0; kk < KSQ && !PRIMAL; ++kk) {
           const uint32_t a0 = buf + kk * 16;
           const uint32_t ag = buf + L::DS_OFF + kk * 16;
           if (L::kV)  // gV += dP^T gtO
@@ -859,17 +912,26 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         tc_fence_after();
         const uint32_t ob = smem_u32(smem + L::OFF_ST + s * L::STAGE) + L::QBLK;  // [gtO ; gO]
         const uint32_t buf = tmem + (t & 1) * L::TM_BUF;
+        if (PRIMAL) {
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // [G^T | V gO^T] = V [gtO ; gO]^T
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(buf + L::G_OFF, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
-                 sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N2Q, kk > 0);
-        }
+          for (int kk = 0; kk < KSD; ++kk) {  // gP1^T = V gO^T
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(buf + L::DS_OFF, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, kk > 0);
+          }
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < KSD; ++kk) {  // V gO^T += dV gtO^T  (= gP1^T)
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(buf + L::GP_OFF, sdesc_sw128(adV + (kk >> 2) * BK * 128 + off, 16, 1024),
-                 sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
+          for (int kk = 0; kk < KSD; ++kk) {  // [G^T | V gO^T] = V [gtO ; gO]^T
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(buf + L::G_OFF, sdesc_sw128(aV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_N2Q, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < KSD; ++kk) {  // V gO^T += dV gtO^T  (= gP1^T)
+            const uint32_t off = (kk & 3) * 32;
+            mma_ss(buf + L::GP_OFF, sdesc_sw128(adV + (kk >> 2) * BK * 128 + off, 16, 1024),
+                   sdesc_sw128(ob + (kk >> 2) * L::QCHUNK + off, 16, 1024), I_NQ, 1u);
+          }
         }
         mma_commit(&ctrl->s_full[t & 1]);
       }
@@ -914,11 +976,15 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         // read (S^T at col, dS^T at DS_OFF + col), so the other halves' inputs stay intact.
         const uint32_t col = bcol + hq * 16;
         uint32_t rs[16], rds[16], rg[16], rgp[16];
-        const uint32_t top = L::kK ? L::GP_OFF : L::DS_OFF;
+        const uint32_t top = (L::kK && !PRIMAL) ? L::GP_OFF : L::DS_OFF;
         const bool cols_ok = JVP_CHECK(col + top + 16 <= 512u && col + L::DS_OFF + 16 <= 512u &&
                                            wg * QW + hq * 16 + 16 <= L::SCAL_BYTES / 16,
                                        status, kChkTmem);
-        if (cols_ok) {
+        if (PRIMAL) {  // S^T and gP1^T; dS = G = 0
+#pragma unroll
+          for (int e = 0; e < 16; ++e) rds[e] = rg[e] = 0u;
+          if (cols_ok) tmem_ld16x2(lb + col + L::S_OFF, lb + col + L::DS_OFF, rs, rgp);
+        } else if (cols_ok) {
           tmem_ld16x2(lb + col + L::S_OFF, lb + col + L::DS_OFF, rs, rds);
           if (L::kK) tmem_ld16x2(lb + col + L::G_OFF, lb + col + L::GP_OFF, rg, rgp);
         }
@@ -960,11 +1026,11 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         }
         if (L::kV && cols_ok) {
           tmem_st8(lb + col + L::S_OFF, pa);
-          tmem_st8(lb + col + L::S_OFF + 8, pb);
+          if (!PRIMAL) tmem_st8(lb + col + L::S_OFF + 8, pb);
         }
         if (L::kK && cols_ok) {
           tmem_st8(lb + col + L::DS_OFF, pc);
-          tmem_st8(lb + col + L::DS_OFF + 8, pd);
+          if (!PRIMAL) tmem_st8(lb + col + L::DS_OFF + 8, pd);
         }
       }
       tmem_st_wait();
@@ -975,11 +1041,12 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
     if (ok) {
       tc_fence_after();
       // Output tensors of this kernel, split between the two warpgroups.
-      constexpr int NOUT = (L::kV ? 2 : 0) + (L::kK ? 2 : 0);
+      constexpr int NOUT = PRIMAL ? 2 : (L::kV ? 2 : 0) + (L::kK ? 2 : 0);
 #pragma unroll 1
       for (int oi = wg; oi < NOUT; oi += 2) {
-        // oi enumerates g_dV, gV (value part) then g_dK, gK (key part)
-        const int which = L::kV ? oi : oi + 2;
+        // oi enumerates g_dV, gV (value part) then g_dK, gK (key part); the
+        // primal's are gV and gK
+        const int which = PRIMAL ? 2 * oi + 1 : L::kV ? oi : oi + 2;
         void* dst = which == 0 ? p.g_dv : which == 1 ? p.g_v : which == 2 ? p.g_dk : p.g_k;
         const Strides& ds = which == 0 ? p.sgdv : which == 1 ? p.sgv : which == 2 ? p.sgdk : p.sgk;
         const uint32_t acol = which == 0 ? A_GDV : which == 1 ? A_GV : which == 2 ? A_GDK : A_GK;
@@ -1038,14 +1105,14 @@ cudaError_t set_smem(int bytes) {
 
 // qmaps: query-major kernel (query side 128-row boxes, key side 64); kmaps:
 // key-major kernel (key side 128-row boxes, query side 32, and 64 in q64 ...).
-template <typename T, int D, int MASK>
+template <typename T, int D, int MASK, bool PRIMAL>
 cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
                                   const BwdParams& p, int num_sms, unsigned int* status,
                                   cudaStream_t stream) {
   const int BH = p.B * p.H;
   {
     using L = BqLayout<D>;
-    constexpr auto kern = bwd_q_tc_kernel<T, D, MASK>;
+    constexpr auto kern = bwd_q_tc_kernel<T, D, MASK, PRIMAL>;
     cudaError_t e = set_smem<kern>(L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int nq = (p.Nq + L::BM - 1) / L::BM;
@@ -1057,8 +1124,8 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
   }
   auto key_side = [&](auto part_tag) -> cudaError_t {
     constexpr int PART = decltype(part_tag)::value;
-    using L = BkLayout<D, PART>;
-    constexpr auto kern = bwd_k_tc_kernel<T, D, MASK, PART>;
+    using L = BkLayout<D, PART, PRIMAL>;
+    constexpr auto kern = bwd_k_tc_kernel<T, D, MASK, PART, PRIMAL>;
     cudaError_t e = set_smem<kern>(L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int nk = (p.Nk + L::BK - 1) / L::BK;
@@ -1069,7 +1136,7 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
            stream>>>(kmaps, p, G, status);
     return cudaGetLastError();
   };
-  if constexpr (D == 64) {
+  if constexpr (D == 64 || PRIMAL) {
     return key_side(std::integral_constant<int, 3>{});
   } else {
     cudaError_t e = key_side(std::integral_constant<int, 1>{});
@@ -1078,19 +1145,23 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool PRIMAL = false>
 cudaError_t launch_bwd_tc_dispatch(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
                                    const BwdParams& p, int num_sms, unsigned int* status,
                                    cudaStream_t stream) {
   switch (mask_kind) {
     case kMaskNone:
-      return launch_bwd_tc_variant<T, D, kMaskNone>(qmaps, kmaps, p, num_sms, status, stream);
+      return launch_bwd_tc_variant<T, D, kMaskNone, PRIMAL>(qmaps, kmaps, p, num_sms, status,
+                                                            stream);
     case kMaskBool:
-      return launch_bwd_tc_variant<T, D, kMaskBool>(qmaps, kmaps, p, num_sms, status, stream);
+      return launch_bwd_tc_variant<T, D, kMaskBool, PRIMAL>(qmaps, kmaps, p, num_sms, status,
+                                                            stream);
     case kMaskAdditive:
-      return launch_bwd_tc_variant<T, D, kMaskAdditive>(qmaps, kmaps, p, num_sms, status, stream);
+      return launch_bwd_tc_variant<T, D, kMaskAdditive, PRIMAL>(qmaps, kmaps, p, num_sms, status,
+                                                                stream);
     case kMaskCausal:
-      return launch_bwd_tc_variant<T, D, kMaskCausal>(qmaps, kmaps, p, num_sms, status, stream);
+      return launch_bwd_tc_variant<T, D, kMaskCausal, PRIMAL>(qmaps, kmaps, p, num_sms, status,
+                                                              stream);
   }
   return cudaErrorInvalidValue;
 }

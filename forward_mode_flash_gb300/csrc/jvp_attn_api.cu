@@ -381,12 +381,13 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   return ok();
 }
 
-// Body of jvp_attn_bwd_dual.
-jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* const* in,
-                      const float* lse, const float* mu, const jvp_strides_t* in_strides,
-                      const jvp_mask_t* mask, float scale, void* const* out,
-                      const jvp_strides_t* out_strides, void* workspace, size_t ws_bytes,
-                      void* stream_ptr) {
+// Body of jvp_attn_bwd_dual and (primal = true: the tangent inputs dq, dk,
+// dv, t_o, g_to, mu and outputs g_dq, g_dk, g_dv are absent) jvp_attn_bwd.
+jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
+                      const void* const* in, const float* lse, const float* mu,
+                      const jvp_strides_t* in_strides, const jvp_mask_t* mask, float scale,
+                      void* const* out, const jvp_strides_t* out_strides, void* workspace,
+                      size_t ws_bytes, void* stream_ptr) {
   t_last_path = 0;
   if (!shape) return fail(JVP_ERR_INVALID_ARG, "shape is NULL");
   const int64_t B = shape->B, H = shape->H, Nq = shape->Nq, Nk = shape->Nk, D = shape->D;
@@ -433,19 +434,23 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   }
   if (q_rows == 0 && k_rows == 0) return ok();  // nothing to compute
   const size_t e = elem_size(dtype);
+  // tangent-side entries: inputs dq dk dv t_o g_to, outputs g_dq g_dk g_dv
+  auto tangent_in = [](int t) { return t == 3 || t == 4 || t == 5 || t == 7 || t == 9; };
   for (int t = 0; t < 10; ++t) {
+    if (primal && tangent_in(t)) continue;
     const bool on_keys = (t == 1 || t == 2 || t == 4 || t == 5);
     if (!in[t] && (!on_keys || Nk > 0) && (on_keys || Nq > 0))
       return fail(JVP_ERR_INVALID_ARG, "input pointer is NULL");
     if (!aligned(in[t], e)) return fail(JVP_ERR_ALIGNMENT, "input not aligned to its element size");
   }
-  for (int t = 0; t < 6; ++t) {
+  for (int t = 0; t < (primal ? 3 : 6); ++t) {
     const bool on_keys = (t == 1 || t == 2 || t == 4 || t == 5);
     if (!out[t] && (!on_keys || Nk > 0) && (on_keys || Nq > 0))
       return fail(JVP_ERR_INVALID_ARG, "output pointer is NULL");
     if (!aligned(out[t], e)) return fail(JVP_ERR_ALIGNMENT, "output not aligned to its element size");
   }
-  if (Nq > 0 && (!lse || !mu)) return fail(JVP_ERR_INVALID_ARG, "lse and mu are required");
+  if (Nq > 0 && !lse) return fail(JVP_ERR_INVALID_ARG, "lse is required");
+  if (Nq > 0 && !primal && !mu) return fail(JVP_ERR_INVALID_ARG, "lse and mu are required");
   if (!aligned(lse, 4) || !aligned(mu, 4)) return fail(JVP_ERR_ALIGNMENT, "lse/mu not 4-byte aligned");
   const size_t need = bwd_workspace_bytes(q_rows);
   if (need > 0 && (!workspace || ws_bytes < need))
@@ -477,6 +482,7 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   for (int t = 0; t < 6; ++t) *sout[t] = to_strides(out_strides[t]);
   p.nu = static_cast<float*>(workspace);
   p.delta = p.nu + q_rows;
+  p.primal = primal ? 1 : 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, at least one row and
@@ -501,6 +507,7 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
     CUtensorMap* kdst_q64[4] = {&km.q64, &km.dq64, &km.go64, &km.gto64};
     CUtensorMap* kdst_k[4] = {&km.k, &km.dk, &km.v, &km.dv};
     for (int u = 0; tc && u < 4; ++u) {
+      if (primal && (u == 1 || u == 3)) continue;  // dq/dk and g_to/dv: absent
       const int a = qidx[u], c = kidx[u];
       tc = encode_map(qdst_q[u], dtype, in[a], B, H, Ns[a], D, in_strides[a], 128) &&
            encode_map(qdst_k[u], dtype, in[c], B, Hkv, Ns[c], D, in_strides[c], 64) &&
@@ -513,7 +520,7 @@ jvp_status_t backward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* c
   if (tc) {
     err = launch_bwd_rows(static_cast<DType>(dtype), p, stream);
     if (err == cudaSuccess)
-      err = launch_bwd_tc(static_cast<DType>(dtype), D <= 64 ? 64 : 128, kind, qm, km, p,
+      err = launch_bwd_tc(static_cast<DType>(dtype), D <= 64 ? 64 : 128, kind, primal, qm, km, p,
                           dev->num_sms, dev->status, stream);
     t_last_path = 1;
   } else {
@@ -546,9 +553,20 @@ cudaError_t launch_fwd_tc(DType dt, int D, int mask_kind, bool tangent, const Tc
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, const BwdTcMaps& qmaps,
+cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, bool primal, const BwdTcMaps& qmaps,
                           const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
                           unsigned int* status, cudaStream_t stream) {
+  if (primal) {
+    if (dt == kF16 && D == 64)
+      return launch_bwd_primal_tc_f16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+    if (dt == kF16 && D == 128)
+      return launch_bwd_primal_tc_f16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+    if (dt == kBF16 && D == 64)
+      return launch_bwd_primal_tc_bf16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+    if (dt == kBF16 && D == 128)
+      return launch_bwd_primal_tc_bf16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+    return cudaErrorInvalidValue;
+  }
   if (dt == kF16 && D == 64)
     return launch_bwd_tc_f16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
   if (dt == kF16 && D == 128)
@@ -626,8 +644,31 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
                                void* workspace, size_t workspace_bytes, void* stream) {
   const void* in[10] = {q, k, v, dq, dk, dv, o, t_o, g_o, g_to};
   void* out[6] = {g_q, g_k, g_v, g_dq, g_dk, g_dv};
-  return jvp::backward(shape, dtype, in, lse, mu, in_strides, mask, scale, out, out_strides,
+  return jvp::backward(false, shape, dtype, in, lse, mu, in_strides, mask, scale, out,
+                       out_strides, workspace, workspace_bytes, stream);
+}
+
+jvp_status_t jvp_attn_bwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                          const void* k, const void* v, const void* o, const float* lse,
+                          const void* g_o, const jvp_strides_t* in_strides,
+                          const jvp_mask_t* mask, float scale, void* g_q, void* g_k, void* g_v,
+                          const jvp_strides_t* out_strides, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!in_strides || !out_strides) return jvp::fail(JVP_ERR_INVALID_ARG, "strides are NULL");
+  // The dual backward's argument layout with the tangent entries absent (a
+  // unit-stride placeholder record each).
+  const jvp_strides_t none{0, 0, 0, 1};
+  const jvp_strides_t ins[10] = {in_strides[0], in_strides[1], in_strides[2], none, none, none,
+                                 in_strides[3], none, in_strides[4], none};
+  const jvp_strides_t outs[6] = {out_strides[0], out_strides[1], out_strides[2], none, none, none};
+  const void* in[10] = {q, k, v, nullptr, nullptr, nullptr, o, nullptr, g_o, nullptr};
+  void* out[6] = {g_q, g_k, g_v, nullptr, nullptr, nullptr};
+  return jvp::backward(true, shape, dtype, in, lse, nullptr, ins, mask, scale, out, outs,
                        workspace, workspace_bytes, stream);
+}
+
+size_t jvp_attn_bwd_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype) {
+  return jvp_attn_bwd_dual_workspace_size(shape, dtype);
 }
 
 size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t) {

@@ -106,6 +106,10 @@ struct BwdParams {
   Strides sgq, sgk, sgv, sgdq, sgdk, sgdv;
   float* nu;
   float* delta;
+  // 1: the backward of attention without tangents (dq, dk, dv, t_o, g_to, mu
+  // are not read and may be NULL; g_dq, g_dk, g_dv are not written; the row
+  // pass stores nu = 0 and delta = gO . O)
+  int primal;
 };
 
 // Workspace bytes of the backward for a problem with `rows` = B * H * Nq query rows.
@@ -126,10 +130,10 @@ struct BwdTcMaps {
   // its value part; the maps above have 32)
   CUtensorMap q64, dq64, go64, gto64;
 };
-// Tensor-core backward (fp16/bf16, D in {64, 128}); the row pre-pass must
-// have been enqueued before.  qmaps: query-major kernel (query-side boxes of
+// Tensor-core backward (fp16/bf16, D in {64, 128}; primal: the backward of
+// attention without tangents); the row pre-pass must have been enqueued before.  qmaps: query-major kernel (query-side boxes of
 // 128 rows, key side 64); kmaps: key-major kernel (key side 128, query side 32).
-cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, const BwdTcMaps& qmaps,
+cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, bool primal, const BwdTcMaps& qmaps,
                           const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
                           unsigned int* status, cudaStream_t stream);
 #define JVP_BWD_TC_DECL(NAME)                                                            \
@@ -140,6 +144,11 @@ JVP_BWD_TC_DECL(launch_bwd_tc_f16_d64)
 JVP_BWD_TC_DECL(launch_bwd_tc_f16_d128)
 JVP_BWD_TC_DECL(launch_bwd_tc_bf16_d64)
 JVP_BWD_TC_DECL(launch_bwd_tc_bf16_d128)
+// The same kernels specialised for the primal backward (p.primal = 1).
+JVP_BWD_TC_DECL(launch_bwd_primal_tc_f16_d64)
+JVP_BWD_TC_DECL(launch_bwd_primal_tc_f16_d128)
+JVP_BWD_TC_DECL(launch_bwd_primal_tc_bf16_d64)
+JVP_BWD_TC_DECL(launch_bwd_primal_tc_bf16_d128)
 #undef JVP_BWD_TC_DECL
 
 // Device status word owned by the library (bit 0: a bounded wait timed out).

@@ -259,6 +259,46 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
 size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
 
 /*
+ * Reverse mode of attention without tangents: the backward that
+ * `jvp_attention` needs when it is used as a plain drop-in for
+ * scaled_dot_product_attention (the project page, Usage section) and trained
+ * by ordinary back-propagation.  Given the cotangent g_o of Loss = <g_o, O>,
+ * writes the gradients with respect to q, k, v; no gradient flows into the
+ * mask.  It is the dual backward with dq = dk = dv = 0 and g_to = 0, without
+ * the work those zeros would cost:
+ *   P = exp(S - lse), delta = rowsum(g_o * O), gP = g_o V^T,
+ *   gS = P * (gP - delta), g_q = scale gS K, g_k = scale gS^T Q, g_v = P^T g_o.
+ *
+ *   q, k, v        the forward inputs (as passed to jvp_attn_fwd)
+ *   o, lse         that call's outputs (lse is required)
+ *   g_o            cotangent, [B,H,Nq,D]
+ *   in_strides     5 records: q, k, v, o, g_o
+ *   g_q, g_k, g_v  outputs, shapes of q, k, v (with grouped-query attention
+ *                  g_k, g_v sum the contributions of every query head of the
+ *                  group); out_strides 3 records in that order
+ *   workspace      device scratch of at least jvp_attn_bwd_workspace_size()
+ *                  bytes, 4-byte aligned, owned by the caller; its contents on
+ *                  entry do not matter and are overwritten.
+ *
+ * Every tensor has the same dtype; mask and scale as in the forward call.
+ * fp16/bf16 with D in {16, 32, 64, 128} and 16-byte aligned tensors run a row
+ * pass and two tcgen05 kernels (query-major for g_q; key-major for g_k and
+ * g_v in one pass at every D); every other case runs three CUDA-core kernels
+ * in fp32.  All are enqueued on `stream`.  Returns JVP_ERR_WORKSPACE if the
+ * workspace is NULL or too small.
+ */
+jvp_status_t jvp_attn_bwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
+                          const void* k, const void* v, const void* o, const float* lse,
+                          const void* g_o, const jvp_strides_t* in_strides,
+                          const jvp_mask_t* mask, float scale, void* g_q, void* g_k, void* g_v,
+                          const jvp_strides_t* out_strides, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Workspace bytes jvp_attn_bwd needs for `shape` (the same as
+ * jvp_attn_bwd_dual_workspace_size: 8 * B * H * Nq, 0 or SIZE_MAX likewise). */
+size_t jvp_attn_bwd_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
+
+/*
  * jvp_attn_bwd_dual for callers that cannot allocate device memory.  The
  * pages have no counterpart to this entry point; it exists for callers such
  * as plugins that run inside someone else's process or memory pool, code

@@ -192,3 +192,39 @@ def test_debug_build_compiles_and_exports_the_same_functions():
         assert hasattr(dbg, n), n
     dbg.jvp_attn_status_string.restype = ctypes.c_char_p
     assert dbg.jvp_attn_status_string(_abi.JVP_ERR_BOUNDS).startswith(b"device-side bounds")
+
+
+def test_primal_backward_validates_before_touching_a_device(lib):
+    # jvp_attn_bwd: the dual backward's checks on its own argument list
+    # (q, k, v, o, lse, g_o; g_q, g_k, g_v), then the device lookup.
+    p = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x100000)
+    none = _abi.Mask(_abi.JVP_MASK_NONE, None, 0, 0, 0, 0)
+
+    def call(shape=(1, 2, 64, 64), ptr=p, ins=None, outs=None, scale=0.125, ws_bytes=1 << 20,
+             lse=p):
+        B, H, N, D = shape
+        sh = _abi.Shape(B, H, N, N, D, 0)
+        ins = ins if ins is not None else _strides(5, shape)
+        outs = outs if outs is not None else _strides(3, shape)
+        return lib.jvp_attn_bwd(ctypes.byref(sh), _abi.JVP_BF16, ptr, ptr, ptr, ptr, lse, ptr, ins,
+                                ctypes.byref(none), scale, ptr, ptr, ptr, outs, ws, ws_bytes, None)
+
+    assert lib.jvp_attn_bwd(None, _abi.JVP_BF16, p, p, p, p, p, p, None, None, 0.125, p, p, p,
+                            None, ws, 1 << 20, None) == _abi.JVP_ERR_INVALID_ARG
+    assert call(shape=(1, 1, 8, 256)) == _abi.JVP_ERR_UNSUPPORTED
+    assert call(scale=float("nan")) == _abi.JVP_ERR_INVALID_ARG
+    assert call(ptr=None) == _abi.JVP_ERR_INVALID_ARG                      # null tensors
+    assert call(ptr=ctypes.c_void_p(0x10001)) == _abi.JVP_ERR_ALIGNMENT    # odd address
+    assert call(lse=None) == _abi.JVP_ERR_INVALID_ARG                      # lse is required
+    bad = _strides(5, (1, 2, 64, 64))
+    bad[4] = _abi.Strides(8192, 4096, 64, 2)
+    assert call(ins=bad) == _abi.JVP_ERR_INVALID_ARG                       # d stride != 1
+    assert call(ws_bytes=8) == _abi.JVP_ERR_WORKSPACE                      # 8*B*H*Nq needed
+    assert call(shape=(0, 2, 64, 64), ptr=None) == _abi.JVP_OK            # empty problem
+    sh = _abi.Shape(2, 8, 2048, 2048, 64, 0)
+    assert lib.jvp_attn_bwd_workspace_size(ctypes.byref(sh), _abi.JVP_BF16) == \
+        lib.jvp_attn_bwd_dual_workspace_size(ctypes.byref(sh), _abi.JVP_BF16) == 8 * 2 * 8 * 2048
+    big = _abi.Shape(1 << 32, 1 << 32, 64, 64, 64, 0)
+    assert lib.jvp_attn_bwd_workspace_size(ctypes.byref(big), _abi.JVP_BF16) == \
+        ctypes.c_size_t(-1).value

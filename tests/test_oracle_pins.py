@@ -442,3 +442,38 @@ def test_reverse_mode_of_the_tangent_is_a_hessian_vector_product(mask):
     g0 = grad_f(q, k, v)
     for a, b in zip(hvp[3:], g0):
         assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(b).max())
+
+
+@pytest.mark.parametrize("mask", MASKS)
+@pytest.mark.parametrize("Nq,Nk", [(9, 9), (5, 13), (13, 5)])
+def test_zero_tangent_reverse_mode_is_the_primal_backward(mask, Nq, Nk):
+    # The primal backward of attention (gradients of <gO, O> with respect to
+    # q, k, v) is the reverse mode of the dual map with dQ = dK = dV = 0 and
+    # gtO = 0; the tangent-side gradients are then those of the linear map
+    # (dq, dk, dv) -> tO at the same point, which gtO = 0 makes zero.  Checked
+    # against torch.autograd of a float64 softmax attention (no jvp involved)
+    # and against central differences of the oracle's own O.
+    q, k, v, _, _, _, m = make(B=1, H=2, N=Nq, D=6, mask=mask, seed=41 + Nq, Nk=Nk)
+    rng = np.random.default_rng(42 + Nk)
+    g_o = rng.standard_normal(q.shape)
+    s = 1 / math.sqrt(6)
+    z = [np.zeros_like(x) for x in (q, k, v)]
+    grads = oracle.bwd_dual(q, k, v, *z, g_o, np.zeros_like(g_o), mask, m)
+    for g in grads[3:]:
+        assert np.abs(g).max() == 0.0
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).requires_grad_(True)
+    ts = [T(x) for x in (q, k, v)]
+    mt = None if m is None else torch.from_numpy(m)
+    o = torch_attention(*ts, mask, mt, s)
+    ref = torch.autograd.grad((torch.from_numpy(g_o) * o).sum(), ts)
+    for g, r in zip(grads[:3], ref):
+        assert np.abs(g - r.detach().numpy()).max() <= 1e-12
+    h = 1e-6
+    for which in range(3):
+        u = rng.standard_normal((q, k, v)[which].shape)
+        xp = [x.copy() for x in (q, k, v)]
+        xm = [x.copy() for x in (q, k, v)]
+        xp[which] += h * u
+        xm[which] -= h * u
+        fd = ((primal(*xp, mask, m)[0] - primal(*xm, mask, m)[0]) * g_o).sum() / (2 * h)
+        assert abs(fd - (grads[which] * u).sum()) <= 1e-6 * max(1.0, abs(fd))
