@@ -244,11 +244,13 @@ def timed_steps(step, steps, flush, stream, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        # A head start of untimed flush writes, so that the host has queued the
-        # first timed call before the device reaches its start event (a host
-        # stall there would otherwise be timed as device time).
-        for _ in range(4):
+        # Two untimed steps right before the timed ones: the device may have
+        # idled (and lowered its clock) while the sampler started, and they
+        # give the host a head start, so that no stall before the first timed
+        # call is timed as device time.
+        for _ in range(2):
             flush.fill_(0.0)
+            step()
         with torch.cuda.nvtx.range(f"timed region: {steps} steps"):
             for s in range(steps):
                 flush.fill_(float(s))  # evict L2 between timed steps (outside the events)
@@ -377,8 +379,9 @@ def run_bwd(args, rank, world, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
-        for _ in range(4):  # device head start (see timed_steps)
+        for _ in range(2):  # untimed steps right before the timed ones (see timed_steps)
             flush.fill_(0.0)
+            step()
         with torch.cuda.nvtx.range(f"{args.mode} timed region: {args.steps} steps"):
             for s in range(args.steps):
                 flush.fill_(float(s))
