@@ -143,6 +143,78 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(BwdParams p) {
   }
 }
 
+// Kernel 1 with 16-byte loads: LPR lanes per row, each reading 16 bytes of
+// O, gO (and tO, gtO) — for 16-byte aligned rows whose head dimension is
+// LPR * 16 bytes (the tensor-core shapes and fp32 at D = 16..128).
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& u, float (&f)[16 / sizeof(T)]);
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& u, float (&f)[4]) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<__half>(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+    f[2 * k] = t.x; f[2 * k + 1] = t.y;
+  }
+}
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(w[k] << 16);
+    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+template <typename T, int LPR>
+__global__ void __launch_bounds__(kThreads) bwd_rows_vec_kernel(BwdParams p) {
+  constexpr int VEC = 16 / sizeof(T);
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = gt / LPR;
+  const int part = static_cast<int>(gt % LPR);
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
+  const bool ok = row < rows;  // every lane takes part in the shuffles below
+  float nu = 0.f, a = 0.f;
+  if (ok) {
+    const int i = static_cast<int>(row % p.Nq);
+    const long long bh = row / p.Nq;
+    const int b = static_cast<int>(bh / p.H), h = static_cast<int>(bh % p.H);
+    auto ld16 = [&](const void* base, const Strides& st) {
+      return *reinterpret_cast<const uint4*>(row_ptr<T>(base, st, b, h, i) + part * VEC);
+    };
+    float o[VEC], go[VEC];
+    unpack16<T>(ld16(p.o, p.so), o);
+    unpack16<T>(ld16(p.g_o, p.sgo), go);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) a = fmaf(go[e], o[e], a);
+    if (!p.primal) {
+      float to[VEC], gto[VEC];
+      unpack16<T>(ld16(p.t_o, p.sto), to);
+      unpack16<T>(ld16(p.g_to, p.sgto), gto);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        nu = fmaf(gto[e], o[e], nu);
+        a = fmaf(gto[e], to[e], a);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) {
+    nu += __shfl_xor_sync(0xffffffffu, nu, off);
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+  }
+  if (ok && part == 0) {
+    p.nu[row] = nu;
+    p.delta[row] = p.primal ? a : a - p.mu[row] * nu;
+  }
+}
+
 // Per (row i, key j) scalars shared by kernels 2 and 3.
 struct PairTerms {
   float P, dP, gS, gdS;
@@ -398,12 +470,48 @@ __global__ void __launch_bounds__(kThreads) bwd_queries_kernel(BwdParams p, int 
   }
 }
 
+// Whether every row that kernel 1 reads starts on a 16-byte boundary.
+inline bool rows_aligned16(const void* base, const Strides& s, size_t e) {
+  return reinterpret_cast<uintptr_t>(base) % 16 == 0 && (s.b * static_cast<long long>(e)) % 16 == 0 &&
+         (s.h * static_cast<long long>(e)) % 16 == 0 && (s.n * static_cast<long long>(e)) % 16 == 0;
+}
+
+template <typename T, int LPR>
+cudaError_t launch_rows_vec(const BwdParams& p, long long rows, cudaStream_t stream) {
+  const long long blocks = (rows * LPR + kThreads - 1) / kThreads;
+  bwd_rows_vec_kernel<T, LPR><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <typename T>
-cudaError_t launch_all(const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_rows_only(const BwdParams& p, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
   const long long row_blocks = (rows * 32 + kThreads - 1) / kThreads;
+  if (row_blocks == 0) return cudaSuccess;
+  // 16-byte loads when the rows allow them: a row of D elements is D * e / 16
+  // lanes (2 to 32, a power of two).
+  constexpr size_t e = sizeof(T);
+  const int lpr = static_cast<int>(p.D * e / 16);
+  bool vec = (p.D * e) % 16 == 0 && lpr >= 2 && lpr <= 32 && (lpr & (lpr - 1)) == 0 &&
+             rows_aligned16(p.o, p.so, e) && rows_aligned16(p.g_o, p.sgo, e);
+  if (vec && !p.primal)
+    vec = rows_aligned16(p.t_o, p.sto, e) && rows_aligned16(p.g_to, p.sgto, e);
+  if (vec) {
+    switch (lpr) {
+      case 2: return launch_rows_vec<T, 2>(p, rows, stream);
+      case 4: return launch_rows_vec<T, 4>(p, rows, stream);
+      case 8: return launch_rows_vec<T, 8>(p, rows, stream);
+      case 16: return launch_rows_vec<T, 16>(p, rows, stream);
+      case 32: return launch_rows_vec<T, 32>(p, rows, stream);
+    }
+  }
   bwd_rows_kernel<T><<<static_cast<unsigned>(row_blocks), kThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_all(const BwdParams& p, cudaStream_t stream) {
+  cudaError_t e = launch_rows_only<T>(p, stream);  // (no launch when there are no rows)
   if (e != cudaSuccess) return e;
   // Lanes per key / row: enough 16-element parts to cover D (a power of two).
   int parts = 1;
@@ -432,14 +540,7 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t stream) {
   return e;
 }
 
-template <typename T>
-cudaError_t launch_rows_only(const BwdParams& p, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
-  const long long row_blocks = (rows * 32 + kThreads - 1) / kThreads;
-  if (row_blocks == 0) return cudaSuccess;
-  bwd_rows_kernel<T><<<static_cast<unsigned>(row_blocks), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
-}
+
 
 }  // namespace
 

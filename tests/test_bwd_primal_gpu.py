@@ -180,3 +180,23 @@ def test_jvp_attention_backward_takes_the_primal_kernels(dtype, D, mask, monkeyp
     o.backward(inp.g_o.cuda())
     assert calls == [] and A.last_path() == 1
     check(w, (q.grad, k.grad, v.grad), reference(w, inp, np64(inp.k), np64(inp.v)))
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f32", 40)])
+@pytest.mark.parametrize("Nq,Nk", [(0, 70), (70, 0)])
+def test_backward_with_an_empty_side(dtype, D, Nq, Nk):
+    # No query rows: the key-side gradients are zero; no keys: the query-side
+    # gradients are zero (and lse = -inf rows give nothing).  Both backward
+    # entry points, no error.
+    dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+    g = torch.Generator().manual_seed(Nq + Nk)
+    mk = lambda n: torch.randn(1, 2, n, D, generator=g).to("cuda", dt)
+    q, dq, go, gto = mk(Nq), mk(Nq), mk(Nq), mk(Nq)
+    k, v, dk, dv = mk(Nk), mk(Nk), mk(Nk), mk(Nk)
+    o, t_o, lse, mu = A.fwd_dual(q, k, v, dq, dk, dv, return_stats=True)
+    for grads in (A.bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, go, gto),
+                  A.bwd(q, k, v, o, lse, go)):
+        torch.cuda.synchronize()
+        assert A.device_status() == 0
+        for x in grads:
+            assert x.numel() == 0 or torch.all(x == 0)
