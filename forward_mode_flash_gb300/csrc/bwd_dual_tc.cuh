@@ -1105,10 +1105,11 @@ cudaError_t set_smem(int bytes) {
 
 // qmaps: query-major kernel (query side 128-row boxes, key side 64); kmaps:
 // key-major kernel (key side 128-row boxes, query side 32, and 64 in q64 ...).
+// The query-major kernel on `stream`, the key-major kernel(s) on `kstream`.
 template <typename T, int D, int MASK, bool PRIMAL>
 cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
                                   const BwdParams& p, int num_sms, unsigned int* status,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, cudaStream_t kstream) {
   const int BH = p.B * p.H;
   {
     using L = BqLayout<D>;
@@ -1133,7 +1134,7 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
     const int G = max(1, min(BHk, num_sms / max(1, nk)));
     static_assert(L::BQ == 32 || L::BQ == 64, "query-side box heights of kmaps");
     kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk), kBwdThreadsK, L::SMEM_BYTES,
-           stream>>>(kmaps, p, G, status);
+           kstream>>>(kmaps, p, G, status);
     return cudaGetLastError();
   };
   if constexpr (D == 64 || PRIMAL) {
@@ -1148,20 +1149,20 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
 template <typename T, int D, bool PRIMAL = false>
 cudaError_t launch_bwd_tc_dispatch(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,
                                    const BwdParams& p, int num_sms, unsigned int* status,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, cudaStream_t kstream) {
   switch (mask_kind) {
     case kMaskNone:
       return launch_bwd_tc_variant<T, D, kMaskNone, PRIMAL>(qmaps, kmaps, p, num_sms, status,
-                                                            stream);
+                                                            stream, kstream);
     case kMaskBool:
       return launch_bwd_tc_variant<T, D, kMaskBool, PRIMAL>(qmaps, kmaps, p, num_sms, status,
-                                                            stream);
+                                                            stream, kstream);
     case kMaskAdditive:
       return launch_bwd_tc_variant<T, D, kMaskAdditive, PRIMAL>(qmaps, kmaps, p, num_sms, status,
-                                                                stream);
+                                                                stream, kstream);
     case kMaskCausal:
       return launch_bwd_tc_variant<T, D, kMaskCausal, PRIMAL>(qmaps, kmaps, p, num_sms, status,
-                                                              stream);
+                                                              stream, kstream);
   }
   return cudaErrorInvalidValue;
 }

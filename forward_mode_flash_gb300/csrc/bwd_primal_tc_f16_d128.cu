@@ -4,8 +4,9 @@
 namespace jvp {
 cudaError_t launch_bwd_primal_tc_f16_d128(int mask_kind, const BwdTcMaps& qmaps,
                                    const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
-                                   unsigned int* status, cudaStream_t stream) {
+                                   unsigned int* status, cudaStream_t stream,
+                                   cudaStream_t kstream) {
   return launch_bwd_tc_dispatch<__half, 128, true>(mask_kind, qmaps, kmaps, p, num_sms, status,
-                                                 stream);
+                                                 stream, kstream);
 }
 }  // namespace jvp

@@ -68,6 +68,7 @@ struct DeviceInfo {
   bool sm103 = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
+  cudaStream_t side = nullptr;  // the backward's key-side kernels (created on first use)
 };
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
@@ -99,6 +100,21 @@ jvp_status_t current_device(DeviceInfo** out) {
     d.queried = true;
   }
   *out = &d;
+  return JVP_OK;
+}
+
+// A second stream of the current device for work that may run beside the
+// caller's stream (joined back to it by an event before the call returns).
+jvp_status_t side_stream(DeviceInfo* d, cudaStream_t* out) {
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!d->side) {
+    cudaError_t e = cudaStreamCreateWithFlags(&d->side, cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+      d->side = nullptr;
+      return fail(JVP_ERR_CUDA, std::string("cudaStreamCreate: ") + cudaGetErrorString(e));
+    }
+  }
+  *out = d->side;
   return JVP_OK;
 }
 
@@ -383,11 +399,13 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
 
 // Body of jvp_attn_bwd_dual and (primal = true: the tangent inputs dq, dk,
 // dv, t_o, g_to, mu and outputs g_dq, g_dk, g_dv are absent) jvp_attn_bwd.
+// fork: the key-side tensor-core kernels run on a second stream beside the
+// query-side one (the two write disjoint gradients), joined back by an event.
 jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
                       const void* const* in, const float* lse, const float* mu,
                       const jvp_strides_t* in_strides, const jvp_mask_t* mask, float scale,
                       void* const* out, const jvp_strides_t* out_strides, void* workspace,
-                      size_t ws_bytes, void* stream_ptr) {
+                      size_t ws_bytes, void* stream_ptr, bool fork = true) {
   t_last_path = 0;
   if (!shape) return fail(JVP_ERR_INVALID_ARG, "shape is NULL");
   const int64_t B = shape->B, H = shape->H, Nq = shape->Nq, Nk = shape->Nk, D = shape->D;
@@ -519,9 +537,31 @@ jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
   cudaError_t err;
   if (tc) {
     err = launch_bwd_rows(static_cast<DType>(dtype), p, stream);
+    // After the row pass the query-major and key-major kernels are
+    // independent: the key side goes to the side stream, so the CTAs of
+    // either fill the SMs the other's last wave leaves idle.
+    cudaStream_t kstream = stream;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    if (err == cudaSuccess && fork) {
+      cudaStream_t side = nullptr;
+      if (side_stream(dev, &side) == JVP_OK &&
+          cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventRecord(ev_fork, stream) == cudaSuccess &&
+          cudaStreamWaitEvent(side, ev_fork, 0) == cudaSuccess) {
+        kstream = side;
+      }
+    }
     if (err == cudaSuccess)
       err = launch_bwd_tc(static_cast<DType>(dtype), D <= 64 ? 64 : 128, kind, primal, qm, km, p,
-                          dev->num_sms, dev->status, stream);
+                          dev->num_sms, dev->status, stream, kstream);
+    if (kstream != stream) {  // join (also after a failed launch)
+      cudaError_t ej = cudaEventRecord(ev_join, kstream);
+      if (ej == cudaSuccess) ej = cudaStreamWaitEvent(stream, ev_join, 0);
+      if (err == cudaSuccess) err = ej;
+    }
+    if (ev_fork) cudaEventDestroy(ev_fork);  // (released once the recorded work completes)
+    if (ev_join) cudaEventDestroy(ev_join);
     t_last_path = 1;
   } else {
     err = launch_bwd_simt(static_cast<DType>(dtype), p, stream);
@@ -555,26 +595,20 @@ cudaError_t launch_fwd_tc(DType dt, int D, int mask_kind, bool tangent, const Tc
 
 cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, bool primal, const BwdTcMaps& qmaps,
                           const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
-                          unsigned int* status, cudaStream_t stream) {
+                          unsigned int* status, cudaStream_t stream, cudaStream_t kstream) {
+#define JVP_BWD_CALL(NAME) NAME(mask_kind, qmaps, kmaps, p, num_sms, status, stream, kstream)
   if (primal) {
-    if (dt == kF16 && D == 64)
-      return launch_bwd_primal_tc_f16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
-    if (dt == kF16 && D == 128)
-      return launch_bwd_primal_tc_f16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
-    if (dt == kBF16 && D == 64)
-      return launch_bwd_primal_tc_bf16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
-    if (dt == kBF16 && D == 128)
-      return launch_bwd_primal_tc_bf16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+    if (dt == kF16 && D == 64) return JVP_BWD_CALL(launch_bwd_primal_tc_f16_d64);
+    if (dt == kF16 && D == 128) return JVP_BWD_CALL(launch_bwd_primal_tc_f16_d128);
+    if (dt == kBF16 && D == 64) return JVP_BWD_CALL(launch_bwd_primal_tc_bf16_d64);
+    if (dt == kBF16 && D == 128) return JVP_BWD_CALL(launch_bwd_primal_tc_bf16_d128);
     return cudaErrorInvalidValue;
   }
-  if (dt == kF16 && D == 64)
-    return launch_bwd_tc_f16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
-  if (dt == kF16 && D == 128)
-    return launch_bwd_tc_f16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
-  if (dt == kBF16 && D == 64)
-    return launch_bwd_tc_bf16_d64(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
-  if (dt == kBF16 && D == 128)
-    return launch_bwd_tc_bf16_d128(mask_kind, qmaps, kmaps, p, num_sms, status, stream);
+  if (dt == kF16 && D == 64) return JVP_BWD_CALL(launch_bwd_tc_f16_d64);
+  if (dt == kF16 && D == 128) return JVP_BWD_CALL(launch_bwd_tc_f16_d128);
+  if (dt == kBF16 && D == 64) return JVP_BWD_CALL(launch_bwd_tc_bf16_d64);
+  if (dt == kBF16 && D == 128) return JVP_BWD_CALL(launch_bwd_tc_bf16_d128);
+#undef JVP_BWD_CALL
   return cudaErrorInvalidValue;
 }
 
@@ -646,6 +680,18 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
   void* out[6] = {g_q, g_k, g_v, g_dq, g_dk, g_dv};
   return jvp::backward(false, shape, dtype, in, lse, mu, in_strides, mask, scale, out,
                        out_strides, workspace, workspace_bytes, stream);
+}
+
+// jvp_attn_bwd_dual on one stream (no side stream, no events): the body of
+// jvp_attn_bwd_dual_noalloc.
+static jvp_status_t bwd_dual_one_stream(const jvp_shape_t* shape, jvp_dtype_t dtype,
+                                        const void* const* in, const float* lse,
+                                        const float* mu, const jvp_strides_t* in_strides,
+                                        const jvp_mask_t* mask, float scale, void* const* out,
+                                        const jvp_strides_t* out_strides, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  return jvp::backward(false, shape, dtype, in, lse, mu, in_strides, mask, scale, out,
+                       out_strides, workspace, workspace_bytes, stream, false);
 }
 
 jvp_status_t jvp_attn_bwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
@@ -992,7 +1038,8 @@ extern "C" jvp_status_t jvp_attn_bwd_dual_noalloc(
   void* scratch = nullptr;
   jvp_status_t s = jvp::noalloc_scratch(&scratch);
   if (s != JVP_OK) return s;
-  return jvp_attn_bwd_dual(shape, dtype, q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
-                           in_strides, mask, scale, g_q, g_k, g_v, g_dq, g_dk, g_dv, out_strides,
-                           scratch, JVP_BWD_NOALLOC_SCRATCH_BYTES, stream);
+  const void* in[10] = {q, k, v, dq, dk, dv, o, t_o, g_o, g_to};
+  void* out[6] = {g_q, g_k, g_v, g_dq, g_dk, g_dv};
+  return bwd_dual_one_stream(shape, dtype, in, lse, mu, in_strides, mask, scale, out, out_strides,
+                             scratch, JVP_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }

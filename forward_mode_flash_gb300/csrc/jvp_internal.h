@@ -133,13 +133,16 @@ struct BwdTcMaps {
 // Tensor-core backward (fp16/bf16, D in {64, 128}; primal: the backward of
 // attention without tangents); the row pre-pass must have been enqueued before.  qmaps: query-major kernel (query-side boxes of
 // 128 rows, key side 64); kmaps: key-major kernel (key side 128, query side 32).
+// The query-major kernel goes to `stream`, the key-major kernel(s) to
+// `kstream` (the same stream, or a second one the caller has made wait for
+// the row pass and joins back).
 cudaError_t launch_bwd_tc(DType dt, int D, int mask_kind, bool primal, const BwdTcMaps& qmaps,
                           const BwdTcMaps& kmaps, const BwdParams& p, int num_sms,
-                          unsigned int* status, cudaStream_t stream);
+                          unsigned int* status, cudaStream_t stream, cudaStream_t kstream);
 #define JVP_BWD_TC_DECL(NAME)                                                            \
   cudaError_t NAME(int mask_kind, const BwdTcMaps& qmaps, const BwdTcMaps& kmaps,        \
                    const BwdParams& p, int num_sms, unsigned int* status,               \
-                   cudaStream_t stream);
+                   cudaStream_t stream, cudaStream_t kstream);
 JVP_BWD_TC_DECL(launch_bwd_tc_f16_d64)
 JVP_BWD_TC_DECL(launch_bwd_tc_f16_d128)
 JVP_BWD_TC_DECL(launch_bwd_tc_bf16_d64)

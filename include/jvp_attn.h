@@ -36,9 +36,10 @@
  *     rejected with JVP_ERR_UNSUPPORTED before anything is enqueued.
  *   - The library caches, per device, device addresses of its own globals
  *     (the status word, the scratch of jvp_attn_bwd_dual_noalloc) the first
- *     time a device is used.  cudaDeviceReset() (or anything else that
- *     destroys the device's primary context) invalidates them: do not call the
- *     library on that device again in the same process after a reset.
+ *     time a device is used, and one non-blocking CUDA stream of its own (see
+ *     jvp_attn_bwd_dual).  cudaDeviceReset() (or anything else that destroys
+ *     the device's primary context) invalidates them: do not call the library
+ *     on that device again in the same process after a reset.
  */
 #ifndef JVP_ATTN_H_
 #define JVP_ATTN_H_
@@ -241,8 +242,13 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
  * row pass and tcgen05 kernels (query-major for g_q, g_dq; key-major for g_k,
  * g_dk, g_v, g_dv), fp32 accumulation (D = 16 and 32 on the D = 64 kernels,
  * with zero-filled columns); every other case runs three CUDA-core kernels in
- * fp32.  All are enqueued on `stream`.  Returns JVP_ERR_WORKSPACE
- * if the workspace is NULL or too small.
+ * fp32.  All work is ordered on `stream`: the key-major kernels run on a
+ * stream the library owns (one per device, created on first use), which waits
+ * for the row pass through an event, and `stream` waits for them through
+ * another event before anything enqueued after this call, so the two
+ * kernels overlap and the caller sees one stream (this fork and join also
+ * records into a stream capture).  Returns JVP_ERR_WORKSPACE if the workspace
+ * is NULL or too small.
  */
 jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
                                const void* k, const void* v, const void* dq, const void* dk,
@@ -283,8 +289,9 @@ size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dt
  * Every tensor has the same dtype; mask and scale as in the forward call.
  * fp16/bf16 with D in {16, 32, 64, 128} and 16-byte aligned tensors run a row
  * pass and two tcgen05 kernels (query-major for g_q; key-major for g_k and
- * g_v in one pass at every D); every other case runs three CUDA-core kernels
- * in fp32.  All are enqueued on `stream`.  Returns JVP_ERR_WORKSPACE if the
+ * g_v in one pass at every D, on the library's second stream as in
+ * jvp_attn_bwd_dual); every other case runs three CUDA-core kernels in fp32.
+ * All work is ordered on `stream`.  Returns JVP_ERR_WORKSPACE if the
  * workspace is NULL or too small.
  */
 jvp_status_t jvp_attn_bwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
@@ -315,6 +322,7 @@ size_t jvp_attn_bwd_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
  *   - Set-up: the first call on each device looks up the array's device
  *     address (with that device current) and caches it; make that first call
  *     before any stream capture.
+ *   - Streams: every kernel runs on `stream` (no second stream, no events).
  *   - Sharing: every call uses the same array.  Nothing in it needs to start
  *     at zero (each call overwrites the part it reads), but calls whose work
  *     overlaps on the GPU (different streams, no ordering between them) race
