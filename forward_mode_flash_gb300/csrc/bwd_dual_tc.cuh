@@ -65,7 +65,7 @@ constexpr int kBwdScoreWarpB = 11;
 
 // ----------------------------------------------------------------------------
 // Query-major kernel.
-template <int D>
+template <int D, bool PRIMAL = false>
 struct BqLayout {
   static constexpr int BM = 128;  // query rows per CTA
   static constexpr int BN = 64;   // keys per tile
@@ -74,19 +74,29 @@ struct BqLayout {
   // score MMAs: at D = 128 two K stages and one V stage fit next to the 128 KB
   // of resident query-side tiles, so the next K tile loads during the current
   // tile's elementwise stage and accumulate MMAs.
-  static constexpr int NSK = (D == 64) ? 3 : 2;
-  static constexpr int NSV = (D == 64) ? 3 : 1;
+  // The primal keeps only Q and gO resident (the dQ and gtO slots go to a
+  // third K stage and a second V stage at D = 128).
+  static constexpr int NSK = (D == 64 || PRIMAL) ? 3 : 2;
+  static constexpr int NSV = (D == 64) ? 3 : PRIMAL ? 2 : 1;
   static constexpr int QT_BYTES = KCH * BM * 128;  // one [128 x D] query-side tile
   static constexpr int KCHUNK = 2 * BN * 128;      // [K rows | dK rows] of one 64-column chunk
   static constexpr int KBLK = KCH * KCHUNK;        // [K ; dK] block of one stage
-  static constexpr int OFF_Q = 0, OFF_DQ = QT_BYTES, OFF_GO = 2 * QT_BYTES, OFF_GTO = 3 * QT_BYTES;
-  static constexpr int OFF_K = 4 * QT_BYTES;
+  static constexpr int OFF_Q = 0, OFF_DQ = QT_BYTES;  // (dQ, gtO: not in the primal)
+  static constexpr int OFF_GO = (PRIMAL ? 1 : 2) * QT_BYTES, OFF_GTO = 3 * QT_BYTES;
+  static constexpr int OFF_K = (PRIMAL ? 2 : 4) * QT_BYTES;
   static constexpr int OFF_V = OFF_K + NSK * KBLK;
   static constexpr int OFF_CTRL = OFF_V + NSV * KBLK;
   static constexpr int CTRL_BYTES = 512;
   static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
-  // TMEM columns
-  static constexpr uint32_t TM_S = 0, TM_DS = 64, TM_G = 128, TM_GP = 192, TM_ACC = 256;
+  // TMEM columns: NBS buffers of [S | dS] (128 columns each), then [G | gP],
+  // then the accumulators.  Two buffers where the accumulators leave room
+  // (D = 64: [g_dQ | gQ] is 128 columns; the primal has gQ alone), so tile
+  // t+1's [S | dS] products run while the elementwise warps work on tile t.
+  static constexpr int NBS = (D == 64 || PRIMAL) ? 2 : 1;
+  static constexpr uint32_t TM_S = 0, TM_DS = 64;  // + 128 * buffer
+  static constexpr uint32_t TM_G = NBS * 128, TM_GP = TM_G + 64, TM_ACC = TM_G + 128;
+  static constexpr uint32_t A_GQ = PRIMAL ? 0 : D;  // gQ within the accumulators
+  static_assert(TM_ACC + A_GQ + D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -94,7 +104,10 @@ template <int NSK, int NSV>
 struct BwdCtrl {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
-  uint64_t s_full, p_full, o_full, drain, drain_b;
+  uint64_t s_full[2];  // [S | dS] of a buffer (warp 1)
+  uint64_t g_full;     // [G | gP] (warp 10)
+  uint64_t p_full[2];  // the elementwise warps are done with a buffer's tile
+  uint64_t o_full, drain, drain_b;
   uint32_t tmem_base;
   int abort;
 };
@@ -127,8 +140,9 @@ template <typename T, int D, int MASK, bool PRIMAL = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_q_tc_kernel(const __grid_constant__ BwdTcMaps maps, const BwdParams p, int group_heads,
                     unsigned int* status) {
-  using L = BqLayout<D>;
+  using L = BqLayout<D, PRIMAL>;
   constexpr int NSK = L::NSK, NSV = L::NSV, BN = L::BN, BM = L::BM;
+  constexpr int NBS = L::NBS;
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSD = D / 16;   // K-steps over the head dimension
   constexpr int KSN = BN / 16;  // K-steps over a key tile
@@ -173,8 +187,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&ctrl->v_full[s], 1);
       mbar_init(&ctrl->v_empty[s], 1);
     }
-    mbar_init(&ctrl->s_full, 2);  // one commit from each score-issuing thread
-    mbar_init(&ctrl->p_full, 256);
+    // With one [S | dS] buffer both score groups complete s_full[0] (two
+    // commits); with two, [G | gP] has its own barrier (warp 1 may commit the
+    // next buffer's products before warp 10 commits this tile's).
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&ctrl->s_full[u], (NBS == 1 && u == 0) ? 2 : 1);
+      mbar_init(&ctrl->p_full[u], 256);
+    }
+    mbar_init(&ctrl->g_full, 1);
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
     mbar_init(&ctrl->drain_b, 1);
@@ -249,21 +269,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = mbar_wait(&ctrl->q_full, 0, abort);
       tc_fence_after();
       const uint32_t aQ = smem_u32(smem + L::OFF_Q), adQ = smem_u32(smem + L::OFF_DQ);
-      // [S | dS] of tile t goes into columns [0, 128) after this thread's
-      // accumulate MMAs of tile t - 1 (which read gS, g_dS there), in issue
-      // order; warp 10 fills [G | gP] in columns [128, 256) meanwhile.
-      for (int t = 0; ok && t < n_kv; ++t) {
+      // [S | dS] of tile t goes into buffer t % NBS.  With two buffers the
+      // products of tile t are issued before the accumulate MMAs of tile
+      // t - 1 (which read gS, g_dS from the other buffer), so they run while
+      // the elementwise warps work on tile t - 1; with one buffer they follow
+      // them in issue order.  Warp 10 fills [G | gP] meanwhile.
+      auto issue_scores = [&](int t) -> bool {
         const int sk = t % NSK;
-        if (!mbar_wait(&ctrl->k_full[sk], (t / NSK) & 1, abort)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&ctrl->k_full[sk], (t / NSK) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t kb = smem_u32(smem + L::OFF_K + sk * L::KBLK);
+        const uint32_t sb = tmem + (t % NBS) * 128;
 #pragma unroll
         for (int kk = 0; kk < KSD; ++kk) {  // [S | Q dK^T] = Q [K ; dK]^T  (primal: S = Q K^T)
           const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_S, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + off, 16, 1024),
+          mma_ss(sb + L::TM_S, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + off, 16, 1024),
                  sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024),
                  PRIMAL ? I_N64 : I_N128, kk > 0);
         }
@@ -271,21 +291,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < KSD; ++kk) {  // Q dK^T += dQ K^T
             const uint32_t off = (kk & 3) * 32;
-            mma_ss(tmem + L::TM_DS, sdesc_sw128(adQ + (kk >> 2) * BM * 128 + off, 16, 1024),
+            mma_ss(sb + L::TM_DS, sdesc_sw128(adQ + (kk >> 2) * BM * 128 + off, 16, 1024),
                    sdesc_sw128(kb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64, 1u);
           }
         }
-        mma_commit(&ctrl->s_full);
-        if (!mbar_wait(&ctrl->p_full, t & 1, abort)) {
-          ok = false;
-          break;
-        }
+        mma_commit(&ctrl->s_full[t % NBS]);
+        return true;
+      };
+      auto issue_accumulate = [&](int t) -> bool {
+        if (!mbar_wait(&ctrl->p_full[t & 1], (t >> 1) & 1, abort)) return false;
         tc_fence_after();
+        const int sk = t % NSK;
+        const uint32_t kb = smem_u32(smem + L::OFF_K + sk * L::KBLK);
+        const uint32_t sb = tmem + (t % NBS) * 128;
         // gS and g_dS of keys [16 kk, 16 kk + 16) (warpgroup kk / 2, half
-        // kk % 2): gS at columns 16 kk, g_dS at 16 kk + 8.
+        // kk % 2): gS at columns 16 kk, g_dS at 16 kk + 8 of the buffer.
 #pragma unroll
         for (int kk = 0; kk < KSN && !PRIMAL; ++kk) {
-          const uint32_t a_gs = tmem + kk * 16;
+          const uint32_t a_gs = sb + kk * 16;
           const uint32_t a_gds = a_gs + 8;
           const uint32_t kx = kb + kk * 16 * 128;  // MN-major: 16 keys per K-step
           const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
@@ -301,12 +324,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
 #pragma unroll
         for (int kk = 0; kk < KSN; ++kk) {  // gQ += gS K  (the first products of the primal)
-          const uint32_t a_gs = tmem + kk * 16;
-          mma_ts(tmem + L::TM_ACC + D, a_gs,
+          const uint32_t a_gs = sb + kk * 16;
+          mma_ts(tmem + L::TM_ACC + L::A_GQ, a_gs,
                  sdesc_sw128(kb + kk * 16 * 128, D == 64 ? BN * 128 : L::KCHUNK, 1024), I_ACC1,
                  PRIMAL ? ((t > 0 || kk > 0) ? 1u : 0u) : 1u);
         }
         mma_commit(&ctrl->k_empty[sk]);
+        return true;
+      };
+      for (int t = 0; ok && t <= n_kv; ++t) {
+        if (NBS == 2) {
+          if (t < n_kv && !issue_scores(t)) ok = false;
+          if (ok && t > 0 && !issue_accumulate(t - 1)) ok = false;
+        } else {
+          if (t > 0 && !issue_accumulate(t - 1)) ok = false;
+          if (ok && t < n_kv && !issue_scores(t)) ok = false;
+        }
       }
       if (ok) mma_commit(&ctrl->o_full);
       if (!ok) record_timeout(status, abort);
@@ -316,15 +349,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kBwdScoreWarpQ) {
     // ------------------------------------------------------------ [G | gP] score MMAs
-    // Columns [128, 256) are free for tile t once the elementwise warps are
-    // done with tile t - 1 (the accumulate MMAs read only columns [0, 128)).
+    // [G | gP] (one buffer) is free for tile t once the elementwise warps are
+    // done with tile t - 1 (the accumulate MMAs read only the [S | dS] buffers).
     if (lane == 0) {
       bool ok = mbar_wait(&ctrl->q_full, 0, abort);
       tc_fence_after();
       const uint32_t aGO = smem_u32(smem + L::OFF_GO), aGTO = smem_u32(smem + L::OFF_GTO);
       for (int t = 0; ok && t < n_kv; ++t) {
         const int sv = t % NSV;
-        if ((t > 0 && !mbar_wait(&ctrl->p_full, (t - 1) & 1, abort)) ||
+        if ((t > 0 && !mbar_wait(&ctrl->p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, abort)) ||
             !mbar_wait(&ctrl->v_full[sv], (t / NSV) & 1, abort)) {
           ok = false;
           break;
@@ -347,7 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  PRIMAL ? (kk > 0 ? 1u : 0u) : 1u);
         }
         mma_commit(&ctrl->v_empty[sv]);
-        mma_commit(&ctrl->s_full);
+        mma_commit(NBS == 1 ? &ctrl->s_full[0] : &ctrl->g_full);
       }
       if (!ok) record_timeout(status, abort);
       mma_commit(&ctrl->drain_b);
@@ -391,16 +424,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // One half of this warpgroup's 32 keys of a tile: gS and g_dS go into
     // the 16 columns of S the half has just read (gS first, g_dS next), so
     // the other half's inputs stay intact.
-    auto half = [&](int j0h, uint32_t col, const MaskRegs<MASK, 16>& mreg) {
+    // sb: the [S | dS] buffer's first column.
+    auto half = [&](int j0h, uint32_t sb, uint32_t col, const MaskRegs<MASK, 16>& mreg) {
       uint32_t rs[16], rds[16], rg[16], rgp[16];
-      const bool cols_ok = JVP_CHECK(L::TM_GP + col + 16 <= 512u && L::TM_DS + col + 16 <= 512u,
+      const bool cols_ok = JVP_CHECK(L::TM_GP + col + 16 <= 512u &&
+                                         sb + L::TM_DS + col + 16 <= L::TM_G,
                                      status, kChkTmem);
       if (PRIMAL) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) rds[e] = rg[e] = 0u;  // dS = G = 0
-        if (cols_ok) tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_GP + col, rs, rgp);
+        if (cols_ok) tmem_ld16x2(lb + sb + L::TM_S + col, lb + L::TM_GP + col, rs, rgp);
       } else if (cols_ok) {
-        tmem_ld16x2(lb + L::TM_S + col, lb + L::TM_DS + col, rs, rds);
+        tmem_ld16x2(lb + sb + L::TM_S + col, lb + sb + L::TM_DS + col, rs, rds);
         tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
       }
       uint32_t pgs[8], pgds[8];
@@ -428,25 +463,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pgds[jj >> 1] = ElemTraits<T>::pack(gds[0], gds[1]);
       }
       if (cols_ok) {
-        tmem_st8(lb + col, pgs);
-        if (!PRIMAL) tmem_st8(lb + col + 8, pgds);
+        tmem_st8(lb + sb + col, pgs);
+        if (!PRIMAL) tmem_st8(lb + sb + col + 8, pgds);
       }
     };
     for (int t = 0; t < n_kv; ++t) {
       const int j0 = t * BN + wg * 32;
       MaskRegs<MASK, 16> m0, m1;
       if (row_ok) m0.load(mp, mrow, j0);
-      if (!warp_wait(&ctrl->s_full, t & 1, status, abort)) {
+      if (!warp_wait(&ctrl->s_full[t % NBS], (t / NBS) & 1, status, abort) ||
+          (NBS == 2 && !warp_wait(&ctrl->g_full, t & 1, status, abort))) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (row_ok) m1.load(mp, mrow, j0 + 16);
-      half(j0, wg * 32, m0);
-      half(j0 + 16, wg * 32 + 16, m1);
+      const uint32_t sb = static_cast<uint32_t>(t % NBS) * 128;
+      half(j0, sb, wg * 32, m0);
+      half(j0 + 16, sb, wg * 32 + 16, m1);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ctrl->p_full);
+      mbar_arrive(&ctrl->p_full[t & 1]);
     }
     if (ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, status, abort);
     if (ok && !(PRIMAL && wg == 0)) {
@@ -454,14 +491,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Warpgroup 0 writes g_dQ, warpgroup 1 writes gQ (both scaled by s);
       // the primal has gQ alone.
       void* dst = wg == 0 ? p.g_dq : p.g_q;
+      const uint32_t acol = L::TM_ACC + (wg == 0 ? 0u : L::A_GQ);
       const Strides& ds = wg == 0 ? p.sgdq : p.sgq;
       T* row = static_cast<T*>(dst) + static_cast<long long>(b) * ds.b +
                static_cast<long long>(h) * ds.h + static_cast<long long>(row_ok ? i : 0) * ds.n;
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
         uint32_t a[32];
-        if (n_kv > 0 && JVP_CHECK(L::TM_ACC + wg * D + col + 32 <= 512u, status, kChkTmem)) {
-          tmem_ld32(lb + L::TM_ACC + wg * D + col, a);
+        if (n_kv > 0 && JVP_CHECK(acol + col + 32 <= 512u, status, kChkTmem)) {
+          tmem_ld32(lb + acol + col, a);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) a[e] = 0u;
@@ -1112,7 +1150,7 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
                                   cudaStream_t stream, cudaStream_t kstream) {
   const int BH = p.B * p.H;
   {
-    using L = BqLayout<D>;
+    using L = BqLayout<D, PRIMAL>;
     constexpr auto kern = bwd_q_tc_kernel<T, D, MASK, PRIMAL>;
     cudaError_t e = set_smem<kern>(L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
