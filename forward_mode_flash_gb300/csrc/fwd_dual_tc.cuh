@@ -611,7 +611,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mreg = mnext;
         if (row_ok && t + 1 < n_kv) mnext.load(p, mrow, j0 + BN);
       } else {
-        if (row_ok) mreg.load(p, mrow, j0);
+        if (row_ok) {
+          // The next two tiles' entries of this row (one 128-byte line each for
+          // contiguous keys) are prefetched into L2, so those in-tile loads hit
+          // there (no registers to hold them a tile ahead at D = 128).
+          if (p.msk == 1) {
+            const float* rowf = static_cast<const float*>(mrow);
+            if (t + 1 < n_kv && j0 + BN < p.Nk)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(rowf + j0 + BN));
+            if (t + 2 < n_kv && j0 + 2 * BN < p.Nk)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(rowf + j0 + 2 * BN));
+          }
+          mreg.load(p, mrow, j0);
+        }
       }
       // With tangents, S is read as soon as it is final and dS (whose
       // dQ K^T part is still accumulating) only when the tangent terms need it.
