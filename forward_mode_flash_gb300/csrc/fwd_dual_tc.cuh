@@ -610,6 +610,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if constexpr (kMaskAhead) {
         mreg = mnext;
         if (row_ok && t + 1 < n_kv) mnext.load(p, mrow, j0 + BN);
+        if constexpr (MASK == kMaskAdditive) {
+          // additive entries two tiles ahead into L2 as well (measured: bool
+          // masks, a quarter the bytes, do not gain)
+          if (row_ok && p.msk == 1 && t + 2 < n_kv && j0 + 2 * BN < p.Nk)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const float*>(mrow) + j0 +
+                                                          2 * BN));
+        }
       } else {
         if (row_ok) {
           // The next two tiles' entries of this row (one 128-byte line each for
