@@ -462,6 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const uint32_t sQ = smem_u32(smem + L::OFF_Q);
       const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
+      // s < 0: -Q K^T, -Q dK^T, -dQ K^T (negate-A bit), with |s| applied later.
+      const uint32_t neg_a = p.neg_scores ? (1u << 13) : 0u;
       for (int t = 0; ok && t < n_kv; ++t) {
         const int s = t % NS;
         if (t >= 2 && !mbar_wait(&ctrl->pv_done[t & 1], ((t - 2) >> 1) & 1, abort)) {
@@ -480,7 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t off = (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
-          mma_ss(d_s, a, bd, IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ss(d_s, a, bd, IDESC_S | neg_a, kk > 0 ? 1u : 0u);
         }
         // S is complete: the softmax starts on it while dQ K^T accumulates into dS.
         if (TANGENT) mma_commit(&ctrl->s_ready[t & 1]);
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t off = (kk & 3) * 32;
             const uint64_t a = sdesc_sw128(sdQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
             const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
-            mma_ss(d_s + BN, a, bd, IDESC_DS, 1u);
+            mma_ss(d_s + BN, a, bd, IDESC_DS | neg_a, 1u);
           }
         }
         mma_commit(&ctrl->kdk_empty[s]);

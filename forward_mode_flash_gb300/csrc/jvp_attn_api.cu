@@ -337,19 +337,24 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   p.status = dev->status;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-  // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, positive scale, at
+  // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, a nonzero scale, at
   // least one key, and every tensor 16-byte aligned with 16-byte-multiple
   // strides.  D = 16 and 32 run the D = 64 kernel: the tensor maps' 64-column
   // boxes reach past the D columns of each row, TMA fills those with zeros
   // (they add nothing to Q K^T, dQ K^T or Q dK^T and give zero columns of
   // A and T), and the output maps' stores drop them.
   bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) &&
-            (D == 16 || D == 32 || D == 64 || D == 128) && scale > 0.f && Nk > 0;
+            (D == 16 || D == 32 || D == 64 || D == 128) && scale != 0.f && Nk > 0;
   const int kernel_d = D <= 64 ? 64 : 128;
   for (int t = 0; tc && t < n_in; ++t)
     tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
   for (int t = 0; tc && t < n_out; ++t)
     tc = aligned(out[t], 16) && strides_aligned16(out_strides[t], e);
+  if (tc && scale < 0.f) {  // negated score products, |scale| (see FwdParams)
+    p.neg_scores = 1;
+    p.scale = -scale;
+    p.scale_log2 = -scale * 1.4426950408889634f;
+  }
   TcMaps maps;
   if (tc) {
     const int64_t Ns[6] = {Nq, Nk, Nk, Nq, Nk, Nk};

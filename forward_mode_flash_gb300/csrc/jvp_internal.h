@@ -22,6 +22,10 @@ struct FwdParams {
   int group_heads;   // tensor-core kernel: (batch, head) pairs per scheduling group
   float scale;       // logit scale s
   float scale_log2;  // s * log2(e)
+  // Tensor-core kernel with s < 0: the score products are formed negated (the
+  // MMA's negate-A bit) and scale, scale_log2 hold |s|, so every later step
+  // sees the same scaled logits and tangents as for a positive scale.
+  int neg_scores;
   const void* mask;  // uint8 (bool) or float (additive); nullptr otherwise
   long long msb, msh, msq, msk;  // mask element strides
   int mask_vec;      // 1: rows are 16-byte aligned and stride_k == 1 (vector loads)

@@ -247,6 +247,7 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
          | ((bf16 ? 1u : 0u) << 7)                   // A format
          | ((bf16 ? 1u : 0u) << 10)                  // B format
          | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness (A is K-major)
+         // (bits 13 and 14 negate A and B; the score products may set bit 13)
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

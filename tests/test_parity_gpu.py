@@ -168,6 +168,29 @@ def test_nondefault_scale():
     compare_full(synth.small("f32", 1, 2, 40, 16, "none", seed=3), scale=0.9, expect_path=2)
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("bf16", 32)])
+@pytest.mark.parametrize("mask", ["none", "causal", "bool", "additive"])
+def test_negative_scale_on_the_tensor_core_path(dtype, D, mask):
+    # The score products are formed negated (the MMA's negate-A bit) with
+    # |scale| applied after them; the result is the oracle's at scale < 0.
+    w = synth.small(dtype, 2, 2, 257, D, mask, seed=D + 41)
+    compare_full(w, scale=-0.11, expect_path=1)
+
+
+def test_negative_scale_split_kv_and_zero_scale():
+    # A key split merges partial states formed with the negated scores; a zero
+    # scale (uniform weights) runs the CUDA-core kernel.
+    w = synth.small("bf16", 1, 1, 64, 64, "none", seed=5, Nk=8192)
+    inp = synth.make_inputs(w)
+    g = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    o, t_o = A.fwd_dual(*g, scale=-0.09)
+    assert A.last_path() == 3
+    ro, rt, _, _ = oracle.fwd_dual(*(np64(x) for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk,
+                                                        inp.dv)), "none", None, scale=-0.09)
+    assert np.abs(np64(o) - ro).max() <= TOL["bf16"] and np.abs(np64(t_o) - rt).max() <= TOL["bf16"]
+    compare_full(synth.small("bf16", 1, 2, 100, 64, "causal", seed=6), scale=0.0, expect_path=2)
+
+
 def test_fully_masked_rows_follow_the_convention():
     w = synth.small("bf16", 1, 2, 96, 64, "bool", seed=11)
     inp = synth.make_inputs(w)
