@@ -247,8 +247,9 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
  * for the row pass through an event, and `stream` waits for them through
  * another event before anything enqueued after this call, so the two
  * kernels overlap and the caller sees one stream (this fork and join also
- * records into a stream capture).  Returns JVP_ERR_WORKSPACE if the workspace
- * is NULL or too small.
+ * records into a stream capture; make the first backward call on a device
+ * outside any capture, since it creates that stream).  Returns
+ * JVP_ERR_WORKSPACE if the workspace is NULL or too small.
  */
 jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
                                const void* k, const void* v, const void* dq, const void* dk,

@@ -138,3 +138,36 @@ def test_bwd_long_sequences_one_head(dtype, D, mask, N):
     # One (b, h) problem with many key and query tiles per CTA.
     w = synth.small(dtype, 1, 1, N, D, mask, seed=N + D)
     check(w, run(w))
+
+
+@pytest.mark.parametrize("dtype,D,mask", [("bf16", 64, "causal"), ("f16", 128, "additive")])
+def test_bwd_negative_scale(dtype, D, mask):
+    # The backward recomputes P from the saved lse with the signed scale (no
+    # running maximum), so a negative scale needs nothing special; the forward
+    # that feeds it takes the tensor-core path with negated score products.
+    w = synth.small(dtype, 1, 2, 130, D, mask, seed=D + 7)
+    inp = synth.make_inputs(w, with_cotangents=True)
+    g = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv)]
+    m = inp.mask.cuda() if inp.mask is not None else None
+    causal = mask == "causal"
+    o, t_o, lse, mu = A.fwd_dual(*g, attn_mask=m, is_causal=causal, scale=-0.1,
+                                 return_stats=True)
+    assert A.last_path() == 1
+    grads = A.bwd_dual(*g, o, t_o, lse, mu, inp.g_o.cuda(), inp.g_to.cuda(), attn_mask=m,
+                       is_causal=causal, scale=-0.1)
+    assert A.last_path() == 1
+    primal = A.bwd(*g[:3], o, lse, inp.g_o.cuda(), attn_mask=m, is_causal=causal, scale=-0.1)
+    torch.cuda.synchronize()
+    assert A.device_status() == 0
+    xs = [np64(x) for x in (inp.q, inp.k, inp.v, inp.dq, inp.dk, inp.dv, inp.g_o, inp.g_to)]
+    mm = None if inp.mask is None else inp.mask.double().numpy()
+    ref = oracle.bwd_dual(*xs, w.mask, mm, scale=-0.1)
+    errs = {n: (np.abs(np64(gg) - r).max(), np.abs(r).max()) for n, gg, r in zip(NAMES, grads, ref)}
+    check(w, errs, "[bwd, scale < 0]")
+    # the primal backward against the zero-tangent reverse mode
+    z = np.zeros_like(xs[0])
+    zk = np.zeros_like(xs[1])
+    ref_p = oracle.bwd_dual(xs[0], xs[1], xs[2], z, zk, zk, xs[6], z, w.mask, mm, scale=-0.1)
+    errs_p = {n: (np.abs(np64(gg) - r).max(), np.abs(r).max())
+              for n, gg, r in zip(NAMES[:3], primal, ref_p[:3])}
+    check(w, errs_p, "[bwd primal, scale < 0]")
