@@ -38,9 +38,17 @@
 // owns half of the columns of a tile, a thread owns a TMEM lane).  The second
 // group of score products ([G | gP], disjoint TMEM columns) has its own
 // issuing warp (query-major: warp 10; key-major key part: warp 11), and the
-// key-major kernel's accumulate products another (warp 10); the query-major
-// kernel's accumulate products follow warp 1's score products in its issue
-// order.  Every wait is bounded.
+// key-major kernel's accumulate products another (warp 10).  The query-major
+// kernel's accumulate products are issued by warp 1 too: after the score
+// products of the same tile when [S | dS] has one TMEM buffer (D = 128), or
+// with two buffers (D = 64, and the primal) after the next tile's score
+// products, so those run while the elementwise warps work.  After the row
+// pass the query-major and key-major kernels are independent; the host puts
+// the key-major ones on a second stream.  Every wait is bounded.
+//
+// The PRIMAL specialisation is the backward of attention without tangents
+// (dQ = dK = dV = 0, gtO = 0): only S, gP1 = gO V^T, gS and the gQ, gK, gV
+// products remain (see the kernels below).
 #pragma once
 
 #include <cuda_bf16.h>
