@@ -514,6 +514,8 @@ def test_split_kv_repeated_calls_are_bit_identical():
     ("bf16", 128, "causal", 1, 2, 16384, 16384),   # long causal rows
     ("f16", 64, "none", 1, 1, 256, 65536),          # long key range: 16-way split-KV
     ("bf16", 64, "bool", 1, 2, 8192, 8192),
+    ("bf16", 128, "causal", 1, 1, 131072, 131072),  # one very long causal head
+    ("f16", 64, "none", 8, 64, 1024, 1024),         # 4096 CTAs (512 heads x 8 tiles)
 ])
 def test_long_sequences_on_sampled_rows(dtype, D, mask, B, H, Nq, Nk):
     w = synth.small(dtype, B, H, Nq, D, mask, seed=Nq // 64 + D, Nk=Nk)
