@@ -35,6 +35,16 @@
 // epilogue stages O and tO in the idle [K;dK] ring and writes them with TMA
 // stores.
 //
+// Masks: a boolean keep-mask (and the additive mask at D = 64) is loaded into
+// registers a tile ahead by each softmax thread for its own row.  At D = 128
+// an additive tile ahead does not fit the registers; when the mask's layout
+// admits a tensor map (contiguous keys, rows that do not broadcast, 16-byte
+// strides) the producer copies each [128 x 64] fp32 tile into a shared-memory
+// slot a tile ahead, in two swizzled [128 x 32] boxes, and the softmax reads
+// its row from there (else: per-row loads in the tile, the next tiles'
+// lines prefetched into L2).  Room for the slot comes from the two [K;dK]
+// stages sharing one dK slot (see TcLayout).
+//
 // Rescaling is conditional: the row maximum used in the exponent is only
 // moved when a tile's maximum exceeds it by more than 2^8, so A, T, l and mu~
 // are rarely touched; the final ratios are exact for any stale maximum.
@@ -83,7 +93,7 @@ struct ElemTraits<__nv_bfloat16> {
   }
 };
 
-template <int D, bool TANGENT>
+template <int D, bool TANGENT, bool MTILE = false>
 struct TcLayout {
   static constexpr int BM = kTcBlockM;              // query rows per CTA
   static constexpr int BN = kTcBlockN;              // keys per tile
@@ -95,11 +105,42 @@ struct TcLayout {
   static constexpr int KDK_BYTES = KCH * KCHUNK_BYTES;
   static constexpr int VCHUNK_BYTES = BN * 128;        // one 64-column chunk of V
   static constexpr int VDV_BYTES = (TANGENT ? 2 : 1) * KCH * VCHUNK_BYTES;
+  // MTILE: the additive mask's [BM x BN] fp32 tile is brought into shared
+  // memory by TMA a tile ahead (D = 128, where a tile ahead does not fit the
+  // registers).  To make room next to the dual rings, the two [K;dK] stages
+  // then share one dK slot: each 64-column chunk holds [K0 | dK | K1], stage 0
+  // reads the 128 rows [K0; dK] and stage 1 the rows [dK; K1], so stage 1's
+  // score products come out as [Q dK^T | S] instead of [S | Q dK^T].  The dK
+  // slot is refilled once the first score product of a tile has read it.
+  static constexpr bool kSharedDK = MTILE && TANGENT && NS == 2;
+  static constexpr int KREGION = kSharedDK ? KCH * 3 * BN * 128 : NS * KDK_BYTES;
+  static constexpr int MSK_BYTES = MTILE ? BM * BN * 4 : 0;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DQ = OFF_Q + Q_BYTES;
   static constexpr int OFF_KDK = OFF_DQ + (TANGENT ? Q_BYTES : 0);
-  static constexpr int OFF_VDV = OFF_KDK + NS * KDK_BYTES;
-  static constexpr int OFF_CTRL = OFF_VDV + NS * VDV_BYTES;
+  static constexpr int OFF_VDV = OFF_KDK + KREGION;
+  static constexpr int OFF_MSK = OFF_VDV + NS * VDV_BYTES;
+  static constexpr int OFF_CTRL = OFF_MSK + MSK_BYTES;
+  // Byte offsets of stage s, 64-column chunk c: the K rows, the dK rows, and
+  // the first row of the 128-row operand of the first score product.
+  static __device__ __forceinline__ int k_off(int s, int c) {
+    return kSharedDK ? OFF_KDK + c * 3 * BN * 128 + s * 2 * BN * 128
+                     : OFF_KDK + s * KDK_BYTES + c * KCHUNK_BYTES;
+  }
+  static __device__ __forceinline__ int dk_off(int s, int c) {
+    return kSharedDK ? OFF_KDK + c * 3 * BN * 128 + BN * 128 : k_off(s, c) + BN * 128;
+  }
+  static __device__ __forceinline__ int m1_off(int s, int c) {
+    return kSharedDK ? OFF_KDK + c * 3 * BN * 128 + s * BN * 128 : k_off(s, c);
+  }
+  // TMEM columns of S and of dS in score buffer buf (stage buf; NS = 2 when
+  // the dK slot is shared, so the stage of a tile is its buffer).
+  static __device__ __forceinline__ uint32_t s_col(int buf) {
+    return static_cast<uint32_t>(buf * 128 + ((kSharedDK && buf) ? BN : 0));
+  }
+  static __device__ __forceinline__ uint32_t ds_col(int buf) {
+    return static_cast<uint32_t>(buf * 128 + ((kSharedDK && buf) ? 0 : BN));
+  }
   static constexpr int CTRL_BYTES = 8192;
   static constexpr int USED = OFF_CTRL + CTRL_BYTES;
   // Padded so that only one CTA fits per SM (each CTA owns all 512 TMEM columns).
@@ -115,6 +156,7 @@ struct TcLayout {
   static constexpr uint32_t TM_COLS = 512;
   static_assert(D == 64 || D == 128, "tensor-core path handles D = 64 or 128");
   static_assert(USED + 1024 <= 227 * 1024, "shared memory budget");
+  static_assert(OFF_MSK % 1024 == 0, "the mask tile's 128-byte swizzle needs 1024-byte alignment");
 };
 
 constexpr int kSoftmaxThreads = 256;           // two warpgroups (warps 2..9)
@@ -139,6 +181,8 @@ struct TcCtrl {
   int abort;
   float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
   float xsum[2][4][kTcBlockM];     // [warpgroup][l, lx, mu, m][row] final half sums
+  uint64_t dk_empty;               // the shared dK slot has been read (MTILE with tangents)
+  uint64_t msk_full, msk_empty;    // the additive-mask tile in shared memory (MTILE)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -287,7 +331,10 @@ constexpr int kPairRecvBytes = kPairRecvStats + 2 * kPairRecvBlock;
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
-  using L = TcLayout<D, TANGENT>;
+  // The additive mask at D = 128 comes through shared memory when its layout
+  // allows a tensor map (p.mask_tma), else by per-row loads in its tile.
+  constexpr bool kMTile = (MASK == kMaskAdditive && D == 128);
+  using L = TcLayout<D, TANGENT, kMTile>;
   constexpr bool kWsSplit = SPLIT == kSplitWorkspace;
   constexpr bool kPair = SPLIT == kSplitCluster;
   static_assert(!kPair || (D == 64 && TANGENT), "the cluster split is built for D = 64 with tangents");
@@ -375,6 +422,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&ctrl->o_staged, kSoftmaxThreads / 32);
     mbar_init(&ctrl->ring_free, 1);    // cluster split: rank 0's rings are idle
     mbar_init(&ctrl->peer_ready, 1);   // cluster split: rank 1's state has landed (with bytes)
+    mbar_init(&ctrl->dk_empty, 1);
+    mbar_init(&ctrl->msk_full, 1);
+    mbar_init(&ctrl->msk_empty, kSoftmaxThreads / 32);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -402,6 +452,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&maps.dk);
         tma_prefetch_desc(&maps.dv);
       }
+      const bool mtma = kMTile && p.mask_tma;
+      // mask coordinates: a broadcast dimension of the mask has extent 1
+      const int mh = p.msh ? h : 0, mb = p.msb ? b : 0;
+      if (mtma) tma_prefetch_desc(&maps.msk);
       mbar_arrive_expect_tx(&ctrl->q_full, (TANGENT ? 2 : 1) * L::Q_BYTES);
       for (int c = 0; c < L::KCH; ++c) {
         tma_load_4d(smem + L::OFF_Q + c * L::BM * 128, &maps.q, &ctrl->q_full, c * 64, q0, h, b);
@@ -409,24 +463,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_load_4d(smem + L::OFF_DQ + c * L::BM * 128, &maps.dq, &ctrl->q_full, c * 64, q0, h,
                       b);
       }
-      int k_fills = 0, v_fills = 0;  // ring fills issued so far
+      int k_fills = 0, v_fills = 0, m_fills = 0;  // ring fills issued so far
       for (int t = 0; t < n_kv; ++t) {
         const int s = t % NS;
         const uint32_t ph = (t / NS) & 1;
         const int j0 = (kv0 + t) * BN;
-        if (!mbar_wait(&ctrl->kdk_empty[s], ph ^ 1, abort)) {
+        if (!mbar_wait(&ctrl->kdk_empty[s], ph ^ 1, abort) ||
+            (L::kSharedDK && !mbar_wait(&ctrl->dk_empty, (t & 1) ^ 1, abort))) {
           record_timeout(p.status, abort);
           break;
         }
-        uint8_t* kdk = smem + L::OFF_KDK + s * L::KDK_BYTES;
         mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_BYTES);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(kdk + c * L::KCHUNK_BYTES, &maps.k, &ctrl->kdk_full[s], c * 64, j0, hk, b);
+          tma_load_4d(smem + L::k_off(s, c), &maps.k, &ctrl->kdk_full[s], c * 64, j0, hk, b);
           if (TANGENT)
-            tma_load_4d(kdk + c * L::KCHUNK_BYTES + BN * 128, &maps.dk, &ctrl->kdk_full[s], c * 64,
-                        j0, hk, b);
+            tma_load_4d(smem + L::dk_off(s, c), &maps.dk, &ctrl->kdk_full[s], c * 64, j0, hk, b);
         }
         ++k_fills;
+        if (mtma) {
+          // one slot: tile t's mask once every softmax warp has read tile t-1's
+          if (!mbar_wait(&ctrl->msk_empty, (t & 1) ^ 1, abort)) {
+            record_timeout(p.status, abort);
+            break;
+          }
+          mbar_arrive_expect_tx(&ctrl->msk_full, L::MSK_BYTES);
+          for (int w = 0; w < 2; ++w)
+            tma_load_4d(smem + L::OFF_MSK + w * L::BM * 128, &maps.msk, &ctrl->msk_full,
+                        j0 + w * (BN / 2), q0, mh, mb);
+          ++m_fills;
+        }
         if (!mbar_wait(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
           record_timeout(p.status, abort);
           break;
@@ -449,6 +514,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_wait(&ctrl->kdk_full[t % NS], (t / NS) & 1, &zero);
         for (int t = max(0, v_fills - NS); t < v_fills; ++t)
           mbar_wait(&ctrl->vdv_full[t % NS], (t / NS) & 1, &zero);
+        if (m_fills > 0) mbar_wait(&ctrl->msk_full, (m_fills - 1) & 1, &zero);
       }
     }
   } else if (warp == 1) {
@@ -475,24 +541,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sK = smem_u32(smem + L::OFF_KDK + s * L::KDK_BYTES);
+        // stage s: chunk c of the first product's operand at sM + c * kChunk,
+        // of the K rows at sK + c * kChunk
+        const uint32_t sK = smem_u32(smem + L::k_off(s, 0));
+        const uint32_t sM = smem_u32(smem + L::m1_off(s, 0));
+        constexpr int kChunk = L::kSharedDK ? 3 * BN * 128 : L::KCHUNK_BYTES;
         const uint32_t d_s = tmem + (t & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS_D; ++kk) {
           const uint32_t off = (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sM + (kk >> 2) * kChunk + off, 16, 1024);
           mma_ss(d_s, a, bd, IDESC_S | neg_a, kk > 0 ? 1u : 0u);
         }
         // S is complete: the softmax starts on it while dQ K^T accumulates into dS.
         if (TANGENT) mma_commit(&ctrl->s_ready[t & 1]);
+        if (L::kSharedDK) mma_commit(&ctrl->dk_empty);  // dK is read only by that product
         if (TANGENT) {
 #pragma unroll
           for (int kk = 0; kk < KSTEPS_D; ++kk) {
             const uint32_t off = (kk & 3) * 32;
             const uint64_t a = sdesc_sw128(sdQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * L::KCHUNK_BYTES + off, 16, 1024);
-            mma_ss(d_s + BN, a, bd, IDESC_DS | neg_a, 1u);
+            const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * kChunk + off, 16, 1024);
+            mma_ss(tmem + L::ds_col(t & 1), a, bd, IDESC_DS | neg_a, 1u);
           }
         }
         mma_commit(&ctrl->kdk_empty[s]);
@@ -525,8 +596,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // accumulators warpgroup kk / 2 stored them at the start of its own S
         // columns, otherwise they are packed; P~ * dS, BN columns further, is
         // always at the start of the warpgroup's own dS columns.
-        const uint32_t p_tm = tmem + buf * 128;
-        const uint32_t pd_tm = tmem + buf * 128 + BN;
+        const uint32_t p_tm = tmem + L::s_col(buf);
+        const uint32_t pd_tm = tmem + L::ds_col(buf);
         auto pcol = [](int kk) -> uint32_t {
           return L::kHalfAcc
                      ? static_cast<uint32_t>((kk / (HN / 16)) * HN + (kk % (HN / 16)) * 8)
@@ -620,7 +691,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                           2 * BN));
         }
       } else {
-        if (row_ok) {
+        bool staged = false;
+        if constexpr (kMTile) {
+          if (p.mask_tma) {
+            // The tile's entries were copied into shared memory by TMA a tile
+            // ahead, one [128 x 32] box per warpgroup with the 128-byte
+            // swizzle: 16-byte piece c of row r sits at piece position
+            // c ^ (r % 8), so the 8 rows of a quarter warp hit distinct banks.
+            // (The slot is released once the entries are consumed, below.)
+            if (!warp_wait(&ctrl->msk_full, t & 1, p.status, abort)) {
+              ok = false;
+              break;
+            }
+            const uint32_t mrow_s = smem_u32(smem + L::OFF_MSK + wg * L::BM * 128 + r * 128);
+#pragma unroll
+            for (int c4 = 0; c4 < HN / 4; ++c4) {
+              const float4 v = ld_shared_v4f(mrow_s + ((c4 ^ (r & 7)) << 4));
+              mreg.a[4 * c4] = v.x;
+              mreg.a[4 * c4 + 1] = v.y;
+              mreg.a[4 * c4 + 2] = v.z;
+              mreg.a[4 * c4 + 3] = v.w;
+            }
+            staged = true;
+          }
+        }
+        if (!staged && row_ok) {
           // The next two tiles' entries of this row (one 128-byte line each for
           // contiguous keys) are prefetched into L2, so those in-tile loads hit
           // there (no registers to hold them a tile ahead at D = 128).
@@ -643,8 +738,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_after();
       uint32_t sa[32], da[32];  // S and dS (raw, unscaled) of this half tile
-      if (JVP_CHECK(buf * 128 + cofs + 32 <= L::TM_COLS, p.status, kChkTmem))
-        tmem_ld32(lane_base + buf * 128 + cofs, sa);
+      if (JVP_CHECK(L::s_col(buf) + cofs + 32 <= L::TM_COLS, p.status, kChkTmem))
+        tmem_ld32(lane_base + L::s_col(buf) + cofs, sa);
       float x[HN];
 #pragma unroll
       for (int jj = 0; jj < HN; ++jj) x[jj] = __uint_as_float(sa[jj]);
@@ -723,8 +818,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // case after the first tile) and compute the weights with it; the
         // decision below is the same either way, so is every value stored.
         ctrl->xmax[buf][wg][r] = m_half;
+        // A mask tile read from shared memory is consumed once m_half is
+        // stored (it depends on every entry, so each lane's reads of the slot
+        // have returned before that store issues): release the slot for the
+        // next tile's copy, the reads ordered before the copy's writes.
+        if (kMTile && p.mask_tma) fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctrl->max_ready[buf]);
+        if (lane == 0) {
+          mbar_arrive(&ctrl->max_ready[buf]);
+          if (kMTile && p.mask_tma) mbar_arrive(&ctrl->msk_empty);
+        }
         spec = __all_sync(0xffffffffu,
                           m_run != -INFINITY && !(m_half > m_run + kRescaleThreshold));
         if (spec) weights(m_run);
@@ -778,8 +881,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ordered both warpgroups' reads first and the two halves are packed
       // side by side.
       const uint32_t pofs = L::kHalfAcc ? cofs : wg * (HN / 2);
-      if (JVP_CHECK(buf * 128 + pofs + 16 <= L::TM_COLS, p.status, kChkTmem))
-        tmem_st16(lane_base + buf * 128 + pofs, pk);
+      if (JVP_CHECK(L::s_col(buf) + pofs + 16 <= L::TM_COLS, p.status, kChkTmem))
+        tmem_st16(lane_base + L::s_col(buf) + pofs, pk);
       if (TANGENT) {
         // Publish P~ first: the P~ [V | dV] products run while the tangent
         // terms wait for dS.
@@ -795,12 +898,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        if (JVP_CHECK(buf * 128 + BN + cofs + 32 <= L::TM_COLS, p.status, kChkTmem))
-          tmem_ld32(lane_base + buf * 128 + BN + cofs, da);
+        if (JVP_CHECK(L::ds_col(buf) + cofs + 32 <= L::TM_COLS, p.status, kChkTmem))
+          tmem_ld32(lane_base + L::ds_col(buf) + cofs, da);
         tangent_terms();
         mu_run += mu_part;
-        if (JVP_CHECK(buf * 128 + BN + cofs + 16 <= L::TM_COLS, p.status, kChkTmem))
-          tmem_st16(lane_base + buf * 128 + BN + cofs, pdk);
+        if (JVP_CHECK(L::ds_col(buf) + cofs + 16 <= L::TM_COLS, p.status, kChkTmem))
+          tmem_st16(lane_base + L::ds_col(buf) + cofs, pdk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -1143,7 +1246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream_t stream) {
-  using L = TcLayout<D, TANGENT>;
+  using L = TcLayout<D, TANGENT, MASK == kMaskAdditive && D == 128>;
   auto kern = fwd_dual_tc_kernel<T, D, MASK, TANGENT, SPLIT>;
   // The attribute is per device; setting it is idempotent, the mask (shared
   // by host threads) only saves calls.

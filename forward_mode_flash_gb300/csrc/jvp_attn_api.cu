@@ -163,6 +163,33 @@ bool encode_map(CUtensorMap* map, int dt, const void* ptr, int64_t B, int64_t H,
   return r == CUDA_SUCCESS;
 }
 
+// 4-D tiled map over an additive fp32 mask [Bm, Hm, Nq, Nk] (Bm, Hm = 1 where
+// it broadcasts) with {32, 128} boxes and the 128-byte swizzle: one box is a
+// softmax warpgroup's half of a [128 x 64] score tile.  Keys must be
+// contiguous, and rows must not broadcast (each of the 128 rows is read).
+bool encode_mask_map(CUtensorMap* map, const void* ptr, int64_t B, int64_t H, int64_t Nq,
+                     int64_t Nk, int64_t msb, int64_t msh, int64_t msq, int64_t msk) {
+  auto enc = tensor_map_encoder();
+  if (!enc || msk != 1 || msq <= 0 || reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
+  const int64_t Hm = msh ? H : 1, Bm = msb ? B : 1;
+  // A size-1 dimension's stride is never used; give it a well-formed value.
+  if (Nq == 1) msq = (Nk + 3) / 4 * 4;
+  const int64_t sh = Hm > 1 ? msh : msq * Nq;
+  const int64_t sb = Bm > 1 ? msb : sh * Hm;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(Nq),
+                        static_cast<cuuint64_t>(Hm), static_cast<cuuint64_t>(Bm)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(msq * 4), static_cast<cuuint64_t>(sh * 4),
+                           static_cast<cuuint64_t>(sb * 4)};
+  for (auto s : strides)
+    if (s == 0 || s % 16 != 0 || s >= (1ull << 40)) return false;
+  cuuint32_t box[4] = {32, static_cast<cuuint32_t>(kTcBlockM), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool strides_aligned16(const jvp_strides_t& s, size_t e) {
@@ -371,6 +398,9 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     if (tc && tangent)
       tc = encode_map(&maps.t_o, dtype, out[1], B, H, Nq, D, out_strides[1], kTcBlockM);
     if (tc && !tangent) maps.t_o = maps.o;
+    // The additive mask at D = 128 through shared memory (else per-row loads).
+    if (tc && kind == JVP_MASK_ADDITIVE && kernel_d == 128)
+      p.mask_tma = encode_mask_map(&maps.msk, mptr, B, H, Nq, Nk, msb, msh, msq, msk) ? 1 : 0;
   }
   cudaError_t err;
   if (tc) {

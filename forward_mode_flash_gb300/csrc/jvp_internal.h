@@ -29,6 +29,7 @@ struct FwdParams {
   const void* mask;  // uint8 (bool) or float (additive); nullptr otherwise
   long long msb, msh, msq, msk;  // mask element strides
   int mask_vec;      // 1: rows are 16-byte aligned and stride_k == 1 (vector loads)
+  int mask_tma;      // 1: TcMaps::msk describes the additive mask (tensor-core kernel, D = 128)
   int causal;        // 1: a bool / additive mask also keeps only keys j <= i
   int kv_group;      // query heads per key/value head (grouped-query attention; 1 = none)
   // Split-KV (tensor-core kernel): `splits` CTAs share a query tile, each over
@@ -69,6 +70,7 @@ cudaError_t launch_fwd_combine(DType dt, bool tangent, const FwdParams& p, cudaS
 struct TcMaps {
   CUtensorMap q, k, v, dq, dk, dv;
   CUtensorMap o, t_o;  // outputs, 128-row boxes (the epilogue's TMA stores)
+  CUtensorMap msk;     // additive mask [B|1, H|1, Nq, Nk] fp32, {32, 128} boxes (if mask_tma)
 };
 
 // Tensor-core kernels (fp16/bf16, D in {64, 128}).  Return a cudaError_t.

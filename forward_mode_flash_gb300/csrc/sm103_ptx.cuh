@@ -198,6 +198,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
                "r"(d)
                : "memory");
 }
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t saddr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
+}
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads of them (TMA stores, tensor-core operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {

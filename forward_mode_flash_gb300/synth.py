@@ -62,6 +62,11 @@ WORKLOADS = {
     "bf16_b4h16n2048d128_causal": Workload("bf16_b4h16n2048d128_causal", "bf16", 4, 16, 2048, 128,
                                            "causal"),
     "f16_b2h8n2048d64_causal": Workload("f16_b2h8n2048d64_causal", "f16", 2, 8, 2048, 64, "causal"),
+    # the headline shape under each mask type (a [B, 1, N, N] mask per batch)
+    "bf16_b4h16n2048d128_bool": Workload("bf16_b4h16n2048d128_bool", "bf16", 4, 16, 2048, 128,
+                                         "bool"),
+    "bf16_b4h16n2048d128_additive": Workload("bf16_b4h16n2048d128_additive", "bf16", 4, 16, 2048,
+                                             128, "additive"),
 }
 
 
