@@ -294,6 +294,7 @@ def causal_companion(args, dev, world, flush, stream, local, peak, pk_src):
             "unit": "TFLOP/s", "steps": args.steps, "flops_per_step": flops,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": recorded_traffic(CAUSAL_WORKLOAD),
                          "peak_source": f"{pk_src} bf16_tflops (burst; kernel timed alone)",
                          "kernel": "fwd_dual_tc_kernel"},
             "clocks": clocks.summary(), "gpu_launches": args.steps,

@@ -332,7 +332,10 @@ template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
   // The additive mask at D = 128 comes through shared memory when its layout
-  // allows a tensor map (p.mask_tma), else by per-row loads in its tile.
+  // allows a tensor map (p.mask_tma), else by per-row loads in its tile.  (At
+  // D = 64 the registers hold a tile ahead; the shared-memory slot measured
+  // slower there: its refill waits for the previous tile's maximum and holds
+  // up the producer's deeper K/V rings.)
   constexpr bool kMTile = (MASK == kMaskAdditive && D == 128);
   using L = TcLayout<D, TANGENT, kMTile>;
   constexpr bool kWsSplit = SPLIT == kSplitWorkspace;
@@ -674,48 +677,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // overlaps a whole tile of work (not the additive mask at D = 128, whose
     // two tiles of 32 floats would not fit the register budget).
     constexpr bool kMaskAhead = !(MASK == kMaskAdditive && D == 128);
+    const bool mstaged = kMTile && p.mask_tma;  // additive tiles through shared memory (D = 128)
     MaskRegs<MASK, HN> mnext;
-    if (kMaskAhead && row_ok && n_kv > 0) mnext.load(p, mrow, kv0 * BN + cofs);
+    if (kMaskAhead && !mstaged && row_ok && n_kv > 0) mnext.load(p, mrow, kv0 * BN + cofs);
     for (int t = 0; t < n_kv; ++t) {
       const int buf = t & 1;
       const int j0 = (kv0 + t) * BN + cofs;  // first key of this half tile
       MaskRegs<MASK, HN> mreg;
-      if constexpr (kMaskAhead) {
-        mreg = mnext;
-        if (row_ok && t + 1 < n_kv) mnext.load(p, mrow, j0 + BN);
-        if constexpr (MASK == kMaskAdditive) {
-          // additive entries two tiles ahead into L2 as well (measured: bool
-          // masks, a quarter the bytes, do not gain)
-          if (row_ok && p.msk == 1 && t + 2 < n_kv && j0 + 2 * BN < p.Nk)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const float*>(mrow) + j0 +
-                                                          2 * BN));
-        }
-      } else {
-        bool staged = false;
-        if constexpr (kMTile) {
-          if (p.mask_tma) {
-            // The tile's entries were copied into shared memory by TMA a tile
-            // ahead, one [128 x 32] box per warpgroup with the 128-byte
-            // swizzle: 16-byte piece c of row r sits at piece position
-            // c ^ (r % 8), so the 8 rows of a quarter warp hit distinct banks.
-            // (The slot is released once the entries are consumed, below.)
-            if (!warp_wait(&ctrl->msk_full, t & 1, p.status, abort)) {
-              ok = false;
-              break;
-            }
-            const uint32_t mrow_s = smem_u32(smem + L::OFF_MSK + wg * L::BM * 128 + r * 128);
+      if constexpr (kMTile) {
+        if (mstaged) {
+          // The tile's entries were copied into shared memory by TMA a tile
+          // ahead, one [128 x 32] box per warpgroup with the 128-byte
+          // swizzle: 16-byte piece c of row r sits at piece position
+          // c ^ (r % 8), so the 8 rows of a quarter warp hit distinct banks.
+          // (The slot is released once the entries are consumed, below.)
+          if (!warp_wait(&ctrl->msk_full, t & 1, p.status, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t mrow_s = smem_u32(smem + L::OFF_MSK + wg * L::BM * 128 + r * 128);
 #pragma unroll
-            for (int c4 = 0; c4 < HN / 4; ++c4) {
-              const float4 v = ld_shared_v4f(mrow_s + ((c4 ^ (r & 7)) << 4));
-              mreg.a[4 * c4] = v.x;
-              mreg.a[4 * c4 + 1] = v.y;
-              mreg.a[4 * c4 + 2] = v.z;
-              mreg.a[4 * c4 + 3] = v.w;
-            }
-            staged = true;
+          for (int c4 = 0; c4 < HN / 4; ++c4) {
+            const float4 v = ld_shared_v4f(mrow_s + ((c4 ^ (r & 7)) << 4));
+            mreg.a[4 * c4] = v.x;
+            mreg.a[4 * c4 + 1] = v.y;
+            mreg.a[4 * c4 + 2] = v.z;
+            mreg.a[4 * c4 + 3] = v.w;
           }
         }
-        if (!staged && row_ok) {
+      }
+      if (!mstaged) {
+        if constexpr (kMaskAhead) {
+          mreg = mnext;
+          if (row_ok && t + 1 < n_kv) mnext.load(p, mrow, j0 + BN);
+          if constexpr (MASK == kMaskAdditive) {
+            // additive entries two tiles ahead into L2 as well (measured: bool
+            // masks, a quarter the bytes, do not gain)
+            if (row_ok && p.msk == 1 && t + 2 < n_kv && j0 + 2 * BN < p.Nk)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const float*>(mrow) + j0 +
+                                                            2 * BN));
+          }
+        } else if (row_ok) {
           // The next two tiles' entries of this row (one 128-byte line each for
           // contiguous keys) are prefetched into L2, so those in-tile loads hit
           // there (no registers to hold them a tile ahead at D = 128).
@@ -822,11 +824,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // stored (it depends on every entry, so each lane's reads of the slot
         // have returned before that store issues): release the slot for the
         // next tile's copy, the reads ordered before the copy's writes.
-        if (kMTile && p.mask_tma) fence_proxy_async_smem();
+        if (mstaged) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&ctrl->max_ready[buf]);
-          if (kMTile && p.mask_tma) mbar_arrive(&ctrl->msk_empty);
+          if (mstaged) mbar_arrive(&ctrl->msk_empty);
         }
         spec = __all_sync(0xffffffffu,
                           m_run != -INFINITY && !(m_half > m_run + kRescaleThreshold));
