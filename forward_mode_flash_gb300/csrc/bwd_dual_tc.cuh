@@ -1163,7 +1163,14 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
     cudaError_t e = set_smem<kern>(L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int nq = (p.Nq + L::BM - 1) / L::BM;
-    const int G = max(1, min(BH, num_sms / max(1, nq)));
+    // About one wave of CTAs per group of heads; causal problems (their tiles
+    // run longest first within a group) take as many heads as keep the key
+    // side's tiles within 32 MB of L2, which shortens the launch's tail.
+    int G = max(1, min(BH, num_sms / max(1, nq)));
+    if (MASK == kMaskCausal || p.causal) {
+      const double kv_head = (PRIMAL ? 2.0 : 4.0) * static_cast<double>(p.Nk) * D * sizeof(T);
+      G = max(G, min(BH, static_cast<int>(32.0 * 1048576.0 / kv_head)));
+    }
     kern<<<static_cast<unsigned>(static_cast<long long>(nq) * BH), kBwdThreads, L::SMEM_BYTES,
            stream>>>(qmaps, p, G, status);
     e = cudaGetLastError();
@@ -1177,7 +1184,12 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
     if (e != cudaSuccess) return e;
     const int nk = (p.Nk + L::BK - 1) / L::BK;
     const int BHk = p.B * (p.H / p.kv_group);
-    const int G = max(1, min(BHk, num_sms / max(1, nk)));
+    int G = max(1, min(BHk, num_sms / max(1, nk)));
+    if (MASK == kMaskCausal || p.causal) {  // as above, for the query side's tiles
+      const double q_head =
+          (PRIMAL ? 2.0 : 4.0) * static_cast<double>(p.Nq) * D * sizeof(T) * p.kv_group;
+      G = max(G, min(BHk, static_cast<int>(32.0 * 1048576.0 / q_head)));
+    }
     static_assert(L::BQ == 32 || L::BQ == 64, "query-side box heights of kmaps");
     kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk), kBwdThreadsK, L::SMEM_BYTES,
            kstream>>>(kmaps, p, G, status);

@@ -407,6 +407,15 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     p.num_q_tiles = static_cast<int>((Nq + kTcBlockM - 1) / kTcBlockM);
     // About one wave of CTAs per group of heads (one CTA per SM).
     p.group_heads = std::max(1, std::min(static_cast<int>(B * H), dev->num_sms / p.num_q_tiles));
+    // Causal: the query tiles of a group run longest first, so a launch ends
+    // on short tiles only within its last group.  Larger groups, as many heads
+    // as keep their key/value tiles within 32 MB of L2, shorten the tail
+    // (measured: 2-6 % at N = 1024..8192, D = 64 and 128).
+    if (kind == JVP_MASK_CAUSAL || causal_flag) {
+      const double kv_head = (tangent ? 4.0 : 2.0) * static_cast<double>(Nk) * D * e;
+      const int g_l2 = static_cast<int>((32.0 * 1048576.0) / kv_head);
+      p.group_heads = std::max(p.group_heads, std::min(static_cast<int>(B * H), g_l2));
+    }
     // Split-KV when the caller gave a large enough workspace and it pays (its
     // partial states are laid out for the kernel's D, so D < 64 does not split).
     const int splits = (D == kernel_d) ? choose_splits(B, H, Nq, Nk, dev->num_sms) : 1;
