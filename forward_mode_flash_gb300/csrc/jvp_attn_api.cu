@@ -871,9 +871,28 @@ struct SlotLayout {
   }
 };
 
-int64_t chunk_pairs(int64_t BH, int chunks) {
-  const int64_t c = std::max<int64_t>(1, std::min<int64_t>(chunks, BH));
-  return (BH + c - 1) / c;
+// Groups of (batch, head) pairs: min(chunks, BH) of them.  Their sizes fall
+// linearly (weights G, G - 1, ..., 1 on the pairs left after one per group),
+// so the last group -- whose kernel and device->host copies are all that
+// follows the last host->device copy -- is the smallest, while the copies of
+// the first groups, which run under no kernel anyway, carry the bulk.
+int64_t num_groups(int64_t BH, int chunks) {
+  return std::max<int64_t>(1, std::min<int64_t>(chunks, BH));
+}
+// First pair of group g of G (g = G gives BH): one pair per group plus the
+// weighted share of the other BH - G.
+int64_t group_edge(int64_t BH, int64_t G, int64_t g) {
+  const unsigned __int128 rest = static_cast<unsigned __int128>(BH - G);
+  const unsigned __int128 w = static_cast<unsigned __int128>(g * G - g * (g - 1) / 2);
+  const unsigned __int128 total = static_cast<unsigned __int128>(G * (G + 1) / 2);
+  return g + static_cast<int64_t>(rest * w / total);
+}
+// Pairs in the largest group (the staging slots hold one group each).
+int64_t max_group(int64_t BH, int chunks) {
+  const int64_t G = num_groups(BH, chunks);
+  int64_t m = 0;
+  for (int64_t g = 0; g < G; ++g) m = std::max(m, group_edge(BH, G, g + 1) - group_edge(BH, G, g));
+  return m;
 }
 
 jvp_status_t host_pipe(HostPipe** out) {
@@ -910,7 +929,7 @@ extern "C" size_t jvp_attn_fwd_dual_host_workspace_size(const jvp_shape_t* shape
   if (!jvp::dims_in_range(shape) || !jvp::checked_product({shape->B, shape->H}, &bh) ||
       !jvp::checked_product({bh, shape->Nq + shape->Nk, shape->D}, &rows) || rows > (1ll << 56))
     return 0;  // the call itself rejects this shape
-  const int64_t n = jvp::chunk_pairs(bh, chunks);
+  const int64_t n = jvp::max_group(bh, chunks);
   return 2 * jvp::SlotLayout(n, shape->Nq, shape->Nk, shape->D, jvp::elem_size(dtype)).bytes;
 }
 
@@ -954,8 +973,8 @@ extern "C" jvp_status_t jvp_attn_fwd_dual_host(
   if (s != JVP_OK) return s;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const size_t e = elem_size(dtype);
-  const int64_t BH = B * H, per = chunk_pairs(BH, chunks);
-  const SlotLayout L(per, Nq, Nk, D, e);
+  const int64_t BH = B * H, groups = num_groups(BH, chunks);
+  const SlotLayout L(max_group(BH, chunks), Nq, Nk, D, e);
   auto cu = [&](cudaError_t err, const char* what) -> jvp_status_t {
     if (err == cudaSuccess) return JVP_OK;
     return fail(JVP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(err));
@@ -967,8 +986,9 @@ extern "C" jvp_status_t jvp_attn_fwd_dual_host(
   if ((s = cu(cudaStreamWaitEvent(hp->out, hp->entry, 0), "cudaStreamWaitEvent")) != JVP_OK) return s;
   int last_path = 0;
   int last_slot = 0;
-  for (int64_t lo = 0, c = 0; lo < BH; lo += per, ++c) {
-    const int64_t n = std::min(per, BH - lo);
+  for (int64_t c = 0; c < groups; ++c) {
+    const int64_t lo = group_edge(BH, groups, c);
+    const int64_t n = group_edge(BH, groups, c + 1) - lo;
     const int sl = static_cast<int>(c & 1);
     last_slot = sl;
     uint8_t* base = static_cast<uint8_t*>(workspace) + sl * L.bytes;

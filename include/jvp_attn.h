@@ -179,8 +179,12 @@ size_t jvp_attn_fwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dt
  *   mask                  as for jvp_attn_fwd_dual, but a mask tensor must be
  *                         a DEVICE tensor shared by every (batch, head)
  *                         (stride_b = stride_h = 0).
- *   chunks                number of groups (>= 1; more groups overlap more but
- *                         launch smaller kernels).
+ *   chunks                number of groups (>= 1, at most B*H are used; more
+ *                         groups overlap more but launch smaller kernels).
+ *                         Group sizes fall linearly (one pair each plus shares
+ *                         weighted G, G-1, ..., 1 of the rest), so the last
+ *                         group -- whose kernel and copies back are all that
+ *                         follows the last copy in -- is the smallest.
  *   workspace             DEVICE scratch of at least
  *                         jvp_attn_fwd_dual_host_workspace_size(shape, dtype,
  *                         chunks) bytes, 256-byte aligned, owned by the caller.
@@ -201,7 +205,8 @@ jvp_status_t jvp_attn_fwd_dual_host(const jvp_shape_t* shape, jvp_dtype_t dtype,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Device staging bytes jvp_attn_fwd_dual_host needs: two slots, each holding
- * one group's six inputs, two outputs, lse and mu (0 for an invalid shape). */
+ * the largest group's six inputs, two outputs, lse and mu (0 for an invalid
+ * shape). */
 size_t jvp_attn_fwd_dual_host_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype,
                                              int chunks);
 
