@@ -123,6 +123,33 @@ struct BwdCtrl {
 // Per-(row, key) backward terms from the score-side values; xm is the
 // base-2 logit minus the row's base-2 log-sum-exp.  keep = false gives
 // all-zero terms (masked key, or a row that keeps no key).
+// One key's mask entries for N query rows (key-major kernel): loaded one by
+// one (the rows are strided in memory), all before they are needed.
+template <int MASK, int N>
+struct MaskCol {  // no per-entry data for none / causal
+  __device__ __forceinline__ void load(int, const void*, long long) {}
+  __device__ __forceinline__ bool keep(int) const { return true; }
+  __device__ __forceinline__ float add(int) const { return 0.f; }
+};
+template <int N>
+struct MaskCol<kMaskBool, N> {
+  uint32_t v[N];
+  __device__ __forceinline__ void load(int r, const void* m, long long idx) {
+    v[r] = static_cast<const uint8_t*>(m)[idx];
+  }
+  __device__ __forceinline__ bool keep(int r) const { return v[r] != 0u; }
+  __device__ __forceinline__ float add(int) const { return 0.f; }
+};
+template <int N>
+struct MaskCol<kMaskAdditive, N> {
+  float v[N];
+  __device__ __forceinline__ void load(int r, const void* m, long long idx) {
+    v[r] = static_cast<const float*>(m)[idx];
+  }
+  __device__ __forceinline__ bool keep(int) const { return true; }
+  __device__ __forceinline__ float add(int r) const { return v[r]; }
+};
+
 struct BwdTerms {
   float gS, gdS, P, dP;
 };
@@ -428,7 +455,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     FwdParams mp{};  // only the mask fields are used by MaskRegs
     mp.Nk = p.Nk;
     mp.msk = p.msk;
-    mp.mask_vec = 0;
+    mp.mask_vec = p.mask_vec;
     // One half of this warpgroup's 32 keys of a tile: gS and g_dS go into
     // the 16 columns of S the half has just read (gS first, g_dS next), so
     // the other half's inputs stay intact.
@@ -477,15 +504,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
     for (int t = 0; t < n_kv; ++t) {
       const int j0 = t * BN + wg * 32;
+      // Both halves' mask entries are requested before the wait for the
+      // tile's scores, so their latency overlaps it.
       MaskRegs<MASK, 16> m0, m1;
-      if (row_ok) m0.load(mp, mrow, j0);
+      if (row_ok) {
+        m0.load(mp, mrow, j0);
+        m1.load(mp, mrow, j0 + 16);
+      }
       if (!warp_wait(&ctrl->s_full[t % NBS], (t / NBS) & 1, status, abort) ||
           (NBS == 2 && !warp_wait(&ctrl->g_full, t & 1, status, abort))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (row_ok) m1.load(mp, mrow, j0 + 16);
       const uint32_t sb = static_cast<uint32_t>(t % NBS) * 128;
       half(j0, sb, wg * 32, m0);
       half(j0 + 16, sb, wg * 32 + 16, m1);
@@ -1004,6 +1035,18 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       const int st_i = t % NS;
       const int h = hk * p.kv_group + t / n_th;            // query head of this tile
       const int i0 = (t_begin + t % n_th) * BQ + wg * QW;  // first query row of this warpgroup
+      // This thread's key's mask entries for the warpgroup's QW rows, requested
+      // before the wait for the tile's scores so that their latency overlaps it
+      // (rows past Nq read row Nq - 1 and are not used).
+      MaskCol<MASK, QW> mcv;
+      if constexpr (MASK == kMaskBool || MASK == kMaskAdditive) {
+        const long long mcol = static_cast<long long>(b) * p.msb +
+                               static_cast<long long>(h) * p.msh +
+                               static_cast<long long>(key_ok ? j : 0) * p.msk;
+#pragma unroll
+        for (int q = 0; q < QW; ++q)
+          mcv.load(q, p.mask, mcol + static_cast<long long>(min(i0 + q, p.Nq - 1)) * p.msq);
+      }
       if (!warp_wait(&ctrl->s_full[t & 1], (t >> 1) & 1, status, abort) ||
           !warp_wait(&ctrl->q_full[st_i], (t / NS) & 1, status, abort)) {
         ok = false;
@@ -1012,11 +1055,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       tc_fence_after();
       const float4* rsc =
           reinterpret_cast<const float4*>(smem + L::OFF_SC + st_i * L::SCAL_BYTES) + wg * QW;
-      // Mask entries of this thread's key for the tile's rows: base + i * msq.
-      const long long mcol = static_cast<long long>(b) * p.msb + static_cast<long long>(h) * p.msh +
-                             static_cast<long long>(key_ok ? j : 0) * p.msk;
       const uint32_t bcol = (t & 1) * L::TM_BUF + wg * QW;
-#pragma unroll 1
+#pragma unroll
       for (int hq = 0; hq < QW / 16; ++hq) {
         // The 16-bit results go only into the 16 columns this half has just
         // read (S^T at col, dS^T at DS_OFF + col), so the other halves' inputs stay intact.
@@ -1045,15 +1085,9 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
             bool keep = key_ok && rv.x != -INFINITY;  // false for rows past Nq
             float x = fmaf(__uint_as_float(rs[qq + e]), c, -rv.x);
             if (causal) keep = keep && j <= i;
-            if constexpr (MASK == kMaskBool) {
-              if (keep)
-                keep = static_cast<const uint8_t*>(p.mask)[mcol + static_cast<long long>(i) * p.msq] != 0;
-            }
+            if constexpr (MASK == kMaskBool) keep = keep && mcv.keep(hq * 16 + qq + e);
             if constexpr (MASK == kMaskAdditive) {
-              const float m =
-                  keep ? static_cast<const float*>(p.mask)[mcol + static_cast<long long>(i) * p.msq]
-                       : 0.f;
-              x = fmaf(m, kLog2e, x);
+              x = fmaf(keep ? mcv.add(hq * 16 + qq + e) : 0.f, kLog2e, x);
               keep = keep && x != -INFINITY;
             }
             const float gv = L::kK ? __uint_as_float(rg[qq + e]) : 0.f;

@@ -534,6 +534,13 @@ jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
   p.kv_group = static_cast<int>(H / Hkv);
   p.mask = mptr;
   p.msb = msb, p.msh = msh, p.msq = msq, p.msk = msk;
+  {
+    const int64_t me = (kind == JVP_MASK_ADDITIVE) ? 4 : 1;
+    p.mask_vec = (mptr && msk == 1 && aligned(mptr, 16) && (msq * me) % 16 == 0 &&
+                  (msh * me) % 16 == 0 && (msb * me) % 16 == 0)
+                     ? 1
+                     : 0;
+  }
   p.q = in[0], p.k = in[1], p.v = in[2], p.dq = in[3], p.dk = in[4], p.dv = in[5];
   p.o = in[6], p.t_o = in[7], p.g_o = in[8], p.g_to = in[9];
   Strides* sin[10] = {&p.sq, &p.sk, &p.sv, &p.sdq, &p.sdk, &p.sdv, &p.so, &p.sto, &p.sgo, &p.sgto};

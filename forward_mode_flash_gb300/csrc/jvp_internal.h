@@ -104,6 +104,7 @@ struct BwdParams {
   int kv_group;  // query heads per key/value head (grouped-query attention; 1 = none)
   const void* mask;
   long long msb, msh, msq, msk;
+  int mask_vec;  // 1: mask rows are 16-byte aligned and stride_k == 1 (vector loads)
   const void *q, *k, *v, *dq, *dk, *dv, *o, *t_o, *g_o, *g_to;
   Strides sq, sk, sv, sdq, sdk, sdv, so, sto, sgo, sgto;
   const float* lse;
