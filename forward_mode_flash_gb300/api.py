@@ -303,9 +303,10 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
 
 def bwd_dual_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,
-                            dtype: torch.dtype = torch.bfloat16) -> int:
-    """Bytes of device scratch jvp_attn_bwd_dual needs for this shape."""
-    shape = _abi.Shape(B, H, Nq, Nk, D)
+                            dtype: torch.dtype = torch.bfloat16, hkv: int = 0) -> int:
+    """Bytes of device scratch jvp_attn_bwd_dual needs for this shape on the
+    current device (``hkv``: key/value heads, 0 = H)."""
+    shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
     return int(_abi.load().jvp_attn_bwd_dual_workspace_size(ctypes.byref(shape), _DT[dtype]))
 
 
@@ -329,7 +330,7 @@ def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
         if t.dtype != torch.float32 or tuple(t.shape) != (B, H, Nq) or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous float32 [B, H, Nq] tensor")
     outs = [torch.empty_like(x) for x in (q, k, v, dq, dk, dv)]
-    need = bwd_dual_workspace_size(B, H, Nq, Nk, D, q.dtype)
+    need = bwd_dual_workspace_size(B, H, Nq, Nk, D, q.dtype, hkv)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)
@@ -349,9 +350,10 @@ def bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, g_o, g_to,
 
 
 def bwd_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int,
-                       dtype: torch.dtype = torch.bfloat16) -> int:
-    """Bytes of device scratch jvp_attn_bwd needs for this shape."""
-    shape = _abi.Shape(B, H, Nq, Nk, D)
+                       dtype: torch.dtype = torch.bfloat16, hkv: int = 0) -> int:
+    """Bytes of device scratch jvp_attn_bwd needs for this shape on the
+    current device (``hkv``: key/value heads, 0 = H)."""
+    shape = _abi.Shape(B, H, Nq, Nk, D, hkv)
     return int(_abi.load().jvp_attn_bwd_workspace_size(ctypes.byref(shape), _DT[dtype]))
 
 
@@ -373,7 +375,7 @@ def bwd(q, k, v, o, lse, g_o, attn_mask: Optional[torch.Tensor] = None, is_causa
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
     outs = [torch.empty_like(x) for x in (q, k, v)]
-    need = bwd_workspace_size(B, H, Nq, Nk, D, q.dtype)
+    need = bwd_workspace_size(B, H, Nq, Nk, D, q.dtype, hkv)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     mask, _keep = _mask_desc(attn_mask, is_causal, B, H, Nq, Nk, q.device)

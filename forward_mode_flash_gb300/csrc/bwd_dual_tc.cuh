@@ -672,8 +672,12 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
   const int BH = p.B * Hkv;
   const int nk = (p.Nk + BK - 1) / BK;
   const int G = group_heads;
-  const int g = blockIdx.x / (G * nk);
-  const int rem = blockIdx.x - g * G * nk;
+  // Key-major split: the ksplits CTAs of one key tile are adjacent.
+  const int KS = p.ksplits > 1 ? p.ksplits : 1;
+  const int split = static_cast<int>(blockIdx.x % KS);
+  const int item = static_cast<int>(blockIdx.x / KS);
+  const int g = item / (G * nk);
+  const int rem = item - g * G * nk;
   const int Gg = min(G, BH - g * G);
   const int k_rank = rem / Gg;
   const int bhk = g * G + rem % Gg;
@@ -685,7 +689,11 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
       (MASK == kMaskCausal) || ((MASK == kMaskBool || MASK == kMaskAdditive) && p.causal != 0);
   const int t_begin = causal ? min(j0 / BQ, nqt) : 0;  // rows i >= j0 only
   const int n_th = nqt - t_begin;                       // query tiles per query head
-  const int n_t = n_th * p.kv_group;                    // tiles over the whole group
+  const int n_all = n_th * p.kv_group;                  // tiles over the whole group
+  // This CTA's tiles [t_lo, t_lo + n_t) of the group's (all of them unless split)
+  const int per_split = (n_all + KS - 1) / KS;
+  const int t_lo = min(n_all, split * per_split);
+  const int n_t = min(n_all, t_lo + per_split) - t_lo;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->k_full, 1);
@@ -748,10 +756,10 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
     const CUtensorMap* mgto = BQ == 64 ? &maps.gto64 : &maps.gto;
     float4 next[RPL];
     auto load_scalars = [&](int t) {
-      const int h = hk * p.kv_group + t / n_th;
+      const int h = hk * p.kv_group + (t_lo + t) / n_th;
 #pragma unroll
       for (int u = 0; u < RPL; ++u) {
-        const int i = (t_begin + t % n_th) * BQ + lane + 32 * u;
+        const int i = (t_begin + (t_lo + t) % n_th) * BQ + lane + 32 * u;
         float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
         if (i < p.Nq && JVP_CHECK(h < p.H, status, kChkGlobalRow)) {
           const long long idx = (static_cast<long long>(b) * p.H + h) * p.Nq + i;
@@ -771,8 +779,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
     auto load_q = [&](int tq) -> bool {
       const int sq = tq % NS;
       if (!mbar_wait(&ctrl->qq_empty[sq], ((tq / NS) & 1) ^ 1, abort)) return false;
-      const int hq = hk * p.kv_group + tq / n_th;
-      const int iq = (t_begin + tq % n_th) * BQ;
+      const int hq = hk * p.kv_group + (t_lo + tq) / n_th;
+      const int iq = (t_begin + (t_lo + tq) % n_th) * BQ;
       uint8_t* stq = smem + L::OFF_ST + sq * L::STAGE;
       mbar_arrive_expect_tx(&ctrl->qq_full[sq], L::QBLK);
       for (int c = 0; c < L::KCH; ++c) {
@@ -789,8 +797,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
     for (int t = 0; q_ok && t < n_t; ++t) {
       const int s = t % NS;
       const uint32_t ph = (t / NS) & 1;
-      const int h = hk * p.kv_group + t / n_th;  // query head of this tile
-      const int i0 = (t_begin + t % n_th) * BQ;
+      const int h = hk * p.kv_group + (t_lo + t) / n_th;  // query head of this tile
+      const int i0 = (t_begin + (t_lo + t) % n_th) * BQ;
       bool got = true;
       if (lane == 0) {
         if (L::kSplitStage && t + 1 < n_t) got = load_q(t + 1);
@@ -1033,8 +1041,8 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
     bool ok = true;
     for (int t = 0; t < n_t; ++t) {
       const int st_i = t % NS;
-      const int h = hk * p.kv_group + t / n_th;            // query head of this tile
-      const int i0 = (t_begin + t % n_th) * BQ + wg * QW;  // first query row of this warpgroup
+      const int h = hk * p.kv_group + (t_lo + t) / n_th;            // query head of this tile
+      const int i0 = (t_begin + (t_lo + t) % n_th) * BQ + wg * QW;  // first query row of this warpgroup
       // This thread's key's mask entries for the warpgroup's QW rows, requested
       // before the wait for the tile's scores so that their latency overlaps it
       // (rows past Nq read row Nq - 1 and are not used).
@@ -1133,6 +1141,10 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
         const float scl = which >= 2 ? s : 1.0f;
         T* row = static_cast<T*>(dst) + static_cast<long long>(b) * ds.b +
                  static_cast<long long>(hk) * ds.h + static_cast<long long>(key_ok ? j : 0) * ds.n;
+        // split: this CTA's fp32 partial row of the gradient
+        float* prow = p.kws + ((static_cast<long long>(split) * 4 + which) * BH + bhk) *
+                                  static_cast<long long>(p.Nk) * D +
+                      static_cast<long long>(key_ok ? j : 0) * D;
 #pragma unroll 1
         for (int col = 0; col < D; col += 32) {
           uint32_t a[32];
@@ -1141,6 +1153,18 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) a[e] = 0u;
+          }
+          if (KS > 1) {
+            if (key_ok && JVP_CHECK(j < p.Nk, status, kChkGlobalCol)) {
+              float4* pd = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                pd[v4] = make_float4(__uint_as_float(a[4 * v4]) * scl,
+                                     __uint_as_float(a[4 * v4 + 1]) * scl,
+                                     __uint_as_float(a[4 * v4 + 2]) * scl,
+                                     __uint_as_float(a[4 * v4 + 3]) * scl);
+            }
+            continue;
           }
           uint32_t po[16];
 #pragma unroll
@@ -1164,6 +1188,38 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Key-major split: adds the ksplits fp32 partial sums of each key-side
+// gradient in `which_mask` (bit w: 0 g_dV, 1 gV, 2 g_dK, 3 gK) and writes the
+// result, in the outputs' dtype, to the D real columns.  One thread per four
+// columns of one row of one gradient.
+template <typename T, int DK>
+__global__ void bwd_key_combine_kernel(const BwdParams p, int which_mask) {
+  const int Hkv = p.H / p.kv_group;
+  const long long rows = static_cast<long long>(p.B) * Hkv * p.Nk;
+  constexpr int kPieces = DK / 4;
+  const long long n = 4 * rows * kPieces;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int which = static_cast<int>(idx / (rows * kPieces));
+    const long long rr = (idx / kPieces) % rows;
+    const int c = static_cast<int>(idx % kPieces) * 4;
+    if (!((which_mask >> which) & 1) || c >= p.D) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < p.ksplits; ++sp) {
+      const float4 v = *reinterpret_cast<const float4*>(
+          p.kws + ((static_cast<long long>(sp) * 4 + which) * rows + rr) * DK + c);
+      acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+    }
+    const long long bhk = rr / p.Nk, jk = rr % p.Nk;
+    const long long b = bhk / Hkv, hk = bhk % Hkv;
+    void* dst = which == 0 ? p.g_dv : which == 1 ? p.g_v : which == 2 ? p.g_dk : p.g_k;
+    const Strides& ds = which == 0 ? p.sgdv : which == 1 ? p.sgv : which == 2 ? p.sgdk : p.sgk;
+    T* o = static_cast<T*>(dst) + b * ds.b + hk * ds.h + jk * ds.n + c;
+    *reinterpret_cast<uint2*>(o) =
+        make_uint2(ElemTraits<T>::pack(acc.x, acc.y), ElemTraits<T>::pack(acc.z, acc.w));
   }
 }
 
@@ -1218,6 +1274,7 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
     if (e != cudaSuccess) return e;
     const int nk = (p.Nk + L::BK - 1) / L::BK;
     const int BHk = p.B * (p.H / p.kv_group);
+    const int KS = p.ksplits > 1 ? p.ksplits : 1;
     int G = max(1, min(BHk, num_sms / max(1, nk)));
     if (MASK == kMaskCausal || p.causal) {  // as above, for the query side's tiles
       const double q_head =
@@ -1225,17 +1282,24 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
       G = max(G, min(BHk, static_cast<int>(32.0 * 1048576.0 / q_head)));
     }
     static_assert(L::BQ == 32 || L::BQ == 64, "query-side box heights of kmaps");
-    kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk), kBwdThreadsK, L::SMEM_BYTES,
-           kstream>>>(kmaps, p, G, status);
+    kern<<<static_cast<unsigned>(static_cast<long long>(nk) * BHk * KS), kBwdThreadsK,
+           L::SMEM_BYTES, kstream>>>(kmaps, p, G, status);
     return cudaGetLastError();
   };
+  cudaError_t e;
   if constexpr (D == 64 || PRIMAL) {
-    return key_side(std::integral_constant<int, 3>{});
+    e = key_side(std::integral_constant<int, 3>{});
   } else {
-    cudaError_t e = key_side(std::integral_constant<int, 1>{});
-    if (e != cudaSuccess) return e;
-    return key_side(std::integral_constant<int, 2>{});
+    e = key_side(std::integral_constant<int, 1>{});
+    if (e == cudaSuccess) e = key_side(std::integral_constant<int, 2>{});
   }
+  if (e == cudaSuccess && p.ksplits > 1) {
+    const long long n = 4LL * p.B * (p.H / p.kv_group) * p.Nk * (D / 4);
+    const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 8LL * num_sms));
+    bwd_key_combine_kernel<T, D><<<blocks, 256, 0, kstream>>>(p, PRIMAL ? 0xA : 0xF);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 template <typename T, int D, bool PRIMAL = false>

@@ -552,6 +552,8 @@ jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
   p.nu = static_cast<float*>(workspace);
   p.delta = p.nu + q_rows;
   p.primal = primal ? 1 : 0;
+  p.ksplits = 1;
+  p.kws = nullptr;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, at least one row and
@@ -587,6 +589,16 @@ jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
   }
   cudaError_t err;
   if (tc) {
+    // Few key-major CTAs (grouped-query heads, small B * Hkv): split each key
+    // tile's query tiles over several CTAs when the workspace has room for
+    // their partial sums.
+    const int ks = bwd_key_splits(B, Hkv, Nq, Nk, H / Hkv, dev->num_sms);
+    const size_t base = (bwd_workspace_bytes(q_rows) + 255) & ~static_cast<size_t>(255);
+    const size_t kbytes = bwd_key_split_bytes(ks, B, Hkv, Nk, D <= 64 ? 64 : 128);
+    if (ks > 1 && aligned(workspace, 16) && ws_bytes >= base + kbytes) {
+      p.ksplits = ks;
+      p.kws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base);
+    }
     err = launch_bwd_rows(static_cast<DType>(dtype), p, stream);
     // After the row pass the query-major and key-major kernels are
     // independent: the key side goes to the side stream, so the CTAs of
@@ -768,13 +780,37 @@ size_t jvp_attn_bwd_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype) 
   return jvp_attn_bwd_dual_workspace_size(shape, dtype);
 }
 
-size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t) {
+namespace jvp {
+// Workspace of the backward without a key-major split: nu and delta.
+size_t bwd_base_workspace_size(const jvp_shape_t* shape) {
   if (!shape || shape->B < 0 || shape->H < 0 || shape->Nq < 0) return 0;
   int64_t rows = 0;
-  if (!jvp::dims_in_range(shape) || !jvp::checked_product({shape->B, shape->H, shape->Nq}, &rows) ||
-      rows > jvp::kMaxDim)
+  if (!dims_in_range(shape) || !checked_product({shape->B, shape->H, shape->Nq}, &rows) ||
+      rows > kMaxDim)
     return SIZE_MAX;  // beyond any launch (jvp_attn_bwd_dual rejects the shape)
-  return jvp::bwd_workspace_bytes(rows);
+  return bwd_workspace_bytes(rows);
+}
+}  // namespace jvp
+
+size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype) {
+  const size_t base = jvp::bwd_base_workspace_size(shape);
+  if (base == 0 || base == SIZE_MAX) return base;
+  // plus the key-major split's partial sums, when the tensor-core path would
+  // split this shape on the current device
+  const int64_t D = shape->D, Hkv = shape->Hkv ? shape->Hkv : shape->H;
+  if ((dtype != JVP_F16 && dtype != JVP_BF16) || !(D == 16 || D == 32 || D == 64 || D == 128) ||
+      shape->Nq <= 0 || shape->Nk <= 0 || Hkv <= 0 || shape->H % Hkv != 0)
+    return base;
+  jvp::DeviceInfo* dev = nullptr;
+  if (jvp::current_device(&dev) != JVP_OK || !dev->sm103) {
+    cudaGetLastError();  // no usable device: no split
+    return base;
+  }
+  const int ks = jvp::bwd_key_splits(shape->B, Hkv, shape->Nq, shape->Nk, shape->H / Hkv,
+                                     dev->num_sms);
+  if (ks <= 1) return base;
+  return ((base + 255) & ~static_cast<size_t>(255)) +
+         jvp::bwd_key_split_bytes(ks, shape->B, Hkv, shape->Nk, D <= 64 ? 64 : 128);
 }
 
 jvp_status_t jvp_attn_get_device_status(void* stream) {
@@ -1101,8 +1137,9 @@ extern "C" jvp_status_t jvp_attn_bwd_dual_noalloc(
   if (!shape) return jvp::fail(JVP_ERR_INVALID_ARG, "shape is NULL");
   // (jvp_attn_bwd_dual_workspace_size returns SIZE_MAX for shapes whose
   // product of sizes overflows, so those are rejected here too)
+  (void)dtype;
   if (shape->B > 0 && shape->H > 0 && shape->Nq > 0 &&
-      jvp_attn_bwd_dual_workspace_size(shape, dtype) > JVP_BWD_NOALLOC_SCRATCH_BYTES)
+      jvp::bwd_base_workspace_size(shape) > JVP_BWD_NOALLOC_SCRATCH_BYTES)
     return jvp::fail(JVP_ERR_WORKSPACE,
                      "problem needs more than the 4 MiB fixed scratch of "
                      "jvp_attn_bwd_dual_noalloc (8 * B * H * Nq bytes); use jvp_attn_bwd_dual");

@@ -117,7 +117,36 @@ struct BwdParams {
   // are not read and may be NULL; g_dq, g_dk, g_dv are not written; the row
   // pass stores nu = 0 and delta = gO . O)
   int primal;
+  // Key-major split (ksplits > 1): each (batch, key/value head, key tile)'s
+  // query tiles are shared by ksplits CTAs, which write fp32 partial sums of
+  // (g_dV, gV, g_dK, gK) to kws [ksplits][4][B*Hkv][Nk][D]; a combine kernel
+  // adds them into the outputs.
+  int ksplits;
+  float* kws;
 };
+
+// Key-major splits of the backward for a problem: >1 when its key-major CTAs
+// (B * Hkv * ceil(Nk / 128)) fill less than half of the SMs and each walks
+// at least 64 query tiles of 64 rows (grouped-query heads, long sequences);
+// every split keeps 32 or more.  (Shorter loops do not repay the partial
+// sums' extra traffic and the combine kernel: measured slower.)
+inline int bwd_key_splits(long long B, long long Hkv, long long Nq, long long Nk, long long group,
+                          int num_sms) {
+  const long long ctas = B * Hkv * ((Nk + 127) / 128);
+  const long long tiles = ((Nq + 63) / 64) * group;  // query tiles of a CTA (64-row tiles)
+  if (ctas <= 0 || 2 * ctas > num_sms || tiles < 64) return 1;
+  long long s = num_sms / ctas;
+  s = s < 16 ? s : 16;
+  s = s < tiles / 32 ? s : tiles / 32;
+  return s > 1 ? static_cast<int>(s) : 1;
+}
+// Bytes of the key-major partial sums for `splits` (0 when not split).
+inline size_t bwd_key_split_bytes(int splits, long long B, long long Hkv, long long Nk,
+                                  long long D) {
+  return splits > 1 ? static_cast<size_t>(splits) * 4 * static_cast<size_t>(B * Hkv * Nk * D) *
+                          sizeof(float)
+                    : 0;
+}
 
 // Workspace bytes of the backward for a problem with `rows` = B * H * Nq query rows.
 inline size_t bwd_workspace_bytes(long long rows) {

@@ -15,7 +15,8 @@ kind, fp16 and bf16.
 * ``memory_scaling`` measures, with the caching allocator's peak counter, the
   device bytes that one call adds on top of its inputs: for ``fwd_dual`` (the
   outputs O, tO, lse, mu; the kernels allocate nothing), for ``bwd_dual`` (six
-  gradients and the 8 B H N byte workspace) and for one reverse-over-forward
+  gradients and its workspace: 8 B H N bytes, plus the key-major split's
+  partial sums, O(Nk), when few CTAs would run the key side) and for one reverse-over-forward
   step through ``JVPAttn.fwd_dual`` (the second-order use the page measures:
   saved tensors, gradients, workspace).  Every term is O(N); nothing N x N is
   ever stored.

@@ -237,10 +237,17 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
  *                         sum the contributions of every query head of the
  *                         group)
  *   out_strides           6 records in that order
- *   workspace             device scratch of at least
- *                         jvp_attn_bwd_dual_workspace_size() bytes, 4-byte
- *                         aligned, owned by the caller; its contents on entry
- *                         do not matter and are overwritten.
+ *   workspace             device scratch of at least 8 * B * H * Nq bytes
+ *                         (nu and delta per query row), 4-byte aligned, owned
+ *                         by the caller; its contents on entry do not matter
+ *                         and are overwritten.  With the (larger, 16-byte
+ *                         aligned) jvp_attn_bwd_dual_workspace_size() bytes,
+ *                         problems whose key-major CTAs would fill less than
+ *                         half of the SMs (few key/value heads, small B * H)
+ *                         share each key tile's query tiles among several
+ *                         CTAs, whose fp32 partial sums a combine kernel adds
+ *                         on the same stream (results differ from the unsplit
+ *                         kernels only by the order of fp32 additions).
  *
  * Every tensor has the same dtype; mask and scale as in the forward call.
  * fp16/bf16 with D in {16, 32, 64, 128} and 16-byte aligned tensors run a
@@ -265,9 +272,12 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
                                void* g_dk, void* g_dv, const jvp_strides_t* out_strides,
                                void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes jvp_attn_bwd_dual needs for `shape` (8 * B * H * Nq); 0 for
- * a NULL shape or a negative size, SIZE_MAX for a shape too large for any
- * launch (a size above 2^31 - 1, or B * H * Nq above it). */
+/* Workspace bytes jvp_attn_bwd_dual takes for `shape` on the current device:
+ * 8 * B * H * Nq, rounded up to 256 and plus splits * 4 * B * Hkv * Nk * D'
+ * * 4 bytes (D' = 64 for D <= 64, else 128; splits chosen from the SM count)
+ * when the tensor-core kernels split the key side of this shape.  0 for a NULL
+ * shape or a negative size, SIZE_MAX for a shape too large for any launch (a
+ * size above 2^31 - 1, or B * H * Nq above it). */
 size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
 
 /*
@@ -307,8 +317,9 @@ jvp_status_t jvp_attn_bwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
                           const jvp_strides_t* out_strides, void* workspace,
                           size_t workspace_bytes, void* stream);
 
-/* Workspace bytes jvp_attn_bwd needs for `shape` (the same as
- * jvp_attn_bwd_dual_workspace_size: 8 * B * H * Nq, 0 or SIZE_MAX likewise). */
+/* Workspace bytes jvp_attn_bwd takes for `shape` (the same as
+ * jvp_attn_bwd_dual_workspace_size; 8 * B * H * Nq bytes suffice, without the
+ * key-major split). */
 size_t jvp_attn_bwd_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);
 
 /*

@@ -1,0 +1,95 @@
+"""The backward's key-major split: when (batch, key/value head, key tile) CTAs
+would fill less than half of the SMs and each would walk 64 or more query
+tiles (grouped-query heads with few key/value heads), each key tile's query
+tiles are shared by several CTAs whose fp32 partial sums of gK, g_dK, gV,
+g_dV a combine kernel adds.
+
+Checked against the float64 oracle's reverse mode (the tolerance reading of
+the other backward tests: max-abs <= 2e-2 * max(1, max |reference|) per
+gradient), against the unsplit kernels (run with a workspace of the base size,
+8 * B * H * Nq bytes, which leaves no room for the partial sums: the two
+differ only by the order of fp32 additions), and for bit-identical repeats.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from forward_mode_flash_gb300 import api as A
+from forward_mode_flash_gb300 import build
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def np64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def make(dtype, B, H, Hkv, Nq, Nk, D, seed):
+    g = torch.Generator().manual_seed(seed)
+    dt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    mk = lambda h, n: torch.randn(B, h, n, D, generator=g).to(dt).cuda()
+    q, dq, go, gto = mk(H, Nq), mk(H, Nq), mk(H, Nq), mk(H, Nq)
+    k, v, dk, dv = mk(Hkv, Nk), mk(Hkv, Nk), mk(Hkv, Nk), mk(Hkv, Nk)
+    return q, k, v, dq, dk, dv, go, gto
+
+
+def reference(args, causal, group, primal):
+    q, k, v, dq, dk, dv, go, gto = (np64(x) for x in args)
+    rep = lambda x: np.repeat(x, group, axis=1)
+    if primal:
+        dq, dk, dv, gto = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv), np.zeros_like(gto)
+    r = oracle.bwd_dual(q, rep(k), rep(v), dq, rep(dk), rep(dv), go, gto,
+                        "causal" if causal else "none", None)
+    out = []
+    for name, x in zip(("g_q", "g_k", "g_v", "g_dq", "g_dk", "g_dv"), r):
+        if name in ("g_k", "g_v", "g_dk", "g_dv") and group > 1:
+            B, _, N, D = x.shape
+            x = x.reshape(B, -1, group, N, D).sum(axis=2)
+        out.append(x)
+    return out[:3] if primal else out
+
+
+def run(args, causal, primal, ws):
+    q, k, v, dq, dk, dv, go, gto = args
+    if primal:
+        o, lse = A.attention(q, k, v, is_causal=causal, return_lse=True)
+        return A.bwd(q, k, v, o, lse, go, is_causal=causal, workspace=ws)
+    o, t_o, lse, mu = A.fwd_dual(q, k, v, dq, dk, dv, is_causal=causal, return_stats=True,
+                                 split_kv=False)
+    return A.bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, go, gto, is_causal=causal,
+                      workspace=ws)
+
+
+@pytest.mark.parametrize("primal", [False, True])
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("bf16", 32)])
+@pytest.mark.parametrize("B,H,Hkv,Nq,Nk,causal", [(1, 8, 1, 512, 512, False),
+                                                 (2, 16, 1, 384, 256, True),
+                                                 (1, 4, 1, 1000, 300, False),
+                                                 (1, 16, 1, 256, 700, True)])
+def test_split_key_side_matches_oracle_and_unsplit(primal, dtype, D, B, H, Hkv, Nq, Nk, causal):
+    args = make(dtype, B, H, Hkv, Nq, Nk, D, seed=Nq + Nk + D)
+    need = A.bwd_dual_workspace_size(B, H, Nq, Nk, D, hkv=Hkv)
+    base = 8 * B * H * Nq
+    assert need > base  # these shapes split on a GB300 (152 SMs)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    got = run(args, causal, primal, ws)
+    torch.cuda.synchronize()
+    assert A.device_status() == 0 and A.last_path() == 1
+    unsplit = run(args, causal, primal, torch.empty(base, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    ref = reference(args, causal, H // Hkv, primal)
+    for x, u, r in zip(got, unsplit, ref):
+        scale = max(1.0, float(np.abs(r).max()))
+        assert np.abs(np64(x) - r).max() <= TOL * scale
+        assert np.abs(np64(x) - np64(u)).max() <= TOL * scale
+    again = run(args, causal, primal, ws)
+    for x, y in zip(got, again):
+        assert torch.equal(x, y)

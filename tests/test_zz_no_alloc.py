@@ -59,7 +59,9 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
     build.build()
     # Both entry points run the same kernels in the same order, so the results
     # must be bit-identical; the workspace of the reference call is filled with
-    # NaN first, so neither side can lean on scratch contents left behind.
+    # NaN first, so neither side can lean on scratch contents left behind.  It
+    # has the base size (8 * B * H * Nq bytes), so the reference does not split
+    # the key side (the fixed scratch holds no partial sums) either.
     B, H, Nq = 8, 16, 4096  # 8 * B * H * Nq == 4 MiB: exactly the fixed scratch
     assert 8 * B * H * Nq == _abi.JVP_BWD_NOALLOC_SCRATCH_BYTES
     cases = [(synth.small("bf16", 2, 4, 300, 64, "causal", seed=31), 1),
@@ -68,8 +70,7 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
              (synth.small("bf16", 1, 2, 130, 128, "causal", seed=34), 1)]
     for w, path in cases:  # calls in a row; each reuses the scratch the previous one left
         g, o, t_o, lse, mu, go, gto, causal = _case(w)
-        ws = torch.full((api.bwd_dual_workspace_size(w.B, w.H, w.N, w.n_keys, w.D) // 4,),
-                        float("nan"), dtype=torch.float32, device="cuda")
+        ws = torch.full((2 * w.B * w.H * w.N,), float("nan"), dtype=torch.float32, device="cuda")
         ref = api.bwd_dual(*g, o, t_o, lse, mu, go, gto, is_causal=causal, workspace=ws)
         got = call_noalloc(*g, o, t_o, lse, mu, go, gto, causal)
         assert api.last_path() == path, (w.name, api.last_path())
