@@ -197,8 +197,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int BH = p.B * p.H;
   const int nq = (p.Nq + BM - 1) / BM;
   const int G = group_heads;
-  const int g = blockIdx.x / (G * nq);
-  const int rem = blockIdx.x - g * G * nq;
+  // Query-major split: the qsplits CTAs of one query tile are adjacent.
+  const int QS = p.qsplits > 1 ? p.qsplits : 1;
+  const int split = static_cast<int>(blockIdx.x % QS);
+  const int item = static_cast<int>(blockIdx.x / QS);
+  const int g = item / (G * nq);
+  const int rem = item - g * G * nq;
   const int Gg = min(G, BH - g * G);
   const int q_rank = rem / Gg;
   const int bh = g * G + rem % Gg;
@@ -209,8 +213,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int b = bh / p.H, h = bh % p.H;
   const int hk = h / p.kv_group;  // key/value head (grouped-query attention)
   const int q0 = qt * BM;
-  int n_kv = (p.Nk + BN - 1) / BN;
-  if (causal) n_kv = min(n_kv, (min(q0 + BM, p.Nq) - 1) / BN + 1);
+  int n_all = (p.Nk + BN - 1) / BN;
+  if (causal) n_all = min(n_all, (min(q0 + BM, p.Nq) - 1) / BN + 1);
+  // This CTA's key tiles [kv_lo, kv_lo + n_kv) (all of them unless split).
+  const int per_split = (n_all + QS - 1) / QS;
+  const int kv_lo = min(n_all, split * per_split);
+  const int n_kv = min(n_all, kv_lo + per_split) - kv_lo;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
@@ -261,7 +269,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int kf = 0, vf = 0;
       for (int t = 0; t < n_kv; ++t) {
         const int sk = t % NSK, sv = t % NSV;
-        const int j0 = t * BN;
+        const int j0 = (kv_lo + t) * BN;
         if (!mbar_wait(&ctrl->k_empty[sk], ((t / NSK) & 1) ^ 1, abort)) {
           record_timeout(status, abort);
           break;
@@ -503,7 +511,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     };
     for (int t = 0; t < n_kv; ++t) {
-      const int j0 = t * BN + wg * 32;
+      const int j0 = (kv_lo + t) * BN + wg * 32;
       // Both halves' mask entries are requested before the wait for the
       // tile's scores, so their latency overlaps it.
       MaskRegs<MASK, 16> m0, m1;
@@ -534,6 +542,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const Strides& ds = wg == 0 ? p.sgdq : p.sgq;
       T* row = static_cast<T*>(dst) + static_cast<long long>(b) * ds.b +
                static_cast<long long>(h) * ds.h + static_cast<long long>(row_ok ? i : 0) * ds.n;
+      // split: this CTA's fp32 partial row (slot 0 g_dQ, 1 gQ)
+      float* prow = p.qws + ((static_cast<long long>(split) * 2 + wg) * BH + bh) *
+                                static_cast<long long>(p.Nq) * D +
+                    static_cast<long long>(row_ok ? i : 0) * D;
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
         uint32_t a[32];
@@ -542,6 +554,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) a[e] = 0u;
+        }
+        if (QS > 1) {
+          if (row_ok && JVP_CHECK(i < p.Nq, status, kChkGlobalCol)) {
+            float4* pd = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              pd[v4] = make_float4(__uint_as_float(a[4 * v4]) * s, __uint_as_float(a[4 * v4 + 1]) * s,
+                                   __uint_as_float(a[4 * v4 + 2]) * s,
+                                   __uint_as_float(a[4 * v4 + 3]) * s);
+          }
+          continue;
         }
         uint32_t po[16];
 #pragma unroll
@@ -1191,6 +1214,36 @@ __global__ void __launch_bounds__(kBwdThreadsK, 1)
   }
 }
 
+// Query-major split: adds the qsplits fp32 partial sums of g_dQ (slot 0, when
+// bit 0 of which_mask) and gQ (slot 1, bit 1) into the outputs' dtype, D real
+// columns.  One thread per four columns of one row.
+template <typename T, int DK>
+__global__ void bwd_query_combine_kernel(const BwdParams p, int which_mask) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
+  constexpr int kPieces = DK / 4;
+  const long long n = 2 * rows * kPieces;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int which = static_cast<int>(idx / (rows * kPieces));
+    const long long rr = (idx / kPieces) % rows;
+    const int c = static_cast<int>(idx % kPieces) * 4;
+    if (!((which_mask >> which) & 1) || c >= p.D) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < p.qsplits; ++sp) {
+      const float4 v = *reinterpret_cast<const float4*>(
+          p.qws + ((static_cast<long long>(sp) * 2 + which) * rows + rr) * DK + c);
+      acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+    }
+    const long long bh = rr / p.Nq, i = rr % p.Nq;
+    const long long b = bh / p.H, h = bh % p.H;
+    void* dst = which == 0 ? p.g_dq : p.g_q;
+    const Strides& ds = which == 0 ? p.sgdq : p.sgq;
+    T* o = static_cast<T*>(dst) + b * ds.b + h * ds.h + i * ds.n + c;
+    *reinterpret_cast<uint2*>(o) =
+        make_uint2(ElemTraits<T>::pack(acc.x, acc.y), ElemTraits<T>::pack(acc.z, acc.w));
+  }
+}
+
 // Key-major split: adds the ksplits fp32 partial sums of each key-side
 // gradient in `which_mask` (bit w: 0 g_dV, 1 gV, 2 g_dK, 3 gK) and writes the
 // result, in the outputs' dtype, to the D real columns.  One thread per four
@@ -1261,10 +1314,18 @@ cudaError_t launch_bwd_tc_variant(const BwdTcMaps& qmaps, const BwdTcMaps& kmaps
       const double kv_head = (PRIMAL ? 2.0 : 4.0) * static_cast<double>(p.Nk) * D * sizeof(T);
       G = max(G, min(BH, static_cast<int>(32.0 * 1048576.0 / kv_head)));
     }
-    kern<<<static_cast<unsigned>(static_cast<long long>(nq) * BH), kBwdThreads, L::SMEM_BYTES,
-           stream>>>(qmaps, p, G, status);
+    const int QS = p.qsplits > 1 ? p.qsplits : 1;
+    kern<<<static_cast<unsigned>(static_cast<long long>(nq) * BH * QS), kBwdThreads,
+           L::SMEM_BYTES, stream>>>(qmaps, p, G, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (QS > 1) {
+      const long long n = 2LL * BH * p.Nq * (D / 4);
+      const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 8LL * num_sms));
+      bwd_query_combine_kernel<T, D><<<blocks, 256, 0, stream>>>(p, PRIMAL ? 0x2 : 0x3);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   auto key_side = [&](auto part_tag) -> cudaError_t {
     constexpr int PART = decltype(part_tag)::value;

@@ -554,6 +554,8 @@ jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
   p.primal = primal ? 1 : 0;
   p.ksplits = 1;
   p.kws = nullptr;
+  p.qsplits = 1;
+  p.qws = nullptr;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, at least one row and
@@ -592,12 +594,25 @@ jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
     // Few key-major CTAs (grouped-query heads, small B * Hkv): split each key
     // tile's query tiles over several CTAs when the workspace has room for
     // their partial sums.
+    // The same for few query-major CTAs walking many key tiles (few queries,
+    // many keys): each query tile's key tiles over several CTAs.
+    const int kd = D <= 64 ? 64 : 128;
     const int ks = bwd_key_splits(B, Hkv, Nq, Nk, H / Hkv, dev->num_sms);
+    const int qs = bwd_query_splits(B, H, Nq, Nk, dev->num_sms);
     const size_t base = (bwd_workspace_bytes(q_rows) + 255) & ~static_cast<size_t>(255);
-    const size_t kbytes = bwd_key_split_bytes(ks, B, Hkv, Nk, D <= 64 ? 64 : 128);
-    if (ks > 1 && aligned(workspace, 16) && ws_bytes >= base + kbytes) {
-      p.ksplits = ks;
-      p.kws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base);
+    const size_t kbytes = bwd_key_split_bytes(ks, B, Hkv, Nk, kd);
+    const size_t qbytes = bwd_query_split_bytes(qs, B, H, Nq, kd);
+    // (The no-allocation entry point, `fork` false, keeps its fixed scratch
+    // for nu and delta and runs unsplit.)
+    if (fork && aligned(workspace, 16) && ws_bytes >= base + kbytes + qbytes) {
+      if (ks > 1) {
+        p.ksplits = ks;
+        p.kws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base);
+      }
+      if (qs > 1) {
+        p.qsplits = qs;
+        p.qws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base + kbytes);
+      }
     }
     err = launch_bwd_rows(static_cast<DType>(dtype), p, stream);
     // After the row pass the query-major and key-major kernels are
@@ -808,9 +823,12 @@ size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dt
   }
   const int ks = jvp::bwd_key_splits(shape->B, Hkv, shape->Nq, shape->Nk, shape->H / Hkv,
                                      dev->num_sms);
-  if (ks <= 1) return base;
+  const int qs = jvp::bwd_query_splits(shape->B, shape->H, shape->Nq, shape->Nk, dev->num_sms);
+  if (ks <= 1 && qs <= 1) return base;
+  const int kd = D <= 64 ? 64 : 128;
   return ((base + 255) & ~static_cast<size_t>(255)) +
-         jvp::bwd_key_split_bytes(ks, shape->B, Hkv, shape->Nk, D <= 64 ? 64 : 128);
+         jvp::bwd_key_split_bytes(ks, shape->B, Hkv, shape->Nk, kd) +
+         jvp::bwd_query_split_bytes(qs, shape->B, shape->H, shape->Nq, kd);
 }
 
 jvp_status_t jvp_attn_get_device_status(void* stream) {

@@ -123,6 +123,11 @@ struct BwdParams {
   // adds them into the outputs.
   int ksplits;
   float* kws;
+  // Query-major split (qsplits > 1): each (batch, head, query tile)'s key
+  // tiles are shared by qsplits CTAs, which write fp32 partial sums of
+  // (g_dQ, gQ) to qws [qsplits][2][B*H][Nq][D]; a combine kernel adds them.
+  int qsplits;
+  float* qws;
 };
 
 // Key-major splits of the backward for a problem: >1 when its key-major CTAs
@@ -139,6 +144,24 @@ inline int bwd_key_splits(long long B, long long Hkv, long long Nq, long long Nk
   s = s < 16 ? s : 16;
   s = s < tiles / 32 ? s : tiles / 32;
   return s > 1 ? static_cast<int>(s) : 1;
+}
+// Query-major splits: the same rule for the query-major CTAs (B * H *
+// ceil(Nq / 128)) walking 64 or more key tiles of 64 (few queries, many keys).
+inline int bwd_query_splits(long long B, long long H, long long Nq, long long Nk, int num_sms) {
+  const long long ctas = B * H * ((Nq + 127) / 128);
+  const long long tiles = (Nk + 63) / 64;
+  if (ctas <= 0 || 2 * ctas > num_sms || tiles < 64) return 1;
+  long long s = num_sms / ctas;
+  s = s < 16 ? s : 16;
+  s = s < tiles / 32 ? s : tiles / 32;
+  return s > 1 ? static_cast<int>(s) : 1;
+}
+// Bytes of the query-major partial sums for `splits` (0 when not split).
+inline size_t bwd_query_split_bytes(int splits, long long B, long long H, long long Nq,
+                                    long long D) {
+  return splits > 1 ? static_cast<size_t>(splits) * 2 * static_cast<size_t>(B * H * Nq * D) *
+                          sizeof(float)
+                    : 0;
 }
 // Bytes of the key-major partial sums for `splits` (0 when not split).
 inline size_t bwd_key_split_bytes(int splits, long long B, long long Hkv, long long Nk,

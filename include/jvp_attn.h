@@ -243,11 +243,14 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
  *                         and are overwritten.  With the (larger, 16-byte
  *                         aligned) jvp_attn_bwd_dual_workspace_size() bytes,
  *                         problems whose key-major CTAs would fill less than
- *                         half of the SMs (few key/value heads, small B * H)
- *                         share each key tile's query tiles among several
- *                         CTAs, whose fp32 partial sums a combine kernel adds
- *                         on the same stream (results differ from the unsplit
- *                         kernels only by the order of fp32 additions).
+ *                         half of the SMs and each walk 64+ query tiles (few
+ *                         key/value heads) share each key tile's query tiles
+ *                         among several CTAs, and likewise each query tile's
+ *                         key tiles when few query-major CTAs walk 64+ key
+ *                         tiles (few queries, many keys); a combine kernel
+ *                         adds the fp32 partial sums on the same stream
+ *                         (results differ from the unsplit kernels only by
+ *                         the order of fp32 additions).
  *
  * Every tensor has the same dtype; mask and scale as in the forward call.
  * fp16/bf16 with D in {16, 32, 64, 128} and 16-byte aligned tensors run a
@@ -273,9 +276,10 @@ jvp_status_t jvp_attn_bwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, cons
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes jvp_attn_bwd_dual takes for `shape` on the current device:
- * 8 * B * H * Nq, rounded up to 256 and plus splits * 4 * B * Hkv * Nk * D'
- * * 4 bytes (D' = 64 for D <= 64, else 128; splits chosen from the SM count)
- * when the tensor-core kernels split the key side of this shape.  0 for a NULL
+ * 8 * B * H * Nq, rounded up to 256, plus ks * 4 * B * Hkv * Nk * D' * 4
+ * bytes when the tensor-core kernels split the key side of this shape into ks
+ * parts and qs * 2 * B * H * Nq * D' * 4 bytes when they split the query side
+ * into qs (D' = 64 for D <= 64, else 128; ks and qs from the SM count).  0 for a NULL
  * shape or a negative size, SIZE_MAX for a shape too large for any launch (a
  * size above 2^31 - 1, or B * H * Nq above it). */
 size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dtype);

@@ -1,8 +1,10 @@
-"""The backward's key-major split: when (batch, key/value head, key tile) CTAs
-would fill less than half of the SMs and each would walk 64 or more query
-tiles (grouped-query heads with few key/value heads), each key tile's query
-tiles are shared by several CTAs whose fp32 partial sums of gK, g_dK, gV,
-g_dV a combine kernel adds.
+"""The backward's splits: when (batch, key/value head, key tile) CTAs would
+fill less than half of the SMs and each would walk 64 or more query tiles
+(grouped-query heads with few key/value heads), each key tile's query tiles
+are shared by several CTAs whose fp32 partial sums of gK, g_dK, gV, g_dV a
+combine kernel adds; likewise each query tile's key tiles when few
+query-major CTAs would walk 64 or more key tiles (few queries, many keys),
+with partial sums of gQ and g_dQ.
 
 Checked against the float64 oracle's reverse mode (the tolerance reading of
 the other backward tests: max-abs <= 2e-2 * max(1, max |reference|) per
@@ -93,3 +95,28 @@ def test_split_key_side_matches_oracle_and_unsplit(primal, dtype, D, B, H, Hkv, 
     again = run(args, causal, primal, ws)
     for x, y in zip(got, again):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("primal", [False, True])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 64), ("bf16", 16)])
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", [(1, 4, 100, 4096, False),
+                                             (2, 2, 300, 5000, False),
+                                             (1, 2, 256, 4100, True)])
+def test_split_query_side_matches_oracle_and_unsplit(primal, dtype, D, B, H, Nq, Nk, causal):
+    # Few queries, many keys: the query-major CTAs (B * H * ceil(Nq / 128))
+    # each walk 64+ key tiles, so each query tile's key tiles are shared by
+    # several CTAs and a combine kernel adds their partial g_dQ, gQ.
+    args = make(dtype, B, H, H, Nq, Nk, D, seed=Nq + 3 * Nk + D)
+    need = A.bwd_dual_workspace_size(B, H, Nq, Nk, D)
+    base = 8 * B * H * Nq
+    assert need > base  # these shapes split on a GB300 (152 SMs)
+    got = run(args, causal, primal, torch.empty(need, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert A.device_status() == 0 and A.last_path() == 1
+    unsplit = run(args, causal, primal, torch.empty(base, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    ref = reference(args, causal, 1, primal)
+    for x, u, r in zip(got, unsplit, ref):
+        scale = max(1.0, float(np.abs(r).max()))
+        assert np.abs(np64(x) - r).max() <= TOL * scale
+        assert np.abs(np64(x) - np64(u)).max() <= TOL * scale
