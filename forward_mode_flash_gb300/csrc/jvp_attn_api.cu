@@ -192,6 +192,10 @@ bool encode_mask_map(CUtensorMap* map, const void* ptr, int64_t B, int64_t H, in
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Head dimensions the tensor-core kernels take (the D = 64 or 128 kernel,
+// columns past D zero-filled by TMA): multiples of 8 (16-byte rows) up to 128.
+bool tc_head_dim(int64_t D) { return D >= 8 && D <= 128 && D % 8 == 0; }
+
 bool strides_aligned16(const jvp_strides_t& s, size_t e) {
   return (s.b * static_cast<int64_t>(e)) % 16 == 0 && (s.h * static_cast<int64_t>(e)) % 16 == 0 &&
          (s.n * static_cast<int64_t>(e)) % 16 == 0;
@@ -364,14 +368,14 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
   p.status = dev->status;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-  // Tensor-core path: fp16/bf16, D in {16, 32, 64, 128}, a nonzero scale, at
-  // least one key, and every tensor 16-byte aligned with 16-byte-multiple
-  // strides.  D = 16 and 32 run the D = 64 kernel: the tensor maps' 64-column
-  // boxes reach past the D columns of each row, TMA fills those with zeros
-  // (they add nothing to Q K^T, dQ K^T or Q dK^T and give zero columns of
-  // A and T), and the output maps' stores drop them.
-  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) &&
-            (D == 16 || D == 32 || D == 64 || D == 128) && scale != 0.f && Nk > 0;
+  // Tensor-core path: fp16/bf16, D a multiple of 8 up to 128, a nonzero
+  // scale, at least one key, and every tensor 16-byte aligned with
+  // 16-byte-multiple strides.  D <= 64 runs the D = 64 kernel and larger D the
+  // D = 128 kernel: the tensor maps' 64-column boxes reach past the D columns
+  // of each row, TMA fills those with zeros (they add nothing to Q K^T,
+  // dQ K^T or Q dK^T and give zero columns of A and T), and the output maps'
+  // stores drop them.
+  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) && tc_head_dim(D) && scale != 0.f && Nk > 0;
   const int kernel_d = D <= 64 ? 64 : 128;
   for (int t = 0; tc && t < n_in; ++t)
     tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
@@ -562,8 +566,7 @@ jvp_status_t backward(bool primal, const jvp_shape_t* shape, jvp_dtype_t dtype,
   // one key, every tensor 16-byte aligned with 16-byte-multiple strides.  As in
   // the forward, D = 16 and 32 run the D = 64 kernels on zero-filled columns
   // (their gradient stores stop at D).
-  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) &&
-            (D == 16 || D == 32 || D == 64 || D == 128) && Nq > 0 && Nk > 0;
+  bool tc = (dtype == JVP_F16 || dtype == JVP_BF16) && tc_head_dim(D) && Nq > 0 && Nk > 0;
   for (int t = 0; tc && t < 10; ++t) tc = aligned(in[t], 16) && strides_aligned16(in_strides[t], e);
   for (int t = 0; tc && t < 6; ++t) tc = aligned(out[t], 16) && strides_aligned16(out_strides[t], e);
   // Tensor maps: qm for the query-major kernel (query side 128 rows, key side
@@ -813,7 +816,7 @@ size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dt
   // plus the key-major split's partial sums, when the tensor-core path would
   // split this shape on the current device
   const int64_t D = shape->D, Hkv = shape->Hkv ? shape->Hkv : shape->H;
-  if ((dtype != JVP_F16 && dtype != JVP_BF16) || !(D == 16 || D == 32 || D == 64 || D == 128) ||
+  if ((dtype != JVP_F16 && dtype != JVP_BF16) || !jvp::tc_head_dim(D) ||
       shape->Nq <= 0 || shape->Nk <= 0 || Hkv <= 0 || shape->H % Hkv != 0)
     return base;
   jvp::DeviceInfo* dev = nullptr;

@@ -121,11 +121,11 @@ typedef struct {
  *   lse, mu        NULL or [B,H,Nq] contiguous float32 outputs (device).
  *   stream         cudaStream_t as void*.
  *
- * fp16/bf16 inputs with D in {16, 32, 64, 128}, 16-byte aligned base pointers
- * and strides take the tensor-core path (TMA + tcgen05 + TMEM, fp32
- * accumulation; D = 16 and 32 run the D = 64 kernel on zero-filled columns);
- * every other valid case (float32, other D) takes the CUDA-core path, which
- * computes in fp32 FFMA.
+ * fp16/bf16 inputs with D a multiple of 8 up to 128, 16-byte aligned base
+ * pointers and strides take the tensor-core path (TMA + tcgen05 + TMEM, fp32
+ * accumulation; D <= 64 runs the D = 64 kernel and larger D the D = 128
+ * kernel, on zero-filled columns past D); every other valid case (float32,
+ * other D) takes the CUDA-core path, which computes in fp32 FFMA.
  */
 jvp_status_t jvp_attn_fwd_dual(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* q,
                                const void* k, const void* v, const void* dq, const void* dk,
@@ -253,11 +253,11 @@ jvp_status_t jvp_attn_fwd(const jvp_shape_t* shape, jvp_dtype_t dtype, const voi
  *                         the order of fp32 additions).
  *
  * Every tensor has the same dtype; mask and scale as in the forward call.
- * fp16/bf16 with D in {16, 32, 64, 128} and 16-byte aligned tensors run a
- * row pass and tcgen05 kernels (query-major for g_q, g_dq; key-major for g_k,
- * g_dk, g_v, g_dv), fp32 accumulation (D = 16 and 32 on the D = 64 kernels,
- * with zero-filled columns); every other case runs three CUDA-core kernels in
- * fp32.  All work is ordered on `stream`: the key-major kernels run on a
+ * fp16/bf16 with D a multiple of 8 up to 128 and 16-byte aligned tensors run
+ * a row pass and tcgen05 kernels (query-major for g_q, g_dq; key-major for
+ * g_k, g_dk, g_v, g_dv), fp32 accumulation (the D = 64 or 128 kernels, with
+ * zero-filled columns past D); every other case runs three CUDA-core kernels
+ * in fp32.  All work is ordered on `stream`: the key-major kernels run on a
  * stream the library owns (one per device, created on first use), which waits
  * for the row pass through an event, and `stream` waits for them through
  * another event before anything enqueued after this call, so the two
@@ -307,8 +307,8 @@ size_t jvp_attn_bwd_dual_workspace_size(const jvp_shape_t* shape, jvp_dtype_t dt
  *                  entry do not matter and are overwritten.
  *
  * Every tensor has the same dtype; mask and scale as in the forward call.
- * fp16/bf16 with D in {16, 32, 64, 128} and 16-byte aligned tensors run a row
- * pass and two tcgen05 kernels (query-major for g_q; key-major for g_k and
+ * fp16/bf16 with D a multiple of 8 up to 128 and 16-byte aligned tensors run
+ * a row pass and two tcgen05 kernels (query-major for g_q; key-major for g_k and
  * g_v in one pass at every D, on the library's second stream as in
  * jvp_attn_bwd_dual); every other case runs three CUDA-core kernels in fp32.
  * All work is ordered on `stream`.  Returns JVP_ERR_WORKSPACE if the

@@ -127,12 +127,22 @@ def test_cuda_core_path_f32(D, mask):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-@pytest.mark.parametrize("D", [16, 32, 80])
+@pytest.mark.parametrize("D", [8, 16, 24, 32, 48, 80, 96, 112, 20, 100])
 def test_half_precision_other_head_dims(dtype, D):
-    # D = 16 and 32 take the tensor-core kernel (zero-filled columns up to 64);
-    # other head dimensions the CUDA-core kernel.
+    # Multiples of 8 up to 128 take the tensor-core kernels (the D = 64 or 128
+    # kernel, columns past D zero-filled); other head dimensions the
+    # CUDA-core kernel.
     w = synth.small(dtype, 1, 2, 70, D, "causal", seed=D)
-    compare_full(w, expect_path=1 if D in (16, 32) else 2)
+    compare_full(w, expect_path=1 if D % 8 == 0 else 2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [8, 40, 72, 96, 120])
+@pytest.mark.parametrize("N", [129, 300])
+@pytest.mark.parametrize("mask", ["none", "causal", "bool", "additive"])
+def test_tensor_core_path_head_dims_between_powers_of_two(dtype, D, N, mask):
+    w = synth.small(dtype, 2, 3, N, D, mask, seed=N + D + len(mask))
+    compare_full(w, expect_path=1)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
