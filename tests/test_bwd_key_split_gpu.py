@@ -120,3 +120,49 @@ def test_split_query_side_matches_oracle_and_unsplit(primal, dtype, D, B, H, Nq,
         scale = max(1.0, float(np.abs(r).max()))
         assert np.abs(np64(x) - r).max() <= TOL * scale
         assert np.abs(np64(x) - np64(u)).max() <= TOL * scale
+
+
+@pytest.mark.parametrize("primal", [False, True])
+@pytest.mark.parametrize("kind", ["bool", "additive"])
+@pytest.mark.parametrize("B,H,Hkv,Nq,Nk", [(1, 8, 1, 512, 512), (1, 4, 4, 100, 4096)])
+def test_splits_with_masks(primal, kind, B, H, Hkv, Nq, Nk):
+    # Both splits under a [B, 1, Nq, Nk] mask (the first shape splits the key
+    # side, the second the query side), with the causal rule on top of it.
+    D = 64
+    args = make("bf16", B, H, Hkv, Nq, Nk, D, seed=Nq + Nk + len(kind))
+    g = torch.Generator().manual_seed(Nk)
+    if kind == "bool":
+        m = torch.rand(B, 1, Nq, Nk, generator=g) < 0.8
+        dense = np.broadcast_to(m.numpy(), (B, H, Nq, Nk)).copy()
+    else:
+        m = torch.randn(B, 1, Nq, Nk, generator=g)
+        dense = np.broadcast_to(m.double().numpy(), (B, H, Nq, Nk)).copy()
+    above = np.triu(np.ones((Nq, Nk), dtype=bool), k=1)
+    dense[..., above] = False if kind == "bool" else -np.inf
+    mc = m.cuda()
+    q, k, v, dq, dk, dv, go, gto = args
+    need = A.bwd_dual_workspace_size(B, H, Nq, Nk, D, hkv=Hkv)
+    assert need > 8 * B * H * Nq
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if primal:
+        o, lse = A.attention(q, k, v, attn_mask=mc, is_causal=True, return_lse=True)
+        got = A.bwd(q, k, v, o, lse, go, attn_mask=mc, is_causal=True, workspace=ws)
+    else:
+        o, t_o, lse, mu = A.fwd_dual(q, k, v, dq, dk, dv, attn_mask=mc, is_causal=True,
+                                     return_stats=True, split_kv=False)
+        got = A.bwd_dual(q, k, v, dq, dk, dv, o, t_o, lse, mu, go, gto, attn_mask=mc,
+                         is_causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert A.device_status() == 0 and A.last_path() == 1
+    xs = [np64(x) for x in args]
+    rep = lambda x: np.repeat(x, H // Hkv, axis=1)
+    if primal:
+        for i in (3, 4, 5, 7):
+            xs[i] = np.zeros_like(xs[i])
+    r = oracle.bwd_dual(xs[0], rep(xs[1]), rep(xs[2]), xs[3], rep(xs[4]), rep(xs[5]), xs[6], xs[7],
+                        kind, dense)
+    for idx, (x, ref) in enumerate(zip(got, r)):
+        if idx in (1, 2, 4, 5) and H // Hkv > 1:
+            ref = ref.reshape(B, Hkv, H // Hkv, Nk, D).sum(axis=2)
+        scale = max(1.0, float(np.abs(ref).max()))
+        assert np.abs(np64(x) - ref).max() <= TOL * scale, idx
