@@ -951,12 +951,21 @@ int64_t group_edge(int64_t BH, int64_t G, int64_t g) {
   const unsigned __int128 total = static_cast<unsigned __int128>(G * (G + 1) / 2);
   return g + static_cast<int64_t>(rest * w / total);
 }
-// Pairs in the largest group (the staging slots hold one group each).
+// Pairs in the largest group (the staging slots hold one group each): exact
+// for up to 2^16 groups; beyond that the bound 2 + floor(R G / T) (group g
+// holds 1 + floor(R w_{g+1} / T) - floor(R w_g / T) pairs, w_{g+1} - w_g <= G).
 int64_t max_group(int64_t BH, int chunks) {
   const int64_t G = num_groups(BH, chunks);
-  int64_t m = 0;
-  for (int64_t g = 0; g < G; ++g) m = std::max(m, group_edge(BH, G, g + 1) - group_edge(BH, G, g));
-  return m;
+  if (G <= (1 << 16)) {
+    int64_t m = 0;
+    for (int64_t g = 0; g < G; ++g)
+      m = std::max(m, group_edge(BH, G, g + 1) - group_edge(BH, G, g));
+    return m;
+  }
+  const unsigned __int128 rest = static_cast<unsigned __int128>(BH - G);
+  const unsigned __int128 total = static_cast<unsigned __int128>(G * (G + 1) / 2);
+  const int64_t bound = 2 + static_cast<int64_t>(rest * static_cast<unsigned __int128>(G) / total);
+  return std::min(BH, bound);
 }
 
 jvp_status_t host_pipe(HostPipe** out) {
