@@ -510,14 +510,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!PRIMAL) tmem_st8(lb + sb + col + 8, pgds);
       }
     };
+    // The mask entries of this warpgroup's 32 keys of a tile are loaded one
+    // tile ahead, so their latency overlaps a whole tile of work.
+    MaskRegs<MASK, 16> n0, n1;
+    if (row_ok && n_kv > 0) {
+      n0.load(mp, mrow, kv_lo * BN + wg * 32);
+      n1.load(mp, mrow, kv_lo * BN + wg * 32 + 16);
+    }
     for (int t = 0; t < n_kv; ++t) {
       const int j0 = (kv_lo + t) * BN + wg * 32;
-      // Both halves' mask entries are requested before the wait for the
-      // tile's scores, so their latency overlaps it.
-      MaskRegs<MASK, 16> m0, m1;
-      if (row_ok) {
-        m0.load(mp, mrow, j0);
-        m1.load(mp, mrow, j0 + 16);
+      const MaskRegs<MASK, 16> m0 = n0, m1 = n1;
+      if (row_ok && t + 1 < n_kv) {
+        n0.load(mp, mrow, j0 + BN);
+        n1.load(mp, mrow, j0 + BN + 16);
       }
       if (!warp_wait(&ctrl->s_full[t % NBS], (t / NBS) & 1, status, abort) ||
           (NBS == 2 && !warp_wait(&ctrl->g_full, t & 1, status, abort))) {
