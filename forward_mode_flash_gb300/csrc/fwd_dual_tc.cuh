@@ -31,7 +31,8 @@
 //   softmax, once M2 is done: P~ * s * dS_raw into its own dS columns
 //   M4  T           += (P~ * dS) V            (N = D)
 // M1/M2 of tile t+2 reuse buffer b once M3/M4 of tile t are done, so the
-// tensor core computes the next scores while the softmax warps work.  The
+// tensor core computes the next scores while the softmax warps work.  (Without
+// tangents there are four 64-column buffers, S alone, reused every 4 tiles.)  The
 // epilogue stages O and tO in the idle [K;dK] ring and writes them with TMA
 // stores.
 //
@@ -98,7 +99,12 @@ struct TcLayout {
   static constexpr int BM = kTcBlockM;              // query rows per CTA
   static constexpr int BN = kTcBlockN;              // keys per tile
   static constexpr int KCH = D / 64;                // 128-byte chunks along D
-  static constexpr int NS = (D == 128) ? 2 : 4;     // pipeline depth
+  static constexpr int NS = (D == 128 && TANGENT) ? 2 : 4;  // K/V ring depth
+  // Score buffers in TMEM: with tangents two of 128 columns ([S | dS]);
+  // without, four of 64 (S alone), so the score products can run up to three
+  // tiles ahead of the softmax.
+  static constexpr int NB = TANGENT ? 2 : 4;
+  static constexpr uint32_t BUF_COLS = TANGENT ? 128 : 64;
   static constexpr int Q_BYTES = KCH * BM * 128;
   static constexpr int KROWS = TANGENT ? 2 * BN : BN;  // rows of the [K;dK] block
   static constexpr int KCHUNK_BYTES = KROWS * 128;     // one 64-column chunk of it
@@ -135,11 +141,14 @@ struct TcLayout {
   }
   // TMEM columns of S and of dS in score buffer buf (stage buf; NS = 2 when
   // the dK slot is shared, so the stage of a tile is its buffer).
+  static __device__ __forceinline__ uint32_t buf_col(int buf) {
+    return static_cast<uint32_t>(buf) * BUF_COLS;
+  }
   static __device__ __forceinline__ uint32_t s_col(int buf) {
-    return static_cast<uint32_t>(buf * 128 + ((kSharedDK && buf) ? BN : 0));
+    return buf_col(buf) + ((kSharedDK && buf) ? BN : 0);
   }
   static __device__ __forceinline__ uint32_t ds_col(int buf) {
-    return static_cast<uint32_t>(buf * 128 + ((kSharedDK && buf) ? 0 : BN));
+    return buf_col(buf) + ((kSharedDK && buf) ? 0 : BN);
   }
   static constexpr int CTRL_BYTES = 8192;
   static constexpr int USED = OFF_CTRL + CTRL_BYTES;
@@ -170,12 +179,13 @@ struct TcCtrl {
   uint64_t q_full;
   uint64_t kdk_full[NS], kdk_empty[NS];
   uint64_t vdv_full[NS], vdv_empty[NS];
-  uint64_t s_full[2], p_full[2], max_ready[2];
-  uint64_t s_ready[2];  // S of a score buffer is final (its dS may still be accumulating)
-  uint64_t p_ready[2];  // P~ of a score buffer is stored (P~ * dS may not be yet)
+  // per score buffer (up to four); max_ready and xmax alternate by tile parity
+  uint64_t s_full[4], p_full[4], max_ready[2];
+  uint64_t s_ready[4];  // S of a score buffer is final (its dS may still be accumulating)
+  uint64_t p_ready[4];  // P~ of a score buffer is stored (P~ * dS may not be yet)
   uint64_t at_done, o_full, drain, drain_pv, sums_ready;
   uint64_t o_staged;  // every softmax warp has staged its O / tO rows in shared memory
-  uint64_t pv_done[2];  // P~V MMAs of the tile in each score buffer are complete
+  uint64_t pv_done[4];  // P~V MMAs of the tile in each score buffer are complete
   uint64_t ring_free, peer_ready;  // cluster split (arrived on by the other CTA)
   uint32_t tmem_base;
   int abort;
@@ -408,16 +418,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&ctrl->vdv_full[s], 1);
       mbar_init(&ctrl->vdv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::NB; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
       mbar_init(&ctrl->s_ready[s], 1);
       mbar_init(&ctrl->p_ready[s], kSoftmaxThreads / 32);
       mbar_init(&ctrl->p_full[s], kSoftmaxThreads / 32);     // one arrival per warp
-      mbar_init(&ctrl->max_ready[s], kSoftmaxThreads / 32);
+      mbar_init(&ctrl->pv_done[s], 1);
     }
+    mbar_init(&ctrl->max_ready[0], kSoftmaxThreads / 32);
+    mbar_init(&ctrl->max_ready[1], kSoftmaxThreads / 32);
     mbar_init(&ctrl->at_done, 1);
-    mbar_init(&ctrl->pv_done[0], 1);
-    mbar_init(&ctrl->pv_done[1], 1);
     mbar_init(&ctrl->drain_pv, 1);
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
@@ -522,8 +532,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ score MMAs
-    // Tile t's score products go into buffer t & 1 once its K tile has landed
-    // and the P~V MMAs of tile t - 2 (the buffer's previous user) are done.
+    // Tile t's score products go into buffer t % NB once its K tile has landed
+    // and the P~V MMAs of tile t - NB (the buffer's previous user) are done.
     // Two issuing threads (this one and the P~V warp) keep the tensor pipe fed
     // while either waits, and interleave the narrow dQ K^T products.
     if (lane == 0) {
@@ -535,7 +545,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t neg_a = p.neg_scores ? (1u << 13) : 0u;
       for (int t = 0; ok && t < n_kv; ++t) {
         const int s = t % NS;
-        if (t >= 2 && !mbar_wait(&ctrl->pv_done[t & 1], ((t - 2) >> 1) & 1, abort)) {
+        const int bb = t % L::NB;  // score buffer
+        if (t >= L::NB && !mbar_wait(&ctrl->pv_done[bb], ((t - L::NB) / L::NB) & 1, abort)) {
           ok = false;
           break;
         }
@@ -549,7 +560,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t sK = smem_u32(smem + L::k_off(s, 0));
         const uint32_t sM = smem_u32(smem + L::m1_off(s, 0));
         constexpr int kChunk = L::kSharedDK ? 3 * BN * 128 : L::KCHUNK_BYTES;
-        const uint32_t d_s = tmem + (t & 1) * 128;
+        const uint32_t d_s = tmem + L::buf_col(bb);
 #pragma unroll
         for (int kk = 0; kk < KSTEPS_D; ++kk) {
           const uint32_t off = (kk & 3) * 32;
@@ -558,7 +569,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_ss(d_s, a, bd, IDESC_S | neg_a, kk > 0 ? 1u : 0u);
         }
         // S is complete: the softmax starts on it while dQ K^T accumulates into dS.
-        if (TANGENT) mma_commit(&ctrl->s_ready[t & 1]);
+        if (TANGENT) mma_commit(&ctrl->s_ready[bb]);
         if (L::kSharedDK) mma_commit(&ctrl->dk_empty);  // dK is read only by that product
         if (TANGENT) {
 #pragma unroll
@@ -566,11 +577,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t off = (kk & 3) * 32;
             const uint64_t a = sdesc_sw128(sdQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
             const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * kChunk + off, 16, 1024);
-            mma_ss(tmem + L::ds_col(t & 1), a, bd, IDESC_DS | neg_a, 1u);
+            mma_ss(tmem + L::ds_col(bb), a, bd, IDESC_DS | neg_a, 1u);
           }
         }
         mma_commit(&ctrl->kdk_empty[s]);
-        mma_commit(&ctrl->s_full[t & 1]);
+        mma_commit(&ctrl->s_full[bb]);
       }
       if (!ok) record_timeout(p.status, abort);
       // Drain: every MMA this thread issued completes before TMEM is freed.
@@ -583,8 +594,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       bool ok = true;
       for (int t = 0; ok && t < n_kv; ++t) {
-        const int buf = t & 1;
-        if (!mbar_wait(TANGENT ? &ctrl->p_ready[buf] : &ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+        const int buf = t % L::NB;
+        const uint32_t bph = (t / L::NB) & 1;
+        if (!mbar_wait(TANGENT ? &ctrl->p_ready[buf] : &ctrl->p_full[buf], bph, abort)) {
           ok = false;
           break;
         }
@@ -620,7 +632,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_ts(acc_base, p_tm + pcol(kk), bd, IDESC_AT, (t > 0 || kk % KH > 0) ? 1u : 0u);
         }
         if (TANGENT) {
-          if (!mbar_wait(&ctrl->p_full[buf], (t >> 1) & 1, abort)) {
+          if (!mbar_wait(&ctrl->p_full[buf], bph, abort)) {
             ok = false;
             break;
           }
@@ -681,7 +693,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     MaskRegs<MASK, HN> mnext;
     if (kMaskAhead && !mstaged && row_ok && n_kv > 0) mnext.load(p, mrow, kv0 * BN + cofs);
     for (int t = 0; t < n_kv; ++t) {
-      const int buf = t & 1;
+      const int buf = t % L::NB;  // score buffer
+      const uint32_t bph = (t / L::NB) & 1;
+      const int xb = t & 1;       // tile parity: the maxima exchange slot
       const int j0 = (kv0 + t) * BN + cofs;  // first key of this half tile
       MaskRegs<MASK, HN> mreg;
       if constexpr (kMTile) {
@@ -733,7 +747,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // With tangents, S is read as soon as it is final and dS (whose
       // dQ K^T part is still accumulating) only when the tangent terms need it.
-      if (!warp_wait(TANGENT ? &ctrl->s_ready[buf] : &ctrl->s_full[buf], (t >> 1) & 1, p.status,
+      if (!warp_wait(TANGENT ? &ctrl->s_ready[buf] : &ctrl->s_full[buf], bph, p.status,
                      abort)) {
         ok = false;
         break;
@@ -819,7 +833,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // other half's maximum is in, assume the row maximum stays (the usual
         // case after the first tile) and compute the weights with it; the
         // decision below is the same either way, so is every value stored.
-        ctrl->xmax[buf][wg][r] = m_half;
+        ctrl->xmax[xb][wg][r] = m_half;
         // A mask tile read from shared memory is consumed once m_half is
         // stored (it depends on every entry, so each lane's reads of the slot
         // have returned before that store issues): release the slot for the
@@ -827,17 +841,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (mstaged) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&ctrl->max_ready[buf]);
+          mbar_arrive(&ctrl->max_ready[xb]);
           if (mstaged) mbar_arrive(&ctrl->msk_empty);
         }
         spec = __all_sync(0xffffffffu,
                           m_run != -INFINITY && !(m_half > m_run + kRescaleThreshold));
         if (spec) weights(m_run);
-        if (!warp_wait(&ctrl->max_ready[buf], (t >> 1) & 1, p.status, abort)) {
+        if (!warp_wait(&ctrl->max_ready[xb], (t >> 1) & 1, p.status, abort)) {
           ok = false;
           break;
         }
-        m_tile = fmaxf(m_half, ctrl->xmax[buf][wg ^ 1][r]);
+        m_tile = fmaxf(m_half, ctrl->xmax[xb][wg ^ 1][r]);
       }
       const bool need = m_tile > m_run + kRescaleThreshold;
       if (!spec || __any_sync(0xffffffffu, need)) {
@@ -895,7 +909,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // dS is complete once the buffer's dQ K^T products are; P~ * dS goes
         // into this warpgroup's own dS columns (the other warpgroup may not
         // have read its dS yet).
-        if (!warp_wait(&ctrl->s_full[buf], (t >> 1) & 1, p.status, abort)) {
+        if (!warp_wait(&ctrl->s_full[buf], bph, p.status, abort)) {
           ok = false;
           break;
         }
