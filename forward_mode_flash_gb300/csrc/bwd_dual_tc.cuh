@@ -113,7 +113,7 @@ struct BwdCtrl {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
   uint64_t s_full[2];  // [S | dS] of a buffer (warp 1)
-  uint64_t g_full;     // [G | gP] (warp 10)
+  uint64_t g_full[2];  // [G | gP] (warp 10; the primal's gP of each buffer has its own)
   uint64_t p_full[2];  // the elementwise warps are done with a buffer's tile
   uint64_t o_full, drain, drain_b;
   uint32_t tmem_base;
@@ -237,7 +237,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&ctrl->s_full[u], (NBS == 1 && u == 0) ? 2 : 1);
       mbar_init(&ctrl->p_full[u], 256);
     }
-    mbar_init(&ctrl->g_full, 1);
+    mbar_init(&ctrl->g_full[0], 1);
+    mbar_init(&ctrl->g_full[1], 1);
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
     mbar_init(&ctrl->drain_b, 1);
@@ -398,9 +399,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = mbar_wait(&ctrl->q_full, 0, abort);
       tc_fence_after();
       const uint32_t aGO = smem_u32(smem + L::OFF_GO), aGTO = smem_u32(smem + L::OFF_GTO);
+      // The primal's gP of tile t goes into the free half of score buffer
+      // t % 2 (no dS there), so it waits only for the elementwise warps to be
+      // done with tile t - 2, the buffer's previous tile.
+      constexpr int kLag = PRIMAL ? 2 : 1;
       for (int t = 0; ok && t < n_kv; ++t) {
         const int sv = t % NSV;
-        if ((t > 0 && !mbar_wait(&ctrl->p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, abort)) ||
+        if ((t >= kLag &&
+             !mbar_wait(&ctrl->p_full[(t - kLag) & 1], ((t - kLag) >> 1) & 1, abort)) ||
             !mbar_wait(&ctrl->v_full[sv], (t / NSV) & 1, abort)) {
           ok = false;
           break;
@@ -418,12 +424,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < KSD; ++kk) {  // gtO dV^T += gO V^T  (primal: gP1 = gO V^T)
           const uint32_t off = (kk & 3) * 32;
-          mma_ss(tmem + L::TM_GP, sdesc_sw128(aGO + (kk >> 2) * BM * 128 + off, 16, 1024),
+          mma_ss(tmem + (PRIMAL ? (t % NBS) * 128 + L::TM_DS : L::TM_GP),
+                 sdesc_sw128(aGO + (kk >> 2) * BM * 128 + off, 16, 1024),
                  sdesc_sw128(vb + (kk >> 2) * L::KCHUNK + off, 16, 1024), I_N64,
                  PRIMAL ? (kk > 0 ? 1u : 0u) : 1u);
         }
         mma_commit(&ctrl->v_empty[sv]);
-        mma_commit(NBS == 1 ? &ctrl->s_full[0] : &ctrl->g_full);
+        mma_commit(NBS == 1 ? &ctrl->s_full[0] : &ctrl->g_full[PRIMAL ? (t & 1) : 0]);
       }
       if (!ok) record_timeout(status, abort);
       mma_commit(&ctrl->drain_b);
@@ -476,7 +483,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (PRIMAL) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) rds[e] = rg[e] = 0u;  // dS = G = 0
-        if (cols_ok) tmem_ld16x2(lb + sb + L::TM_S + col, lb + L::TM_GP + col, rs, rgp);
+        if (cols_ok) tmem_ld16x2(lb + sb + L::TM_S + col, lb + sb + L::TM_DS + col, rs, rgp);
       } else if (cols_ok) {
         tmem_ld16x2(lb + sb + L::TM_S + col, lb + sb + L::TM_DS + col, rs, rds);
         tmem_ld16x2(lb + L::TM_G + col, lb + L::TM_GP + col, rg, rgp);
@@ -525,7 +532,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         n1.load(mp, mrow, j0 + BN + 16);
       }
       if (!warp_wait(&ctrl->s_full[t % NBS], (t / NBS) & 1, status, abort) ||
-          (NBS == 2 && !warp_wait(&ctrl->g_full, t & 1, status, abort))) {
+          (NBS == 2 && !warp_wait(&ctrl->g_full[PRIMAL ? (t & 1) : 0],
+                                  PRIMAL ? ((t >> 1) & 1) : (t & 1), status, abort))) {
         ok = false;
         break;
       }
