@@ -154,11 +154,12 @@ struct TcLayout {
   static constexpr int USED = OFF_CTRL + CTRL_BYTES;
   // Padded so that only one CTA fits per SM (each CTA owns all 512 TMEM columns).
   static constexpr int SMEM_BYTES = (USED + 1024 < 120 * 1024 ? 120 * 1024 : USED + 1024);
-  // TMEM columns.  At D = 64 each softmax warpgroup keeps its own running
-  // max, sums and [A | T] accumulator for its half of every key tile (the two
-  // accumulators fit next to the score buffers), so no per-tile exchange of
-  // half-row maxima is needed; the halves are merged in the epilogue.
-  static constexpr bool kHalfAcc = (D == 64);
+  // TMEM columns.  At D = 64, and without tangents at D = 128 too, each
+  // softmax warpgroup keeps its own running max, sums and [A | T] (or A)
+  // accumulator for its half of every key tile (the two accumulators fit next
+  // to the score buffers), so no per-tile exchange of half-row maxima is
+  // needed; the halves are merged in the epilogue.
+  static constexpr bool kHalfAcc = (D == 64) || !TANGENT;
   static constexpr uint32_t ACC_STRIDE = kHalfAcc ? 128 : 0;  // warpgroup w: TM_A + w * stride
   static constexpr uint32_t TM_A = 256;
   static constexpr uint32_t TM_T = 256 + D;
@@ -852,6 +853,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         m_tile = fmaxf(m_half, ctrl->xmax[xb][wg ^ 1][r]);
+      } else if (mstaged) {
+        // No exchange here: the same store of the half-row maximum (into the
+        // otherwise unused exchange area) orders the mask slot's reads before
+        // its release.
+        ctrl->xmax[xb][wg][r] = m_half;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->msk_empty);
       }
       const bool need = m_tile > m_run + kRescaleThreshold;
       if (!spec || __any_sync(0xffffffffu, need)) {
