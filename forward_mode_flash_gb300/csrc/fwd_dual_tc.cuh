@@ -208,9 +208,10 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, volatile in
 // Bounded wait taken by every lane of a warp, with a warp-uniform outcome, so
 // that the warp-collective TMEM instructions after it never run diverged.
 // (Waiters sleep inside try_wait, so polling adds little shared-memory traffic.)
+template <bool kHint = true>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
                                           volatile int* abort) {
-  const bool got = mbar_wait(bar, parity, abort);
+  const bool got = mbar_wait<kHint>(bar, parity, abort);
   if (!got) record_timeout(status, abort);
   return __all_sync(0xffffffffu, got);
 }
@@ -348,6 +349,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // slower there: its refill waits for the previous tile's maximum and holds
   // up the producer's deeper K/V rings.)
   constexpr bool kMTile = (MASK == kMaskAdditive && D == 128);
+  // Waits without a suspend-time hint at D = 64 (measured faster there).
+  constexpr bool kHint = (D != 64);
   using L = TcLayout<D, TANGENT, kMTile>;
   constexpr bool kWsSplit = SPLIT == kSplitWorkspace;
   constexpr bool kPair = SPLIT == kSplitCluster;
@@ -482,8 +485,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = t % NS;
         const uint32_t ph = (t / NS) & 1;
         const int j0 = (kv0 + t) * BN;
-        if (!mbar_wait(&ctrl->kdk_empty[s], ph ^ 1, abort) ||
-            (L::kSharedDK && !mbar_wait(&ctrl->dk_empty, (t & 1) ^ 1, abort))) {
+        if (!mbar_wait<kHint>(&ctrl->kdk_empty[s], ph ^ 1, abort) ||
+            (L::kSharedDK && !mbar_wait<kHint>(&ctrl->dk_empty, (t & 1) ^ 1, abort))) {
           record_timeout(p.status, abort);
           break;
         }
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ++k_fills;
         if (mtma) {
           // one slot: tile t's mask once every softmax warp has read tile t-1's
-          if (!mbar_wait(&ctrl->msk_empty, (t & 1) ^ 1, abort)) {
+          if (!mbar_wait<kHint>(&ctrl->msk_empty, (t & 1) ^ 1, abort)) {
             record_timeout(p.status, abort);
             break;
           }
@@ -506,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         j0 + w * (BN / 2), q0, mh, mb);
           ++m_fills;
         }
-        if (!mbar_wait(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
+        if (!mbar_wait<kHint>(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
           record_timeout(p.status, abort);
           break;
         }
@@ -523,12 +526,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (*abort) {
         // Let every copy already issued land before the CTA can exit.
         const int zero = 0;
-        mbar_wait(&ctrl->q_full, 0, &zero);
+        mbar_wait<kHint>(&ctrl->q_full, 0, &zero);
         for (int t = max(0, k_fills - NS); t < k_fills; ++t)
-          mbar_wait(&ctrl->kdk_full[t % NS], (t / NS) & 1, &zero);
+          mbar_wait<kHint>(&ctrl->kdk_full[t % NS], (t / NS) & 1, &zero);
         for (int t = max(0, v_fills - NS); t < v_fills; ++t)
-          mbar_wait(&ctrl->vdv_full[t % NS], (t / NS) & 1, &zero);
-        if (m_fills > 0) mbar_wait(&ctrl->msk_full, (m_fills - 1) & 1, &zero);
+          mbar_wait<kHint>(&ctrl->vdv_full[t % NS], (t / NS) & 1, &zero);
+        if (m_fills > 0) mbar_wait<kHint>(&ctrl->msk_full, (m_fills - 1) & 1, &zero);
       }
     }
   } else if (warp == 1) {
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Two issuing threads (this one and the P~V warp) keep the tensor pipe fed
     // while either waits, and interleave the narrow dQ K^T products.
     if (lane == 0) {
-      bool ok = mbar_wait(&ctrl->q_full, 0, abort);
+      bool ok = mbar_wait<kHint>(&ctrl->q_full, 0, abort);
       tc_fence_after();
       const uint32_t sQ = smem_u32(smem + L::OFF_Q);
       const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
@@ -547,11 +550,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int t = 0; ok && t < n_kv; ++t) {
         const int s = t % NS;
         const int bb = t % L::NB;  // score buffer
-        if (t >= L::NB && !mbar_wait(&ctrl->pv_done[bb], ((t - L::NB) / L::NB) & 1, abort)) {
+        if (t >= L::NB && !mbar_wait<kHint>(&ctrl->pv_done[bb], ((t - L::NB) / L::NB) & 1, abort)) {
           ok = false;
           break;
         }
-        if (!mbar_wait(&ctrl->kdk_full[s], (t / NS) & 1, abort)) {
+        if (!mbar_wait<kHint>(&ctrl->kdk_full[s], (t / NS) & 1, abort)) {
           ok = false;
           break;
         }
@@ -588,7 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Drain: every MMA this thread issued completes before TMEM is freed.
       mma_commit(&ctrl->drain);
       const int zero = 0;
-      mbar_wait(&ctrl->drain, 0, &zero);
+      mbar_wait<kHint>(&ctrl->drain, 0, &zero);
     }
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ P~V MMAs
@@ -597,12 +600,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int t = 0; ok && t < n_kv; ++t) {
         const int buf = t % L::NB;
         const uint32_t bph = (t / L::NB) & 1;
-        if (!mbar_wait(TANGENT ? &ctrl->p_ready[buf] : &ctrl->p_full[buf], bph, abort)) {
+        if (!mbar_wait<kHint>(TANGENT ? &ctrl->p_ready[buf] : &ctrl->p_full[buf], bph, abort)) {
           ok = false;
           break;
         }
         const int s = t % NS;
-        if (!mbar_wait(&ctrl->vdv_full[s], (t / NS) & 1, abort)) {
+        if (!mbar_wait<kHint>(&ctrl->vdv_full[s], (t / NS) & 1, abort)) {
           ok = false;
           break;
         }
@@ -633,7 +636,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_ts(acc_base, p_tm + pcol(kk), bd, IDESC_AT, (t > 0 || kk % KH > 0) ? 1u : 0u);
         }
         if (TANGENT) {
-          if (!mbar_wait(&ctrl->p_full[buf], bph, abort)) {
+          if (!mbar_wait<kHint>(&ctrl->p_full[buf], bph, abort)) {
             ok = false;
             break;
           }
@@ -655,7 +658,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       mma_commit(&ctrl->drain_pv);
       const int zero = 0;
-      mbar_wait(&ctrl->drain_pv, 0, &zero);
+      mbar_wait<kHint>(&ctrl->drain_pv, 0, &zero);
     }
   } else if (warp >= 2 && warp < 2 + kSoftmaxThreads / 32) {
     // ------------------------------------------------------------ softmax
@@ -706,7 +709,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // swizzle: 16-byte piece c of row r sits at piece position
           // c ^ (r % 8), so the 8 rows of a quarter warp hit distinct banks.
           // (The slot is released once the entries are consumed, below.)
-          if (!warp_wait(&ctrl->msk_full, t & 1, p.status, abort)) {
+          if (!warp_wait<kHint>(&ctrl->msk_full, t & 1, p.status, abort)) {
             ok = false;
             break;
           }
@@ -748,7 +751,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // With tangents, S is read as soon as it is final and dS (whose
       // dQ K^T part is still accumulating) only when the tangent terms need it.
-      if (!warp_wait(TANGENT ? &ctrl->s_ready[buf] : &ctrl->s_full[buf], bph, p.status,
+      if (!warp_wait<kHint>(TANGENT ? &ctrl->s_ready[buf] : &ctrl->s_full[buf], bph, p.status,
                      abort)) {
         ok = false;
         break;
@@ -848,7 +851,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         spec = __all_sync(0xffffffffu,
                           m_run != -INFINITY && !(m_half > m_run + kRescaleThreshold));
         if (spec) weights(m_run);
-        if (!warp_wait(&ctrl->max_ready[xb], (t >> 1) & 1, p.status, abort)) {
+        if (!warp_wait<kHint>(&ctrl->max_ready[xb], (t >> 1) & 1, p.status, abort)) {
           ok = false;
           break;
         }
@@ -872,7 +875,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (t > 0 && __any_sync(0xffffffffu, need)) {
           // A and T hold tile t-1's contributions once its MMAs are done; each
           // warpgroup rescales half of the [A | T] columns of its rows.
-          if (!warp_wait(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
+          if (!warp_wait<kHint>(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
             ok = false;
             break;
           }
@@ -918,7 +921,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // dS is complete once the buffer's dQ K^T products are; P~ * dS goes
         // into this warpgroup's own dS columns (the other warpgroup may not
         // have read its dS yet).
-        if (!warp_wait(&ctrl->s_full[buf], bph, p.status, abort)) {
+        if (!warp_wait<kHint>(&ctrl->s_full[buf], bph, p.status, abort)) {
           ok = false;
           break;
         }
@@ -944,15 +947,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ctrl->xsum[wg][2][r] = mu_run;
       ctrl->xsum[wg][3][r] = m_run;
       mbar_arrive(&ctrl->sums_ready);
-      ok = warp_wait(&ctrl->sums_ready, 0, p.status, abort);
+      ok = warp_wait<kHint>(&ctrl->sums_ready, 0, p.status, abort);
     }
     // The accumulators are final once the last P~V products are: the cluster
     // split waits here (rank 0's rings are then idle for the peer's state),
     // the other variants only before their first TMEM load, so the row
     // statistics below are formed while those products finish.
-    if (kPair && ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
+    if (kPair && ok && n_kv > 0) ok = warp_wait<kHint>(&ctrl->o_full, 0, p.status, abort);
     auto wait_acc = [&]() {
-      if (!kPair && ok && n_kv > 0) ok = warp_wait(&ctrl->o_full, 0, p.status, abort);
+      if (!kPair && ok && n_kv > 0) ok = warp_wait<kHint>(&ctrl->o_full, 0, p.status, abort);
       tc_fence_after();
     };
     // O and tO rows are staged in the (now idle) [K;dK] ring, laid out as the
@@ -998,7 +1001,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             st_shared_v4(recv + r * 16, __float_as_uint(m_all), __float_as_uint(l_all),
                                     __float_as_uint(lx_all), __float_as_uint(mu_all));
         } else {
-          ok = warp_wait(&ctrl->peer_ready, 0, p.status, abort);
+          ok = warp_wait<kHint>(&ctrl->peer_ready, 0, p.status, abort);
           if (ok) {
             float4 st;
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -1239,7 +1242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->o_staged);
       if (warp == 2 && lane == 0) {
-        if (mbar_wait(&ctrl->o_staged, 0, abort)) {
+        if (mbar_wait<kHint>(&ctrl->o_staged, 0, abort)) {
           for (int c = 0; c < L::KCH; ++c) {
             tma_store_4d(&maps.o, smem + L::OFF_KDK + c * L::BM * 128, c * 64, q0, h, b);
             if (TANGENT)

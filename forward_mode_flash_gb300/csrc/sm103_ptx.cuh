@@ -55,6 +55,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// The same without a suspend-time hint (the system's own limit applies).
+__device__ __forceinline__ bool mbar_try_wait_nohint(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // One test of the phase without suspending: true if it has completed.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;
@@ -70,13 +83,21 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
 // false if the wait ran past the limit or *abort became nonzero meanwhile.
+// kHint: each test may suspend for up to kSuspendHintNs; without it, for the
+// system's own limit (measured shorter wake-ups where the per-tile chain is
+// short, at D = 64).
+template <bool kHint = true>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort,
                                           long long limit = kWaitLimitCycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto test = [&]() {
+    if constexpr (kHint) return mbar_try_wait(bar, parity);
+    else return mbar_try_wait_nohint(bar, parity);
+  };
+  if (test()) return true;
   const long long start = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (test()) return true;
     if (*abort) return false;
     if (clock64() - start > limit) return false;
   }
