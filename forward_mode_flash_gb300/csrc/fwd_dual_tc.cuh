@@ -320,6 +320,28 @@ __device__ __forceinline__ float tree_max(const float (&x)[N]) {
   }
 }
 
+// One TMEM row piece of 32 or 64 columns of this thread's lane, into or out
+// of registers (one wait for the load).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 32 || N == 64, "32 or 64 columns");
+  if constexpr (N == 32) {
+    tmem_ld32(taddr, r);
+  } else {
+    tmem_ld32x2(taddr, taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[0]),
+                *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  }
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 16) {
+    tmem_st16(taddr, r);
+  } else {
+    tmem_st32(taddr, r);
+  }
+}
+
 // SPLIT: 0 single pass; kSplitWorkspace: split-KV over p.splits CTAs per
 // query tile, partial states to p.split_ws for fwd_combine_kernel;
 // kSplitCluster (D = 64): the key range of a query tile split between the two
@@ -360,6 +382,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int NS = L::NS;
   constexpr int BN = L::BN;
   constexpr int HN = BN / 2;  // key columns per softmax warpgroup
+  // Without tangents (and without an additive mask) the two softmax
+  // warpgroups take alternate key tiles whole, warpgroup w the tiles t with
+  // t % 2 == w, each into its own accumulator, instead of half of every
+  // tile: a thread's fixed per-tile costs (waits, TMEM round trips, the row
+  // maximum, publishing) then cover 64 keys instead of 32, and the two warps
+  // that share a sub-partition run different phases of their tiles.
+  constexpr bool kAlt = !TANGENT && MASK != kMaskAdditive;
+  constexpr int KW = kAlt ? BN : HN;  // keys of a tile per softmax thread
+  constexpr int TSTEP = kAlt ? 2 : 1;  // a warpgroup's tiles are t, t + TSTEP, ...
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSTEPS_D = D / 16;   // MMA K-steps over the head dimension
   constexpr int KSTEPS_N = BN / 16;  // MMA K-steps over a key tile
@@ -426,7 +457,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&ctrl->s_full[s], 1);
       mbar_init(&ctrl->s_ready[s], 1);
       mbar_init(&ctrl->p_ready[s], kSoftmaxThreads / 32);
-      mbar_init(&ctrl->p_full[s], kSoftmaxThreads / 32);     // one arrival per warp
+      // one arrival per softmax warp working on the buffer's tile
+      mbar_init(&ctrl->p_full[s], (kAlt ? kSoftmaxThreads / 2 : kSoftmaxThreads) / 32);
       mbar_init(&ctrl->pv_done[s], 1);
     }
     mbar_init(&ctrl->max_ready[0], kSoftmaxThreads / 32);
@@ -618,7 +650,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t p_tm = tmem + L::s_col(buf);
         const uint32_t pd_tm = tmem + L::ds_col(buf);
         auto pcol = [](int kk) -> uint32_t {
-          return L::kHalfAcc
+          return (L::kHalfAcc && !kAlt)
                      ? static_cast<uint32_t>((kk / (HN / 16)) * HN + (kk % (HN / 16)) * 8)
                      : static_cast<uint32_t>(kk * 8);
         };
@@ -627,13 +659,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           return static_cast<uint32_t>((kk / (HN / 16)) * HN + (kk % (HN / 16)) * 8);
         };
         // With per-warpgroup accumulators, K-steps [w * KH, w * KH + KH) (the
-        // keys of warpgroup w) go to warpgroup w's [A | T].
-        constexpr int KH = L::kHalfAcc ? KSTEPS_N / 2 : KSTEPS_N;
+        // keys of warpgroup w) go to warpgroup w's [A | T]; with alternate
+        // tiles, all of tile t's go to warpgroup t % 2's accumulator.
+        constexpr int KH = (L::kHalfAcc && !kAlt) ? KSTEPS_N / 2 : KSTEPS_N;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS_N; ++kk) {
           const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
-          const uint32_t acc_base = tmem + L::TM_A + (kk / KH) * L::ACC_STRIDE;
-          mma_ts(acc_base, p_tm + pcol(kk), bd, IDESC_AT, (t > 0 || kk % KH > 0) ? 1u : 0u);
+          const int acc_w = kAlt ? (t & 1) : kk / KH;
+          const uint32_t acc_base = tmem + L::TM_A + acc_w * L::ACC_STRIDE;
+          mma_ts(acc_base, p_tm + pcol(kk), bd, IDESC_AT,
+                 (t >= TSTEP || kk % KH > 0) ? 1u : 0u);
         }
         if (TANGENT) {
           if (!mbar_wait<kHint>(&ctrl->p_full[buf], bph, abort)) {
@@ -663,7 +698,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp >= 2 && warp < 2 + kSoftmaxThreads / 32) {
     // ------------------------------------------------------------ softmax
     // Two warpgroups; warpgroup wg owns key columns [wg*HN, wg*HN + HN) of
-    // every tile and, in the epilogue, output columns [wg*D/2, wg*D/2 + D/2).
+    // every tile (with alternate tiles: every column of tiles wg, wg + 2, ...)
+    // and, in the epilogue, output columns [wg*D/2, wg*D/2 + D/2).
     // Thread (warp, lane) owns query row r = 32 * (warp % 4) + lane (its TMEM lane).
     const int wg = (warp - 2) >> 2;
     const int sub = warp & 3;
@@ -671,7 +707,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int i = q0 + r;
     const bool row_ok = i < p.Nq;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
-    const int cofs = wg * HN;
+    const int cofs = kAlt ? 0 : wg * HN;
     const float c = p.scale_log2;
     const float s_scale = p.scale;
     float m_run = -INFINITY;  // running max, log2 units of the scaled logits (whole row)
@@ -694,14 +730,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // two tiles of 32 floats would not fit the register budget).
     constexpr bool kMaskAhead = !(MASK == kMaskAdditive && D == 128);
     const bool mstaged = kMTile && p.mask_tma;  // additive tiles through shared memory (D = 128)
-    MaskRegs<MASK, HN> mnext;
-    if (kMaskAhead && !mstaged && row_ok && n_kv > 0) mnext.load(p, mrow, kv0 * BN + cofs);
-    for (int t = 0; t < n_kv; ++t) {
+    const int t_first = kAlt ? wg : 0;
+    MaskRegs<MASK, KW> mnext;
+    if (kMaskAhead && !mstaged && row_ok && t_first < n_kv)
+      mnext.load(p, mrow, (kv0 + t_first) * BN + cofs);
+    for (int t = t_first; t < n_kv; t += TSTEP) {
       const int buf = t % L::NB;  // score buffer
       const uint32_t bph = (t / L::NB) & 1;
       const int xb = t & 1;       // tile parity: the maxima exchange slot
-      const int j0 = (kv0 + t) * BN + cofs;  // first key of this half tile
-      MaskRegs<MASK, HN> mreg;
+      const int j0 = (kv0 + t) * BN + cofs;  // first key of this thread's part of the tile
+      MaskRegs<MASK, KW> mreg;
       if constexpr (kMTile) {
         if (mstaged) {
           // The tile's entries were copied into shared memory by TMA a tile
@@ -727,7 +765,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!mstaged) {
         if constexpr (kMaskAhead) {
           mreg = mnext;
-          if (row_ok && t + 1 < n_kv) mnext.load(p, mrow, j0 + BN);
+          if (row_ok && t + TSTEP < n_kv) mnext.load(p, mrow, j0 + TSTEP * BN);
           if constexpr (MASK == kMaskAdditive) {
             // additive entries two tiles ahead into L2 as well (measured: bool
             // masks, a quarter the bytes, do not gain)
@@ -757,44 +795,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sa[32], da[32];  // S and dS (raw, unscaled) of this half tile
-      if (JVP_CHECK(L::s_col(buf) + cofs + 32 <= L::TM_COLS, p.status, kChkTmem))
-        tmem_ld32(lane_base + L::s_col(buf) + cofs, sa);
-      float x[HN];
+      uint32_t sa[KW], da[HN];  // S and dS (raw, unscaled) of this thread's keys
+      if (JVP_CHECK(L::s_col(buf) + cofs + KW <= L::TM_COLS, p.status, kChkTmem))
+        tmem_ld_cols(lane_base + L::s_col(buf) + cofs, sa);
+      float x[KW];
 #pragma unroll
-      for (int jj = 0; jj < HN; ++jj) x[jj] = __uint_as_float(sa[jj]);
+      for (int jj = 0; jj < KW; ++jj) x[jj] = __uint_as_float(sa[jj]);
       // Masking (raw-score domain unless additive, which is pre-scaled).
       if constexpr (MASK == kMaskAdditive) {
 #pragma unroll
         for (int jj = 0; jj < HN; ++jj) x[jj] = fmaf(x[jj], c, mreg.a[jj] * kLog2e);
       } else if constexpr (MASK == kMaskBool) {
 #pragma unroll
-        for (int jj = 0; jj < HN; ++jj)
+        for (int jj = 0; jj < KW; ++jj)
           if (!mreg.keep(jj)) x[jj] = -INFINITY;
       }
-      if (j0 + HN > p.Nk) {
+      if (j0 + KW > p.Nk) {
 #pragma unroll
-        for (int jj = 0; jj < HN; ++jj)
+        for (int jj = 0; jj < KW; ++jj)
           if (j0 + jj >= p.Nk) x[jj] = -INFINITY;
       }
-      if (causal && j0 + HN - 1 > q0) {
+      if (causal && j0 + KW - 1 > q0) {
 #pragma unroll
-        for (int jj = 0; jj < HN; ++jj)
+        for (int jj = 0; jj < KW; ++jj)
           if (j0 + jj > i) x[jj] = -INFINITY;
       }
       // p~ = 2^(x - m_use) (kept in e), P~ packed to 16 bits, and the sums of
       // the packed values (l) and of the fp32 p~ (lx); x is left as it is.
-      uint32_t pk[HN / 2], pdk[HN / 2];
-      float e[HN];
+      uint32_t pk[KW / 2], pdk[HN / 2];
+      float e[KW];
       float l_part = 0.f, lx_part = 0.f, mu_part = 0.f;
       auto weights = [&](float m_use) {
         if (MASK == kMaskAdditive) {
 #pragma unroll
-          for (int jj = 0; jj < HN; ++jj) e[jj] = ex2_approx(x[jj] - m_use);
+          for (int jj = 0; jj < KW; ++jj) e[jj] = ex2_approx(x[jj] - m_use);
         } else {
           const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
-          for (int jj = 0; jj < HN; jj += 2) {
+          for (int jj = 0; jj < KW; jj += 2) {
             const float2 arg = fma2(make_float2(x[jj], x[jj + 1]), c2, nm2);
             e[jj] = ex2_approx(arg.x);
             e[jj + 1] = ex2_approx(arg.y);
@@ -803,7 +841,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float2 lsum[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         float2 xsum[2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-        for (int jj = 0; jj < HN; jj += 2) {
+        for (int jj = 0; jj < KW; jj += 2) {
           pk[jj >> 1] = ElemTraits<T>::pack(e[jj], e[jj + 1]);
           lsum[(jj >> 1) & 3] = add2(lsum[(jj >> 1) & 3], ElemTraits<T>::unpack(pk[jj >> 1]));
           xsum[(jj >> 1) & 1] = add2(xsum[(jj >> 1) & 1], make_float2(e[jj], e[jj + 1]));
@@ -872,9 +910,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l_run *= alpha;
         lx_run *= alpha;
         mu_run *= alpha;
-        if (t > 0 && __any_sync(0xffffffffu, need)) {
+        if (t >= TSTEP && __any_sync(0xffffffffu, need)) {
           // A and T hold tile t-1's contributions once its MMAs are done; each
-          // warpgroup rescales half of the [A | T] columns of its rows.
+          // warpgroup rescales half of the [A | T] columns of its rows.  (With
+          // alternate tiles the accumulator's last tile is t - 2, and tile
+          // t - 1's products, which complete after it, are the latest whose
+          // completion can be awaited: tile t's need this thread's P~.)
           if (!warp_wait<kHint>(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
             ok = false;
             break;
@@ -909,8 +950,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ordered both warpgroups' reads first and the two halves are packed
       // side by side.
       const uint32_t pofs = L::kHalfAcc ? cofs : wg * (HN / 2);
-      if (JVP_CHECK(L::s_col(buf) + pofs + 16 <= L::TM_COLS, p.status, kChkTmem))
-        tmem_st16(lane_base + L::s_col(buf) + pofs, pk);
+      if (JVP_CHECK(L::s_col(buf) + pofs + KW / 2 <= L::TM_COLS, p.status, kChkTmem))
+        tmem_st_cols(lane_base + L::s_col(buf) + pofs, pk);
       if (TANGENT) {
         // Publish P~ first: the P~ [V | dV] products run while the tangent
         // terms wait for dS.
@@ -1037,6 +1078,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           JVP_CHECK(R < static_cast<long long>(p.splits) * rows, p.status, kChkGlobalRow))
         reinterpret_cast<float4*>(p.split_ws)[R] = make_float4(m_all, l_all, lx_all, mu_all);
       wait_acc();
+      // With alternate tiles and a single key tile, warpgroup 1's accumulator
+      // was never written (its weight is 0, its contents undefined).
+      const bool only_acc0 = kAlt && n_kv == 1;
 #pragma unroll 1
       for (int col = wg * (D / 2); ok && col < (wg + 1) * (D / 2); col += 16) {
         float fa[16], ft[16];
@@ -1051,7 +1095,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            fa[e] = a_own * __uint_as_float(a0[e]) + a_oth * __uint_as_float(a1[e]);
+            fa[e] = only_acc0 ? __uint_as_float(wg == 0 ? a0[e] : a1[e])
+                              : a_own * __uint_as_float(a0[e]) + a_oth * __uint_as_float(a1[e]);
             ft[e] = TANGENT ? a_own * __uint_as_float(t0[e]) + a_oth * __uint_as_float(t1[e]) : 0.f;
           }
         } else {
