@@ -32,13 +32,16 @@
 //   M4  T           += (P~ * dS) V            (N = D)
 // M1/M2 of tile t+2 reuse buffer b once M3/M4 of tile t are done, so the
 // tensor core computes the next scores while the softmax warps work.  (Without
-// tangents there are four 64-column buffers, S alone, reused every 4 tiles.)  The
+// tangents there are four 64-column buffers, S alone, reused every 4 tiles;
+// the softmax warpgroups then take whole tiles, and at D = 128 the score
+// products come in pairs of tiles.)  The
 // epilogue stages O and tO in the idle [K;dK] ring and writes them with TMA
 // stores.
 //
-// Masks: a boolean keep-mask (and the additive mask at D = 64) is loaded into
-// registers a tile ahead by each softmax thread for its own row.  At D = 128
-// an additive tile ahead does not fit the registers; when the mask's layout
+// Masks: a boolean keep-mask (and the additive mask at D = 64 or without
+// tangents) is loaded into registers a tile ahead by each softmax thread for
+// its own row.  At D = 128 with tangents an additive tile ahead does not fit
+// the registers; when the mask's layout
 // admits a tensor map (contiguous keys, rows that do not broadcast, 16-byte
 // strides) the producer copies each [128 x 64] fp32 tile into a shared-memory
 // slot a tile ahead, in two swizzled [128 x 32] boxes, and the softmax reads
@@ -127,11 +130,19 @@ struct TcLayout {
   static constexpr int OFF_VDV = OFF_KDK + KREGION;
   static constexpr int OFF_MSK = OFF_VDV + NS * VDV_BYTES;
   static constexpr int OFF_CTRL = OFF_MSK + MSK_BYTES;
+  // Without tangents the K ring is laid out chunk by chunk (chunk c of stage
+  // s at (c * NS + s) * KCHUNK_BYTES), so that chunk c of stages s and s + 1
+  // are 128 contiguous rows: one N = 128 score product covers two key tiles.
+  static constexpr bool kChunkMajorK = !TANGENT;
+  // Byte distance between the 64-column chunks of one stage's K rows.
+  static constexpr int K_CHUNK_STRIDE =
+      kSharedDK ? 3 * BN * 128 : kChunkMajorK ? NS * KCHUNK_BYTES : KCHUNK_BYTES;
   // Byte offsets of stage s, 64-column chunk c: the K rows, the dK rows, and
   // the first row of the 128-row operand of the first score product.
   static __device__ __forceinline__ int k_off(int s, int c) {
-    return kSharedDK ? OFF_KDK + c * 3 * BN * 128 + s * 2 * BN * 128
-                     : OFF_KDK + s * KDK_BYTES + c * KCHUNK_BYTES;
+    return kSharedDK      ? OFF_KDK + c * 3 * BN * 128 + s * 2 * BN * 128
+           : kChunkMajorK ? OFF_KDK + (c * NS + s) * KCHUNK_BYTES
+                          : OFF_KDK + s * KDK_BYTES + c * KCHUNK_BYTES;
   }
   static __device__ __forceinline__ int dk_off(int s, int c) {
     return kSharedDK ? OFF_KDK + c * 3 * BN * 128 + BN * 128 : k_off(s, c) + BN * 128;
@@ -365,12 +376,12 @@ constexpr int kPairRecvBytes = kPairRecvStats + 2 * kPairRecvBlock;
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
-  // The additive mask at D = 128 comes through shared memory when its layout
-  // allows a tensor map (p.mask_tma), else by per-row loads in its tile.  (At
-  // D = 64 the registers hold a tile ahead; the shared-memory slot measured
-  // slower there: its refill waits for the previous tile's maximum and holds
-  // up the producer's deeper K/V rings.)
-  constexpr bool kMTile = (MASK == kMaskAdditive && D == 128);
+  // The additive mask at D = 128 with tangents comes through shared memory
+  // when its layout allows a tensor map (p.mask_tma), else by per-row loads
+  // in its tile.  (At D = 64, and without tangents, the registers hold a tile
+  // ahead; the shared-memory slot measured slower there: its refill waits for
+  // the previous tile's maximum and holds up the producer's deeper K/V rings.)
+  constexpr bool kMTile = (MASK == kMaskAdditive && D == 128 && TANGENT);
   // Waits without a suspend-time hint at D = 64 (measured faster there).
   constexpr bool kHint = (D != 64);
   using L = TcLayout<D, TANGENT, kMTile>;
@@ -382,20 +393,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int NS = L::NS;
   constexpr int BN = L::BN;
   constexpr int HN = BN / 2;  // key columns per softmax warpgroup
+  // Without tangents at D = 128 the score products of two key tiles are
+  // issued as one N = 128 product (see the score warp); not with a boolean
+  // mask, where single tiles measured faster (bf16 B=4 H=16 N=2048: 187.5 us
+  // against 190.3 with pairs taken by alternate warpgroups, 195.2 with the
+  // pairs' ownership below).
+  constexpr bool kPairS = !TANGENT && D == 128 && MASK != kMaskBool;
   // Without tangents (and without an additive mask) the two softmax
-  // warpgroups take alternate key tiles whole, warpgroup w the tiles t with
-  // t % 2 == w, each into its own accumulator, instead of half of every
-  // tile: a thread's fixed per-tile costs (waits, TMEM round trips, the row
-  // maximum, publishing) then cover 64 keys instead of 32, and the two warps
-  // that share a sub-partition run different phases of their tiles.
+  // warpgroups take whole key tiles, each into its own accumulator, instead
+  // of half of every tile: a thread's fixed per-tile costs (waits, TMEM round
+  // trips, the row maximum, publishing) then cover 64 keys instead of 32.
+  // Warpgroup w takes the tiles t with t % 2 == w, or, where the score
+  // products come in pairs, the pairs with (t / 2) % 2 == w: the two tiles of
+  // a pair complete together, so the warpgroups start their pairs one pair
+  // apart rather than both at once (the warps of a sub-partition then do not
+  // all want the exponential unit at the same time).
   constexpr bool kAlt = !TANGENT && MASK != kMaskAdditive;
+  constexpr bool kPairOwn = kAlt && kPairS;
   constexpr int KW = kAlt ? BN : HN;  // keys of a tile per softmax thread
-  constexpr int TSTEP = kAlt ? 2 : 1;  // a warpgroup's tiles are t, t + TSTEP, ...
+  // The next tile of the warpgroup that takes tile t, and whether tile t is
+  // the first of its accumulator.
+  auto next_tile = [](int t) {
+    return kPairOwn ? t + ((t & 1) ? 3 : 1) : kAlt ? t + 2 : t + 1;
+  };
+  auto first_of_acc = [](int t) {
+    return kPairOwn ? (t < 4 && (t & 1) == 0) : kAlt ? t < 2 : t == 0;
+  };
   constexpr bool kBF16 = ElemTraits<T>::kBF16;
   constexpr int KSTEPS_D = D / 16;   // MMA K-steps over the head dimension
   constexpr int KSTEPS_N = BN / 16;  // MMA K-steps over a key tile
   constexpr int ACC_COLS = TANGENT ? 2 * D : D;  // TMEM columns of [A | T]
   constexpr uint32_t IDESC_S = idesc_f16(kBF16, 128, TANGENT ? 2 * BN : BN, false);
+  constexpr uint32_t IDESC_S2 = idesc_f16(kBF16, 128, 2 * BN, false);  // S of two key tiles
   constexpr uint32_t IDESC_DS = idesc_f16(kBF16, 128, BN, false);
   constexpr uint32_t IDESC_AT = idesc_f16(kBF16, 128, ACC_COLS, true);
   constexpr uint32_t IDESC_T = idesc_f16(kBF16, 128, D, true);
@@ -513,22 +542,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       b);
       }
       int k_fills = 0, v_fills = 0, m_fills = 0;  // ring fills issued so far
-      for (int t = 0; t < n_kv; ++t) {
+      // Key tile u into stage u % NS once the stage's previous score products
+      // are done.  The K tiles are issued KLEAD tiles ahead
+      // of the V tiles (whose stages wait for the far later P~V products), so
+      // both tiles of a score pair have landed when the pair's buffers free
+      // (with paired score products).
+      constexpr int KLEAD = kPairS ? 2 : 0;
+      auto load_k = [&](int u) -> bool {
+        const int su = u % NS;
+        if (!mbar_wait<kHint>(&ctrl->kdk_empty[su], ((u / NS) & 1) ^ 1, abort) ||
+            (L::kSharedDK && !mbar_wait<kHint>(&ctrl->dk_empty, (u & 1) ^ 1, abort)))
+          return false;
+        const int ju = (kv0 + u) * BN;
+        mbar_arrive_expect_tx(&ctrl->kdk_full[su], L::KDK_BYTES);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_4d(smem + L::k_off(su, c), &maps.k, &ctrl->kdk_full[su], c * 64, ju, hk, b);
+          if (TANGENT)
+            tma_load_4d(smem + L::dk_off(su, c), &maps.dk, &ctrl->kdk_full[su], c * 64, ju, hk,
+                        b);
+        }
+        ++k_fills;
+        return true;
+      };
+      bool k_ok = true;
+      for (int u = 0; k_ok && u < KLEAD && u < n_kv; ++u) k_ok = load_k(u);
+      if (!k_ok) record_timeout(p.status, abort);
+      for (int t = 0; k_ok && t < n_kv; ++t) {
         const int s = t % NS;
         const uint32_t ph = (t / NS) & 1;
         const int j0 = (kv0 + t) * BN;
-        if (!mbar_wait<kHint>(&ctrl->kdk_empty[s], ph ^ 1, abort) ||
-            (L::kSharedDK && !mbar_wait<kHint>(&ctrl->dk_empty, (t & 1) ^ 1, abort))) {
+        if (t + KLEAD < n_kv && !load_k(t + KLEAD)) {
           record_timeout(p.status, abort);
           break;
         }
-        mbar_arrive_expect_tx(&ctrl->kdk_full[s], L::KDK_BYTES);
-        for (int c = 0; c < L::KCH; ++c) {
-          tma_load_4d(smem + L::k_off(s, c), &maps.k, &ctrl->kdk_full[s], c * 64, j0, hk, b);
-          if (TANGENT)
-            tma_load_4d(smem + L::dk_off(s, c), &maps.dk, &ctrl->kdk_full[s], c * 64, j0, hk, b);
-        }
-        ++k_fills;
         if (mtma) {
           // one slot: tile t's mask once every softmax warp has read tile t-1's
           if (!mbar_wait<kHint>(&ctrl->msk_empty, (t & 1) ^ 1, abort)) {
@@ -571,7 +617,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Tile t's score products go into buffer t % NB once its K tile has landed
     // and the P~V MMAs of tile t - NB (the buffer's previous user) are done.
     // Two issuing threads (this one and the P~V warp) keep the tensor pipe fed
-    // while either waits, and interleave the narrow dQ K^T products.
+    // while either waits, and interleave the narrow dQ K^T products.  Without
+    // tangents at D = 128 the products of two key tiles (t even, t + 1) are issued as
+    // one pair of N = 128 products into the adjacent buffers t % 4 and
+    // t % 4 + 1 from the adjacent stages t % 4 and t % 4 + 1: half the
+    // instructions of two N = 64 sets (one thread issues a tcgen05.mma about
+    // every 70 cycles) and less tensor time (a narrow product is paced by
+    // reading its A tile from shared memory).
+    static_assert(!kPairS || (NS % 2 == 0 && L::NB % 2 == 0), "pairs of stages and buffers");
     if (lane == 0) {
       bool ok = mbar_wait<kHint>(&ctrl->q_full, 0, abort);
       tc_fence_after();
@@ -579,14 +632,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
       // s < 0: -Q K^T, -Q dK^T, -dQ K^T (negate-A bit), with |s| applied later.
       const uint32_t neg_a = p.neg_scores ? (1u << 13) : 0u;
-      for (int t = 0; ok && t < n_kv; ++t) {
+      constexpr int SSTEP = kPairS ? 2 : 1;  // key tiles per step
+      for (int t = 0; ok && t < n_kv; t += SSTEP) {
+        const bool pair = kPairS && t + 1 < n_kv;
         const int s = t % NS;
         const int bb = t % L::NB;  // score buffer
         if (t >= L::NB && !mbar_wait<kHint>(&ctrl->pv_done[bb], ((t - L::NB) / L::NB) & 1, abort)) {
           ok = false;
           break;
         }
-        if (!mbar_wait<kHint>(&ctrl->kdk_full[s], (t / NS) & 1, abort)) {
+        if (pair && t + 1 >= L::NB &&
+            !mbar_wait<kHint>(&ctrl->pv_done[bb + 1], ((t + 1 - L::NB) / L::NB) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait<kHint>(&ctrl->kdk_full[s], (t / NS) & 1, abort) ||
+            (pair && !mbar_wait<kHint>(&ctrl->kdk_full[s + 1], ((t + 1) / NS) & 1, abort))) {
           ok = false;
           break;
         }
@@ -595,14 +656,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // of the K rows at sK + c * kChunk
         const uint32_t sK = smem_u32(smem + L::k_off(s, 0));
         const uint32_t sM = smem_u32(smem + L::m1_off(s, 0));
-        constexpr int kChunk = L::kSharedDK ? 3 * BN * 128 : L::KCHUNK_BYTES;
+        constexpr int kChunk = L::K_CHUNK_STRIDE;
         const uint32_t d_s = tmem + L::buf_col(bb);
 #pragma unroll
         for (int kk = 0; kk < KSTEPS_D; ++kk) {
           const uint32_t off = (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * L::BM * 128 + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(sM + (kk >> 2) * kChunk + off, 16, 1024);
-          mma_ss(d_s, a, bd, IDESC_S | neg_a, kk > 0 ? 1u : 0u);
+          mma_ss(d_s, a, bd, (pair ? IDESC_S2 : IDESC_S) | neg_a, kk > 0 ? 1u : 0u);
         }
         // S is complete: the softmax starts on it while dQ K^T accumulates into dS.
         if (TANGENT) mma_commit(&ctrl->s_ready[bb]);
@@ -617,7 +678,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         mma_commit(&ctrl->kdk_empty[s]);
+        if (pair) mma_commit(&ctrl->kdk_empty[s + 1]);
         mma_commit(&ctrl->s_full[bb]);
+        if (pair) mma_commit(&ctrl->s_full[bb + 1]);
       }
       if (!ok) record_timeout(p.status, abort);
       // Drain: every MMA this thread issued completes before TMEM is freed.
@@ -659,16 +722,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           return static_cast<uint32_t>((kk / (HN / 16)) * HN + (kk % (HN / 16)) * 8);
         };
         // With per-warpgroup accumulators, K-steps [w * KH, w * KH + KH) (the
-        // keys of warpgroup w) go to warpgroup w's [A | T]; with alternate
-        // tiles, all of tile t's go to warpgroup t % 2's accumulator.
+        // keys of warpgroup w) go to warpgroup w's [A | T]; with whole tiles,
+        // all of tile t's go to the accumulator of the warpgroup that took it.
         constexpr int KH = (L::kHalfAcc && !kAlt) ? KSTEPS_N / 2 : KSTEPS_N;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS_N; ++kk) {
           const uint64_t bd = sdesc_sw128(sV + kk * 16 * 128, L::VCHUNK_BYTES, 1024);
-          const int acc_w = kAlt ? (t & 1) : kk / KH;
+          const int acc_w = kPairOwn ? ((t >> 1) & 1) : kAlt ? (t & 1) : kk / KH;
           const uint32_t acc_base = tmem + L::TM_A + acc_w * L::ACC_STRIDE;
           mma_ts(acc_base, p_tm + pcol(kk), bd, IDESC_AT,
-                 (t >= TSTEP || kk % KH > 0) ? 1u : 0u);
+                 (!first_of_acc(t) || kk % KH > 0) ? 1u : 0u);
         }
         if (TANGENT) {
           if (!mbar_wait<kHint>(&ctrl->p_full[buf], bph, abort)) {
@@ -726,15 +789,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // Mask entries are loaded one tile ahead, so their global-memory latency
-    // overlaps a whole tile of work (not the additive mask at D = 128, whose
-    // two tiles of 32 floats would not fit the register budget).
-    constexpr bool kMaskAhead = !(MASK == kMaskAdditive && D == 128);
+    // overlaps a whole tile of work (not the additive mask at D = 128 with
+    // tangents, whose two tiles of 32 floats would not fit the register
+    // budget next to the tangent terms).
+    constexpr bool kMaskAhead = !(MASK == kMaskAdditive && D == 128 && TANGENT);
     const bool mstaged = kMTile && p.mask_tma;  // additive tiles through shared memory (D = 128)
-    const int t_first = kAlt ? wg : 0;
-    MaskRegs<MASK, KW> mnext;
-    if (kMaskAhead && !mstaged && row_ok && t_first < n_kv)
+    const int t_first = kPairOwn ? 2 * wg : kAlt ? wg : 0;
+    // The next own tile's entries (with whole tiles also the one after it:
+    // with paired ownership the next tile may follow at once).
+    MaskRegs<MASK, KW> mnext, mnext2;
+    if (kMaskAhead && !mstaged && row_ok && t_first < n_kv) {
       mnext.load(p, mrow, (kv0 + t_first) * BN + cofs);
-    for (int t = t_first; t < n_kv; t += TSTEP) {
+      if (kAlt && next_tile(t_first) < n_kv)
+        mnext2.load(p, mrow, (kv0 + next_tile(t_first)) * BN + cofs);
+    }
+    for (int t = t_first; t < n_kv; t = next_tile(t)) {
       const int buf = t % L::NB;  // score buffer
       const uint32_t bph = (t / L::NB) & 1;
       const int xb = t & 1;       // tile parity: the maxima exchange slot
@@ -765,7 +834,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!mstaged) {
         if constexpr (kMaskAhead) {
           mreg = mnext;
-          if (row_ok && t + TSTEP < n_kv) mnext.load(p, mrow, j0 + TSTEP * BN);
+          if constexpr (kAlt) {
+            mnext = mnext2;
+            const int t2 = next_tile(next_tile(t));
+            if (row_ok && t2 < n_kv) mnext2.load(p, mrow, (kv0 + t2) * BN + cofs);
+          } else {
+            if (row_ok && t + 1 < n_kv) mnext.load(p, mrow, j0 + BN);
+          }
           if constexpr (MASK == kMaskAdditive) {
             // additive entries two tiles ahead into L2 as well (measured: bool
             // masks, a quarter the bytes, do not gain)
@@ -910,12 +985,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l_run *= alpha;
         lx_run *= alpha;
         mu_run *= alpha;
-        if (t >= TSTEP && __any_sync(0xffffffffu, need)) {
+        if (!first_of_acc(t) && __any_sync(0xffffffffu, need)) {
           // A and T hold tile t-1's contributions once its MMAs are done; each
           // warpgroup rescales half of the [A | T] columns of its rows.  (With
-          // alternate tiles the accumulator's last tile is t - 2, and tile
-          // t - 1's products, which complete after it, are the latest whose
-          // completion can be awaited: tile t's need this thread's P~.)
+          // whole tiles the accumulator's last tile may be t - 3; tile t - 1's
+          // products complete after it, and no later tile's can complete
+          // before this thread publishes tile t's P~.)
           if (!warp_wait<kHint>(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
             ok = false;
             break;
@@ -1078,9 +1153,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           JVP_CHECK(R < static_cast<long long>(p.splits) * rows, p.status, kChkGlobalRow))
         reinterpret_cast<float4*>(p.split_ws)[R] = make_float4(m_all, l_all, lx_all, mu_all);
       wait_acc();
-      // With alternate tiles and a single key tile, warpgroup 1's accumulator
-      // was never written (its weight is 0, its contents undefined).
-      const bool only_acc0 = kAlt && n_kv == 1;
+      // With whole tiles and only warpgroup 0's first tile (or pair) of keys,
+      // warpgroup 1's accumulator was never written (its weight is 0, its
+      // contents undefined).
+      const bool only_acc0 = kAlt && n_kv <= (kPairOwn ? 2 : 1);
 #pragma unroll 1
       for (int col = wg * (D / 2); ok && col < (wg + 1) * (D / 2); col += 16) {
         float fa[16], ft[16];
