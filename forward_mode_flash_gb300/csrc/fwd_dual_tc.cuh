@@ -195,7 +195,7 @@ struct TcCtrl {
   uint64_t s_full[4], p_full[4], max_ready[2];
   uint64_t s_ready[4];  // S of a score buffer is final (its dS may still be accumulating)
   uint64_t p_ready[4];  // P~ of a score buffer is stored (P~ * dS may not be yet)
-  uint64_t at_done, o_full, drain, drain_pv, sums_ready;
+  uint64_t o_full, drain, drain_pv, sums_ready;
   uint64_t o_staged;  // every softmax warp has staged its O / tO rows in shared memory
   uint64_t pv_done[4];  // P~V MMAs of the tile in each score buffer are complete
   uint64_t ring_free, peer_ready;  // cluster split (arrived on by the other CTA)
@@ -373,6 +373,13 @@ constexpr int kPairRecvRowBytes = 2 * 32 * 4 + 16;
 constexpr int kPairRecvBlock = 128 * kPairRecvRowBytes;
 constexpr int kPairRecvBytes = kPairRecvStats + 2 * kPairRecvBlock;
 
+// Whether the kernel brings the additive mask's tiles through a shared-memory
+// slot (the layout parameter MTILE; kernel and launcher must agree).
+template <int D, int MASK, bool TANGENT>
+constexpr bool tc_mask_tile() {
+  return MASK == kMaskAdditive && D == 128 && TANGENT;
+}
+
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
@@ -381,7 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // in its tile.  (At D = 64, and without tangents, the registers hold a tile
   // ahead; the shared-memory slot measured slower there: its refill waits for
   // the previous tile's maximum and holds up the producer's deeper K/V rings.)
-  constexpr bool kMTile = (MASK == kMaskAdditive && D == 128 && TANGENT);
+  constexpr bool kMTile = tc_mask_tile<D, MASK, TANGENT>();
   // Waits without a suspend-time hint at D = 64 (measured faster there).
   constexpr bool kHint = (D != 64);
   using L = TcLayout<D, TANGENT, kMTile>;
@@ -492,7 +499,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(&ctrl->max_ready[0], kSoftmaxThreads / 32);
     mbar_init(&ctrl->max_ready[1], kSoftmaxThreads / 32);
-    mbar_init(&ctrl->at_done, 1);
     mbar_init(&ctrl->drain_pv, 1);
     mbar_init(&ctrl->o_full, 1);
     mbar_init(&ctrl->drain, 1);
@@ -746,7 +752,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         mma_commit(&ctrl->vdv_empty[s]);
-        mma_commit(&ctrl->at_done);
         mma_commit(&ctrl->pv_done[buf]);
       }
       if (ok) {
@@ -792,7 +797,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // overlaps a whole tile of work (not the additive mask at D = 128 with
     // tangents, whose two tiles of 32 floats would not fit the register
     // budget next to the tangent terms).
-    constexpr bool kMaskAhead = !(MASK == kMaskAdditive && D == 128 && TANGENT);
+    constexpr bool kMaskAhead = !tc_mask_tile<D, MASK, TANGENT>();
     const bool mstaged = kMTile && p.mask_tma;  // additive tiles through shared memory (D = 128)
     const int t_first = kPairOwn ? 2 * wg : kAlt ? wg : 0;
     // The next own tile's entries (with whole tiles also the one after it:
@@ -986,12 +991,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         lx_run *= alpha;
         mu_run *= alpha;
         if (!first_of_acc(t) && __any_sync(0xffffffffu, need)) {
-          // A and T hold tile t-1's contributions once its MMAs are done; each
-          // warpgroup rescales half of the [A | T] columns of its rows.  (With
+          // A and T hold tile t-1's contributions once its MMAs are done (with
           // whole tiles the accumulator's last tile may be t - 3; tile t - 1's
-          // products complete after it, and no later tile's can complete
-          // before this thread publishes tile t's P~.)
-          if (!warp_wait<kHint>(&ctrl->at_done, (t - 1) & 1, p.status, abort)) {
+          // products complete after it); each warpgroup rescales half of the
+          // [A | T] columns of its rows.  The wait is on the completions of
+          // tile t - 1's score buffer, which a parity wait follows exactly:
+          // the buffer's previous user, tile t - 1 - NB, is done (tile t's
+          // scores needed tile t - NB's products done), and its next, tile
+          // t - 1 + NB, cannot be before this thread publishes tile t's P~.
+          // (One barrier for all tiles would not do: with four buffers its
+          // completions may lag tile t - 1 by three, and a parity wait cannot
+          // tell a phase from the one two before it.)
+          const int tb = t - 1;
+          if (!warp_wait<kHint>(&ctrl->pv_done[tb % L::NB], (tb / L::NB) & 1, p.status, abort)) {
             ok = false;
             break;
           }
@@ -1395,7 +1407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream_t stream) {
-  using L = TcLayout<D, TANGENT, MASK == kMaskAdditive && D == 128>;
+  using L = TcLayout<D, TANGENT, tc_mask_tile<D, MASK, TANGENT>()>;
   auto kern = fwd_dual_tc_kernel<T, D, MASK, TANGENT, SPLIT>;
   // The attribute is per device; setting it is idempotent, the mask (shared
   // by host threads) only saves calls.

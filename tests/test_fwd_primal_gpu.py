@@ -128,3 +128,42 @@ def test_primal_forward_matches_the_dual_forwards_output():
     torch.cuda.synchronize()
     assert (o_p.float() - o_d.float()).abs().max().item() <= 1.6e-2
     assert (lse_p - lse_d).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("mask", ["none", "causal", "bool", "additive"])
+@pytest.mark.parametrize("dt,D", [("bf16", 128), ("f16", 64)])
+def test_primal_forward_rescales_when_the_maximum_jumps(mask, dt, D):
+    # Logits that grow by ~10 (14 in log2 units, above the 2^8 rescale
+    # threshold) from one key tile to the next, so every tile moves the
+    # running maximum and rescales its accumulator while the products of
+    # earlier tiles may still be in flight.
+    B, H, N = 2, 2, 1024
+    w = synth.small(dt, B, H, N, D, mask, seed=17)
+    inp = synth.make_inputs(w)
+    g = torch.Generator().manual_seed(17)
+    q = (torch.ones(B, H, N, D) + 0.1 * torch.randn(B, H, N, D, generator=g))
+    tile = (torch.arange(N) // 64).to(torch.float32)
+    k = (tile * 10.0 / D ** 0.5)[None, None, :, None] * torch.ones(B, H, N, D)
+    k = k + 0.1 * torch.randn(B, H, N, D, generator=g)
+    dt_t = {"bf16": torch.bfloat16, "f16": torch.float16}[dt]
+    q, k = q.to(dt_t), k.to(dt_t)
+    v = inp.v
+    dev = "cuda"
+    m = inp.mask.to(dev) if inp.mask is not None else None
+    causal = mask == "causal"
+    runs = [A.attention(q.to(dev), k.to(dev), v.to(dev), attn_mask=m, is_causal=causal,
+                        return_lse=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert A.device_status() == 0 and A.last_path() == 1
+    for o, lse in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(lse, runs[0][1])
+    kind, mm = mask, None
+    if mask == "bool":
+        mm = inp.mask.numpy()
+    elif mask == "additive":
+        mm = inp.mask.double().numpy()
+    ro, _, rl, _ = oracle.fwd_dual(np64(q), np64(k), np64(v), mask_kind=kind, mask=mm)
+    o, lse = runs[0]
+    assert np.abs(np64(o) - ro).max() <= TOL[dt]
+    fin = np.isfinite(rl)
+    assert np.abs(np64(lse)[fin] - rl[fin]).max() <= max(1e-3, 1e-4 * float(np.abs(rl[fin]).max()))
