@@ -49,8 +49,9 @@ def parse():
     ap.add_argument("--no-causal", action="store_true",
                     help="skip the causal companion timing of the default workload")
     ap.add_argument("--mode", default="fwd_dual",
-                    choices=["fwd_dual", "bwd_dual", "bwd", "sweep", "memory"],
-                    help="fwd_dual (the headline), the backward of the dual computation (bwd_dual) "
+                    choices=["fwd_dual", "fwd", "bwd_dual", "bwd", "sweep", "memory"],
+                    help="fwd_dual (the headline), the forward without tangents (fwd), the "
+                         "backward of the dual computation (bwd_dual) "
                          "or of attention without tangents (bwd), the "
                          "sequence-length sweep (one JSON line per configuration) or the "
                          "memory-scaling report (one JSON line per N)")
@@ -465,6 +466,103 @@ def run_bwd(args, rank, world, local):
     return 0
 
 
+def run_fwd(args, rank, world, local):
+    """Times jvp_attn_fwd, the forward of attention without tangents (O and the
+    log-sum-exp), on one workload (--mode fwd): the plain attention forward of
+    jvp_attention outside torch.func.jvp."""
+    import torch
+
+    import oracle
+    from forward_mode_flash_gb300 import api, build, metrics, replicas, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    name = args.workload
+    w = synth.WORKLOADS[name]
+    causal = w.mask == "causal"
+    inp = synth.make_inputs(w, device=str(dev))
+    o = torch.empty_like(inp.q)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        return api.attention(inp.q, inp.k, inp.v, attn_mask=inp.mask, is_causal=causal,
+                             return_lse=True, out=o)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    tensor_core = api.last_path() == 1
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        for _ in range(2):  # untimed steps right before the timed ones (see timed_steps)
+            flush.fill_(0.0)
+            step()
+        with torch.cuda.nvtx.range(f"fwd timed region: {args.steps} steps"):
+            for s in range(args.steps):
+                flush.fill_(float(s))
+                starts[s].record(stream)
+                with torch.cuda.nvtx.range("step"):
+                    step()
+                ends[s].record(stream)
+            torch.cuda.synchronize()
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = replicas.max_over_ranks(sum(per_ms), device=dev)
+    ms_step = total_ms / args.steps
+    flops = metrics.flops_fwd(w.B, w.H, w.N, w.N, w.D, causal)
+    value = replicas.aggregate_throughput(world, flops, args.steps, total_ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    if tensor_core:
+        tc_peak = float(pk.get("bf16_tflops", 1900.0))  # fp16 and bf16 share the dense rate
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tc_peak, "traffic": None,
+                    "flops": "algorithmic: 4 B H Nq Nk D (half for causal), Q K^T and P V",
+                    "peak_source": f"{pk_src} bf16 dense (cuBLAS burst)",
+                    "kernel": "fwd_dual_tc_kernel without tangents"}
+    else:
+        clk = pk.get("sm_max_mhz", 2070.0) * 1e6
+        n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = n_sms * FP32_LANES_PER_SM * 2 * clk / 1e12
+        roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                    "frac": achieved / alu_peak, "traffic": None,
+                    "peak_source": f"{n_sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 x "
+                                   f"{clk / 1e6:.0f} MHz (CUDA-core fp32)",
+                    "kernel": "fwd_dual_simt_kernel without tangents"}
+    line = {
+        "metric": "fwd (attention forward without tangents) TFLOP/s", "mode": args.mode,
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{w.dtype} (fp32 accumulate)" if tensor_core else "f32", "data": "synthetic",
+        "config": {"workload": name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "mask": w.mask,
+                   "input_dtype": w.dtype, "algorithmic_flops_per_step": flops,
+                   "l2": "flushed: 256 MiB written between timed steps (outside the events)"},
+        "roofline": roofline,
+        "clocks": clocks.summary(), "gpu_launches": args.steps, "e2e": None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # The float64 oracle on one whole head of the same workload (zero tangents).
+        x = [t[:1, :1].double().cpu().numpy() for t in (inp.q, inp.k, inp.v)]
+        m = inp.mask
+        kind, mm = w.mask, None
+        if m is not None:
+            mm = m[:1, :1].double().cpu().numpy() if w.mask == "additive" else m[:1, :1].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.fwd_dual(*x, mask_kind=kind, mask=mm)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": flops / (w.B * w.H) / dt / 1e12,
+                                "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                "sample": f"one (b, h) head of {name}, float64 forward "
+                                          f"(the oracle's dual evaluation with zero tangents), "
+                                          f"{dt:.1f} s wall (the oracle threads over heads)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_report(args, rank, world, local):
     """The sequence-length sweep or the memory-scaling report (rank 0 only)."""
     import torch
@@ -508,8 +606,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     if args.mode in ("sweep", "memory"):
         return run_report(args, rank, world, local)
-    if args.mode in ("bwd_dual", "bwd"):
-        rc = run_bwd(args, rank, world, local)
+    if args.mode in ("bwd_dual", "bwd", "fwd"):
+        rc = (run_fwd if args.mode == "fwd" else run_bwd)(args, rank, world, local)
         if world > 1:
             dist.barrier()
             dist.destroy_process_group()
