@@ -102,7 +102,9 @@ struct TcLayout {
   static constexpr int BM = kTcBlockM;              // query rows per CTA
   static constexpr int BN = kTcBlockN;              // keys per tile
   static constexpr int KCH = D / 64;                // 128-byte chunks along D
-  static constexpr int NS = (D == 128 && TANGENT) ? 2 : 4;  // K/V ring depth
+  // K/V ring depth (three stages without tangents when two additive-mask
+  // slots take the room of the fourth)
+  static constexpr int NS = (D == 128 && TANGENT) ? 2 : (MTILE ? 3 : 4);
   // Score buffers in TMEM: with tangents two of 128 columns ([S | dS]);
   // without, four of 64 (S alone), so the score products can run up to three
   // tiles ahead of the softmax.
@@ -115,15 +117,18 @@ struct TcLayout {
   static constexpr int VCHUNK_BYTES = BN * 128;        // one 64-column chunk of V
   static constexpr int VDV_BYTES = (TANGENT ? 2 : 1) * KCH * VCHUNK_BYTES;
   // MTILE: the additive mask's [BM x BN] fp32 tile is brought into shared
-  // memory by TMA a tile ahead (D = 128, where a tile ahead does not fit the
-  // registers).  To make room next to the dual rings, the two [K;dK] stages
+  // memory by TMA a tile ahead (D = 128: one slot with tangents, where a tile
+  // ahead does not fit the registers; two without, each thread's row loads
+  // touching a line per row).  To make room next to the dual rings, the two [K;dK] stages
   // then share one dK slot: each 64-column chunk holds [K0 | dK | K1], stage 0
   // reads the 128 rows [K0; dK] and stage 1 the rows [dK; K1], so stage 1's
   // score products come out as [Q dK^T | S] instead of [S | Q dK^T].  The dK
   // slot is refilled once the first score product of a tile has read it.
   static constexpr bool kSharedDK = MTILE && TANGENT && NS == 2;
   static constexpr int KREGION = kSharedDK ? KCH * 3 * BN * 128 : NS * KDK_BYTES;
-  static constexpr int MSK_BYTES = MTILE ? BM * BN * 4 : 0;
+  static constexpr int NMS = MTILE ? (TANGENT ? 1 : 2) : 0;  // mask slots
+  static constexpr int MSK_TILE = BM * BN * 4;                // one slot
+  static constexpr int MSK_BYTES = NMS * MSK_TILE;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DQ = OFF_Q + Q_BYTES;
   static constexpr int OFF_KDK = OFF_DQ + (TANGENT ? Q_BYTES : 0);
@@ -204,7 +209,7 @@ struct TcCtrl {
   float xmax[2][2][kTcBlockM];     // [tile parity][warpgroup][row] half-row maxima
   float xsum[2][4][kTcBlockM];     // [warpgroup][l, lx, mu, m][row] final half sums
   uint64_t dk_empty;               // the shared dK slot has been read (MTILE with tangents)
-  uint64_t msk_full, msk_empty;    // the additive-mask tile in shared memory (MTILE)
+  uint64_t msk_full[2], msk_empty[2];  // the additive-mask slots in shared memory (MTILE)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -377,21 +382,22 @@ constexpr int kPairRecvBytes = kPairRecvStats + 2 * kPairRecvBlock;
 // slot (the layout parameter MTILE; kernel and launcher must agree).
 template <int D, int MASK, bool TANGENT>
 constexpr bool tc_mask_tile() {
-  return MASK == kMaskAdditive && D == 128 && TANGENT;
+  return MASK == kMaskAdditive && D == 128;
 }
 
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
-  // The additive mask at D = 128 with tangents comes through shared memory
-  // when its layout allows a tensor map (p.mask_tma), else by per-row loads
-  // in its tile.  (At D = 64, and without tangents, the registers hold a tile
+  // The additive mask at D = 128 comes through shared memory when its layout
+  // allows a tensor map (p.mask_tma), else by per-row loads in its tile (one
+  // slot with tangents, two without).  (At D = 64 the registers hold a tile
   // ahead; the shared-memory slot measured slower there: its refill waits for
   // the previous tile's maximum and holds up the producer's deeper K/V rings.)
   constexpr bool kMTile = tc_mask_tile<D, MASK, TANGENT>();
   // Waits without a suspend-time hint at D = 64 (measured faster there).
   constexpr bool kHint = (D != 64);
   using L = TcLayout<D, TANGENT, kMTile>;
+  constexpr int NMS = L::NMS > 0 ? L::NMS : 1;  // additive-mask slots (MTILE)
   constexpr bool kWsSplit = SPLIT == kSplitWorkspace;
   constexpr bool kPair = SPLIT == kSplitCluster;
   static_assert(!kPair || (D == 64 && TANGENT), "the cluster split is built for D = 64 with tangents");
@@ -404,8 +410,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // issued as one N = 128 product (see the score warp); not with a boolean
   // mask, where single tiles measured faster (bf16 B=4 H=16 N=2048: 187.5 us
   // against 190.3 with pairs taken by alternate warpgroups, 195.2 with the
-  // pairs' ownership below).
-  constexpr bool kPairS = !TANGENT && D == 128 && MASK != kMaskBool;
+  // pairs' ownership below), nor with an additive one (the same time either
+  // way; its three-stage rings make room for two mask slots).
+  constexpr bool kPairS = !TANGENT && D == 128 && (MASK == kMaskNone || MASK == kMaskCausal);
   // Without tangents (and without an additive mask) the two softmax
   // warpgroups take whole key tiles, each into its own accumulator, instead
   // of half of every tile: a thread's fixed per-tile costs (waits, TMEM round
@@ -507,8 +514,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&ctrl->ring_free, 1);    // cluster split: rank 0's rings are idle
     mbar_init(&ctrl->peer_ready, 1);   // cluster split: rank 1's state has landed (with bytes)
     mbar_init(&ctrl->dk_empty, 1);
-    mbar_init(&ctrl->msk_full, 1);
-    mbar_init(&ctrl->msk_empty, kSoftmaxThreads / 32);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctrl->msk_full[s], 1);
+      mbar_init(&ctrl->msk_empty[s], kSoftmaxThreads / 32);
+    }
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -582,15 +591,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         if (mtma) {
-          // one slot: tile t's mask once every softmax warp has read tile t-1's
-          if (!mbar_wait<kHint>(&ctrl->msk_empty, (t & 1) ^ 1, abort)) {
+          // slot t % NMS: tile t's mask once every softmax warp has read the
+          // slot's previous tile (t - NMS)
+          const int ms = t % NMS;
+          if (!mbar_wait<kHint>(&ctrl->msk_empty[ms], ((t / NMS) & 1) ^ 1, abort)) {
             record_timeout(p.status, abort);
             break;
           }
-          mbar_arrive_expect_tx(&ctrl->msk_full, L::MSK_BYTES);
+          mbar_arrive_expect_tx(&ctrl->msk_full[ms], L::MSK_TILE);
           for (int w = 0; w < 2; ++w)
-            tma_load_4d(smem + L::OFF_MSK + w * L::BM * 128, &maps.msk, &ctrl->msk_full,
-                        j0 + w * (BN / 2), q0, mh, mb);
+            tma_load_4d(smem + L::OFF_MSK + ms * L::MSK_TILE + w * L::BM * 128, &maps.msk,
+                        &ctrl->msk_full[ms], j0 + w * (BN / 2), q0, mh, mb);
           ++m_fills;
         }
         if (!mbar_wait<kHint>(&ctrl->vdv_empty[s], ph ^ 1, abort)) {
@@ -615,7 +626,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_wait<kHint>(&ctrl->kdk_full[t % NS], (t / NS) & 1, &zero);
         for (int t = max(0, v_fills - NS); t < v_fills; ++t)
           mbar_wait<kHint>(&ctrl->vdv_full[t % NS], (t / NS) & 1, &zero);
-        if (m_fills > 0) mbar_wait<kHint>(&ctrl->msk_full, (m_fills - 1) & 1, &zero);
+        for (int u = max(0, m_fills - NMS); u < m_fills; ++u)
+          mbar_wait<kHint>(&ctrl->msk_full[u % NMS], (u / NMS) & 1, &zero);
       }
     }
   } else if (warp == 1) {
@@ -794,9 +806,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // Mask entries are loaded one tile ahead, so their global-memory latency
-    // overlaps a whole tile of work (not the additive mask at D = 128 with
-    // tangents, whose two tiles of 32 floats would not fit the register
-    // budget next to the tangent terms).
+    // overlaps a whole tile of work (not the additive mask at D = 128, whose
+    // two tiles of 32 floats would not fit the register budget next to the
+    // tangent terms, and which comes through shared memory).
     constexpr bool kMaskAhead = !tc_mask_tile<D, MASK, TANGENT>();
     const bool mstaged = kMTile && p.mask_tma;  // additive tiles through shared memory (D = 128)
     const int t_first = kPairOwn ? 2 * wg : kAlt ? wg : 0;
@@ -821,11 +833,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // swizzle: 16-byte piece c of row r sits at piece position
           // c ^ (r % 8), so the 8 rows of a quarter warp hit distinct banks.
           // (The slot is released once the entries are consumed, below.)
-          if (!warp_wait<kHint>(&ctrl->msk_full, t & 1, p.status, abort)) {
+          if (!warp_wait<kHint>(&ctrl->msk_full[t % NMS], (t / NMS) & 1, p.status, abort)) {
             ok = false;
             break;
           }
-          const uint32_t mrow_s = smem_u32(smem + L::OFF_MSK + wg * L::BM * 128 + r * 128);
+          const uint32_t mrow_s = smem_u32(smem + L::OFF_MSK + (t % NMS) * L::MSK_TILE +
+                                           wg * L::BM * 128 + r * 128);
 #pragma unroll
           for (int c4 = 0; c4 < HN / 4; ++c4) {
             const float4 v = ld_shared_v4f(mrow_s + ((c4 ^ (r & 7)) << 4));
@@ -964,7 +977,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&ctrl->max_ready[xb]);
-          if (mstaged) mbar_arrive(&ctrl->msk_empty);
+          if (mstaged) mbar_arrive(&ctrl->msk_empty[t % NMS]);
         }
         spec = __all_sync(0xffffffffu,
                           m_run != -INFINITY && !(m_half > m_run + kRescaleThreshold));
@@ -981,7 +994,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ctrl->xmax[xb][wg][r] = m_half;
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctrl->msk_empty);
+        if (lane == 0) mbar_arrive(&ctrl->msk_empty[t % NMS]);
       }
       const bool need = m_tile > m_run + kRescaleThreshold;
       if (!spec || __any_sync(0xffffffffu, need)) {

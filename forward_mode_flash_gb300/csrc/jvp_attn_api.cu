@@ -402,9 +402,8 @@ jvp_status_t forward(const jvp_shape_t* shape, jvp_dtype_t dtype, const void* co
     if (tc && tangent)
       tc = encode_map(&maps.t_o, dtype, out[1], B, H, Nq, D, out_strides[1], kTcBlockM);
     if (tc && !tangent) maps.t_o = maps.o;
-    // The additive mask at D = 128 with tangents through shared memory (else
-    // per-row loads; without tangents the kernel holds a tile ahead in registers).
-    if (tc && tangent && kind == JVP_MASK_ADDITIVE && kernel_d == 128)
+    // The additive mask at D = 128 through shared memory (else per-row loads).
+    if (tc && kind == JVP_MASK_ADDITIVE && kernel_d == 128)
       p.mask_tma = encode_mask_map(&maps.msk, mptr, B, H, Nq, Nk, msb, msh, msq, msk) ? 1 : 0;
   }
   cudaError_t err;
