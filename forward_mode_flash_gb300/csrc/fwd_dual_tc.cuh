@@ -189,6 +189,9 @@ constexpr int kSoftmaxThreads = 256;           // two warpgroups (warps 2..9)
 // + producer warp (0), score-MMA warp (1) and P~V-MMA warp (10)
 constexpr int kTcThreads = 96 + kSoftmaxThreads;
 constexpr int kPvWarp = 10;
+// Second score and P~V issuing warps (forward without tangents at D = 64,
+// where a tile's products are narrow and one thread's issue rate paces them).
+constexpr int kScoreWarp2 = 11, kPvWarp2 = 12;
 
 // Control block in shared memory.
 template <int NS>
@@ -201,6 +204,7 @@ struct TcCtrl {
   uint64_t s_ready[4];  // S of a score buffer is final (its dS may still be accumulating)
   uint64_t p_ready[4];  // P~ of a score buffer is stored (P~ * dS may not be yet)
   uint64_t o_full, drain, drain_pv, sums_ready;
+  uint64_t drain2, drain_pv2;  // the second issuing threads' drains (split issue)
   uint64_t o_staged;  // every softmax warp has staged its O / tO rows in shared memory
   uint64_t pv_done[4];  // P~V MMAs of the tile in each score buffer are complete
   uint64_t ring_free, peer_ready;  // cluster split (arrived on by the other CTA)
@@ -384,9 +388,22 @@ template <int D, int MASK, bool TANGENT>
 constexpr bool tc_mask_tile() {
   return MASK == kMaskAdditive && D == 128;
 }
+// Whether alternate tiles' products are issued by two score and two P~V
+// threads (without tangents at D = 64, where whole tiles alternate between
+// the warpgroups, so each accumulator still has one issuing thread), and the
+// block size that follows.  Not with a mask: the two extra warps leave the
+// boolean mask's two tiles of entries ahead too few registers.
+template <int D, int MASK, bool TANGENT>
+constexpr bool tc_split_issue() {
+  return !TANGENT && D == 64 && (MASK == kMaskNone || MASK == kMaskCausal);
+}
+template <int D, int MASK, bool TANGENT>
+constexpr int tc_threads() {
+  return kTcThreads + (tc_split_issue<D, MASK, TANGENT>() ? 64 : 0);
+}
 
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(tc_threads<D, MASK, TANGENT>(), 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
   // The additive mask at D = 128 comes through shared memory when its layout
   // allows a tensor map (p.mask_tma), else by per-row loads in its tile (one
@@ -424,6 +441,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // all want the exponential unit at the same time).
   constexpr bool kAlt = !TANGENT && MASK != kMaskAdditive;
   constexpr bool kPairOwn = kAlt && kPairS;
+  constexpr bool kIssue2 = tc_split_issue<D, MASK, TANGENT>();
+  static_assert(!kIssue2 || (kAlt && !kPairS), "split issue: alternate single tiles");
   constexpr int KW = kAlt ? BN : HN;  // keys of a tile per softmax thread
   // The next tile of the warpgroup that takes tile t, and whether tile t is
   // the first of its accumulator.
@@ -507,8 +526,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&ctrl->max_ready[0], kSoftmaxThreads / 32);
     mbar_init(&ctrl->max_ready[1], kSoftmaxThreads / 32);
     mbar_init(&ctrl->drain_pv, 1);
-    mbar_init(&ctrl->o_full, 1);
+    mbar_init(&ctrl->o_full, kIssue2 ? 2 : 1);  // one commit per P~V-issuing thread
     mbar_init(&ctrl->drain, 1);
+    mbar_init(&ctrl->drain2, 1);
+    mbar_init(&ctrl->drain_pv2, 1);
     mbar_init(&ctrl->sums_ready, kSoftmaxThreads);
     mbar_init(&ctrl->o_staged, kSoftmaxThreads / 32);
     mbar_init(&ctrl->ring_free, 1);    // cluster split: rank 0's rings are idle
@@ -630,7 +651,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_wait<kHint>(&ctrl->msk_full[u % NMS], (u / NMS) & 1, &zero);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (kIssue2 && warp == kScoreWarp2)) {
     // ------------------------------------------------------------ score MMAs
     // Tile t's score products go into buffer t % NB once its K tile has landed
     // and the P~V MMAs of tile t - NB (the buffer's previous user) are done.
@@ -641,7 +662,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // t % 4 + 1 from the adjacent stages t % 4 and t % 4 + 1: half the
     // instructions of two N = 64 sets (one thread issues a tcgen05.mma about
     // every 70 cycles) and less tensor time (a narrow product is paced by
-    // reading its A tile from shared memory).
+    // reading its A tile from shared memory).  With split issue this warp
+    // takes the even tiles and the second score warp the odd ones.
     static_assert(!kPairS || (NS % 2 == 0 && L::NB % 2 == 0), "pairs of stages and buffers");
     if (lane == 0) {
       bool ok = mbar_wait<kHint>(&ctrl->q_full, 0, abort);
@@ -650,8 +672,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
       // s < 0: -Q K^T, -Q dK^T, -dQ K^T (negate-A bit), with |s| applied later.
       const uint32_t neg_a = p.neg_scores ? (1u << 13) : 0u;
-      constexpr int SSTEP = kPairS ? 2 : 1;  // key tiles per step
-      for (int t = 0; ok && t < n_kv; t += SSTEP) {
+      constexpr int SSTEP = (kPairS || kIssue2) ? 2 : 1;  // key tiles per step
+      const int s_first = (kIssue2 && warp != 1) ? 1 : 0;
+      uint64_t* const s_drain = (kIssue2 && warp != 1) ? &ctrl->drain2 : &ctrl->drain;
+      for (int t = s_first; ok && t < n_kv; t += SSTEP) {
         const bool pair = kPairS && t + 1 < n_kv;
         const int s = t % NS;
         const int bb = t % L::NB;  // score buffer
@@ -702,15 +726,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) record_timeout(p.status, abort);
       // Drain: every MMA this thread issued completes before TMEM is freed.
-      mma_commit(&ctrl->drain);
+      mma_commit(s_drain);
       const int zero = 0;
-      mbar_wait<kHint>(&ctrl->drain, 0, &zero);
+      mbar_wait<kHint>(s_drain, 0, &zero);
     }
-  } else if (warp == kPvWarp) {
+  } else if (warp == kPvWarp || (kIssue2 && warp == kPvWarp2)) {
     // ------------------------------------------------------------ P~V MMAs
+    // (with split issue: this warp the even tiles, the second P~V warp the odd
+    // ones, each into its warpgroup's accumulator)
     if (lane == 0) {
       bool ok = true;
-      for (int t = 0; ok && t < n_kv; ++t) {
+      const int p_first = (kIssue2 && warp != kPvWarp) ? 1 : 0;
+      uint64_t* const p_drain = (kIssue2 && warp != kPvWarp) ? &ctrl->drain_pv2 : &ctrl->drain_pv;
+      for (int t = p_first; ok && t < n_kv; t += kIssue2 ? 2 : 1) {
         const int buf = t % L::NB;
         const uint32_t bph = (t / L::NB) & 1;
         if (!mbar_wait<kHint>(TANGENT ? &ctrl->p_ready[buf] : &ctrl->p_full[buf], bph, abort)) {
@@ -771,9 +799,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else {
         record_timeout(p.status, abort);
       }
-      mma_commit(&ctrl->drain_pv);
+      mma_commit(p_drain);
       const int zero = 0;
-      mbar_wait<kHint>(&ctrl->drain_pv, 0, &zero);
+      mbar_wait<kHint>(p_drain, 0, &zero);
     }
   } else if (warp >= 2 && warp < 2 + kSoftmaxThreads / 32) {
     // ------------------------------------------------------------ softmax
@@ -1015,7 +1043,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // (One barrier for all tiles would not do: with four buffers its
           // completions may lag tile t - 1 by three, and a parity wait cannot
           // tell a phase from the one two before it.)
-          const int tb = t - 1;
+          // (With split issue the accumulator's products come from one thread
+          // whose commits cover only its own: wait on its last tile, t - 2,
+          // exact by the same argument with t - 2 for t - 1.)
+          const int tb = kIssue2 ? t - 2 : t - 1;
           if (!warp_wait<kHint>(&ctrl->pv_done[tb % L::NB], (tb / L::NB) & 1, p.status, abort)) {
             ok = false;
             break;
@@ -1438,7 +1469,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     // the two CTAs of a query tile (consecutive blocks) form a cluster
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(tc_threads<D, MASK, TANGENT>());
     cfg.dynamicSmemBytes = L::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1450,7 +1481,8 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, maps, p);
   }
-  kern<<<static_cast<unsigned>(grid), kTcThreads, L::SMEM_BYTES, stream>>>(maps, p);
+  kern<<<static_cast<unsigned>(grid), tc_threads<D, MASK, TANGENT>(), L::SMEM_BYTES, stream>>>(maps,
+                                                                                          p);
   return cudaGetLastError();
 }
 
