@@ -8,7 +8,9 @@ kernel through a tensor map: [128 x 32] boxes copied into shared memory a
 tile ahead.  Any other layout takes per-row loads.  Both must give the same
 result as the oracle, to the forward tolerance (max-abs 2e-2 for fp16/bf16 on
 O and tO); the layouts below cover both routes, and at D = 64 (the
-register route for every layout) as a control.
+register route for every layout) as a control.  Each case also runs the
+forward without tangents on the same mask (two shared-memory slots at D = 128
+where the layout allows the tensor map) against the oracle's O and lse.
 """
 
 import numpy as np
@@ -93,6 +95,16 @@ def check(dtype, D, kind, layout, B, H, Nq, Nk, causal=False, seed=0):
     assert np.array_equal(np.isfinite(np64(lse)), fin)
     if fin.any():
         assert np.abs(np64(lse)[fin] - rl[fin]).max() <= 1e-3
+    # The forward without tangents on the same mask (its own mask routes: two
+    # shared-memory slots at D = 128, registers a tile ahead at D = 64).
+    po, plse = A.attention(*(x.cuda() for x in (q, k, v)), attn_mask=m, is_causal=causal,
+                           return_lse=True)
+    torch.cuda.synchronize()
+    assert A.device_status() == 0 and A.last_path() == 1
+    assert np.abs(np64(po) - ro).max() <= TOL, layout
+    assert np.array_equal(np.isfinite(np64(plse)), fin)
+    if fin.any():
+        assert np.abs(np64(plse)[fin] - rl[fin]).max() <= 1e-3
 
 
 @pytest.mark.parametrize("D", [128, 64])
