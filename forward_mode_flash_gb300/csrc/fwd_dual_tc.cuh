@@ -397,13 +397,27 @@ template <int D, int MASK, bool TANGENT>
 constexpr bool tc_split_issue() {
   return !TANGENT && D == 64 && (MASK == kMaskNone || MASK == kMaskCausal);
 }
-template <int D, int MASK, bool TANGENT>
+// Whether a second score warp issues the odd tiles' score products: with
+// split issue above, and with tangents at D = 128 without a mask or causal
+// (sixteen products per tile, eight of them N = 64, pace one issuing thread:
+// bf16 B=4 H=16 N=2048 290.8 -> 280.9 us, causal 175.0 -> 172.2; with a
+// boolean mask 301.6 -> 304.1 and at D = 64 202.0 -> 203.4, so not there).
+// Each tile's products come from one thread, so their accumulation order
+// stays fixed.
+template <int D, int MASK, bool TANGENT, int SPLIT>
+constexpr bool tc_score2() {
+  return tc_split_issue<D, MASK, TANGENT>() ||
+         (TANGENT && D == 128 && (MASK == kMaskNone || MASK == kMaskCausal) &&
+          SPLIT != kSplitCluster);
+}
+template <int D, int MASK, bool TANGENT, int SPLIT>
 constexpr int tc_threads() {
-  return kTcThreads + (tc_split_issue<D, MASK, TANGENT>() ? 64 : 0);
+  return kTcThreads + (tc_score2<D, MASK, TANGENT, SPLIT>() ? 32 : 0) +
+         (tc_split_issue<D, MASK, TANGENT>() ? 32 : 0);
 }
 
 template <typename T, int D, int MASK, bool TANGENT, int SPLIT>
-__global__ void __launch_bounds__(tc_threads<D, MASK, TANGENT>(), 1)
+__global__ void __launch_bounds__(tc_threads<D, MASK, TANGENT, SPLIT>(), 1)
     fwd_dual_tc_kernel(const __grid_constant__ TcMaps maps, const FwdParams p) {
   // The additive mask at D = 128 comes through shared memory when its layout
   // allows a tensor map (p.mask_tma), else by per-row loads in its tile (one
@@ -441,8 +455,10 @@ __global__ void __launch_bounds__(tc_threads<D, MASK, TANGENT>(), 1)
   // all want the exponential unit at the same time).
   constexpr bool kAlt = !TANGENT && MASK != kMaskAdditive;
   constexpr bool kPairOwn = kAlt && kPairS;
-  constexpr bool kIssue2 = tc_split_issue<D, MASK, TANGENT>();
+  constexpr bool kIssue2 = tc_split_issue<D, MASK, TANGENT>();  // second P~V warp
+  constexpr bool kScore2 = tc_score2<D, MASK, TANGENT, SPLIT>();  // second score warp
   static_assert(!kIssue2 || (kAlt && !kPairS), "split issue: alternate single tiles");
+  static_assert(!kScore2 || !kPairS, "a second score warp takes single tiles");
   constexpr int KW = kAlt ? BN : HN;  // keys of a tile per softmax thread
   // The next tile of the warpgroup that takes tile t, and whether tile t is
   // the first of its accumulator.
@@ -651,7 +667,7 @@ __global__ void __launch_bounds__(tc_threads<D, MASK, TANGENT>(), 1)
           mbar_wait<kHint>(&ctrl->msk_full[u % NMS], (u / NMS) & 1, &zero);
       }
     }
-  } else if (warp == 1 || (kIssue2 && warp == kScoreWarp2)) {
+  } else if (warp == 1 || (kScore2 && warp == kScoreWarp2)) {
     // ------------------------------------------------------------ score MMAs
     // Tile t's score products go into buffer t % NB once its K tile has landed
     // and the P~V MMAs of tile t - NB (the buffer's previous user) are done.
@@ -672,9 +688,9 @@ __global__ void __launch_bounds__(tc_threads<D, MASK, TANGENT>(), 1)
       const uint32_t sdQ = smem_u32(smem + L::OFF_DQ);
       // s < 0: -Q K^T, -Q dK^T, -dQ K^T (negate-A bit), with |s| applied later.
       const uint32_t neg_a = p.neg_scores ? (1u << 13) : 0u;
-      constexpr int SSTEP = (kPairS || kIssue2) ? 2 : 1;  // key tiles per step
-      const int s_first = (kIssue2 && warp != 1) ? 1 : 0;
-      uint64_t* const s_drain = (kIssue2 && warp != 1) ? &ctrl->drain2 : &ctrl->drain;
+      constexpr int SSTEP = (kPairS || kScore2) ? 2 : 1;  // key tiles per step
+      const int s_first = (kScore2 && warp != 1) ? 1 : 0;
+      uint64_t* const s_drain = (kScore2 && warp != 1) ? &ctrl->drain2 : &ctrl->drain;
       for (int t = s_first; ok && t < n_kv; t += SSTEP) {
         const bool pair = kPairS && t + 1 < n_kv;
         const int s = t % NS;
@@ -1469,7 +1485,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     // the two CTAs of a query tile (consecutive blocks) form a cluster
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(tc_threads<D, MASK, TANGENT>());
+    cfg.blockDim = dim3(tc_threads<D, MASK, TANGENT, SPLIT>());
     cfg.dynamicSmemBytes = L::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1481,8 +1497,8 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const FwdParams& p, cudaStream
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, maps, p);
   }
-  kern<<<static_cast<unsigned>(grid), tc_threads<D, MASK, TANGENT>(), L::SMEM_BYTES, stream>>>(maps,
-                                                                                          p);
+  kern<<<static_cast<unsigned>(grid), tc_threads<D, MASK, TANGENT, SPLIT>(), L::SMEM_BYTES,
+         stream>>>(maps, p);
   return cudaGetLastError();
 }
 
