@@ -13,7 +13,8 @@
 // (p~ = exp(S - m)), then O = A / l, mu = mu~ / l, tO = T / l - mu O.
 //
 // Work decomposition: one CTA per (128-row query tile, batch*head), eleven
-// warps, one CTA per SM (it owns all 512 TMEM columns).
+// warps (twelve or thirteen where more warps issue MMAs, see tc_threads), one
+// CTA per SM (it owns all 512 TMEM columns).
 //   warp 0      TMA producer: Q, dQ once; then per 64-key tile the [K;dK]
 //               block and the [V|dV] block, through an NS-deep ring.
 //   warp 1      TMEM allocator; one thread issues the score MMAs.
@@ -22,6 +23,8 @@
 //               exchange their maxima through shared memory each tile.  The
 //               epilogue splits the output columns the same way.
 //   warp 10     one thread issues the P~V MMAs.
+//   warps 11,12 (some variants) a second score and a second P~V issuing
+//               thread, each taking the odd tiles.
 // Per key tile t (buffer b = t % 2 of the double-buffered score region):
 //   M1  [S | Q dK^T] = Q [K ; dK]^T          (N = 128, SMEM x SMEM)
 //       -> S is final: the softmax starts (max, exchange, exponentials)
